@@ -1,0 +1,153 @@
+"""Seeded synthetic inputs shared by the tests, the smoke check and the benchmark.
+
+This module holds random number generation and the workload recipes only -- none of the
+quantizer's arithmetic (no fp8 / e2m1 / e8m0 encoding happens here).  It is portable across
+machines: every draw comes from a counter-based splitmix64 stream keyed by (seed, tensor id),
+turned into uniforms from the top 53 bits and into normals by the Box-Muller transform, in
+numpy uint64 / float64 arithmetic.
+
+Workload recipes (the served model's linear shapes: hidden 5120, MLP 17408, merged gate_up
+34816 = 17408 + 17408; attention qkv 10240 x 5120):
+
+* tiny:     x bf16 ~ N(0, 1), each element x8 with probability 0.01; W fp32 ~ N(0, 0.02).
+* decode:   x bf16 ~ N(0, 1); weight bytes uniform 0..255; e8m0 uniform in {118..121}.
+* prefill:  x bf16 ~ N(0, 1) * r_m, r_m ~ LogNormal(0, 1) per row; nibbles uniform;
+            e8m0 uniform in {118..124}.
+* int4:     qweight int32 of uniform nibbles [K/8, N]; scales fp16(|N(0, 0.003)|) [K/128, N];
+            qzeros 0x77777777 [K/128, N/8]; x bf16 ~ N(0, 1).
+* requant:  W fp32 ~ N(0, 0.02) [N, K], split into row partitions.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+_GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+# Tensor ids: one independent stream per tensor role.
+T_X, T_OUTLIER, T_OUTLIER_PICK, T_W, T_E, T_ROWSCALE, T_QW, T_QS, T_WREQ = range(1, 10)
+
+GATE_UP = (34816, 5120)
+DOWN = (5120, 17408)
+QKV = (10240, 5120)
+GATE_UP_PARTITIONS = (17408, 17408)
+
+
+def _mix(z: np.ndarray) -> np.ndarray:
+    with np.errstate(over="ignore"):
+        z = (z ^ (z >> np.uint64(30))) * _M1
+        z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def u64(seed: int, tensor: int, n: int, offset: int = 0) -> np.ndarray:
+    """n pseudo-random uint64 from the counter-based stream (seed, tensor)."""
+    key = _mix(np.array([(seed * 1000003 + tensor) & 0xFFFFFFFFFFFFFFFF], np.uint64))[0]
+    ctr = np.arange(offset + 1, offset + n + 1, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        return _mix(key + ctr * _GOLDEN)
+
+
+def uniform(seed: int, tensor: int, n: int) -> np.ndarray:
+    """Uniform float64 in [0, 1)."""
+    return (u64(seed, tensor, n) >> np.uint64(11)).astype(np.float64) * (1.0 / 9007199254740992.0)
+
+
+def normal(seed: int, tensor: int, n: int, chunk: int = 1 << 24) -> np.ndarray:
+    """Standard normals; element 2j is r*cos(t) and element 2j+1 is r*sin(t) for the uniform
+    pair at counters (2j, 2j+1), so the stream does not depend on the chunk size."""
+    out = np.empty(n, np.float64)
+    for a in range(0, n, chunk):  # chunk is even, so pairs never straddle chunks
+        b = min(n, a + chunk)
+        h = (b - a + 1) // 2
+        u = (u64(seed, tensor, 2 * h, offset=a) >> np.uint64(11)).astype(np.float64)
+        u *= 1.0 / 9007199254740992.0
+        r = np.sqrt(-2.0 * np.log(1.0 - u[0::2]))
+        t = 2.0 * np.pi * u[1::2]
+        z = np.empty(2 * h, np.float64)
+        z[0::2] = r * np.cos(t)
+        z[1::2] = r * np.sin(t)
+        out[a:b] = z[: b - a]
+    return out
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float -> bfloat16 bit patterns (uint16), round to nearest even (finite inputs)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_float(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def activations(M: int, K: int, seed: int = 0, outliers: bool = False,
+                lognormal_rows: bool = False) -> np.ndarray:
+    """bf16 bits [M, K]."""
+    x = normal(seed, T_X, M * K).reshape(M, K)
+    if outliers:
+        pick = uniform(seed, T_OUTLIER_PICK, M * K).reshape(M, K) < 0.01
+        x = np.where(pick, 8.0 * x, x)
+    if lognormal_rows:
+        r = np.exp(normal(seed, T_ROWSCALE, M))
+        x = x * r[:, None]
+    return to_bf16_bits(x.astype(np.float32))
+
+
+def uniform_bytes(n_rows: int, n_cols: int, seed: int, tensor: int) -> np.ndarray:
+    n = n_rows * n_cols
+    words = u64(seed, tensor, (n + 7) // 8)
+    return words.view(np.uint8)[:n].reshape(n_rows, n_cols).copy()
+
+
+def uniform_ints(n: int, lo: int, hi: int, seed: int, tensor: int) -> np.ndarray:
+    """Uniform integers in [lo, hi] inclusive."""
+    span = np.uint64(hi - lo + 1)
+    return lo + (u64(seed, tensor, n) % span).astype(np.int64)
+
+
+def mxfp4_weights(N: int, K: int, seed: int = 0, e_lo: int = 118, e_hi: int = 121):
+    """(packed [N, K/2] uint8 with uniform bytes, e8m0 [N, K/32] uniform in [e_lo, e_hi])."""
+    packed = uniform_bytes(N, K // 2, seed, T_W)
+    e8m0 = uniform_ints(N * (K // 32), e_lo, e_hi, seed, T_E).astype(np.uint8)
+    return packed, e8m0.reshape(N, K // 32)
+
+
+def decode_case(M: int, N: int, K: int, seed: int = 0):
+    x = activations(M, K, seed)
+    w, e = mxfp4_weights(N, K, seed, 118, 121)
+    return x, w, e
+
+
+def prefill_case(M: int, N: int, K: int, seed: int = 0):
+    x = activations(M, K, seed, lognormal_rows=True)
+    w, e = mxfp4_weights(N, K, seed, 118, 124)
+    return x, w, e
+
+
+def int4_weights(N: int, K: int, seed: int = 0):
+    """(qweight int32 [K/8, N], scales fp16 bits uint16 [K/128, N], qzeros int32 [K/128, N/8])."""
+    n_words = (K // 8) * N
+    q = u64(seed, T_QW, (n_words + 1) // 2).view(np.uint32)[:n_words]
+    qweight = q.view(np.int32).reshape(K // 8, N).copy()
+    s = np.abs(normal(seed, T_QS, (K // 128) * N) * 0.003).astype(np.float16)
+    scales = s.view(np.uint16).reshape(K // 128, N).copy()
+    qzeros = np.full((K // 128, max(N // 8, 1)), 0x77777777, np.uint32).view(np.int32)
+    return qweight, scales, qzeros
+
+
+def int4_case(M: int, N: int, K: int, seed: int = 0):
+    x = activations(M, K, seed)
+    qw, sc, qz = int4_weights(N, K, seed)
+    return x, qw, sc, qz
+
+
+def gaussian_weights(N: int, K: int, sigma: float = 0.02, seed: int = 0,
+                     row_gain=None) -> np.ndarray:
+    """fp32 [N, K] ~ N(0, sigma); row_gain (optional [N]) multiplies each row."""
+    w = normal(seed, T_WREQ, N * K).reshape(N, K) * sigma
+    if row_gain is not None:
+        w = w * np.asarray(row_gain, np.float64)[:, None]
+    return w.astype(np.float32)

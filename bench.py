@@ -1,0 +1,452 @@
+"""W4A8 quantized-linear benchmark (decode band, MXFP4).
+
+Workload (one step): for each of the two served shapes -- gate_up N=34816 K=5120 and down
+N=5120 K=17408 -- and each decode batch M in {1, 8, 32, 64}: per-token fp8 activation quant
+of x [M, K] followed by the MXFP4 W4A8 GEMM, 16 kernel launches in all.  Each (shape, M)
+pair owns its own weight copy, so one step streams 568 MB of weights (more than the 129 MB
+L2): every GEMM reads its weights from HBM.  The step is captured once in a CUDA graph and
+replayed.
+
+Metric: decode weight GB/s = weight bytes (N*K*(1/2 + 1/32) per GEMM) per step / step time.
+
+Also reported on the same line:
+  roofline      the decode GEMM kernel's achieved weight GB/s against the measured HBM copy
+                bandwidth, from CUDA events around each GEMM in a graph replay pass;
+  e2e           the same metric through the public Python API with host buffers: pinned host
+                x -> device, act quant + GEMM, bf16 output -> host, every step;
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload;
+  prefill / int4 / requant   the other hot-path kernels on their workloads (--extras).
+
+--impl reference times the CPU oracle (the only reference implementation this project has)
+on the same workload, as a bounded sample per step.
+Multi-GPU (torchrun): independent replicas, one per GPU; value = all ranks' bytes / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from int4_quantized_linear_gb300 import synth  # noqa: E402
+
+SHAPES = [("gate_up", synth.GATE_UP), ("down", synth.DOWN)]
+DECODE_M = [1, 8, 32, 64]
+METRIC = "W4A8 GEMM: decode weight GB/s and prefill TFLOP/s, % of GB300 roofline"
+WORKLOAD = ("decode band MXFP4 W4A8: M in {1,8,32,64} x {gate_up N=34816 K=5120, down N=5120 "
+            "K=17408}; act quant + GEMM per (shape, M)")
+
+
+def weight_bytes(N, K):
+    return N * K // 2 + N * K // 32
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons in the background."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+
+        def reader():
+            for line in self.proc.stdout:
+                self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        rows = [r for t, r in self.rows if t0 <= t <= t1]
+        window = "timed region"
+        if len(rows) < 3:  # short timed region: widen to the surrounding load phase
+            mid = 0.5 * (t0 + t1)
+            rows = [r for t, r in self.rows if abs(t - mid) <= max(1.0, 0.5 * (t1 - t0))]
+            window = "timed region +-1 s"
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm = []
+        smax = None
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+            except (ValueError, IndexError):
+                continue
+            for i, n in enumerate(names):
+                if len(r) > 5 + i and r[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(rows), "window": window}
+
+
+# ---------------------------------------------------------------------------------- CPU side
+
+def oracle_sample(orc, cases, budget_s):
+    """Time the oracle GEMM (act quant of the sample rows + dequantize-and-matmul) over a
+    column sample of every (shape, M) case; returns (weight bytes processed, seconds)."""
+    done_bytes = 0
+    total_t = 0.0
+    per_case = budget_s / len(cases)
+    for (name, (N, K), M, x, w, e) in cases:
+        # calibrate columns so this case costs about per_case seconds
+        cols = 8
+        t_start = time.perf_counter()
+        xq, xs = orc.act_quant(x)
+        while True:
+            n_idx = np.arange(cols) % N
+            im = np.repeat(np.arange(M), cols)
+            inn = np.tile(n_idx, M)
+            t0 = time.perf_counter()
+            orc.mxfp4_linear_pairs(xq, xs, w, e, im, inn)
+            dt = time.perf_counter() - t0
+            if dt >= per_case * 0.5 or cols >= N:
+                break
+            cols = min(N, int(cols * max(2.0, per_case / max(dt, 1e-4))))
+        total_t += time.perf_counter() - t_start
+        done_bytes += cols * (K // 2 + K // 32)
+    return done_bytes, total_t
+
+
+def make_host_cases(seed=0):
+    cases = []
+    for name, (N, K) in SHAPES:
+        w, e = synth.mxfp4_weights(N, K, seed, 118, 121)
+        for M in DECODE_M:
+            cases.append((name, (N, K), M, synth.activations(M, K, seed + M), w, e))
+    return cases
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle as orc
+    orc.build()
+    cases = make_host_cases()
+    budget = float(os.environ.get("W4A8_REF_STEP_S", "1.0"))
+    for _ in range(args.warmup):
+        oracle_sample(orc, cases, budget * 0.25)
+    tot_b, tot_t = 0, 0.0
+    for _ in range(args.steps):
+        b, t = oracle_sample(orc, cases, budget)
+        tot_b += b
+        tot_t += t
+    value = tot_b / tot_t / 1e9
+    cores = orc.num_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 (oracle: e4m3 x e2m1 dequantized exactly, fp64 accumulate)",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "parallelism": "cpu oracle",
+                                        "sample": "output-column sample per (shape, M)"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"~{budget:.1f} s of oracle GEMM per step over column samples of all 8 (shape, M) cases"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------- GPU side
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from int4_quantized_linear_gb300 import binding as lib
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lib.load()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    def to_dev_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    # ---- workload: one weight copy per (shape, M), inputs resident in HBM
+    calls = []
+    for name, (N, K) in SHAPES:
+        w_host, e_host = synth.mxfp4_weights(N, K, 0, 118, 121)
+        w0, e0 = to_dev(w_host), to_dev(e_host)
+        for i, M in enumerate(DECODE_M):
+            w = w0 if i == 0 else w0.clone()
+            e = e0 if i == 0 else e0.clone()
+            x_host = synth.activations(M, K, seed=M)
+            x = to_dev_bf16(x_host)
+            xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
+            xs = torch.empty((M,), dtype=torch.float32, device=dev)
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ws = lib.make_workspace(lib.workspace_bytes(M, N, K), dev)
+            calls.append(dict(name=name, N=N, K=K, M=M, w=w, e=e, x=x, x_host=x_host, xq=xq, xs=xs,
+                              out=out, ws=ws, bytes=weight_bytes(N, K)))
+    step_bytes = sum(c["bytes"] for c in calls)
+    clib = lib.load()
+    stream = torch.cuda.Stream(device=dev)
+
+    def launch(c, s):
+        st = clib.w4a8_act_quant(c["x"].data_ptr(), c["xq"].data_ptr(), c["xs"].data_ptr(), c["M"], c["K"], s)
+        if st:
+            raise lib.W4A8Error("w4a8_act_quant", st)
+        ws = c["ws"]
+        st = clib.w4a8_mxfp4_linear(c["xq"].data_ptr(), c["xs"].data_ptr(), c["w"].data_ptr(),
+                                    c["e"].data_ptr(), c["out"].data_ptr(), c["M"], c["N"], c["K"],
+                                    None if ws is None else ws.data_ptr(),
+                                    0 if ws is None else ws.numel(), s)
+        if st:
+            raise lib.W4A8Error("w4a8_mxfp4_linear", st)
+
+    # eager warm-up (also makes the library's lazy per-device set-up happen outside capture)
+    with torch.cuda.stream(stream):
+        for c in calls:
+            launch(c, stream.cuda_stream)
+    stream.synchronize()
+
+    # ---- step graph, and a second graph with timing events around every GEMM
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for c in calls:
+            launch(c, stream.cuda_stream)
+    ev_graph = None
+    evs = None
+    try:
+        evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in calls]
+        ev_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ev_graph, stream=stream):
+            for c, (a, b) in zip(calls, evs):
+                st = clib.w4a8_act_quant(c["x"].data_ptr(), c["xq"].data_ptr(), c["xs"].data_ptr(),
+                                         c["M"], c["K"], stream.cuda_stream)
+                a.record(stream)
+                ws = c["ws"]
+                clib.w4a8_mxfp4_linear(c["xq"].data_ptr(), c["xs"].data_ptr(), c["w"].data_ptr(),
+                                       c["e"].data_ptr(), c["out"].data_ptr(), c["M"], c["N"], c["K"],
+                                       None if ws is None else ws.data_ptr(),
+                                       0 if ws is None else ws.numel(), stream.cuda_stream)
+                b.record(stream)
+    except (TypeError, RuntimeError):
+        ev_graph = None
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    # keep the GPU busy for a moment so the clock samples see the load
+    t_load = time.time()
+    while time.time() - t_load < 0.5:
+        graph.replay()
+        torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    elapsed_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    value = world * step_bytes * args.steps / (elapsed_ms * 1e-3) / 1e9
+
+    # ---- per-kernel durations of the decode GEMM (same graph, event-bracketed GEMMs)
+    gemm_ms = [0.0] * len(calls)
+    reps = max(3, min(args.steps, 50))
+    if ev_graph is not None:
+        for _ in range(reps):
+            ev_graph.replay()
+            torch.cuda.synchronize()
+            for i, (a, b) in enumerate(evs):
+                gemm_ms[i] += a.elapsed_time(b) / reps
+    t_kern_end = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    peaks, peak_src = load_peaks()
+    roofline = None
+    if ev_graph is not None:
+        ach = sum(c["bytes"] for c in calls) / (sum(gemm_ms) * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                    "kernel": "decode-band MXFP4 GEMM (w4a8_mxfp4_linear, M<=64)",
+                    "peak_source": peak_src,
+                    "per_case_us": {f"{c['name']}_M{c['M']}": round(1e3 * g, 2) for c, g in zip(calls, gemm_ms)}}
+
+    # ---- e2e through the public API with host buffers
+    h2d = sum(c["M"] * c["K"] * 2 for c in calls)
+    d2h = sum(c["M"] * c["N"] * 2 for c in calls)
+    pinned_x = [torch.from_numpy(c["x_host"].view(np.int16)).view(torch.bfloat16).pin_memory() for c in calls]
+    pinned_o = [torch.empty((c["M"], c["N"]), dtype=torch.bfloat16).pin_memory() for c in calls]
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for c, hx, ho in zip(calls, pinned_x, pinned_o):
+                xd = hx.to(dev, non_blocking=True)
+                o = lib.linear(xd, c["w"], c["e"], workspace=c["ws"], stream=stream)
+                ho.copy_(o, non_blocking=True)
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e_val = step_bytes * e2e_steps / e2e_s / 1e9
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e2m1 (fp32 accumulate)",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "weight_bytes_per_step": step_bytes,
+                   "l2": "inputs larger than L2: 8 distinct weight copies, 568 MB per step",
+                   "graph": "step captured in a CUDA graph", "parallelism": f"replicas x{world}"},
+        "roofline": roofline,
+        "clocks": clocks,
+        "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "path": "binding.linear per (shape, M), eager, pinned host x in / bf16 out"},
+        "gpu_launches": 2 * len(calls) * args.steps,
+    }
+    if args.extras and rank == 0:
+        line["extras"] = run_extras(lib, dev, peaks)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle as orc
+        orc.build()
+        b, t = oracle_sample(orc, make_host_cases(), float(os.environ.get("W4A8_CPU_BASELINE_S", "12")))
+        line["cpu_baseline"] = {"value": b / t / 1e9, "unit": "GB/s", "cores": orc.num_threads(),
+                                "kind": "oracle",
+                                "sample": f"oracle act quant + GEMM on output-column samples of all 8 (shape, M) cases, {t:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_extras(lib, dev, peaks):
+    """Prefill, int4 and requant kernels on their workloads (event-timed, inputs > L2)."""
+    import torch
+    out = {}
+
+    def timeit(fn, reps=5):
+        fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    def to_dev(arr):
+        return torch.from_numpy(np.ascontiguousarray(arr)).to(dev)
+
+    fp8_peak = 2.0 * peaks.get("bf16_tflops", 1900.0)
+    pf = {}
+    for name, (N, K) in SHAPES + [("qkv", synth.QKV)]:
+        w, e = synth.mxfp4_weights(N, K, 0, 118, 124)
+        wd, ed = to_dev(w), to_dev(e)
+        for M in (512, 2048, 4096):
+            x = torch.randn((M, K), device=dev).to(torch.bfloat16)
+            xq, xs = lib.act_quant(x)
+            o = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ms = timeit(lambda: lib.mxfp4_linear(xq, xs, wd, ed, out=o))
+            tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+            pf[f"{name}_M{M}"] = {"ms": round(ms, 4), "tflops": round(tf, 1),
+                                  "frac_of_fp8_peak": round(tf / fp8_peak, 4)}
+    out["prefill"] = {"fp8_peak_tflops": fp8_peak,
+                      "peak_note": "2 x measured bf16 burst (fp8 dense rate is twice bf16)", "cases": pf}
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--extras", action="store_true", help="also time prefill / int4 / requant")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,150 @@
+/*
+ * w4a8.h -- C ABI of the GB300 (sm_103a) W4A8 quantized-linear library (libw4a8.so).
+ *
+ * The method (web pages this library follows):
+ *   "radiance_nvfp4.py"        -- NVFP4 -> MXFP4 requant at load (dequant_nvfp4,
+ *                                 _block_exponent, e2m1_index, _encode_blocks, quant_mxfp4,
+ *                                 process_weights_after_loading) and the MXFP4 weight layout
+ *                                 (module docstring, item 3).
+ *   "vllm-radiance (MXFP4)"    -- section "How the MXFP4 path works", subsection "The W4A8
+ *                                 fp8-WMMA kernel": fp8 activations x e2m1 weights with the
+ *                                 e8m0 scale folded in, a prefill tiling and a decode tiling
+ *                                 with a fused split-K whose last arrival reduces.
+ *   "radiance_autoround.py"    -- AutoRound int4 group-128 symmetric W4A8 (module docstring,
+ *                                 autoround_linear, _exact_ref, _ensure_scratch).
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer unless it says "host".  The caller owns all
+ *     memory; no entry point allocates or frees device memory.
+ *   - All work is enqueued on `stream` (asynchronous); a return of W4A8_OK means the work was
+ *     launched, not that it finished.  Launch failures come back as W4A8_ERR_CUDA.
+ *   - Arguments are validated before anything is launched; on any error nothing is launched
+ *     and outputs are untouched.  M == 0 is a no-op that returns W4A8_OK.
+ *   - Tensors are dense and row-major.  Outputs must not alias inputs.
+ *   - bf16 and fp16 values travel as their 16-bit patterns (uint16_t).
+ *   - e4m3 means OCP FP8 E4M3 (bias 7, max 448, no infinities, 0x7F/0xFF NaN).
+ *     e2m1 code: bit 3 sign, bits 0-2 index the grid {0, .5, 1, 1.5, 2, 3, 4, 6}.
+ *     e8m0 code c is the scale 2^(c - 127).
+ */
+#ifndef W4A8_H_
+#define W4A8_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define W4A8_API __attribute__((visibility("default")))
+#else
+#define W4A8_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    W4A8_OK = 0,
+    W4A8_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad mode, bad partitions */
+    W4A8_ERR_UNSUPPORTED_SHAPE = 2, /* K not a multiple of the format's block */
+    W4A8_ERR_MISALIGNED = 3,        /* a pointer violates the stated alignment */
+    W4A8_ERR_WORKSPACE = 4,         /* workspace missing or smaller than required */
+    W4A8_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed */
+    W4A8_ERR_TIMEOUT = 6            /* a bounded device-side wait gave up (see below) */
+} w4a8_status;
+
+/* Per-token dynamic fp8 activation quant ("radiance_autoround.py", autoround_linear: the
+ * per-token dynamic fp8 cast before the GEMM; "vllm-radiance (MXFP4)", "fp8 activations").
+ *   x_bf16  [M, K] bf16 (16-byte aligned)
+ *   xq      [M, K] e4m3 codes, written (8-byte aligned)
+ *   x_scale [M] fp32, written: amax_m / 448 (correctly rounded); an all-zero row gets 1.0
+ *   xq[m,k] = e4m3_rn_satfinite(x[m,k] / x_scale[m]) with a correctly rounded fp32 division.
+ * K must be a multiple of 8. */
+W4A8_API w4a8_status w4a8_act_quant(const uint16_t *x_bf16, uint8_t *xq, float *x_scale, int64_t M,
+                           int64_t K, cudaStream_t stream);
+
+/* MXFP4 W4A8 linear ("vllm-radiance (MXFP4)", "The W4A8 fp8-WMMA kernel"; weight layout from
+ * "radiance_nvfp4.py" module docstring item 3):
+ *   out[m,n] = bf16( x_scale[m] * sum_k e4m3(xq[m,k]) * e2m1(W[n,k]) * 2^(E[n,k/32]-127) )
+ *   xq       [M, K]   e4m3 codes (16-byte aligned)
+ *   x_scale  [M]      fp32 per-token scale
+ *   w_packed [N, K/2] two e2m1 codes per byte, the even k in the low nibble (32-byte aligned
+ *                     for the tensor-core path; 16-byte aligned otherwise)
+ *   w_e8m0   [N, K/32] block scales (4-byte aligned)
+ *   out_bf16 [M, N]   written (4-byte aligned)
+ *   workspace: device scratch of at least w4a8_workspace_bytes(M, N, K) bytes (may be NULL
+ *   when that is 0).  It holds fp32 split-K partials and per-tile arrival counters; the
+ *   counters must be zero before the first call that uses the buffer and are left at zero by
+ *   every call, so one buffer can be reused call after call on one stream.  Two calls that
+ *   run at the same time must not share a workspace.
+ * K must be a multiple of 32.  M <= 64 takes the decode tiling (split-K over K), larger M the
+ * prefill tiling; both are chosen inside this call. */
+W4A8_API w4a8_status w4a8_mxfp4_linear(const uint8_t *xq, const float *x_scale, const uint8_t *w_packed,
+                              const uint8_t *w_e8m0, uint16_t *out_bf16, int64_t M, int64_t N,
+                              int64_t K, void *workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
+
+/* Bytes of workspace w4a8_mxfp4_linear needs for this shape (0 if none). */
+W4A8_API size_t w4a8_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* NVFP4 -> MXFP4 requant of a (merged) linear ("radiance_nvfp4.py": dequant_nvfp4,
+ * _block_exponent, e2m1_index, _encode_blocks, quant_mxfp4, requant_rows,
+ * RadianceNvfp4ToMxfp4.process_weights_after_loading).  Per 32-block of each row n in
+ * partition p:
+ *   R1  w = fl( e2m1 * fl( fp32(e4m3 scale per 16) / divisor[p] ) )
+ *   R2  block exponent e: mode 0 ocp floor(log2 amax) - 2; mode 1 noclip ceil(log2(amax/6));
+ *       mode 2 mse: noclip or one binade finer, whichever has the strictly lower squared
+ *       error (fp32 squares summed in ascending k); amax = 0 gives e = 0; e in [-127, 127]
+ *   R3  code = e2m1_index(|w| / 2^e) (ties to the even index), sign bit only for index != 0
+ *   R4  out_packed byte j = code[2j] | code[2j+1] << 4; out_e8m0 = e + 127
+ *   nv_packed      [N, K/2] e2m1 codes, low nibble = even k (16-byte aligned)
+ *   nv_scale_e4m3  [N, K/16] e4m3 scale codes (2-byte aligned)
+ *   global_divisor [P] fp32, the checkpoint's weight_global_scale as stored (6*448/amax)
+ *   partition_rows [P] HOST array of row counts, in order, summing to N; 1 <= P <= 16
+ *   out_packed [N, K/2] (16-byte aligned), out_e8m0 [N, K/32], written
+ *   err_ssq    [P][2] fp64 or NULL; written with {sum of squared requant error, sum of
+ *              squared dequantized weights} per partition (relRMS = sqrt(err/ssq))
+ * K must be a multiple of 32. */
+W4A8_API w4a8_status nvfp4_to_mxfp4_requant(const uint8_t *nv_packed, const uint8_t *nv_scale_e4m3,
+                                   const float *global_divisor, const int64_t *partition_rows,
+                                   int P, int64_t N, int64_t K, int mode, uint8_t *out_packed,
+                                   uint8_t *out_e8m0, double *err_ssq, cudaStream_t stream);
+
+/* AutoRound int4 group-128 symmetric W4A8 linear ("radiance_autoround.py": module docstring,
+ * _exact_ref; the symmetric zero point 8 is folded in, so code c means c - 8):
+ *   out[m,n] = bf16( x_scale[m] * sum_k e4m3(xq[m,k]) * (c[k,n] - 8) * fp16(s[k/128, n]) )
+ *   qweight     [K/8, N] int32, nibble j of word (i, n) holds k = 8i + j (checkpoint layout;
+ *               16-byte aligned)
+ *   scales_fp16 [K/128, N] fp16 bits
+ *   workspace / workspace_bytes: as for w4a8_mxfp4_linear, sized by
+ *   w4a8_int4g128_workspace_bytes.
+ * The caller checks qzeros == 0x77777777 before calling (the Python binding does).
+ * K must be a multiple of 128. */
+W4A8_API w4a8_status w4a8_int4g128_linear(const uint8_t *xq, const float *x_scale, const int32_t *qweight,
+                                 const uint16_t *scales_fp16, uint16_t *out_bf16, int64_t M,
+                                 int64_t N, int64_t K, void *workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+
+W4A8_API size_t w4a8_int4g128_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* Human-readable name of a status code (static storage). */
+W4A8_API const char *w4a8_status_string(w4a8_status s);
+
+/* Kernel selection for the GEMM entry points: 0 = automatic (default), 1 = always the CUDA-core
+ * kernels, 2 = the tensor-core (tcgen05) kernels wherever the shape allows.  Process-wide; meant
+ * for tests and measurements. */
+W4A8_API void w4a8_set_gemm_policy(int policy);
+
+/* Every device-side wait in the tensor-core kernels is bounded.  A wait that gives up records
+ * a code in a device status word and the kernel returns early (its output is then invalid).
+ * This call synchronizes `stream`, reads and clears that word, and returns W4A8_ERR_TIMEOUT if
+ * any wait gave up since the last check, W4A8_OK otherwise. */
+W4A8_API w4a8_status w4a8_check_device_status(cudaStream_t stream);
+
+/* Decode-band threshold: M <= this takes the decode tiling (64). */
+W4A8_API int w4a8_decode_max_m(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* W4A8_H_ */

@@ -1,0 +1,233 @@
+"""Thin Python binding over the C ABI of ``libw4a8.so`` (declared in ``include/w4a8.h``).
+
+Argument marshalling only: PyTorch allocates device memory and supplies the stream; every
+step of the path runs in the library's CUDA kernels.  There is no fallback: if the library is
+missing or a call fails, these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+_lib = None
+
+OK = 0
+STATUS = {0: "W4A8_OK", 1: "W4A8_ERR_INVALID_ARG", 2: "W4A8_ERR_UNSUPPORTED_SHAPE",
+          3: "W4A8_ERR_MISALIGNED", 4: "W4A8_ERR_WORKSPACE", 5: "W4A8_ERR_CUDA",
+          6: "W4A8_ERR_TIMEOUT"}
+MODES = {"ocp": 0, "noclip": 1, "mse": 2}
+EXPORTS = ("w4a8_act_quant", "w4a8_mxfp4_linear", "w4a8_workspace_bytes",
+           "nvfp4_to_mxfp4_requant", "w4a8_int4g128_linear", "w4a8_int4g128_workspace_bytes",
+           "w4a8_status_string", "w4a8_set_gemm_policy", "w4a8_check_device_status",
+           "w4a8_decode_max_m")
+
+
+class W4A8Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+        self.status = status
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = True):
+    """Load libw4a8.so (building it in-tree first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_missing and not _build.up_to_date():
+        _build.build()
+    if not os.path.exists(_build.LIB_PATH):
+        raise RuntimeError(f"libw4a8.so not found at {_build.LIB_PATH}; run build()")
+    lib = ctypes.CDLL(_build.LIB_PATH)
+    P, I64, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    I = ctypes.c_int
+    sig = {
+        "w4a8_act_quant": (I, [P, P, P, I64, I64, P]),
+        "w4a8_mxfp4_linear": (I, [P, P, P, P, P, I64, I64, I64, P, SZ, P]),
+        "w4a8_workspace_bytes": (SZ, [I64, I64, I64]),
+        "nvfp4_to_mxfp4_requant": (I, [P, P, P, P, I, I64, I64, I, P, P, P, P]),
+        "w4a8_int4g128_linear": (I, [P, P, P, P, P, I64, I64, I64, P, SZ, P]),
+        "w4a8_int4g128_workspace_bytes": (SZ, [I64, I64, I64]),
+        "w4a8_status_string": (ctypes.c_char_p, [I]),
+        "w4a8_set_gemm_policy": (None, [I]),
+        "w4a8_check_device_status": (I, [P]),
+        "w4a8_decode_max_m": (I, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(fn: str, status: int):
+    if status != OK:
+        raise W4A8Error(fn, status)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+# --------------------------------------------------------------------------------------------
+
+def set_gemm_policy(policy: int) -> None:
+    """0 automatic, 1 CUDA-core kernels only, 2 tensor-core kernels wherever possible."""
+    load().w4a8_set_gemm_policy(int(policy))
+
+
+def decode_max_m() -> int:
+    return load().w4a8_decode_max_m()
+
+
+def check_device_status(stream=None) -> None:
+    _check("w4a8_check_device_status", load().w4a8_check_device_status(_stream(stream)))
+
+
+def act_quant(x: torch.Tensor, xq: torch.Tensor | None = None, x_scale: torch.Tensor | None = None,
+              stream=None):
+    """x bf16 [M, K] -> (xq uint8 e4m3 codes [M, K], x_scale float32 [M])."""
+    _dev(x, "x", torch.bfloat16)
+    M, K = x.shape
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if x_scale is None:
+        x_scale = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _check("w4a8_act_quant", load().w4a8_act_quant(_ptr(x), _ptr(xq), _ptr(x_scale), M, K,
+                                                   _stream(stream)))
+    return xq, x_scale
+
+
+def workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load().w4a8_workspace_bytes(M, N, K))
+
+
+def int4_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load().w4a8_int4g128_workspace_bytes(M, N, K))
+
+
+def make_workspace(nbytes: int, device) -> torch.Tensor | None:
+    """Zero-initialised workspace (the arrival counters must start at zero)."""
+    if nbytes == 0:
+        return None
+    return torch.zeros((nbytes + 15) // 16 * 16, dtype=torch.uint8, device=device)
+
+
+def mxfp4_linear(xq, x_scale, w_packed, w_e8m0, out=None, workspace=None, stream=None):
+    """out[m, n] = bf16(x_scale[m] * sum_k e4m3(xq) * e2m1(W) * 2^(E - 127))."""
+    for t, n, d in ((xq, "xq", torch.uint8), (x_scale, "x_scale", torch.float32),
+                    (w_packed, "w_packed", torch.uint8), (w_e8m0, "w_e8m0", torch.uint8)):
+        _dev(t, n, d)
+    M, K = xq.shape
+    N = w_packed.shape[0]
+    if w_packed.shape != (N, K // 2) or w_e8m0.shape != (N, K // 32):
+        raise ValueError("weight shapes do not match K")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    need = workspace_bytes(M, N, K)
+    if need and workspace is None:
+        workspace = make_workspace(need, xq.device)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("w4a8_mxfp4_linear", load().w4a8_mxfp4_linear(
+        _ptr(xq), _ptr(x_scale), _ptr(w_packed), _ptr(w_e8m0), _ptr(out), M, N, K,
+        _ptr(workspace), wsb, _stream(stream)))
+    return out
+
+
+def check_symmetric_qzeros(qzeros: torch.Tensor) -> None:
+    """radiance_autoround.py, process_weights_after_loading: the kernel folds a constant zero
+    point of 8, so every qzeros word must be 0x77777777."""
+    z = qzeros.view(torch.int32)
+    bad = int((z != 0x77777777).sum())
+    if bad:
+        raise ValueError(f"AutoRound checkpoint is not symmetric: {bad} of {z.numel()} qzeros "
+                         "words differ from 0x77777777")
+
+
+def check_autoround_config(bits: int, group_size: int, sym: bool) -> None:
+    """radiance_autoround.py, AutoRoundConfig.from_config: 4 bits, group 128, symmetric."""
+    if bits != 4:
+        raise ValueError(f"int4 kernel supports 4 bits only, got {bits}")
+    if group_size != 128:
+        raise ValueError(f"int4 kernel is built for group_size=128, got {group_size}")
+    if not sym:
+        raise ValueError("int4 kernel requires sym=true")
+
+
+def int4g128_linear(xq, x_scale, qweight, scales_fp16, out=None, workspace=None, qzeros=None,
+                    stream=None):
+    """out[m, n] = bf16(x_scale[m] * sum_k e4m3(xq) * (c - 8) * fp16(s[k/128, n]))."""
+    _dev(xq, "xq", torch.uint8)
+    _dev(x_scale, "x_scale", torch.float32)
+    _dev(qweight, "qweight", torch.int32)
+    _dev(scales_fp16, "scales", torch.float16)
+    if qzeros is not None:
+        check_symmetric_qzeros(qzeros)
+    M, K = xq.shape
+    N = qweight.shape[1]
+    if qweight.shape != (K // 8, N) or scales_fp16.shape != (K // 128, N):
+        raise ValueError("int4 weight shapes do not match K")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    need = int4_workspace_bytes(M, N, K)
+    if need and workspace is None:
+        workspace = make_workspace(need, xq.device)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("w4a8_int4g128_linear", load().w4a8_int4g128_linear(
+        _ptr(xq), _ptr(x_scale), _ptr(qweight), _ptr(scales_fp16), _ptr(out), M, N, K,
+        _ptr(workspace), wsb, _stream(stream)))
+    return out
+
+
+def requant(nv_packed, nv_scale, divisors, partition_rows, mode="mse", out_packed=None,
+            out_e8m0=None, err_ssq=True, stream=None):
+    """NVFP4 -> MXFP4.  Returns (packed uint8 [N, K/2], e8m0 uint8 [N, K/32], err_ssq float64
+    [P, 2] or None)."""
+    _dev(nv_packed, "nv_packed", torch.uint8)
+    if nv_scale.dtype == torch.float8_e4m3fn:
+        nv_scale = nv_scale.view(torch.uint8)
+    _dev(nv_scale, "nv_scale", torch.uint8)
+    _dev(divisors, "divisors", torch.float32)
+    N, K2 = nv_packed.shape
+    K = 2 * K2
+    rows = (ctypes.c_int64 * len(partition_rows))(*[int(r) for r in partition_rows])
+    P = len(partition_rows)
+    if out_packed is None:
+        out_packed = torch.empty((N, K // 2), dtype=torch.uint8, device=nv_packed.device)
+    if out_e8m0 is None:
+        out_e8m0 = torch.empty((N, K // 32), dtype=torch.uint8, device=nv_packed.device)
+    es = torch.empty((P, 2), dtype=torch.float64, device=nv_packed.device) if err_ssq else None
+    _check("nvfp4_to_mxfp4_requant", load().nvfp4_to_mxfp4_requant(
+        _ptr(nv_packed), _ptr(nv_scale), _ptr(divisors), ctypes.cast(rows, ctypes.c_void_p), P, N,
+        K, MODES[mode] if isinstance(mode, str) else int(mode), _ptr(out_packed), _ptr(out_e8m0),
+        _ptr(es), _stream(stream)))
+    return out_packed, out_e8m0, es
+
+
+def linear(x: torch.Tensor, w_packed: torch.Tensor, w_e8m0: torch.Tensor, workspace=None,
+           stream=None) -> torch.Tensor:
+    """The whole W4A8 MXFP4 linear: per-token fp8 activation quant, then the GEMM."""
+    xq, xs = act_quant(x, stream=stream)
+    return mxfp4_linear(xq, xs, w_packed, w_e8m0, workspace=workspace, stream=stream)

@@ -1,0 +1,122 @@
+// api.cu -- argument validation and kernel dispatch for the GEMM entry points, the status
+// strings, the kernel-selection policy and the device status word of the bounded waits.
+//
+// Dispatch ("vllm-radiance (MXFP4)", "The W4A8 fp8-WMMA kernel": a prefill tiling and a decode
+// tiling, chosen inside the native call so no shape branch is visible to the caller;
+// "radiance_autoround.py", autoround_linear: the prefill/decode choice is made natively).
+#include <atomic>
+
+#include "common.cuh"
+#include "dispatch.h"
+
+static std::atomic<int> g_policy{0};
+
+// Device status word written by bounded waits that give up (0 = clean).
+__device__ unsigned int g_w4a8_device_status = 0;
+
+unsigned int *w4a8_device_status_ptr()
+{
+    static unsigned int *ptr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_w4a8_device_status) != cudaSuccess) return nullptr;
+        ptr[dev] = static_cast<unsigned int *>(p);
+    }
+    return ptr[dev];
+}
+
+int w4a8_gemm_policy() { return g_policy.load(std::memory_order_relaxed); }
+
+extern "C" void w4a8_set_gemm_policy(int policy) { g_policy.store(policy, std::memory_order_relaxed); }
+
+extern "C" int w4a8_decode_max_m(void) { return W4A8_DECODE_MAX_M; }
+
+extern "C" const char *w4a8_status_string(w4a8_status s)
+{
+    switch (s) {
+    case W4A8_OK: return "W4A8_OK";
+    case W4A8_ERR_INVALID_ARG: return "W4A8_ERR_INVALID_ARG";
+    case W4A8_ERR_UNSUPPORTED_SHAPE: return "W4A8_ERR_UNSUPPORTED_SHAPE";
+    case W4A8_ERR_MISALIGNED: return "W4A8_ERR_MISALIGNED";
+    case W4A8_ERR_WORKSPACE: return "W4A8_ERR_WORKSPACE";
+    case W4A8_ERR_CUDA: return "W4A8_ERR_CUDA";
+    case W4A8_ERR_TIMEOUT: return "W4A8_ERR_TIMEOUT";
+    }
+    return "W4A8_ERR_UNKNOWN";
+}
+
+extern "C" w4a8_status w4a8_check_device_status(cudaStream_t stream)
+{
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return W4A8_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_w4a8_device_status, sizeof(v)) != cudaSuccess) return W4A8_ERR_CUDA;
+    if (v) {
+        unsigned int z = 0;
+        if (cudaMemcpyToSymbol(g_w4a8_device_status, &z, sizeof(z)) != cudaSuccess) return W4A8_ERR_CUDA;
+        return W4A8_ERR_TIMEOUT;
+    }
+    return W4A8_OK;
+}
+
+extern "C" size_t w4a8_workspace_bytes(int64_t M, int64_t N, int64_t K)
+{
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    return w4a8_tc_workspace_bytes(M, N, K, w4a8_gemm_policy());
+}
+
+extern "C" size_t w4a8_int4g128_workspace_bytes(int64_t M, int64_t N, int64_t K)
+{
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    return w4a8_tc_int4_workspace_bytes(M, N, K, w4a8_gemm_policy());
+}
+
+extern "C" w4a8_status w4a8_mxfp4_linear(const uint8_t *xq, const float *x_scale,
+                                         const uint8_t *w_packed, const uint8_t *w_e8m0,
+                                         uint16_t *out_bf16, int64_t M, int64_t N, int64_t K,
+                                         void *workspace, size_t workspace_bytes,
+                                         cudaStream_t stream)
+{
+    if (M < 0 || N < 0 || K < 0) return W4A8_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return W4A8_OK;
+    if (K == 0 || !xq || !x_scale || !w_packed || !w_e8m0 || !out_bf16) return W4A8_ERR_INVALID_ARG;
+    if (K % 32 != 0) return W4A8_ERR_UNSUPPORTED_SHAPE;
+    if (!w4a8_aligned(xq, 16) || !w4a8_aligned(w_packed, 16) || !w4a8_aligned(x_scale, 4) ||
+        !w4a8_aligned(out_bf16, 2))
+        return W4A8_ERR_MISALIGNED;
+    const int policy = w4a8_gemm_policy();
+    if (policy != 1 && w4a8_tc_mxfp4_supported(xq, w_packed, w_e8m0, out_bf16, M, N, K)) {
+        const size_t need = w4a8_tc_workspace_bytes(M, N, K, policy);
+        if (need && (!workspace || workspace_bytes < need)) return W4A8_ERR_WORKSPACE;
+        if (need && !w4a8_aligned(workspace, 16)) return W4A8_ERR_MISALIGNED;
+        return w4a8_launch_mxfp4_tc(xq, x_scale, w_packed, w_e8m0, out_bf16, M, N, K, workspace,
+                                    policy, stream);
+    }
+    return w4a8_launch_mxfp4_simt(xq, x_scale, w_packed, w_e8m0, out_bf16, M, N, K, stream);
+}
+
+extern "C" w4a8_status w4a8_int4g128_linear(const uint8_t *xq, const float *x_scale,
+                                            const int32_t *qweight, const uint16_t *scales_fp16,
+                                            uint16_t *out_bf16, int64_t M, int64_t N, int64_t K,
+                                            void *workspace, size_t workspace_bytes,
+                                            cudaStream_t stream)
+{
+    if (M < 0 || N < 0 || K < 0) return W4A8_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return W4A8_OK;
+    if (K == 0 || !xq || !x_scale || !qweight || !scales_fp16 || !out_bf16)
+        return W4A8_ERR_INVALID_ARG;
+    if (K % 128 != 0) return W4A8_ERR_UNSUPPORTED_SHAPE;
+    if (!w4a8_aligned(xq, 16) || !w4a8_aligned(qweight, 4) || !w4a8_aligned(scales_fp16, 2) ||
+        !w4a8_aligned(x_scale, 4) || !w4a8_aligned(out_bf16, 2))
+        return W4A8_ERR_MISALIGNED;
+    const int policy = w4a8_gemm_policy();
+    if (policy != 1 && w4a8_tc_int4_supported(xq, qweight, scales_fp16, out_bf16, M, N, K)) {
+        const size_t need = w4a8_tc_int4_workspace_bytes(M, N, K, policy);
+        if (need && (!workspace || workspace_bytes < need)) return W4A8_ERR_WORKSPACE;
+        if (need && !w4a8_aligned(workspace, 16)) return W4A8_ERR_MISALIGNED;
+        return w4a8_launch_int4_tc(xq, x_scale, qweight, scales_fp16, out_bf16, M, N, K, workspace,
+                                   policy, stream);
+    }
+    return w4a8_launch_int4_simt(xq, x_scale, qweight, scales_fp16, out_bf16, M, N, K, stream);
+}

@@ -1,0 +1,202 @@
+// requant.cu -- NVFP4 -> MXFP4 requant of a (merged) linear at load time.
+//
+// "radiance_nvfp4.py": dequant_nvfp4 (W = e2m1 * fp32(e4m3 scale per 16) / global divisor,
+// per partition of a merged linear), _block_exponent (ocp / noclip), quant_mxfp4 (mse: the
+// no-clip exponent or one binade finer, whichever has the lower squared error), e2m1_index
+// (nearest grid point, ties to the even code), _encode_blocks, and the packing of item 3 of
+// the module docstring (low nibble = even k, e8m0 = e + 127).
+//
+// One thread per 32-block: a 16-byte load of 32 NVFP4 codes plus two e4m3 scale bytes in,
+// a 16-byte store of 32 MXFP4 codes plus one e8m0 byte out, so a warp moves 512 contiguous
+// bytes each way.  The whole block lives in registers; the page's fp32 transient and its row
+// chunking are not needed.  Every fp32 operation is written with an explicit rounding
+// intrinsic so that no multiply-add is contracted and the results match the oracle bit for
+// bit: the exponent comes from the float's bits (exact), the scaling by 2^-e is an exact
+// power-of-two product, and the squared errors are summed in ascending k.
+#include "common.cuh"
+
+namespace w4a8 {
+
+constexpr int RQ_THREADS = 256;
+constexpr int RQ_MAX_PARTS = 16;
+
+struct Partitions {
+    int P;
+    int64_t row_end[RQ_MAX_PARTS];
+};
+
+// floor(log2 a) for finite a > 0, from the bits (subnormals normalised).
+W4A8_DEVICE int floor_log2_exact(float a)
+{
+    uint32_t u = __float_as_uint(a);
+    int ex = (u >> 23) & 0xff;
+    if (ex) return ex - 127;
+    return (31 - __clz(u)) - 149;
+}
+
+// Is the significand of a (in [1, 2)) at most 1.5?
+W4A8_DEVICE bool significand_le_1p5(float a)
+{
+    uint32_t u = __float_as_uint(a);
+    int ex = (u >> 23) & 0xff;
+    uint32_t f = ex ? (u & 0x7fffffu) : ((u << (__clz(u) - 8)) & 0x7fffffu);
+    return f <= 0x400000u;
+}
+
+// _block_exponent: mode 0 ocp -> floor(log2 amax) - 2; otherwise noclip -> the smallest e
+// with amax <= 6 * 2^e, i.e. ceil(log2(amax / 6)).  amax = 0 -> 0; clamped to [-127, 127].
+W4A8_DEVICE int block_exponent(float amax, int mode)
+{
+    if (!(amax > 0.0f)) return 0;
+    int fl = floor_log2_exact(amax);
+    int e = (mode == 0) ? fl - 2 : (significand_le_1p5(amax) ? fl - 2 : fl - 1);
+    return min(127, max(-127, e));
+}
+
+// Encode 32 values at exponent e.  Returns the squared error in scale units (fp32, squares
+// rounded and added in ascending k) and the 32 codes as four words of eight nibbles.
+W4A8_DEVICE float encode_block(const float (&w)[32], int e, uint32_t (&codes)[4])
+{
+    const float inv = exp2i(-e);
+    float S = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) codes[j] = 0;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        float av = fabsf(__fmul_rn(w[k], inv));
+        float a = fminf(av, 6.0f);
+        // e2m1_index: step 0.5 below 2, step 1 below 4, step 2 above; round half to even
+        float f = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
+        float finv = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
+        float off = a < 2.0f ? 0.0f : (a < 4.0f ? 2.0f : 4.0f);
+        float q = rintf(__fmul_rn(a, f));
+        float g = __fmul_rn(q, finv);  // the grid value; exact (powers of two)
+        uint32_t idx = (uint32_t)(q + off);
+        float d = __fsub_rn(av, g);
+        S = __fadd_rn(S, __fmul_rn(d, d));
+        uint32_t c = idx | ((idx != 0u && signbit(w[k])) ? 8u : 0u);
+        codes[k >> 3] |= c << (4 * (k & 7));
+    }
+    return S;
+}
+
+__global__ void __launch_bounds__(RQ_THREADS)
+requant_kernel(const uint8_t *__restrict__ nv_packed, const uint8_t *__restrict__ nv_scale,
+               const float *__restrict__ divisor, Partitions parts, int64_t N, int64_t K,
+               int mode, uint8_t *__restrict__ out_packed, uint8_t *__restrict__ out_e8m0,
+               double *__restrict__ err_ssq)
+{
+    const int64_t KB = K / 32;
+    const int64_t g = (int64_t)blockIdx.x * RQ_THREADS + threadIdx.x;
+    const bool valid = g < N * KB;
+    int p = -1;
+    double err = 0.0, ssq = 0.0;
+    if (valid) {
+        const int64_t n = g / KB, b = g - n * KB;
+        p = 0;
+        while (p < parts.P - 1 && n >= parts.row_end[p]) ++p;
+        const uint4 pk = *reinterpret_cast<const uint4 *>(nv_packed + n * (K / 2) + b * 16);
+        const uint16_t sc = *reinterpret_cast<const uint16_t *>(nv_scale + n * (K / 16) + b * 2);
+        const float dv = divisor[p];
+        const float2 s2 = e4m3x2_to_float2(sc);
+        const float sd0 = __fdiv_rn(s2.x, dv), sd1 = __fdiv_rn(s2.y, dv);
+        // R1: dequantize (one rounded product per element)
+        float w[32];
+        const uint32_t words[4] = {pk.x, pk.y, pk.z, pk.w};
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            float2 gv = e2m1x2_to_float2((words[j >> 2] >> (8 * (j & 3))) & 0xffu);
+            float sd = j < 8 ? sd0 : sd1;
+            w[2 * j] = __fmul_rn(gv.x, sd);
+            w[2 * j + 1] = __fmul_rn(gv.y, sd);
+            amax = fmaxf(amax, fmaxf(fabsf(w[2 * j]), fabsf(w[2 * j + 1])));
+        }
+        // R2 + R3: exponent rule and encode
+        uint32_t codes[4];
+        int e;
+        float S;
+        if (mode == 2) {
+            const int e0 = block_exponent(amax, 1);
+            uint32_t c0[4];
+            const float S0 = encode_block(w, e0, c0);
+            bool take1 = false;
+            uint32_t c1[4] = {0, 0, 0, 0};
+            float S1 = 0.0f;
+            if (e0 > -127) {
+                S1 = encode_block(w, e0 - 1, c1);
+                take1 = S1 < __fmul_rn(4.0f, S0);
+            }
+            e = take1 ? e0 - 1 : e0;
+            S = take1 ? S1 : S0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) codes[j] = take1 ? c1[j] : c0[j];
+        } else {
+            e = block_exponent(amax, mode);
+            S = encode_block(w, e, codes);
+        }
+        // R4: pack (nibble k of word j is element 8j + k: the even k lands in the low nibble)
+        *reinterpret_cast<uint4 *>(out_packed + n * (K / 2) + b * 16) =
+            make_uint4(codes[0], codes[1], codes[2], codes[3]);
+        out_e8m0[n * KB + b] = (uint8_t)(e + 127);
+        if (err_ssq) {
+            err = ldexp((double)S, 2 * e);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) ssq = fma((double)w[k], (double)w[k], ssq);
+        }
+    }
+    if (err_ssq) {
+        const int p0 = __shfl_sync(0xffffffffu, p, 0);
+        if (__all_sync(0xffffffffu, p == p0) && p0 >= 0) {
+            err = warp_sum_d(err);
+            ssq = warp_sum_d(ssq);
+            if ((threadIdx.x & 31) == 0) {
+                atomicAdd(&err_ssq[2 * p0], err);
+                atomicAdd(&err_ssq[2 * p0 + 1], ssq);
+            }
+        } else if (valid) {
+            atomicAdd(&err_ssq[2 * p], err);
+            atomicAdd(&err_ssq[2 * p + 1], ssq);
+        }
+    }
+}
+
+}  // namespace w4a8
+
+extern "C" w4a8_status nvfp4_to_mxfp4_requant(const uint8_t *nv_packed, const uint8_t *nv_scale_e4m3,
+                                              const float *global_divisor,
+                                              const int64_t *partition_rows, int P, int64_t N,
+                                              int64_t K, int mode, uint8_t *out_packed,
+                                              uint8_t *out_e8m0, double *err_ssq,
+                                              cudaStream_t stream)
+{
+    if (N < 0 || K < 0 || mode < 0 || mode > 2) return W4A8_ERR_INVALID_ARG;
+    if (P < 1 || P > w4a8::RQ_MAX_PARTS || !partition_rows) return W4A8_ERR_INVALID_ARG;
+    w4a8::Partitions parts;
+    parts.P = P;
+    int64_t total = 0;
+    for (int p = 0; p < P; ++p) {
+        if (partition_rows[p] < 0) return W4A8_ERR_INVALID_ARG;
+        total += partition_rows[p];
+        parts.row_end[p] = total;
+    }
+    for (int p = P; p < w4a8::RQ_MAX_PARTS; ++p) parts.row_end[p] = total;
+    if (total != N) return W4A8_ERR_INVALID_ARG;
+    if (K % 32 != 0) return W4A8_ERR_UNSUPPORTED_SHAPE;
+    if (N == 0 || K == 0) return W4A8_OK;
+    if (!nv_packed || !nv_scale_e4m3 || !global_divisor || !out_packed || !out_e8m0)
+        return W4A8_ERR_INVALID_ARG;
+    if (!w4a8_aligned(nv_packed, 16) || !w4a8_aligned(out_packed, 16) ||
+        !w4a8_aligned(nv_scale_e4m3, 2) || !w4a8_aligned(global_divisor, 4) ||
+        (err_ssq && !w4a8_aligned(err_ssq, 8)))
+        return W4A8_ERR_MISALIGNED;
+    if (err_ssq && cudaMemsetAsync(err_ssq, 0, sizeof(double) * 2 * P, stream) != cudaSuccess)
+        return W4A8_ERR_CUDA;
+    const int64_t blocks = N * (K / 32);
+    const int64_t grid = (blocks + w4a8::RQ_THREADS - 1) / w4a8::RQ_THREADS;
+    if (grid > 0x7fffffffLL) return W4A8_ERR_UNSUPPORTED_SHAPE;
+    w4a8::requant_kernel<<<(unsigned)grid, w4a8::RQ_THREADS, 0, stream>>>(
+        nv_packed, nv_scale_e4m3, global_divisor, parts, N, K, mode, out_packed, out_e8m0,
+        err_ssq);
+    return w4a8_launch_status();
+}

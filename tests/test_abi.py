@@ -1,0 +1,80 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU, exports every entry point that
+include/w4a8.h declares, and validates arguments on the host (these calls return an error
+before any CUDA call, so they run on a machine without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from int4_quantized_linear_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_entry_points():
+    with open(os.path.join(ROOT, "include", "w4a8.h")) as fh:
+        src = fh.read()
+    return sorted(set(re.findall(r"^W4A8_API\s+[^;(]*?\b(\w+)\s*\(", src, re.M)))
+
+
+@pytest.fixture(scope="module")
+def clib():
+    return binding.load()
+
+
+def test_header_declares_the_four_operations():
+    names = declared_entry_points()
+    for n in ("w4a8_act_quant", "w4a8_mxfp4_linear", "nvfp4_to_mxfp4_requant",
+              "w4a8_int4g128_linear"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(clib):
+    names = declared_entry_points()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(clib, n), n
+    assert set(binding.EXPORTS) <= set(names)
+
+
+def test_status_strings(clib):
+    for code, name in binding.STATUS.items():
+        assert clib.w4a8_status_string(code).decode() == name
+    assert clib.w4a8_decode_max_m() == 64
+
+
+NULL = None
+
+
+def test_host_validation_without_gpu(clib):
+    # errors are returned before anything touches the device
+    assert clib.w4a8_act_quant(NULL, NULL, NULL, -1, 16, NULL) == 1
+    assert clib.w4a8_act_quant(NULL, NULL, NULL, 0, 16, NULL) == 0          # M = 0: no-op
+    assert clib.w4a8_act_quant(NULL, NULL, NULL, 2, 16, NULL) == 1          # null pointers
+    fake = ctypes.c_void_p(0x1000)
+    odd = ctypes.c_void_p(0x1001)
+    assert clib.w4a8_act_quant(fake, fake, fake, 2, 12, NULL) == 2          # K % 8
+    assert clib.w4a8_act_quant(odd, fake, fake, 2, 16, NULL) == 3           # misaligned x
+    assert clib.w4a8_mxfp4_linear(fake, fake, fake, fake, fake, 2, 8, 48, NULL, 0, NULL) == 2
+    assert clib.w4a8_mxfp4_linear(odd, fake, fake, fake, fake, 2, 8, 64, NULL, 0, NULL) == 3
+    assert clib.w4a8_mxfp4_linear(NULL, NULL, NULL, NULL, NULL, 0, 8, 64, NULL, 0, NULL) == 0
+    assert clib.w4a8_int4g128_linear(fake, fake, fake, fake, fake, 2, 8, 64, NULL, 0, NULL) == 2
+    rows = (ctypes.c_int64 * 2)(3, 4)
+    r = ctypes.cast(rows, ctypes.c_void_p)
+    assert clib.nvfp4_to_mxfp4_requant(fake, fake, fake, r, 2, 8, 64, 2, fake, fake, NULL, NULL) == 1
+    assert clib.nvfp4_to_mxfp4_requant(fake, fake, fake, r, 2, 7, 64, 3, fake, fake, NULL, NULL) == 1
+    assert clib.nvfp4_to_mxfp4_requant(fake, fake, fake, r, 2, 7, 48, 2, fake, fake, NULL, NULL) == 2
+    assert clib.nvfp4_to_mxfp4_requant(fake, fake, fake, r, 0, 7, 64, 2, fake, fake, NULL, NULL) == 1
+    assert clib.w4a8_workspace_bytes(0, 8, 64) == 0
+
+
+def test_symmetric_zero_point_check():
+    import torch
+    binding.check_symmetric_qzeros(torch.full((2, 4), 0x77777777, dtype=torch.int32))
+    with pytest.raises(ValueError):
+        binding.check_symmetric_qzeros(torch.full((2, 4), 0x77777778, dtype=torch.int32))
+    binding.check_autoround_config(4, 128, True)
+    for bad in ((8, 128, True), (4, 64, True), (4, 128, False)):
+        with pytest.raises(ValueError):
+            binding.check_autoround_config(*bad)

@@ -1,0 +1,251 @@
+"""GPU parity: every kernel against the oracle, through the C ABI (via the binding).
+
+Bit-exact: act-quant codes and scales, requant codes and e8m0 bytes.  GEMMs: the acceptance
+bound of helpers.gemm_check against the oracle fed the same fp8 codes.  Sizes span several
+tiles with ragged tails; the full workload sizes are checked on sampled outputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import bf16_to_f64, gemm_check, host, to_dev, to_dev_bf16, to_dev_fp16
+from int4_quantized_linear_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+GATE_UP, DOWN, QKV = synth.GATE_UP, synth.DOWN, synth.QKV
+
+
+# ---------------------------------------------------------------------------- act quant
+
+@pytest.mark.parametrize("M,K", [(1, 512), (3, 520), (64, 5120), (5, 17408), (257, 1024)])
+def test_act_quant_bit_exact(lib, orc, M, K):
+    x = synth.activations(M, K, seed=M + K, outliers=True, lognormal_rows=True)
+    xq, xs = lib.act_quant(to_dev_bf16(x))
+    rq, rs = orc.act_quant(x)
+    assert np.array_equal(host(xs), rs)
+    assert np.array_equal(host(xq), rq)
+
+
+def test_act_quant_edge_rows(lib, orc):
+    K = 256
+    x = np.zeros((4, K), np.float32)
+    x[0, 7] = -0.0                       # all-zero row with a signed zero
+    x[1] = 1e-30 * (np.arange(K) - 100)  # tiny magnitudes, negatives that round to -0
+    x[2, :] = 3.0
+    x[2, 5] = -448.0 * 1024              # huge amax
+    x[3] = synth.bf16_bits_to_float(synth.activations(1, K, seed=9))[0]
+    xb = synth.to_bf16_bits(x)
+    xq, xs = lib.act_quant(to_dev_bf16(xb))
+    rq, rs = orc.act_quant(xb)
+    assert np.array_equal(host(xs), rs)
+    assert np.array_equal(host(xq), rq)
+
+
+@pytest.mark.slow
+def test_act_quant_full_prefill(lib, orc):
+    M, K = 4096, 17408
+    x = synth.activations(M, K, seed=1, lognormal_rows=True)
+    xq, xs = lib.act_quant(to_dev_bf16(x))
+    rq, rs = orc.act_quant(x)
+    assert np.array_equal(host(xs), rs)
+    assert np.array_equal(host(xq), rq)
+
+
+def test_act_quant_rejects(lib):
+    x = torch.zeros((2, 12), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(lib.W4A8Error):
+        lib.act_quant(x)
+
+
+# ---------------------------------------------------------------------------- requant
+
+def _nvfp4_case(orc, N, K, parts, seed, gain2=1.0):
+    gain = np.ones(N)
+    gain[parts[0]:] = gain2
+    w = synth.gaussian_weights(N, K, 0.02, seed, row_gain=gain)
+    return orc.nvfp4_quantize(w, parts)
+
+
+@pytest.mark.parametrize("mode", ["ocp", "noclip", "mse"])
+@pytest.mark.parametrize("N,K,parts,gain2", [(96, 512, [40, 56], 0.25), (33, 160, [33], 1.0),
+                                             (300, 2048, [100, 150, 50], 4.0)])
+def test_requant_bit_exact(lib, orc, mode, N, K, parts, gain2):
+    packed, scale, div = _nvfp4_case(orc, N, K, parts, seed=N, gain2=gain2)
+    gp, ge, gs = lib.requant(to_dev(packed), to_dev(scale), to_dev(div), parts, mode)
+    rp, re_, rs = orc.requant(packed, scale, div, parts, mode)
+    assert np.array_equal(host(ge), re_)
+    assert np.array_equal(host(gp), rp)
+    assert np.allclose(host(gs), rs, rtol=1e-9)
+
+
+def test_requant_degenerate_blocks(lib, orc):
+    # all-zero blocks, one-element blocks, subnormal-scale blocks, huge divisor
+    N, K = 8, 128
+    packed = synth.uniform_bytes(N, K // 2, 3, 1)
+    packed[0] = 0
+    packed[1, :16] = 0x08                # -0 codes only
+    scale = synth.uniform_ints(N * K // 16, 0, 0x7e, 3, 2).astype(np.uint8).reshape(N, K // 16)
+    scale[2] = 0x01                      # subnormal e4m3 scales
+    scale[3, :2] = 0
+    div = np.array([1.0e6], np.float32)
+    for mode in ("ocp", "noclip", "mse"):
+        gp, ge, gs = lib.requant(to_dev(packed), to_dev(scale), to_dev(div), [N], mode)
+        rp, re_, rs = orc.requant(packed, scale, div, [N], mode)
+        assert np.array_equal(host(ge), re_)
+        assert np.array_equal(host(gp), rp)
+
+
+@pytest.mark.slow
+def test_requant_full_gate_up(lib, orc):
+    N, K = GATE_UP
+    parts = list(synth.GATE_UP_PARTITIONS)
+    packed, scale, div = _nvfp4_case(orc, N, K, parts, seed=0, gain2=0.25)
+    for mode in ("ocp", "noclip", "mse"):
+        gp, ge, gs = lib.requant(to_dev(packed), to_dev(scale), to_dev(div), parts, mode)
+        rp, re_, rs = orc.requant(packed, scale, div, parts, mode)
+        assert np.array_equal(host(ge), re_), mode
+        assert np.array_equal(host(gp), rp), mode
+        assert np.allclose(host(gs), rs, rtol=1e-6), mode
+        rel_g = orc.rel_rms(host(gs))
+        assert abs(rel_g - orc.rel_rms(rs)) <= 1e-5 * orc.rel_rms(rs)
+
+
+def test_requant_rejects(lib):
+    p = torch.zeros((4, 16), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((4, 2), dtype=torch.uint8, device="cuda")
+    d = torch.ones(2, dtype=torch.float32, device="cuda")
+    with pytest.raises(lib.W4A8Error):
+        lib.requant(p, s, d, [2, 1], "mse")  # rows do not sum to N
+
+
+# ---------------------------------------------------------------------------- GEMMs
+
+POLICIES = [1, 2]  # CUDA-core kernels, tensor-core kernels where the shape allows
+
+
+@pytest.fixture(params=POLICIES, ids=["simt", "tc"])
+def policy(request, lib):
+    lib.set_gemm_policy(request.param)
+    yield request.param
+    lib.set_gemm_policy(0)
+
+
+def _mx_gemm(lib, orc, x, w, e, pairs=None):
+    xq, xs = lib.act_quant(to_dev_bf16(x))
+    out = lib.mxfp4_linear(xq, xs, to_dev(w), to_dev(e))
+    lib.check_device_status()
+    hq, hs = host(xq), host(xs)
+    got = bf16_to_f64(out)
+    if pairs is None:
+        return got, orc.mxfp4_linear(hq, hs, w, e)
+    im, inn = pairs
+    return got[im, inn], orc.mxfp4_linear_pairs(hq, hs, w, e, im, inn)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (4, 256, 512), (7, 384, 640), (33, 200, 256),
+                                   (64, 1024, 1024), (65, 256, 384), (130, 520, 1152),
+                                   (300, 384, 256), (3, 96, 96)])
+def test_mxfp4_linear_small(lib, orc, policy, M, N, K):
+    x, w, e = synth.prefill_case(M, N, K, seed=M * 7 + N)
+    got, ref = _mx_gemm(lib, orc, x, w, e)
+    gemm_check(got, ref, f"mxfp4 M={M} N={N} K={K} policy={policy}")
+
+
+def _sample_pairs(M, N, n_cols=192, seed=0):
+    cols = np.unique(np.concatenate([[0, N - 1, 127, 128, N // 2],
+                                     synth.uniform_ints(n_cols, 0, N - 1, seed, 77)]))
+    im = np.repeat(np.arange(M), cols.size)
+    inn = np.tile(cols, M)
+    return im, inn
+
+
+@pytest.mark.parametrize("shape", [GATE_UP, DOWN], ids=["gate_up", "down"])
+@pytest.mark.parametrize("M", [1, 8, 32, 64])
+def test_mxfp4_decode_full_sampled(lib, orc, shape, M):
+    N, K = shape
+    x, w, e = synth.decode_case(M, N, K, seed=0)
+    got, ref = _mx_gemm(lib, orc, x, w, e, pairs=_sample_pairs(M, N))
+    gemm_check(got, ref, f"decode M={M} N={N} K={K}")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("shape", [GATE_UP, DOWN, QKV], ids=["gate_up", "down", "qkv"])
+@pytest.mark.parametrize("M", [512, 4096])
+def test_mxfp4_prefill_full_sampled(lib, orc, shape, M):
+    N, K = shape
+    x, w, e = synth.prefill_case(M, N, K, seed=0)
+    rows = np.unique(np.concatenate([[0, 127, 128, M - 1], synth.uniform_ints(12, 0, M - 1, 1, 5)]))
+    cols = np.unique(np.concatenate([[0, 255, 256, N - 1], synth.uniform_ints(48, 0, N - 1, 1, 6)]))
+    im = np.repeat(rows, cols.size)
+    inn = np.tile(cols, rows.size)
+    got, ref = _mx_gemm(lib, orc, x, w, e, pairs=(im, inn))
+    gemm_check(got, ref, f"prefill M={M} N={N} K={K}")
+
+
+def test_mxfp4_tiny_config_end_to_end(lib, orc):
+    """M=4, N=256, K=512: W ~ N(0, 0.02) -> NVFP4 -> requant (mse) -> W4A8 GEMM."""
+    M, N, K = 4, 256, 512
+    x = synth.activations(M, K, seed=0, outliers=True)
+    w32 = synth.gaussian_weights(N, K, 0.02, seed=0)
+    packed, scale, div = orc.nvfp4_quantize(w32, [N])
+    gp, ge, _ = lib.requant(to_dev(packed), to_dev(scale), to_dev(div), [N], "mse")
+    rp, re_, _ = orc.requant(packed, scale, div, [N], "mse")
+    assert np.array_equal(host(gp), rp) and np.array_equal(host(ge), re_)
+    xq, xs = lib.act_quant(to_dev_bf16(x))
+    out = lib.mxfp4_linear(xq, xs, gp, ge)
+    gemm_check(bf16_to_f64(out), orc.mxfp4_linear(host(xq), host(xs), rp, re_), "tiny")
+
+
+def test_mxfp4_rejects(lib):
+    xq = torch.zeros((2, 48), dtype=torch.uint8, device="cuda")
+    xs = torch.ones(2, dtype=torch.float32, device="cuda")
+    w = torch.zeros((8, 24), dtype=torch.uint8, device="cuda")
+    e = torch.zeros((8, 1), dtype=torch.uint8, device="cuda")
+    with pytest.raises((lib.W4A8Error, ValueError)):
+        lib.mxfp4_linear(xq, xs, w, e)  # K = 48 is not a multiple of 32
+
+
+def _i4_gemm(lib, orc, x, qw, s16, qz, pairs=None):
+    xq, xs = lib.act_quant(to_dev_bf16(x))
+    out = lib.int4g128_linear(xq, xs, to_dev(qw), to_dev_fp16(s16), qzeros=to_dev(qz))
+    lib.check_device_status()
+    hq, hs = host(xq), host(xs)
+    got = bf16_to_f64(out)
+    if pairs is None:
+        return got, orc.int4g128_linear(hq, hs, qw, s16)
+    im, inn = pairs
+    return got[im, inn], orc.int4g128_linear_pairs(hq, hs, qw, s16, im, inn)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (8, 256, 512), (33, 136, 384), (64, 512, 1024),
+                                   (100, 264, 256), (200, 128, 640)])
+def test_int4_linear_small(lib, orc, policy, M, N, K):
+    x, qw, s16, qz = synth.int4_case(M, N, K, seed=M + N)
+    got, ref = _i4_gemm(lib, orc, x, qw, s16, qz)
+    gemm_check(got, ref, f"int4 M={M} N={N} K={K} policy={policy}")
+
+
+@pytest.mark.parametrize("shape", [GATE_UP, DOWN], ids=["gate_up", "down"])
+@pytest.mark.parametrize("M", [1, 8, 64, 4096])
+def test_int4_full_sampled(lib, orc, shape, M):
+    N, K = shape
+    x, qw, s16, qz = synth.int4_case(M, N, K, seed=0)
+    if M > 64:
+        rows = np.unique(np.concatenate([[0, 127, 128, M - 1], synth.uniform_ints(6, 0, M - 1, 2, 5)]))
+        cols = np.unique(np.concatenate([[0, 255, 256, N - 1], synth.uniform_ints(32, 0, N - 1, 2, 6)]))
+        pairs = (np.repeat(rows, cols.size), np.tile(cols, rows.size))
+    else:
+        pairs = _sample_pairs(M, N, 96)
+    got, ref = _i4_gemm(lib, orc, x, qw, s16, qz, pairs=pairs)
+    gemm_check(got, ref, f"int4 M={M} N={N} K={K}")
+
+
+def test_int4_rejects_asymmetric(lib):
+    xq = torch.zeros((1, 128), dtype=torch.uint8, device="cuda")
+    xs = torch.ones(1, dtype=torch.float32, device="cuda")
+    qw = torch.zeros((16, 8), dtype=torch.int32, device="cuda")
+    s = torch.ones((1, 8), dtype=torch.float16, device="cuda")
+    qz = torch.full((1, 1), 0x77777776, dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):
+        lib.int4g128_linear(xq, xs, qw, s, qzeros=qz)

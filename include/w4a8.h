@@ -141,6 +141,12 @@ W4A8_API void w4a8_set_gemm_policy(int policy);
  * any wait gave up since the last check, W4A8_OK otherwise. */
 W4A8_API w4a8_status w4a8_check_device_status(cudaStream_t stream);
 
+/* Diagnostic: synchronizes the device, copies the raw device status block to out4 (host, 4
+ * words: [0] one bit per kind of bounded wait that ran out -- 1 TMA producer, 2 MMA issuer,
+ * 4 scale staging, 8 epilogue; [1] loop index and [2], [3] raw barrier state of the first such
+ * event) and clears it.  Returns a w4a8_status value. */
+W4A8_API int w4a8_debug_status_words(unsigned int *out4);
+
 /* Decode-band threshold: M <= this takes the decode tiling (64). */
 W4A8_API int w4a8_decode_max_m(void);
 

@@ -23,7 +23,7 @@ MODES = {"ocp": 0, "noclip": 1, "mse": 2}
 EXPORTS = ("w4a8_act_quant", "w4a8_mxfp4_linear", "w4a8_workspace_bytes",
            "nvfp4_to_mxfp4_requant", "w4a8_int4g128_linear", "w4a8_int4g128_workspace_bytes",
            "w4a8_status_string", "w4a8_set_gemm_policy", "w4a8_check_device_status",
-           "w4a8_decode_max_m")
+           "w4a8_decode_max_m", "w4a8_debug_status_words")
 
 
 class W4A8Error(RuntimeError):
@@ -59,6 +59,7 @@ def load(build_if_missing: bool = True):
         "w4a8_set_gemm_policy": (None, [I]),
         "w4a8_check_device_status": (I, [P]),
         "w4a8_decode_max_m": (I, []),
+        "w4a8_debug_status_words": (I, [P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -104,6 +105,13 @@ def decode_max_m() -> int:
 
 def check_device_status(stream=None) -> None:
     _check("w4a8_check_device_status", load().w4a8_check_device_status(_stream(stream)))
+
+
+def debug_status_words():
+    """Raw device status block (see w4a8_debug_status_words); clears it."""
+    buf = (ctypes.c_uint * 4)()
+    _check("w4a8_debug_status_words", load().w4a8_debug_status_words(ctypes.cast(buf, ctypes.c_void_p)))
+    return list(buf)
 
 
 def act_quant(x: torch.Tensor, xq: torch.Tensor | None = None, x_scale: torch.Tensor | None = None,

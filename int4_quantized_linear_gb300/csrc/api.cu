@@ -12,7 +12,7 @@
 static std::atomic<int> g_policy{0};
 
 // Device status word written by bounded waits that give up (0 = clean).
-__device__ unsigned int g_w4a8_device_status = 0;
+__device__ unsigned int g_w4a8_device_status[4] = {0, 0, 0, 0};
 
 unsigned int *w4a8_device_status_ptr()
 {
@@ -53,10 +53,20 @@ extern "C" w4a8_status w4a8_check_device_status(cudaStream_t stream)
     unsigned int v = 0;
     if (cudaMemcpyFromSymbol(&v, g_w4a8_device_status, sizeof(v)) != cudaSuccess) return W4A8_ERR_CUDA;
     if (v) {
-        unsigned int z = 0;
-        if (cudaMemcpyToSymbol(g_w4a8_device_status, &z, sizeof(z)) != cudaSuccess) return W4A8_ERR_CUDA;
+        unsigned int z[4] = {0, 0, 0, 0};
+        if (cudaMemcpyToSymbol(g_w4a8_device_status, z, sizeof(z)) != cudaSuccess) return W4A8_ERR_CUDA;
         return W4A8_ERR_TIMEOUT;
     }
+    return W4A8_OK;
+}
+
+extern "C" int w4a8_debug_status_words(unsigned int *out4)
+{
+    unsigned int z[4] = {0, 0, 0, 0};
+    if (!out4) return W4A8_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return W4A8_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(out4, g_w4a8_device_status, sizeof(z)) != cudaSuccess) return W4A8_ERR_CUDA;
+    if (cudaMemcpyToSymbol(g_w4a8_device_status, z, sizeof(z)) != cudaSuccess) return W4A8_ERR_CUDA;
     return W4A8_OK;
 }
 

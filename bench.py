@@ -247,6 +247,7 @@ def run_ours(args, rank, world, local_rank):
         for c in calls:
             launch(c, stream.cuda_stream)
     stream.synchronize()
+    lib.check_device_status(stream)  # a bounded wait that ran out means the kernels are broken
 
     # ---- step graph, and a second graph with timing events around every GEMM
     graph = torch.cuda.CUDAGraph()

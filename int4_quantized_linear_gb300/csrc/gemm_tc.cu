@@ -22,7 +22,6 @@
 // Every mbarrier wait is bounded; a wait that gives up sets a bit in the library's device
 // status word, the CTA drains what it started and returns.
 #include <cudaTypedefs.h>
-#include <stdlib.h>
 
 #include "common.cuh"
 #include "dispatch.h"
@@ -49,12 +48,14 @@ struct Params {
     int *counters;         // [m_tiles * n_tiles] arrival counters (KS > 1)
     unsigned int *status;  // device status word
     int M, N, K, KS, KT;
-    int w_tx_bytes;        // transaction bytes of one weight tile
 };
 
 template <int BN, int STAGES>
 struct Layout {
     static constexpr int W_BYTES = BM * 128;   // 128 rows x 128 K, 4-bit codes in 16-byte slots
+    // The transaction count of a 16U4_ALIGN16B tile is the packed bytes read from global memory
+    // (64 per row), not its padded shared-memory footprint.
+    static constexpr int W_TX_BYTES = BM * 64;
     static constexpr int X_BYTES = BN * 128;   // BN tokens x 128 K bytes
     static constexpr int SF_BYTES = BM * 16;   // 128 rows x (scale word x 4)
     static constexpr int W_OFF = 0;
@@ -154,7 +155,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                     *abort_flag = 1;
                     break;
                 }
-                tc::mbar_arrive_expect_tx(&full[s], p.w_tx_bytes + L::X_BYTES);
+                tc::mbar_arrive_expect_tx(&full[s], L::W_TX_BYTES + L::X_BYTES);
                 const int k = (kt_begin + i) * BK;
                 tc::tma_load_2d(smem + L::W_OFF + s * L::W_BYTES, &tmap_w, &full[s], k, n0);
                 tc::tma_load_2d(smem + L::X_OFF + s * L::X_BYTES, &tmap_x, &full[s], k, m0);
@@ -470,10 +471,6 @@ w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const 
     prm.K = (int)K;
     prm.KS = c.KS;
     prm.KT = (int)(K / BK);
-    {
-        const char *e = getenv("W4A8_DEBUG_W_TX");
-        prm.w_tx_bytes = e ? atoi(e) : BM * 128;
-    }
     if (c.KS > 1) {
         size_t part = (size_t)c.KS * (size_t)M * (size_t)N * 4;
         part = (part + 255) / 256 * 256;

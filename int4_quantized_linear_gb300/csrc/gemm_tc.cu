@@ -61,7 +61,10 @@ struct Layout {
     static constexpr int W_OFF = 0;
     static constexpr int X_OFF = W_OFF + STAGES * W_BYTES;
     static constexpr int SF_OFF = X_OFF + STAGES * X_BYTES;
-    static constexpr int BAR_OFF = SF_OFF + STAGES * SF_BYTES;
+    static constexpr int SFR_SLOTS = 2;        // raw scale tiles (128 rows x 16 bytes = 4 k-tiles)
+    static constexpr int SFR_BYTES = BM * 16;
+    static constexpr int SFR_OFF = SF_OFF + STAGES * SF_BYTES;
+    static constexpr int BAR_OFF = SFR_OFF + SFR_SLOTS * SFR_BYTES;
     static constexpr int TOTAL = BAR_OFF + 256 + 1024;  // barriers, flags, alignment slack
     static constexpr int TMEM_NEED = BN + 8 + 4 * STAGES;
     static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64
@@ -83,10 +86,13 @@ __device__ __forceinline__ void fail(unsigned int *status, unsigned int bit, uin
     }
 }
 
-template <int BN, int STAGES>
+// SF_TMA: the weight scales of 4 consecutive k-tiles arrive as one [128 rows x 16 bytes] TMA
+// tile (needs K a multiple of 512 so the scale rows are 16-byte strided, and split boundaries
+// on multiples of 4 k-tiles); otherwise the staging warp reads them with plain loads.
+template <int BN, int STAGES, bool SF_TMA>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
-                const Params p)
+                const __grid_constant__ CUtensorMap tmap_sf, const Params p)
 {
     using L = Layout<BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
@@ -94,16 +100,22 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);
     uint64_t *empty = full + STAGES;
     uint64_t *accf = empty + STAGES;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accf + 1);
+    uint64_t *sfr_full = accf + 1;
+    uint64_t *sfr_empty = sfr_full + L::SFR_SLOTS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sfr_empty + L::SFR_SLOTS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *last_flag = reinterpret_cast<int *>(tmem_slot + 2);
     int *consumed = reinterpret_cast<int *>(tmem_slot + 3);
     int *issued = reinterpret_cast<int *>(tmem_slot + 4);
+    int *sfr_issued = reinterpret_cast<int *>(tmem_slot + 5);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN, split = blockIdx.z;
-    const int kt_begin = (int)((long long)split * p.KT / p.KS);
-    const int kt_end = (int)((long long)(split + 1) * p.KT / p.KS);
+    // split boundaries: whole groups of 4 k-tiles when the scales come by TMA
+    const int unit = SF_TMA ? 4 : 1;
+    const int n_units = p.KT / unit;
+    const int kt_begin = unit * (int)((long long)split * n_units / p.KS);
+    const int kt_end = unit * (int)((long long)(split + 1) * n_units / p.KS);
     const int nkt = kt_end - kt_begin;
 
     if (threadIdx.x == 0) {
@@ -112,13 +124,19 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             tc::mbar_init(&empty[s], 1);  // tcgen05.commit of the stage's MMAs
         }
         tc::mbar_init(accf, 1);
+        for (int r = 0; r < L::SFR_SLOTS; ++r) {
+            tc::mbar_init(&sfr_full[r], 1);
+            tc::mbar_init(&sfr_empty[r], 1);
+        }
         *abort_flag = 0;
         *last_flag = 0;
         *consumed = 0;
         *issued = 0;
+        *sfr_issued = 0;
         tc::fence_mbar_init();
         tc::tma_prefetch_desc(&tmap_w);
         tc::tma_prefetch_desc(&tmap_x);
+        if (SF_TMA) tc::tma_prefetch_desc(&tmap_sf);
     }
     if (warp == 1) {
         tc::tmem_alloc(tmem_slot, L::TMEM_COLS);
@@ -149,6 +167,19 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             for (int i = 0; i < nkt; ++i) {
                 const int s = i % STAGES;
                 const uint32_t ph = (i / STAGES) & 1;
+                if (SF_TMA && (i & 3) == 0) {
+                    const int g = i >> 2, rs = g % L::SFR_SLOTS;
+                    const int w = tc::mbar_wait(&sfr_empty[rs], ((g / L::SFR_SLOTS) & 1) ^ 1, abort_flag, WAIT_BUDGET);
+                    if (w) {
+                        if (w == 1) fail(p.status, ST_TIMEOUT_PRODUCER, &sfr_empty[rs], i);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    tc::mbar_arrive_expect_tx(&sfr_full[rs], L::SFR_BYTES);
+                    tc::tma_load_2d(smem + L::SFR_OFF + rs * L::SFR_BYTES, &tmap_sf, &sfr_full[rs],
+                                    4 * (kt_begin + i), n0);
+                    *sfr_issued = g + 1;
+                }
                 const int w = tc::mbar_wait(&empty[s], ph ^ 1, abort_flag, WAIT_BUDGET);
                 if (w) {
                     if (w == 1) fail(p.status, ST_TIMEOUT_PRODUCER, &empty[s], i);
@@ -196,48 +227,94 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------------------------------ scale staging
-        const int kb_row = p.K / 32;
-        uint32_t ring[SF_PREFETCH][4];
-        auto load = [&](int kt, uint32_t(&w)[4]) {
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int n = n0 + lane + 32 * r;
-                w[r] = n < p.N ? __ldg(reinterpret_cast<const uint32_t *>(p.we + (size_t)n * kb_row + 4 * kt))
-                               : 0x7f7f7f7fu;
-            }
-        };
-#pragma unroll
-        for (int j = 0; j < SF_PREFETCH; ++j)
-            if (j < nkt) load(kt_begin + j, ring[j]);
-        bool ok = true;
-        for (int base = 0; base < nkt && ok; base += SF_PREFETCH) {
-#pragma unroll
-            for (int j = 0; j < SF_PREFETCH; ++j) {
-                const int i = base + j;
-                if (i >= nkt) break;
-                const int s = i % STAGES;
-                const uint32_t ph = (i / STAGES) & 1;
+        if constexpr (SF_TMA) {
+            bool ok = true;
+            for (int g = 0; 4 * g < nkt && ok; ++g) {
+                const int rs = g % L::SFR_SLOTS;
                 int w = 0;
-                if (lane == 0) w = tc::mbar_wait(&empty[s], ph ^ 1, abort_flag, WAIT_BUDGET);
+                if (lane == 0) w = tc::mbar_wait(&sfr_full[rs], (g / L::SFR_SLOTS) & 1, abort_flag, WAIT_BUDGET);
                 w = __shfl_sync(0xffffffffu, w, 0);
                 if (w) {
                     if (lane == 0) {
-                        if (w == 1) fail(p.status, ST_TIMEOUT_SF, &empty[s], i);
+                        if (w == 1) fail(p.status, ST_TIMEOUT_SF, &sfr_full[rs], g);
                         *abort_flag = 1;
                     }
-                    ok = false;
                     break;
                 }
-                uint8_t *dst = smem + L::SF_OFF + s * L::SF_BYTES;
+                const uint8_t *raw = smem + L::SFR_OFF + rs * L::SFR_BYTES;
+                for (int t = 0; t < 4; ++t) {
+                    const int i = 4 * g + t;
+                    if (i >= nkt) break;
+                    const int s = i % STAGES;
+                    w = 0;
+                    if (lane == 0) w = tc::mbar_wait(&empty[s], ((i / STAGES) & 1) ^ 1, abort_flag, WAIT_BUDGET);
+                    w = __shfl_sync(0xffffffffu, w, 0);
+                    if (w) {
+                        if (lane == 0) {
+                            if (w == 1) fail(p.status, ST_TIMEOUT_SF, &empty[s], i);
+                            *abort_flag = 1;
+                        }
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *dst = smem + L::SF_OFF + s * L::SF_BYTES;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int row = lane + 32 * r;
+                        const uint32_t v = *reinterpret_cast<const uint32_t *>(raw + row * 16 + 4 * t);
+                        *reinterpret_cast<uint4 *>(dst + row * 16) = make_uint4(v, v, v, v);
+                    }
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&full[s]);
+                }
+                __syncwarp();
+                if (lane == 0 && ok) tc::mbar_arrive(&sfr_empty[rs]);
+            }
+        } else {
+            const int kb_row = p.K / 32;
+            uint32_t ring[SF_PREFETCH][4];
+            auto load = [&](int kt, uint32_t(&w)[4]) {
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
-                    const uint32_t w = ring[j][r];
-                    *reinterpret_cast<uint4 *>(dst + (lane + 32 * r) * 16) = make_uint4(w, w, w, w);
+                    const int n = n0 + lane + 32 * r;
+                    w[r] = n < p.N ? __ldg(reinterpret_cast<const uint32_t *>(p.we + (size_t)n * kb_row + 4 * kt))
+                                   : 0x7f7f7f7fu;
                 }
-                tc::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&full[s]);
-                if (i + SF_PREFETCH < nkt) load(kt_begin + i + SF_PREFETCH, ring[j]);
+            };
+#pragma unroll
+            for (int j = 0; j < SF_PREFETCH; ++j)
+                if (j < nkt) load(kt_begin + j, ring[j]);
+            bool ok = true;
+            for (int base = 0; base < nkt && ok; base += SF_PREFETCH) {
+#pragma unroll
+                for (int j = 0; j < SF_PREFETCH; ++j) {
+                    const int i = base + j;
+                    if (i >= nkt) break;
+                    const int s = i % STAGES;
+                    const uint32_t ph = (i / STAGES) & 1;
+                    int w = 0;
+                    if (lane == 0) w = tc::mbar_wait(&empty[s], ph ^ 1, abort_flag, WAIT_BUDGET);
+                    w = __shfl_sync(0xffffffffu, w, 0);
+                    if (w) {
+                        if (lane == 0) {
+                            if (w == 1) fail(p.status, ST_TIMEOUT_SF, &empty[s], i);
+                            *abort_flag = 1;
+                        }
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *dst = smem + L::SF_OFF + s * L::SF_BYTES;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const uint32_t w = ring[j][r];
+                        *reinterpret_cast<uint4 *>(dst + (lane + 32 * r) * 16) = make_uint4(w, w, w, w);
+                    }
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&full[s]);
+                    if (i + SF_PREFETCH < nkt) load(kt_begin + i + SF_PREFETCH, ring[j]);
+                }
             }
         }
     } else {
@@ -303,6 +380,8 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         int zero = 0;
         for (int i = *consumed; i < *issued; ++i)
             if (tc::mbar_wait(&full[i % STAGES], (i / STAGES) & 1, &zero, DRAIN_BUDGET)) break;
+        for (int g = max(0, *sfr_issued - L::SFR_SLOTS); g < *sfr_issued; ++g)
+            tc::mbar_wait(&sfr_full[g % L::SFR_SLOTS], (g / L::SFR_SLOTS) & 1, &zero, DRAIN_BUDGET);
         tc::mbar_wait(accf, 0, &zero, WAIT_BUDGET);
     }
     __syncthreads();
@@ -341,7 +420,8 @@ bool tmap_w_fp4(CUtensorMap *m, const void *w, int64_t N, int64_t K)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool tmap_bytes(CUtensorMap *m, const void *x, int64_t rows, int64_t cols, int box_rows, int box_cols)
+bool tmap_bytes(CUtensorMap *m, const void *x, int64_t rows, int64_t cols, int box_rows, int box_cols,
+                CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B)
 {
     auto enc = encode_fn();
     if (!enc) return false;
@@ -350,7 +430,7 @@ bool tmap_bytes(CUtensorMap *m, const void *x, int64_t rows, int64_t cols, int b
     cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     cuuint32_t es[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(x), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -370,6 +450,7 @@ int num_sms()
 
 struct Cfg {
     int BN, KS, m_tiles, n_tiles;
+    bool sf_tma;
 };
 
 Cfg choose(int64_t M, int64_t N, int64_t K)
@@ -379,6 +460,8 @@ Cfg choose(int64_t M, int64_t N, int64_t K)
     c.n_tiles = (int)((N + BM - 1) / BM);
     c.m_tiles = (int)((M + c.BN - 1) / c.BN);
     const int KT = (int)(K / BK);
+    c.sf_tma = (K % 512) == 0;
+    const int units = c.sf_tma ? KT / 4 : KT;  // split granularity
     const long long tiles = (long long)c.n_tiles * c.m_tiles;
     const int sms = num_sms();
     c.KS = 1;
@@ -387,7 +470,7 @@ Cfg choose(int64_t M, int64_t N, int64_t K)
         // their bytes (written and read back, mostly in L2) against the weight bytes
         double best = -1e30;
         const double wbytes = (double)N * K * 17.0 / 32.0;
-        for (int ks = 1; ks <= KT && ks <= 32; ++ks) {
+        for (int ks = 1; ks <= units && ks <= 32; ++ks) {
             const long long ctas = tiles * ks;
             const long long waves = (ctas + sms - 1) / sms;
             const double eff = (double)ctas / (double)(waves * sms);
@@ -410,14 +493,19 @@ size_t workspace_for(const Cfg &c, int64_t M, int64_t N)
     return part + (size_t)c.m_tiles * c.n_tiles * 4;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool SF_TMA>
 w4a8_status launch(const CUtensorMap &tw, const uint8_t *xq, const Params &prm, const Cfg &c,
                    cudaStream_t stream)
 {
     using L = Layout<BN, STAGES>;
-    CUtensorMap tx;
+    CUtensorMap tx, tsf;
     if (!tmap_bytes(&tx, xq, prm.M, prm.K, BN, 128)) return W4A8_ERR_CUDA;
-    auto kern = mxfp4_tc_kernel<BN, STAGES>;
+    if (SF_TMA) {
+        if (!tmap_bytes(&tsf, prm.we, prm.N, prm.K / 32, BM, 16, CU_TENSOR_MAP_SWIZZLE_NONE)) return W4A8_ERR_CUDA;
+    } else {
+        tsf = tx;  // unused
+    }
+    auto kern = mxfp4_tc_kernel<BN, STAGES, SF_TMA>;
     static int attr_done[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -427,7 +515,7 @@ w4a8_status launch(const CUtensorMap &tw, const uint8_t *xq, const Params &prm, 
         attr_done[dev] = 1;
     }
     dim3 grid(c.n_tiles, c.m_tiles, c.KS);
-    kern<<<grid, NUM_THREADS, L::TOTAL, stream>>>(tw, tx, prm);
+    kern<<<grid, NUM_THREADS, L::TOTAL, stream>>>(tw, tx, tsf, prm);
     return w4a8_launch_status();
 }
 
@@ -479,12 +567,21 @@ w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const 
     }
     CUtensorMap tw;
     if (!tmap_w_fp4(&tw, wp, N, K)) return W4A8_ERR_CUDA;
+    if (c.sf_tma && w4a8_aligned(we, 16)) {
+        switch (c.BN) {
+        case 16: return launch<16, 10, true>(tw, xq, prm, c, stream);
+        case 32: return launch<32, 9, true>(tw, xq, prm, c, stream);
+        case 64: return launch<64, 8, true>(tw, xq, prm, c, stream);
+        case 128: return launch<128, 6, true>(tw, xq, prm, c, stream);
+        default: return launch<256, 4, true>(tw, xq, prm, c, stream);
+        }
+    }
     switch (c.BN) {
-    case 16: return launch<16, 10>(tw, xq, prm, c, stream);
-    case 32: return launch<32, 9>(tw, xq, prm, c, stream);
-    case 64: return launch<64, 8>(tw, xq, prm, c, stream);
-    case 128: return launch<128, 6>(tw, xq, prm, c, stream);
-    default: return launch<256, 4>(tw, xq, prm, c, stream);
+    case 16: return launch<16, 10, false>(tw, xq, prm, c, stream);
+    case 32: return launch<32, 9, false>(tw, xq, prm, c, stream);
+    case 64: return launch<64, 8, false>(tw, xq, prm, c, stream);
+    case 128: return launch<128, 6, false>(tw, xq, prm, c, stream);
+    default: return launch<256, 4, false>(tw, xq, prm, c, stream);
     }
 }
 

@@ -1,42 +1,46 @@
-// gemm_tc.cu -- tensor-core (tcgen05, sm_103a) MXFP4 W4A8 GEMM.
+// gemm_tc.cu -- tensor-core (tcgen05, sm_103a) MXFP4 W4A8 GEMM, persistent stream-K.
 //
 // "vllm-radiance (MXFP4)", "The W4A8 fp8-WMMA kernel": fp8 (e4m3) activations times e2m1
-// weights with the e8m0 block scale folded into the matrix instruction, a prefill tiling and
-// a decode tiling whose split-K partials are reduced by the last CTA to arrive (no second
-// launch).  The pages' kernel is an RDNA4 WMMA design; this one is built for Blackwell:
+// weights with the e8m0 block scale folded into the matrix instruction; a prefill tiling and a
+// decode tiling; the decode K-splits are reduced in place by the last CTA to arrive, with no
+// second launch and a result independent of arrival order.  The pages' kernel is an RDNA4 WMMA
+// design; this one is built for Blackwell:
 //
-//   * swap-AB: the weights are the MMA "M" operand (128 weight rows per tile) and the tokens
-//     the "N" operand (16..256), so a decode batch of 1-64 tokens still fills the instruction;
-//   * tcgen05.mma kind::mxf8f6f4 with block_scale.scale_vec::1X: A = e2m1 weights with their
-//     ue8m0 scale per 32 along K, B = e4m3 activations with a unit scale (0x7F), fp32
-//     accumulator in tensor memory; the per-token scale is applied in the epilogue;
-//   * weights reach shared memory through TMA in the 16U4_ALIGN16B form (each 16 packed e2m1
-//     codes land in a 16-byte slot, the layout the f8f6f4 instruction reads for 4-bit
-//     operands), activations through TMA as bytes, both with the 128-byte swizzle;
-//   * the weight scales of each stage are staged by a helper warp into a 128 x 16-byte block
-//     (row r holds its 4-byte scale word four times) and copied to tensor memory with
-//     tcgen05.cp, so lane r of every scale column holds row r's word;
-//   * warp roles: warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer, warp 2 scale
-//     staging, warps 3-6 epilogue (each reads the TMEM lane quarter its warp index selects).
+//   * swap-AB: the weights are the MMA "M" operand (128 weight rows per tile) and the tokens the
+//     "N" operand (16..256), so a decode batch of 1-64 tokens still fills the instruction;
+//   * tcgen05.mma kind::mxf8f6f4 block_scale.scale_vec::1X: A = e2m1 weights with their ue8m0
+//     scale per 32 along K, B = e4m3 activations with a unit scale (0x7F), fp32 accumulators in
+//     tensor memory; the per-token scale multiplies in the epilogue;
+//   * TMA brings the weights in the 16U4_ALIGN16B form (16 packed e2m1 codes per 16-byte slot,
+//     the shared-memory form the instruction reads for 4-bit operands) and the activations as
+//     bytes, both with the 128-byte swizzle; the weight scales arrive as one [128 x 16-byte] TMA
+//     tile per 4 k-tiles and a helper warp widens each row's 4-byte word into a 16-byte row, which
+//     tcgen05.cp copies to tensor memory (lane r of each scale column holds row r's word);
+//   * persistent stream-K: one CTA per SM walks a contiguous range of (tile, 4-k-tile unit)
+//     work, so the TMA ring never drains between tiles and every SM gets the same number of
+//     units; a tile whose K range is split between CTAs is finished by the last contributor,
+//     which adds the fp32 partials in CTA order;
+//   * two accumulator buffers in tensor memory (one for 256-token tiles) let the MMAs of the next
+//     tile run while the epilogue drains the previous one;
+//   * warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2 scale staging, 3-6 epilogue
+//     (each reads the TMEM lane quarter its warp index selects).
 //
-// Every mbarrier wait is bounded; a wait that gives up sets a bit in the library's device
-// status word, the CTA drains what it started and returns.
-#include <cudaTypedefs.h>
-
+// Every mbarrier wait is bounded; a wait that runs out sets a bit in the library's device status
+// word and the CTA winds down (draining what it started) instead of hanging.
 #include "common.cuh"
 #include "dispatch.h"
+#include "tc_host.cuh"
 #include "tc_ptx.cuh"
 
 namespace w4a8 {
 namespace tcg {
 
 constexpr int BM = 128;            // weight rows per tile (MMA M)
-constexpr int BK = 128;            // K elements per pipeline stage
+constexpr int BK = 128;            // K elements per pipeline stage (one k-tile)
 constexpr int NUM_THREADS = 224;   // 7 warps
 constexpr int EPI_WARP0 = 3;
 constexpr long long WAIT_BUDGET = 1ll << 29;  // clock cycles (a quarter second or so)
 constexpr long long DRAIN_BUDGET = 1ll << 24;
-constexpr int SF_PREFETCH = 8;     // k-tiles of scale words kept in flight by the staging warp
 
 enum : unsigned { ST_TIMEOUT_PRODUCER = 1, ST_TIMEOUT_MMA = 2, ST_TIMEOUT_SF = 4, ST_TIMEOUT_EPI = 8 };
 
@@ -44,29 +48,33 @@ struct Params {
     const uint8_t *we;     // [N, K/32] e8m0
     const float *xs;       // [M] per-token scale
     uint16_t *out;         // [M, N] bf16
-    float *partials;       // [KS, M, N] fp32 split-K partials (KS > 1)
-    int *counters;         // [m_tiles * n_tiles] arrival counters (KS > 1)
-    unsigned int *status;  // device status word
-    int M, N, K, KS, KT;
+    float *partials;       // [G][2][BN][128] fp32 stream-K partial tiles
+    int *counters;         // [tiles] arrival counters, zero between calls
+    unsigned int *status;  // device status block
+    int M, N, K;
+    int m_tiles, n_tiles;
+    int U;                 // 4-k-tile units per tile
+    long long TU;          // total units
+    int G;                 // CTAs
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int ACC_BUFS>
 struct Layout {
-    static constexpr int W_BYTES = BM * 128;   // 128 rows x 128 K, 4-bit codes in 16-byte slots
-    // The transaction count of a 16U4_ALIGN16B tile is the packed bytes read from global memory
-    // (64 per row), not its padded shared-memory footprint.
-    static constexpr int W_TX_BYTES = BM * 64;
-    static constexpr int X_BYTES = BN * 128;   // BN tokens x 128 K bytes
-    static constexpr int SF_BYTES = BM * 16;   // 128 rows x (scale word x 4)
+    static constexpr int W_BYTES = BM * 128;    // 128 rows x 128 K, 4-bit codes in 16-byte slots
+    static constexpr int W_TX_BYTES = BM * 64;  // a 16U4_ALIGN16B tile counts its packed bytes
+    static constexpr int X_BYTES = BN * 128;    // BN tokens x 128 K bytes
+    static constexpr int SF_BYTES = BM * 16;    // 128 rows x (scale word x 4)
+    static constexpr int SFR_SLOTS = 2;         // raw scale tiles, 128 rows x 16 bytes = 4 k-tiles
+    static constexpr int SFR_BYTES = BM * 16;
     static constexpr int W_OFF = 0;
     static constexpr int X_OFF = W_OFF + STAGES * W_BYTES;
     static constexpr int SF_OFF = X_OFF + STAGES * X_BYTES;
-    static constexpr int SFR_SLOTS = 2;        // raw scale tiles (128 rows x 16 bytes = 4 k-tiles)
-    static constexpr int SFR_BYTES = BM * 16;
     static constexpr int SFR_OFF = SF_OFF + STAGES * SF_BYTES;
     static constexpr int BAR_OFF = SFR_OFF + SFR_SLOTS * SFR_BYTES;
-    static constexpr int TOTAL = BAR_OFF + 256 + 1024;  // barriers, flags, alignment slack
-    static constexpr int TMEM_NEED = BN + 8 + 4 * STAGES;
+    static constexpr int TOTAL = BAR_OFF + 512 + 1024;  // barriers, flags, alignment slack
+    static constexpr int T_SFB = ACC_BUFS * BN;         // TMEM column of the unit B scales
+    static constexpr int T_SFA = T_SFB + 8;             // TMEM columns of the A scales, 4 per stage
+    static constexpr int TMEM_NEED = T_SFA + 4 * STAGES;
     static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64
                                      : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
     static_assert(TMEM_NEED <= 512, "tensor memory");
@@ -74,7 +82,7 @@ struct Layout {
 };
 
 // Record a bounded wait that ran out: the role's bit in word 0 of the status block; the first
-// such event also leaves the barrier's raw state (words 2-3) and the loop index (word 1).
+// such event also leaves its loop index (word 1) and the barrier's raw state (words 2-3).
 __device__ __forceinline__ void fail(unsigned int *status, unsigned int bit, uint64_t *bar, int iter)
 {
     const unsigned int prev = atomicOr(status, bit);
@@ -86,23 +94,26 @@ __device__ __forceinline__ void fail(unsigned int *status, unsigned int bit, uin
     }
 }
 
-// SF_TMA: the weight scales of 4 consecutive k-tiles arrive as one [128 rows x 16 bytes] TMA
-// tile (needs K a multiple of 512 so the scale rows are 16-byte strided, and split boundaries
-// on multiples of 4 k-tiles); otherwise the staging warp reads them with plain loads.
-template <int BN, int STAGES, bool SF_TMA>
+// First unit of CTA c, and the CTA that owns unit u, for the even split of TU units over G CTAs.
+__device__ __forceinline__ long long unit_start(long long c, long long TU, int G) { return c * TU / G; }
+__device__ __forceinline__ int unit_owner(long long u, long long TU, int G) { return (int)(((u + 1) * G - 1) / TU); }
+
+template <int BN, int STAGES, int ACC_BUFS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_sf, const Params p)
 {
-    using L = Layout<BN, STAGES>;
+    using L = Layout<BN, STAGES, ACC_BUFS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);
     uint64_t *empty = full + STAGES;
-    uint64_t *accf = empty + STAGES;
-    uint64_t *sfr_full = accf + 1;
+    uint64_t *sfr_full = empty + STAGES;
     uint64_t *sfr_empty = sfr_full + L::SFR_SLOTS;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sfr_empty + L::SFR_SLOTS);
+    uint64_t *acc_full = sfr_empty + L::SFR_SLOTS;
+    uint64_t *acc_empty = acc_full + ACC_BUFS;
+    uint64_t *mma_done = acc_empty + ACC_BUFS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *last_flag = reinterpret_cast<int *>(tmem_slot + 2);
     int *consumed = reinterpret_cast<int *>(tmem_slot + 3);
@@ -110,24 +121,24 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     int *sfr_issued = reinterpret_cast<int *>(tmem_slot + 5);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN, split = blockIdx.z;
-    // split boundaries: whole groups of 4 k-tiles when the scales come by TMA
-    const int unit = SF_TMA ? 4 : 1;
-    const int n_units = p.KT / unit;
-    const int kt_begin = unit * (int)((long long)split * n_units / p.KS);
-    const int kt_end = unit * (int)((long long)(split + 1) * n_units / p.KS);
-    const int nkt = kt_end - kt_begin;
+    const int cta = blockIdx.x;
+    const long long u_begin = unit_start(cta, p.TU, p.G);
+    const long long u_end = unit_start(cta + 1, p.TU, p.G);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             tc::mbar_init(&full[s], 2);   // producer expect_tx + scale-staging warp
             tc::mbar_init(&empty[s], 1);  // tcgen05.commit of the stage's MMAs
         }
-        tc::mbar_init(accf, 1);
         for (int r = 0; r < L::SFR_SLOTS; ++r) {
             tc::mbar_init(&sfr_full[r], 1);
             tc::mbar_init(&sfr_empty[r], 1);
         }
+        for (int b = 0; b < ACC_BUFS; ++b) {
+            tc::mbar_init(&acc_full[b], 1);   // tcgen05.commit after a tile's last MMA
+            tc::mbar_init(&acc_empty[b], 1);  // epilogue finished reading the buffer
+        }
+        tc::mbar_init(mma_done, 1);
         *abort_flag = 0;
         *last_flag = 0;
         *consumed = 0;
@@ -136,7 +147,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         tc::fence_mbar_init();
         tc::tma_prefetch_desc(&tmap_w);
         tc::tma_prefetch_desc(&tmap_x);
-        if (SF_TMA) tc::tma_prefetch_desc(&tmap_sf);
+        tc::tma_prefetch_desc(&tmap_sf);
     }
     if (warp == 1) {
         tc::tmem_alloc(tmem_slot, L::TMEM_COLS);
@@ -146,14 +157,10 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t t_acc = tmem;
-    const uint32_t t_sfb = tmem + BN;
-    const uint32_t t_sfa = tmem + BN + 8;
 
     // Unit scale (2^0) for the activation operand: 0x7F in every byte of the B-scale columns.
     if (warp >= EPI_WARP0) {
-        const uint32_t q = warp & 3;
-        const uint32_t base = t_sfb + ((32u * q) << 16);
+        const uint32_t base = tmem + L::T_SFB + ((32u * (warp & 3)) << 16);
         tc::tmem_st4(base, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
         tc::tmem_st4(base + 4, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
         tc::tmem_st_wait();
@@ -164,33 +171,34 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            for (int i = 0; i < nkt; ++i) {
-                const int s = i % STAGES;
-                const uint32_t ph = (i / STAGES) & 1;
-                if (SF_TMA && (i & 3) == 0) {
-                    const int g = i >> 2, rs = g % L::SFR_SLOTS;
-                    const int w = tc::mbar_wait(&sfr_empty[rs], ((g / L::SFR_SLOTS) & 1) ^ 1, abort_flag, WAIT_BUDGET);
-                    if (w) {
-                        if (w == 1) fail(p.status, ST_TIMEOUT_PRODUCER, &sfr_empty[rs], i);
-                        *abort_flag = 1;
-                        break;
-                    }
-                    tc::mbar_arrive_expect_tx(&sfr_full[rs], L::SFR_BYTES);
-                    tc::tma_load_2d(smem + L::SFR_OFF + rs * L::SFR_BYTES, &tmap_sf, &sfr_full[rs],
-                                    4 * (kt_begin + i), n0);
-                    *sfr_issued = g + 1;
-                }
-                const int w = tc::mbar_wait(&empty[s], ph ^ 1, abort_flag, WAIT_BUDGET);
+            int i = 0, g = 0;
+            for (long long u = u_begin; u < u_end && !*abort_flag; ++u, ++g) {
+                const int t = (int)(u / p.U), ku = (int)(u - (long long)t * p.U);
+                const int n0 = (t / p.m_tiles) * BM, m0 = (t % p.m_tiles) * BN;
+                const int rs = g % L::SFR_SLOTS;
+                int w = tc::mbar_wait(&sfr_empty[rs], ((g / L::SFR_SLOTS) & 1) ^ 1, abort_flag, WAIT_BUDGET);
                 if (w) {
-                    if (w == 1) fail(p.status, ST_TIMEOUT_PRODUCER, &empty[s], i);
+                    if (w == 1) fail(p.status, ST_TIMEOUT_PRODUCER, &sfr_empty[rs], g);
                     *abort_flag = 1;
                     break;
                 }
-                tc::mbar_arrive_expect_tx(&full[s], L::W_TX_BYTES + L::X_BYTES);
-                const int k = (kt_begin + i) * BK;
-                tc::tma_load_2d(smem + L::W_OFF + s * L::W_BYTES, &tmap_w, &full[s], k, n0);
-                tc::tma_load_2d(smem + L::X_OFF + s * L::X_BYTES, &tmap_x, &full[s], k, m0);
-                *issued = i + 1;
+                tc::mbar_arrive_expect_tx(&sfr_full[rs], L::SFR_BYTES);
+                tc::tma_load_2d(smem + L::SFR_OFF + rs * L::SFR_BYTES, &tmap_sf, &sfr_full[rs], 16 * ku, n0);
+                *sfr_issued = g + 1;
+                for (int j = 0; j < 4; ++j, ++i) {
+                    const int s = i % STAGES;
+                    w = tc::mbar_wait(&empty[s], ((i / STAGES) & 1) ^ 1, abort_flag, WAIT_BUDGET);
+                    if (w) {
+                        if (w == 1) fail(p.status, ST_TIMEOUT_PRODUCER, &empty[s], i);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    tc::mbar_arrive_expect_tx(&full[s], L::W_TX_BYTES + L::X_BYTES);
+                    const int k = (4 * ku + j) * BK;
+                    tc::tma_load_2d(smem + L::W_OFF + s * L::W_BYTES, &tmap_w, &full[s], k, n0);
+                    tc::tma_load_2d(smem + L::X_OFF + s * L::X_BYTES, &tmap_x, &full[s], k, m0);
+                    *issued = i + 1;
+                }
             }
         }
         __syncwarp();
@@ -198,159 +206,153 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             tc::tc_fence_after();
-            for (int i = 0; i < nkt; ++i) {
-                const int s = i % STAGES;
-                const uint32_t ph = (i / STAGES) & 1;
-                const int w = tc::mbar_wait(&full[s], ph, abort_flag, WAIT_BUDGET);
+            int i = 0, seg = 0;
+            long long u = u_begin;
+            while (u < u_end && !*abort_flag) {
+                const int t = (int)(u / p.U);
+                const long long ue = min(u_end, (long long)(t + 1) * p.U);
+                const int b = seg % ACC_BUFS;
+                int w = tc::mbar_wait(&acc_empty[b], ((seg / ACC_BUFS) & 1) ^ 1, abort_flag, WAIT_BUDGET);
                 if (w) {
-                    if (w == 1) fail(p.status, ST_TIMEOUT_MMA, &full[s], i);
+                    if (w == 1) fail(p.status, ST_TIMEOUT_MMA, &acc_empty[b], seg);
                     *abort_flag = 1;
                     break;
                 }
-                *consumed = i + 1;
                 tc::tc_fence_after();
-                const uint32_t sfa = t_sfa + 4 * s;
-                tc::tc_cp_128x128b(sfa, tc::smem_desc(tc::smem_u32(smem + L::SF_OFF + s * L::SF_BYTES), 128, 128, 0));
-                const uint32_t wa = tc::smem_u32(smem + L::W_OFF + s * L::W_BYTES);
-                const uint32_t xa = tc::smem_u32(smem + L::X_OFF + s * L::X_BYTES);
+                const uint32_t t_acc = tmem + b * BN;
+                bool first = true;
+                for (long long k4 = 4 * (ue - u); k4 > 0; --k4, ++i) {
+                    const int s = i % STAGES;
+                    w = tc::mbar_wait(&full[s], (i / STAGES) & 1, abort_flag, WAIT_BUDGET);
+                    if (w) {
+                        if (w == 1) fail(p.status, ST_TIMEOUT_MMA, &full[s], i);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    *consumed = i + 1;
+                    tc::tc_fence_after();
+                    const uint32_t sfa = tmem + L::T_SFA + 4 * s;
+                    tc::tc_cp_128x128b(sfa, tc::smem_desc(tc::smem_u32(smem + L::SF_OFF + s * L::SF_BYTES), 128, 128, 0));
+                    const uint32_t wa = tc::smem_u32(smem + L::W_OFF + s * L::W_BYTES);
+                    const uint32_t xa = tc::smem_u32(smem + L::X_OFF + s * L::X_BYTES);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t ad = tc::smem_desc(wa + 32 * kk, 16, 1024, 2);
-                    const uint64_t bd = tc::smem_desc(xa + 32 * kk, 16, 1024, 2);
-                    tc::mma_mxf8f6f4(t_acc, ad, bd, tc::idesc_mxf8f6f4(5, 0, BM, BN, kk, 0), sfa, t_sfb,
-                                     (i | kk) != 0);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = tc::smem_desc(wa + 32 * kk, 16, 1024, 2);
+                        const uint64_t bd = tc::smem_desc(xa + 32 * kk, 16, 1024, 2);
+                        tc::mma_mxf8f6f4(t_acc, ad, bd, tc::idesc_mxf8f6f4(5, 0, BM, BN, kk, 0), sfa,
+                                         tmem + L::T_SFB, (first && kk == 0) ? 0u : 1u);
+                    }
+                    first = false;
+                    tc::tc_commit(&empty[s]);
                 }
-                tc::tc_commit(&empty[s]);
+                if (w) break;
+                tc::tc_commit(&acc_full[b]);
+                ++seg;
+                u = ue;
             }
-            tc::tc_commit(accf);  // always: the epilogue / teardown wait on it
+            tc::tc_commit(mma_done);  // always: teardown waits on it before freeing TMEM
         }
         __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------------------------------ scale staging
-        if constexpr (SF_TMA) {
-            bool ok = true;
-            for (int g = 0; 4 * g < nkt && ok; ++g) {
-                const int rs = g % L::SFR_SLOTS;
-                int w = 0;
-                if (lane == 0) w = tc::mbar_wait(&sfr_full[rs], (g / L::SFR_SLOTS) & 1, abort_flag, WAIT_BUDGET);
+        int i = 0, g = 0;
+        for (long long u = u_begin; u < u_end; ++u, ++g) {
+            const int rs = g % L::SFR_SLOTS;
+            int w = 0;
+            if (lane == 0) w = tc::mbar_wait(&sfr_full[rs], (g / L::SFR_SLOTS) & 1, abort_flag, WAIT_BUDGET);
+            w = __shfl_sync(0xffffffffu, w, 0);
+            if (w) {
+                if (lane == 0) {
+                    if (w == 1) fail(p.status, ST_TIMEOUT_SF, &sfr_full[rs], g);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            const uint8_t *raw = smem + L::SFR_OFF + rs * L::SFR_BYTES;
+            for (int j = 0; j < 4; ++j, ++i) {
+                const int s = i % STAGES;
+                if (lane == 0) w = tc::mbar_wait(&empty[s], ((i / STAGES) & 1) ^ 1, abort_flag, WAIT_BUDGET);
                 w = __shfl_sync(0xffffffffu, w, 0);
                 if (w) {
                     if (lane == 0) {
-                        if (w == 1) fail(p.status, ST_TIMEOUT_SF, &sfr_full[rs], g);
+                        if (w == 1) fail(p.status, ST_TIMEOUT_SF, &empty[s], i);
                         *abort_flag = 1;
                     }
                     break;
                 }
-                const uint8_t *raw = smem + L::SFR_OFF + rs * L::SFR_BYTES;
-                for (int t = 0; t < 4; ++t) {
-                    const int i = 4 * g + t;
-                    if (i >= nkt) break;
-                    const int s = i % STAGES;
-                    w = 0;
-                    if (lane == 0) w = tc::mbar_wait(&empty[s], ((i / STAGES) & 1) ^ 1, abort_flag, WAIT_BUDGET);
-                    w = __shfl_sync(0xffffffffu, w, 0);
-                    if (w) {
-                        if (lane == 0) {
-                            if (w == 1) fail(p.status, ST_TIMEOUT_SF, &empty[s], i);
-                            *abort_flag = 1;
-                        }
-                        ok = false;
-                        break;
-                    }
-                    uint8_t *dst = smem + L::SF_OFF + s * L::SF_BYTES;
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const int row = lane + 32 * r;
-                        const uint32_t v = *reinterpret_cast<const uint32_t *>(raw + row * 16 + 4 * t);
-                        *reinterpret_cast<uint4 *>(dst + row * 16) = make_uint4(v, v, v, v);
-                    }
-                    tc::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&full[s]);
-                }
-                __syncwarp();
-                if (lane == 0 && ok) tc::mbar_arrive(&sfr_empty[rs]);
-            }
-        } else {
-            const int kb_row = p.K / 32;
-            uint32_t ring[SF_PREFETCH][4];
-            auto load = [&](int kt, uint32_t(&w)[4]) {
+                uint8_t *dst = smem + L::SF_OFF + s * L::SF_BYTES;
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
-                    const int n = n0 + lane + 32 * r;
-                    w[r] = n < p.N ? __ldg(reinterpret_cast<const uint32_t *>(p.we + (size_t)n * kb_row + 4 * kt))
-                                   : 0x7f7f7f7fu;
+                    const int row = lane + 32 * r;
+                    const uint32_t v = *reinterpret_cast<const uint32_t *>(raw + row * 16 + 4 * j);
+                    *reinterpret_cast<uint4 *>(dst + row * 16) = make_uint4(v, v, v, v);
                 }
-            };
-#pragma unroll
-            for (int j = 0; j < SF_PREFETCH; ++j)
-                if (j < nkt) load(kt_begin + j, ring[j]);
-            bool ok = true;
-            for (int base = 0; base < nkt && ok; base += SF_PREFETCH) {
-#pragma unroll
-                for (int j = 0; j < SF_PREFETCH; ++j) {
-                    const int i = base + j;
-                    if (i >= nkt) break;
-                    const int s = i % STAGES;
-                    const uint32_t ph = (i / STAGES) & 1;
-                    int w = 0;
-                    if (lane == 0) w = tc::mbar_wait(&empty[s], ph ^ 1, abort_flag, WAIT_BUDGET);
-                    w = __shfl_sync(0xffffffffu, w, 0);
-                    if (w) {
-                        if (lane == 0) {
-                            if (w == 1) fail(p.status, ST_TIMEOUT_SF, &empty[s], i);
-                            *abort_flag = 1;
-                        }
-                        ok = false;
-                        break;
-                    }
-                    uint8_t *dst = smem + L::SF_OFF + s * L::SF_BYTES;
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const uint32_t w = ring[j][r];
-                        *reinterpret_cast<uint4 *>(dst + (lane + 32 * r) * 16) = make_uint4(w, w, w, w);
-                    }
-                    tc::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&full[s]);
-                    if (i + SF_PREFETCH < nkt) load(kt_begin + i + SF_PREFETCH, ring[j]);
-                }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&full[s]);
             }
+            if (w) break;
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&sfr_empty[rs]);
         }
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
-        const int n = n0 + 32 * q + lane;
-        int w = 0;
-        if (lane == 0) w = tc::mbar_wait(accf, 0, abort_flag, WAIT_BUDGET);
-        w = __shfl_sync(0xffffffffu, w, 0);
-        if (w == 0 && !*abort_flag) {
+        const int first_tile = (int)(u_begin / p.U);
+        int seg = 0;
+        long long u = u_begin;
+        while (u < u_end) {
+            const int t = (int)(u / p.U);
+            const long long t_lo = (long long)t * p.U, t_hi = t_lo + p.U;
+            const long long ue = min(u_end, t_hi);
+            const bool whole = (u == t_lo) && (ue == t_hi);
+            const int b = seg % ACC_BUFS;
+            int w = 0;
+            if (lane == 0) w = tc::mbar_wait(&acc_full[b], (seg / ACC_BUFS) & 1, abort_flag, WAIT_BUDGET);
+            w = __shfl_sync(0xffffffffu, w, 0);
+            if (w) {
+                if (lane == 0) {
+                    if (w == 1) fail(p.status, ST_TIMEOUT_EPI, &acc_full[b], seg);
+                    *abort_flag = 1;
+                }
+                break;
+            }
             tc::tc_fence_after();
-            const uint32_t row_addr = t_acc + ((32u * q) << 16);
+            const int n0 = (t / p.m_tiles) * BM, m0 = (t % p.m_tiles) * BN;
+            const int row = 32 * q + lane;
+            const int n = n0 + row;
+            const uint32_t t_acc = tmem + b * BN + ((32u * q) << 16);
+            float *slot = p.partials + ((size_t)cta * 2 + (t == first_tile ? 0 : 1)) * (size_t)(BM * BN);
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 16) {
                 uint32_t r[16];
-                tc::tmem_ld16(row_addr + c0, r);
+                tc::tmem_ld16(t_acc + c0, r);
                 tc::tmem_ld_wait();
+                if (whole) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int m = m0 + c0 + j;
-                    if (m < p.M && n < p.N) {
-                        const float v = __uint_as_float(r[j]);
-                        if (p.KS == 1)
-                            p.out[(size_t)m * p.N + n] = float_to_bf16_bits(v * __ldg(p.xs + m));
-                        else
-                            p.partials[((size_t)split * p.M + m) * p.N + n] = v;
+                    for (int j = 0; j < 16; ++j) {
+                        const int m = m0 + c0 + j;
+                        if (m < p.M && n < p.N)
+                            p.out[(size_t)m * p.N + n] = float_to_bf16_bits(__uint_as_float(r[j]) * __ldg(p.xs + m));
                     }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) slot[(c0 + j) * BM + row] = __uint_as_float(r[j]);
                 }
             }
-            if (p.KS > 1) {
+            // release the accumulator buffer to the MMA issuer
+            tc::tc_fence_before();
+            tc::named_bar_sync(1, 128);
+            if (threadIdx.x == EPI_WARP0 * 32) tc::mbar_arrive(&acc_empty[b]);
+            if (!whole) {
+                // stream-K fix-up: the last contributor of tile t adds the partials in CTA order
+                const int c_first = unit_owner(t_lo, p.TU, p.G);
+                const int c_last = unit_owner(t_hi - 1, p.TU, p.G);
                 __threadfence();
                 tc::named_bar_sync(1, 128);
-                const int tile = blockIdx.y * gridDim.x + blockIdx.x;
                 if (threadIdx.x == EPI_WARP0 * 32) {
-                    const int old = atomicAdd(p.counters + tile, 1);
-                    *last_flag = (old == p.KS - 1);
+                    const int old = atomicAdd(p.counters + t, 1);
+                    *last_flag = (old == c_last - c_first);
                 }
                 tc::named_bar_sync(1, 128);
                 if (*last_flag) {
@@ -359,30 +361,34 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                         const int m_end = min(m0 + BN, p.M);
                         for (int m = m0; m < m_end; ++m) {
                             float acc = 0.0f;
-                            for (int z = 0; z < p.KS; ++z)
-                                acc += __ldcg(p.partials + ((size_t)z * p.M + m) * p.N + n);
+                            for (int c = c_first; c <= c_last; ++c) {
+                                const int sl = (t == (int)(unit_start(c, p.TU, p.G) / p.U)) ? 0 : 1;
+                                acc += __ldcg(p.partials + ((size_t)c * 2 + sl) * (size_t)(BM * BN) + (m - m0) * BM + row);
+                            }
                             p.out[(size_t)m * p.N + n] = float_to_bf16_bits(acc * __ldg(p.xs + m));
                         }
                     }
-                    if (threadIdx.x == EPI_WARP0 * 32) p.counters[tile] = 0;
+                    if (threadIdx.x == EPI_WARP0 * 32) p.counters[t] = 0;
                 }
+                tc::named_bar_sync(1, 128);  // last_flag is reused by the next tile
             }
-        } else if (lane == 0 && w) {
-            if (w == 1) fail(p.status, ST_TIMEOUT_EPI, accf, 0);
-            *abort_flag = 1;
+            ++seg;
+            u = ue;
         }
     }
 
     tc::tc_fence_before();
     __syncthreads();
-    if (threadIdx.x == 0 && *abort_flag) {
-        // drain: TMA copies issued but not consumed, and the MMAs behind the final commit
+    if (threadIdx.x == 0) {
         int zero = 0;
-        for (int i = *consumed; i < *issued; ++i)
-            if (tc::mbar_wait(&full[i % STAGES], (i / STAGES) & 1, &zero, DRAIN_BUDGET)) break;
-        for (int g = max(0, *sfr_issued - L::SFR_SLOTS); g < *sfr_issued; ++g)
-            tc::mbar_wait(&sfr_full[g % L::SFR_SLOTS], (g / L::SFR_SLOTS) & 1, &zero, DRAIN_BUDGET);
-        tc::mbar_wait(accf, 0, &zero, WAIT_BUDGET);
+        if (*abort_flag) {
+            // drain: TMA copies issued but not consumed
+            for (int i = *consumed; i < *issued; ++i)
+                if (tc::mbar_wait(&full[i % STAGES], (i / STAGES) & 1, &zero, DRAIN_BUDGET)) break;
+            for (int g = max(0, *sfr_issued - L::SFR_SLOTS); g < *sfr_issued; ++g)
+                tc::mbar_wait(&sfr_full[g % L::SFR_SLOTS], (g / L::SFR_SLOTS) & 1, &zero, DRAIN_BUDGET);
+        }
+        tc::mbar_wait(mma_done, 0, &zero, WAIT_BUDGET);  // every MMA finished before TMEM is freed
     }
     __syncthreads();
     if (warp == 1) {
@@ -393,64 +399,9 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 
 // ------------------------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
-    return fn;
-}
-
-bool tmap_w_fp4(CUtensorMap *m, const void *w, int64_t N, int64_t K)
-{
-    auto enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
-    cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-    cuuint32_t box[2] = {128, (cuuint32_t)BM};
-    cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void *>(w), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool tmap_bytes(CUtensorMap *m, const void *x, int64_t rows, int64_t cols, int box_rows, int box_cols,
-                CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B)
-{
-    auto enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols};
-    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
-    cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(x), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int num_sms()
-{
-    static int cache[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return 148;
-    if (!cache[dev]) {
-        int v = 0;
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        cache[dev] = v > 0 ? v : 148;
-    }
-    return cache[dev];
-}
-
 struct Cfg {
-    int BN, KS, m_tiles, n_tiles;
-    bool sf_tma;
+    int BN, m_tiles, n_tiles, U, G;
+    long long TU;
 };
 
 Cfg choose(int64_t M, int64_t N, int64_t K)
@@ -459,63 +410,39 @@ Cfg choose(int64_t M, int64_t N, int64_t K)
     c.BN = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
     c.n_tiles = (int)((N + BM - 1) / BM);
     c.m_tiles = (int)((M + c.BN - 1) / c.BN);
-    const int KT = (int)(K / BK);
-    c.sf_tma = (K % 512) == 0;
-    const int units = c.sf_tma ? KT / 4 : KT;  // split granularity
-    const long long tiles = (long long)c.n_tiles * c.m_tiles;
-    const int sms = num_sms();
-    c.KS = 1;
-    if (tiles < 2LL * sms) {
-        // split K so the grid fills the SMs evenly; fp32 partials cost traffic, so weigh
-        // their bytes (written and read back, mostly in L2) against the weight bytes
-        double best = -1e30;
-        const double wbytes = (double)N * K * 17.0 / 32.0;
-        for (int ks = 1; ks <= units && ks <= 32; ++ks) {
-            const long long ctas = tiles * ks;
-            const long long waves = (ctas + sms - 1) / sms;
-            const double eff = (double)ctas / (double)(waves * sms);
-            const double part = ks > 1 ? 8.0 * ks * (double)M * N / wbytes : 0.0;
-            const double score = eff - 0.25 * part - 0.002 * ks;
-            if (score > best) {
-                best = score;
-                c.KS = ks;
-            }
-        }
-    }
+    c.U = (int)(K / 512);
+    c.TU = (long long)c.n_tiles * c.m_tiles * c.U;
+    c.G = (int)std::min<long long>(tch::num_sms(), c.TU);
     return c;
 }
 
-size_t workspace_for(const Cfg &c, int64_t M, int64_t N)
+size_t partial_bytes(const Cfg &c)
 {
-    if (c.KS <= 1) return 0;
-    size_t part = (size_t)c.KS * (size_t)M * (size_t)N * 4;
-    part = (part + 255) / 256 * 256;
-    return part + (size_t)c.m_tiles * c.n_tiles * 4;
+    size_t b = (size_t)c.G * 2 * BM * c.BN * 4;
+    return (b + 255) / 256 * 256;
 }
 
-template <int BN, int STAGES, bool SF_TMA>
-w4a8_status launch(const CUtensorMap &tw, const uint8_t *xq, const Params &prm, const Cfg &c,
-                   cudaStream_t stream)
+size_t workspace_for(const Cfg &c)
 {
-    using L = Layout<BN, STAGES>;
-    CUtensorMap tx, tsf;
-    if (!tmap_bytes(&tx, xq, prm.M, prm.K, BN, 128)) return W4A8_ERR_CUDA;
-    if (SF_TMA) {
-        if (!tmap_bytes(&tsf, prm.we, prm.N, prm.K / 32, BM, 16, CU_TENSOR_MAP_SWIZZLE_NONE)) return W4A8_ERR_CUDA;
-    } else {
-        tsf = tx;  // unused
-    }
-    auto kern = mxfp4_tc_kernel<BN, STAGES, SF_TMA>;
+    return partial_bytes(c) + (size_t)c.m_tiles * c.n_tiles * 4;
+}
+
+template <int BN, int STAGES, int ACC_BUFS>
+w4a8_status launch(const uint8_t *wp, const uint8_t *xq, const Params &prm, cudaStream_t stream)
+{
+    using L = Layout<BN, STAGES, ACC_BUFS>;
+    CUtensorMap tw, tx, tsf;
+    if (!tch::tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wp, prm.N, prm.K, prm.K / 2, BM, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !tch::tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, prm.M, prm.K, prm.K, BN, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !tch::tmap_2d(&tsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, prm.we, prm.N, prm.K / 32, prm.K / 32, BM, 16,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
+        return W4A8_ERR_CUDA;
+    auto kern = mxfp4_tc_kernel<BN, STAGES, ACC_BUFS>;
     static int attr_done[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL) != cudaSuccess)
-            return W4A8_ERR_CUDA;
-        attr_done[dev] = 1;
-    }
-    dim3 grid(c.n_tiles, c.m_tiles, c.KS);
-    kern<<<grid, NUM_THREADS, L::TOTAL, stream>>>(tw, tx, tsf, prm);
+    if (!tch::set_smem_once(kern, L::TOTAL, attr_done)) return W4A8_ERR_CUDA;
+    kern<<<prm.G, NUM_THREADS, L::TOTAL, stream>>>(tw, tx, tsf, prm);
     return w4a8_launch_status();
 }
 
@@ -527,18 +454,19 @@ using namespace w4a8::tcg;
 bool w4a8_tc_mxfp4_supported(const void *xq, const void *wp, const void *we, const void *out, int64_t M,
                              int64_t N, int64_t K)
 {
-    if (K % 128 != 0 || K < 128 || K > (1ll << 30) || M < 1 || M > (1ll << 30) || N < 1 || N > (1ll << 30))
+    // TMA needs 16-byte-strided scale rows (K a multiple of 512), a 32-byte aligned 4-bit tensor
+    // and 16-byte aligned byte tensors.
+    if (K % 512 != 0 || K > (1ll << 30) || M < 1 || M > (1ll << 30) || N < 1 || N > (1ll << 30))
         return false;
-    if (!w4a8_aligned(wp, 32) || !w4a8_aligned(xq, 16) || !w4a8_aligned(we, 4) || !w4a8_aligned(out, 2))
+    if (!w4a8_aligned(wp, 32) || !w4a8_aligned(xq, 16) || !w4a8_aligned(we, 16) || !w4a8_aligned(out, 2))
         return false;
-    const Cfg c = choose(M, N, K);
-    return c.m_tiles <= 65535 && encode_fn() != nullptr;
+    return w4a8::tch::encode_fn() != nullptr;
 }
 
 size_t w4a8_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int policy)
 {
-    if (policy == 1 || K % 128 != 0 || K < 128) return 0;
-    return workspace_for(choose(M, N, K), M, N);
+    if (policy == 1 || K % 512 != 0 || K <= 0 || M <= 0 || N <= 0) return 0;
+    return workspace_for(choose(M, N, K));
 }
 
 w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const uint8_t *wp, const uint8_t *we,
@@ -550,38 +478,24 @@ w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const 
     prm.we = we;
     prm.xs = x_scale;
     prm.out = out;
-    prm.partials = nullptr;
-    prm.counters = nullptr;
+    prm.partials = static_cast<float *>(workspace);
+    prm.counters = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) + partial_bytes(c));
     prm.status = w4a8_device_status_ptr();
     if (!prm.status) return W4A8_ERR_CUDA;
     prm.M = (int)M;
     prm.N = (int)N;
     prm.K = (int)K;
-    prm.KS = c.KS;
-    prm.KT = (int)(K / BK);
-    if (c.KS > 1) {
-        size_t part = (size_t)c.KS * (size_t)M * (size_t)N * 4;
-        part = (part + 255) / 256 * 256;
-        prm.partials = static_cast<float *>(workspace);
-        prm.counters = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) + part);
-    }
-    CUtensorMap tw;
-    if (!tmap_w_fp4(&tw, wp, N, K)) return W4A8_ERR_CUDA;
-    if (c.sf_tma && w4a8_aligned(we, 16)) {
-        switch (c.BN) {
-        case 16: return launch<16, 10, true>(tw, xq, prm, c, stream);
-        case 32: return launch<32, 9, true>(tw, xq, prm, c, stream);
-        case 64: return launch<64, 8, true>(tw, xq, prm, c, stream);
-        case 128: return launch<128, 6, true>(tw, xq, prm, c, stream);
-        default: return launch<256, 4, true>(tw, xq, prm, c, stream);
-        }
-    }
+    prm.m_tiles = c.m_tiles;
+    prm.n_tiles = c.n_tiles;
+    prm.U = c.U;
+    prm.TU = c.TU;
+    prm.G = c.G;
     switch (c.BN) {
-    case 16: return launch<16, 10, false>(tw, xq, prm, c, stream);
-    case 32: return launch<32, 9, false>(tw, xq, prm, c, stream);
-    case 64: return launch<64, 8, false>(tw, xq, prm, c, stream);
-    case 128: return launch<128, 6, false>(tw, xq, prm, c, stream);
-    default: return launch<256, 4, false>(tw, xq, prm, c, stream);
+    case 16: return launch<16, 10, 2>(wp, xq, prm, stream);
+    case 32: return launch<32, 9, 2>(wp, xq, prm, stream);
+    case 64: return launch<64, 8, 2>(wp, xq, prm, stream);
+    case 128: return launch<128, 6, 2>(wp, xq, prm, stream);
+    default: return launch<256, 4, 1>(wp, xq, prm, stream);
     }
 }
 

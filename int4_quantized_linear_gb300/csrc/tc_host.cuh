@@ -1,0 +1,69 @@
+// tc_host.cuh -- host helpers shared by the tensor-core kernels: TMA tensor-map encoding
+// (through the driver entry point, so the library needs no link-time libcuda), SM count.
+#pragma once
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace w4a8 {
+namespace tch {
+
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 2-D tensor map over a row-major [rows, cols] array of 1-byte (or 4-bit) elements.
+inline bool tmap_2d(CUtensorMap *m, CUtensorMapDataType type, const void *base, uint64_t rows,
+                    uint64_t cols_elems, uint64_t row_stride_bytes, uint32_t box_rows,
+                    uint32_t box_cols_elems, CUtensorMapSwizzle swz)
+{
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols_elems, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_stride_bytes};
+    cuuint32_t box[2] = {box_cols_elems, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, type, 2, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline int num_sms()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cache[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = v > 0 ? v : 148;
+    }
+    return cache[dev];
+}
+
+// Set the dynamic shared-memory limit of a kernel once per device.
+template <typename K>
+inline bool set_smem_once(K kern, int bytes, int (&done)[64])
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (!done[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+            return false;
+        done[dev] = 1;
+    }
+    return true;
+}
+
+}  // namespace tch
+}  // namespace w4a8

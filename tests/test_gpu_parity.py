@@ -145,7 +145,12 @@ def _mx_gemm(lib, orc, x, w, e, pairs=None):
 
 @pytest.mark.parametrize("M,N,K", [(1, 128, 128), (4, 256, 512), (7, 384, 640), (33, 200, 256),
                                    (64, 1024, 1024), (65, 256, 384), (130, 520, 1152),
-                                   (300, 384, 256), (3, 96, 96)])
+                                   (300, 384, 256), (3, 96, 96),
+                                   # K a multiple of 512: the tensor-core path (stream-K splits,
+                                   # ragged token and weight-row tails, every token tile width)
+                                   (1, 128, 512), (5, 384, 1024), (17, 200, 512), (33, 520, 1536),
+                                   (64, 1000, 2048), (65, 256, 512), (130, 520, 1024),
+                                   (257, 384, 512), (300, 640, 1536), (16, 4096, 512)])
 def test_mxfp4_linear_small(lib, orc, policy, M, N, K):
     x, w, e = synth.prefill_case(M, N, K, seed=M * 7 + N)
     got, ref = _mx_gemm(lib, orc, x, w, e)

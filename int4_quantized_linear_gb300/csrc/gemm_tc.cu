@@ -11,19 +11,22 @@
 //   * tcgen05.mma kind::mxf8f6f4 block_scale.scale_vec::1X: A = e2m1 weights with their ue8m0
 //     scale per 32 along K, B = e4m3 activations with a unit scale (0x7F), fp32 accumulators in
 //     tensor memory; the per-token scale multiplies in the epilogue;
-//   * TMA brings the weights in the 16U4_ALIGN16B form (16 packed e2m1 codes per 16-byte slot,
-//     the shared-memory form the instruction reads for 4-bit operands) and the activations as
-//     bytes, both with the 128-byte swizzle; the weight scales arrive as one [128 x 16-byte] TMA
-//     tile per 4 k-tiles and a helper warp widens each row's 4-byte word into a 16-byte row, which
-//     tcgen05.cp copies to tensor memory (lane r of each scale column holds row r's word);
+//   * TMA brings the packed weights (64 bytes per row per k-tile), the activations (128-byte
+//     swizzle) and, once per 4 k-tiles, a [128 x 16-byte] tile of weight scales.  A converter
+//     warpgroup rewrites each packed weight tile into the form the instruction reads for 4-bit
+//     operands -- 16 codes in the low 8 bytes of each 16-byte slot, 128-byte swizzle -- and widens
+//     each row's 4-byte scale word into a 16-byte row, which tcgen05.cp copies to tensor memory
+//     (lane r of each scale column then holds row r's word).  (TMA can do the 4-bit padding itself
+//     with its 16U4_ALIGN16B type, but measured on GB300 that path moves only about 16 GB/s of
+//     packed data per SM, far below an SM's share of HBM bandwidth.);
 //   * persistent stream-K: one CTA per SM walks a contiguous range of (tile, 4-k-tile unit)
 //     work, so the TMA ring never drains between tiles and every SM gets the same number of
 //     units; a tile whose K range is split between CTAs is finished by the last contributor,
 //     which adds the fp32 partials in CTA order;
 //   * two accumulator buffers in tensor memory (one for 256-token tiles) let the MMAs of the next
 //     tile run while the epilogue drains the previous one;
-//   * warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2 scale staging, 3-6 epilogue
-//     (each reads the TMEM lane quarter its warp index selects).
+//   * warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2-5 converters, 6-9 epilogue
+//     (each epilogue warp reads the TMEM lane quarter its warp index selects).
 //
 // Every mbarrier wait is bounded; a wait that runs out sets a bit in the library's device status
 // word and the CTA winds down (draining what it started) instead of hanging.
@@ -37,12 +40,13 @@ namespace tcg {
 
 constexpr int BM = 128;            // weight rows per tile (MMA M)
 constexpr int BK = 128;            // K elements per pipeline stage (one k-tile)
-constexpr int NUM_THREADS = 224;   // 7 warps
-constexpr int EPI_WARP0 = 3;
+constexpr int NUM_THREADS = 320;   // 10 warps
+constexpr int CONV_WARP0 = 2;      // warps 2-5
+constexpr int EPI_WARP0 = 6;       // warps 6-9
 constexpr long long WAIT_BUDGET = 1ll << 29;  // clock cycles (a quarter second or so)
 constexpr long long DRAIN_BUDGET = 1ll << 24;
 
-enum : unsigned { ST_TIMEOUT_PRODUCER = 1, ST_TIMEOUT_MMA = 2, ST_TIMEOUT_SF = 4, ST_TIMEOUT_EPI = 8 };
+enum : unsigned { ST_TIMEOUT_PRODUCER = 1, ST_TIMEOUT_MMA = 2, ST_TIMEOUT_CONV = 4, ST_TIMEOUT_EPI = 8 };
 
 struct Params {
     const uint8_t *we;     // [N, K/32] e8m0
@@ -58,27 +62,32 @@ struct Params {
     int G;                 // CTAs
 };
 
-template <int BN, int STAGES, int ACC_BUFS>
+// Two rings: A (depth STAGES) holds what TMA writes for a k-tile -- the packed weights and the
+// activation tile; B (depth PSTAGES) holds what the converters write -- the padded weight tile
+// and the widened scales.  A is deep to cover HBM latency; B only covers conversion.
+template <int BN, int STAGES, int PSTAGES, int ACC_BUFS>
 struct Layout {
-    static constexpr int W_BYTES = BM * 128;    // 128 rows x 128 K, 4-bit codes in 16-byte slots
-    static constexpr int W_TX_BYTES = BM * 64;  // a 16U4_ALIGN16B tile counts its packed bytes
-    static constexpr int X_BYTES = BN * 128;    // BN tokens x 128 K bytes
+    static constexpr int WP_BYTES = BM * 64;    // packed weights: 128 rows x 64 bytes
+    static constexpr int X_BYTES = BN * 128;    // BN tokens x 128 K bytes (128-byte swizzle)
+    static constexpr int W_BYTES = BM * 128;    // padded weights: 128 rows x 8 slots of 16 bytes
     static constexpr int SF_BYTES = BM * 16;    // 128 rows x (scale word x 4)
     static constexpr int SFR_SLOTS = 2;         // raw scale tiles, 128 rows x 16 bytes = 4 k-tiles
     static constexpr int SFR_BYTES = BM * 16;
-    static constexpr int W_OFF = 0;
-    static constexpr int X_OFF = W_OFF + STAGES * W_BYTES;
-    static constexpr int SF_OFF = X_OFF + STAGES * X_BYTES;
-    static constexpr int SFR_OFF = SF_OFF + STAGES * SF_BYTES;
+    static constexpr int X_OFF = 0;             // 1024-aligned (swizzled)
+    static constexpr int W_OFF = X_OFF + STAGES * X_BYTES;
+    static constexpr int WP_OFF = W_OFF + PSTAGES * W_BYTES;
+    static constexpr int SF_OFF = WP_OFF + STAGES * WP_BYTES;
+    static constexpr int SFR_OFF = SF_OFF + PSTAGES * SF_BYTES;
     static constexpr int BAR_OFF = SFR_OFF + SFR_SLOTS * SFR_BYTES;
     static constexpr int TOTAL = BAR_OFF + 512 + 1024;  // barriers, flags, alignment slack
     static constexpr int T_SFB = ACC_BUFS * BN;         // TMEM column of the unit B scales
-    static constexpr int T_SFA = T_SFB + 8;             // TMEM columns of the A scales, 4 per stage
-    static constexpr int TMEM_NEED = T_SFA + 4 * STAGES;
+    static constexpr int T_SFA = T_SFB + 8;             // TMEM columns of the A scales, 4 per B slot
+    static constexpr int TMEM_NEED = T_SFA + 4 * PSTAGES;
     static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64
                                      : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
     static_assert(TMEM_NEED <= 512, "tensor memory");
     static_assert(TOTAL <= 232448, "shared memory");
+    static_assert((X_BYTES % 1024) == 0 && (W_OFF % 1024) == 0, "swizzled tiles are 1024-aligned");
 };
 
 // Record a bounded wait that ran out: the role's bit in word 0 of the status block; the first
@@ -98,17 +107,19 @@ __device__ __forceinline__ void fail(unsigned int *status, unsigned int bit, uin
 __device__ __forceinline__ long long unit_start(long long c, long long TU, int G) { return c * TU / G; }
 __device__ __forceinline__ int unit_owner(long long u, long long TU, int G) { return (int)(((u + 1) * G - 1) / TU); }
 
-template <int BN, int STAGES, int ACC_BUFS>
+template <int BN, int STAGES, int PSTAGES, int ACC_BUFS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_sf, const Params p)
 {
-    using L = Layout<BN, STAGES, ACC_BUFS>;
+    using L = Layout<BN, STAGES, PSTAGES, ACC_BUFS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);
-    uint64_t *empty = full + STAGES;
-    uint64_t *sfr_full = empty + STAGES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);  // ring A: TMA landed
+    uint64_t *empty = full + STAGES;                                    // ring A: free again
+    uint64_t *pfull = empty + STAGES;                                   // ring B: converted
+    uint64_t *pempty = pfull + PSTAGES;                                 // ring B: free again
+    uint64_t *sfr_full = pempty + PSTAGES;
     uint64_t *sfr_empty = sfr_full + L::SFR_SLOTS;
     uint64_t *acc_full = sfr_empty + L::SFR_SLOTS;
     uint64_t *acc_empty = acc_full + ACC_BUFS;
@@ -127,12 +138,16 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            tc::mbar_init(&full[s], 2);   // producer expect_tx + scale-staging warp
-            tc::mbar_init(&empty[s], 1);  // tcgen05.commit of the stage's MMAs
+            tc::mbar_init(&full[s], 1);   // producer expect_tx
+            tc::mbar_init(&empty[s], 5);  // 4 converter warps done with the packed tile + MMA commit
+        }
+        for (int s = 0; s < PSTAGES; ++s) {
+            tc::mbar_init(&pfull[s], 4);  // one arrival per converter warp
+            tc::mbar_init(&pempty[s], 1); // tcgen05.commit of the k-tile's MMAs
         }
         for (int r = 0; r < L::SFR_SLOTS; ++r) {
             tc::mbar_init(&sfr_full[r], 1);
-            tc::mbar_init(&sfr_empty[r], 1);
+            tc::mbar_init(&sfr_empty[r], 4);  // one arrival per converter warp
         }
         for (int b = 0; b < ACC_BUFS; ++b) {
             tc::mbar_init(&acc_full[b], 1);   // tcgen05.commit after a tile's last MMA
@@ -193,9 +208,9 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                         *abort_flag = 1;
                         break;
                     }
-                    tc::mbar_arrive_expect_tx(&full[s], L::W_TX_BYTES + L::X_BYTES);
+                    tc::mbar_arrive_expect_tx(&full[s], L::WP_BYTES + L::X_BYTES);
                     const int k = (4 * ku + j) * BK;
-                    tc::tma_load_2d(smem + L::W_OFF + s * L::W_BYTES, &tmap_w, &full[s], k, n0);
+                    tc::tma_load_2d(smem + L::WP_OFF + s * L::WP_BYTES, &tmap_w, &full[s], k / 2, n0);
                     tc::tma_load_2d(smem + L::X_OFF + s * L::X_BYTES, &tmap_x, &full[s], k, m0);
                     *issued = i + 1;
                 }
@@ -222,18 +237,19 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 const uint32_t t_acc = tmem + b * BN;
                 bool first = true;
                 for (long long k4 = 4 * (ue - u); k4 > 0; --k4, ++i) {
-                    const int s = i % STAGES;
+                    const int s = i % STAGES, ps = i % PSTAGES;
                     w = tc::mbar_wait(&full[s], (i / STAGES) & 1, abort_flag, WAIT_BUDGET);
+                    if (!w) w = tc::mbar_wait(&pfull[ps], (i / PSTAGES) & 1, abort_flag, WAIT_BUDGET);
                     if (w) {
-                        if (w == 1) fail(p.status, ST_TIMEOUT_MMA, &full[s], i);
+                        if (w == 1) fail(p.status, ST_TIMEOUT_MMA, &pfull[ps], i);
                         *abort_flag = 1;
                         break;
                     }
                     *consumed = i + 1;
                     tc::tc_fence_after();
-                    const uint32_t sfa = tmem + L::T_SFA + 4 * s;
-                    tc::tc_cp_128x128b(sfa, tc::smem_desc(tc::smem_u32(smem + L::SF_OFF + s * L::SF_BYTES), 128, 128, 0));
-                    const uint32_t wa = tc::smem_u32(smem + L::W_OFF + s * L::W_BYTES);
+                    const uint32_t sfa = tmem + L::T_SFA + 4 * ps;
+                    tc::tc_cp_128x128b(sfa, tc::smem_desc(tc::smem_u32(smem + L::SF_OFF + ps * L::SF_BYTES), 128, 128, 0));
+                    const uint32_t wa = tc::smem_u32(smem + L::W_OFF + ps * L::W_BYTES);
                     const uint32_t xa = tc::smem_u32(smem + L::X_OFF + s * L::X_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
@@ -244,6 +260,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                     }
                     first = false;
                     tc::tc_commit(&empty[s]);
+                    tc::tc_commit(&pempty[ps]);
                 }
                 if (w) break;
                 tc::tc_commit(&acc_full[b]);
@@ -253,46 +270,60 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             tc::tc_commit(mma_done);  // always: teardown waits on it before freeing TMEM
         }
         __syncwarp();
-    } else if (warp == 2) {
-        // ------------------------------------------------------------ scale staging
+    } else if (warp < EPI_WARP0) {
+        // ------------------------------------------------------------ converters (warps 2-5)
+        // packed tile: row r, 16-code chunk c at byte 64r + 8c  ->  padded tile: row r at 128r
+        // (rows in 1024-byte groups of 8), chunk c in slot c ^ (r & 7), low 8 bytes, zero pad.
+        const int ct = threadIdx.x - CONV_WARP0 * 32;  // 0..127
         int i = 0, g = 0;
-        for (long long u = u_begin; u < u_end; ++u, ++g) {
+        int w = 0;
+        for (long long u = u_begin; u < u_end && !w; ++u, ++g) {
             const int rs = g % L::SFR_SLOTS;
-            int w = 0;
             if (lane == 0) w = tc::mbar_wait(&sfr_full[rs], (g / L::SFR_SLOTS) & 1, abort_flag, WAIT_BUDGET);
             w = __shfl_sync(0xffffffffu, w, 0);
             if (w) {
                 if (lane == 0) {
-                    if (w == 1) fail(p.status, ST_TIMEOUT_SF, &sfr_full[rs], g);
+                    if (w == 1) fail(p.status, ST_TIMEOUT_CONV, &sfr_full[rs], g);
                     *abort_flag = 1;
                 }
                 break;
             }
             const uint8_t *raw = smem + L::SFR_OFF + rs * L::SFR_BYTES;
             for (int j = 0; j < 4; ++j, ++i) {
-                const int s = i % STAGES;
-                if (lane == 0) w = tc::mbar_wait(&empty[s], ((i / STAGES) & 1) ^ 1, abort_flag, WAIT_BUDGET);
+                const int s = i % STAGES, ps = i % PSTAGES;
+                if (lane == 0) {
+                    w = tc::mbar_wait(&full[s], (i / STAGES) & 1, abort_flag, WAIT_BUDGET);
+                    if (!w) w = tc::mbar_wait(&pempty[ps], ((i / PSTAGES) & 1) ^ 1, abort_flag, WAIT_BUDGET);
+                }
                 w = __shfl_sync(0xffffffffu, w, 0);
                 if (w) {
                     if (lane == 0) {
-                        if (w == 1) fail(p.status, ST_TIMEOUT_SF, &empty[s], i);
+                        if (w == 1) fail(p.status, ST_TIMEOUT_CONV, &pempty[ps], i);
                         *abort_flag = 1;
                     }
                     break;
                 }
-                uint8_t *dst = smem + L::SF_OFF + s * L::SF_BYTES;
+                const uint8_t *src = smem + L::WP_OFF + s * L::WP_BYTES;
+                uint8_t *dst = smem + L::W_OFF + ps * L::W_BYTES;
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int row = lane + 32 * r;
-                    const uint32_t v = *reinterpret_cast<const uint32_t *>(raw + row * 16 + 4 * j);
-                    *reinterpret_cast<uint4 *>(dst + row * 16) = make_uint4(v, v, v, v);
+                for (int q = 0; q < 8; ++q) {
+                    const int idx = ct + 128 * q;  // (row, chunk) pair
+                    const int r = idx >> 3, c = idx & 7;
+                    const uint2 v = *reinterpret_cast<const uint2 *>(src + r * 64 + c * 8);
+                    *reinterpret_cast<uint4 *>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = make_uint4(v.x, v.y, 0u, 0u);
+                }
+                {
+                    const uint32_t sw = *reinterpret_cast<const uint32_t *>(raw + ct * 16 + 4 * j);
+                    *reinterpret_cast<uint4 *>(smem + L::SF_OFF + ps * L::SF_BYTES + ct * 16) = make_uint4(sw, sw, sw, sw);
                 }
                 tc::fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&full[s]);
+                if (lane == 0) {
+                    tc::mbar_arrive(&pfull[ps]);
+                    tc::mbar_arrive(&empty[s]);  // the packed tile is no longer needed
+                }
             }
             if (w) break;
-            __syncwarp();
             if (lane == 0) tc::mbar_arrive(&sfr_empty[rs]);
         }
     } else {
@@ -357,15 +388,39 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 tc::named_bar_sync(1, 128);
                 if (*last_flag) {
                     __threadfence();
-                    if (n < p.N) {
-                        const int m_end = min(m0 + BN, p.M);
-                        for (int m = m0; m < m_end; ++m) {
-                            float acc = 0.0f;
-                            for (int c = c_first; c <= c_last; ++c) {
-                                const int sl = (t == (int)(unit_start(c, p.TU, p.G) / p.U)) ? 0 : 1;
-                                acc += __ldcg(p.partials + ((size_t)c * 2 + sl) * (size_t)(BM * BN) + (m - m0) * BM + row);
+                    // 16 columns at a time, up to 4 contributors' loads in flight together; the
+                    // additions still run in CTA order, so the result does not depend on timing
+                    const int m_cnt = min(BN, p.M - m0);
+                    for (int c0 = 0; c0 < m_cnt; c0 += 16) {
+                        float acc[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+                        for (int cb = c_first; cb <= c_last; cb += 4) {
+                            float v[4][16];
+#pragma unroll
+                            for (int cc = 0; cc < 4; ++cc) {
+                                const int c = cb + cc;
+                                if (c <= c_last) {
+                                    const int sl = (t == (int)(unit_start(c, p.TU, p.G) / p.U)) ? 0 : 1;
+                                    const float *src = p.partials + ((size_t)c * 2 + sl) * (size_t)(BM * BN) + c0 * BM + row;
+#pragma unroll
+                                    for (int j = 0; j < 16; ++j) v[cc][j] = __ldcg(src + j * BM);
+                                }
                             }
-                            p.out[(size_t)m * p.N + n] = float_to_bf16_bits(acc * __ldg(p.xs + m));
+#pragma unroll
+                            for (int cc = 0; cc < 4; ++cc)
+                                if (cb + cc <= c_last) {
+#pragma unroll
+                                    for (int j = 0; j < 16; ++j) acc[j] += v[cc][j];
+                                }
+                        }
+                        if (n < p.N) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int m = m0 + c0 + j;
+                                if (c0 + j < m_cnt)
+                                    p.out[(size_t)m * p.N + n] = float_to_bf16_bits(acc[j] * __ldg(p.xs + m));
+                            }
                         }
                     }
                     if (threadIdx.x == EPI_WARP0 * 32) p.counters[t] = 0;
@@ -427,19 +482,19 @@ size_t workspace_for(const Cfg &c)
     return partial_bytes(c) + (size_t)c.m_tiles * c.n_tiles * 4;
 }
 
-template <int BN, int STAGES, int ACC_BUFS>
+template <int BN, int STAGES, int PSTAGES, int ACC_BUFS>
 w4a8_status launch(const uint8_t *wp, const uint8_t *xq, const Params &prm, cudaStream_t stream)
 {
-    using L = Layout<BN, STAGES, ACC_BUFS>;
+    using L = Layout<BN, STAGES, PSTAGES, ACC_BUFS>;
     CUtensorMap tw, tx, tsf;
-    if (!tch::tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wp, prm.N, prm.K, prm.K / 2, BM, 128,
-                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+    if (!tch::tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wp, prm.N, prm.K / 2, prm.K / 2, BM, 64,
+                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !tch::tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, prm.M, prm.K, prm.K, BN, 128,
                       CU_TENSOR_MAP_SWIZZLE_128B) ||
         !tch::tmap_2d(&tsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, prm.we, prm.N, prm.K / 32, prm.K / 32, BM, 16,
                       CU_TENSOR_MAP_SWIZZLE_NONE))
         return W4A8_ERR_CUDA;
-    auto kern = mxfp4_tc_kernel<BN, STAGES, ACC_BUFS>;
+    auto kern = mxfp4_tc_kernel<BN, STAGES, PSTAGES, ACC_BUFS>;
     static int attr_done[64] = {0};
     if (!tch::set_smem_once(kern, L::TOTAL, attr_done)) return W4A8_ERR_CUDA;
     kern<<<prm.G, NUM_THREADS, L::TOTAL, stream>>>(tw, tx, tsf, prm);
@@ -454,11 +509,10 @@ using namespace w4a8::tcg;
 bool w4a8_tc_mxfp4_supported(const void *xq, const void *wp, const void *we, const void *out, int64_t M,
                              int64_t N, int64_t K)
 {
-    // TMA needs 16-byte-strided scale rows (K a multiple of 512), a 32-byte aligned 4-bit tensor
-    // and 16-byte aligned byte tensors.
+    // TMA needs 16-byte-strided scale rows (K a multiple of 512) and 16-byte aligned tensors.
     if (K % 512 != 0 || K > (1ll << 30) || M < 1 || M > (1ll << 30) || N < 1 || N > (1ll << 30))
         return false;
-    if (!w4a8_aligned(wp, 32) || !w4a8_aligned(xq, 16) || !w4a8_aligned(we, 16) || !w4a8_aligned(out, 2))
+    if (!w4a8_aligned(wp, 16) || !w4a8_aligned(xq, 16) || !w4a8_aligned(we, 16) || !w4a8_aligned(out, 2))
         return false;
     return w4a8::tch::encode_fn() != nullptr;
 }
@@ -491,11 +545,11 @@ w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const 
     prm.TU = c.TU;
     prm.G = c.G;
     switch (c.BN) {
-    case 16: return launch<16, 10, 2>(wp, xq, prm, stream);
-    case 32: return launch<32, 9, 2>(wp, xq, prm, stream);
-    case 64: return launch<64, 8, 2>(wp, xq, prm, stream);
-    case 128: return launch<128, 6, 2>(wp, xq, prm, stream);
-    default: return launch<256, 4, 1>(wp, xq, prm, stream);
+    case 16: return launch<16, 12, 3, 2>(wp, xq, prm, stream);
+    case 32: return launch<32, 12, 3, 2>(wp, xq, prm, stream);
+    case 64: return launch<64, 10, 3, 2>(wp, xq, prm, stream);
+    case 128: return launch<128, 6, 3, 2>(wp, xq, prm, stream);
+    default: return launch<256, 4, 2, 1>(wp, xq, prm, stream);
     }
 }
 

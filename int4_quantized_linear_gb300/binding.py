@@ -23,7 +23,7 @@ MODES = {"ocp": 0, "noclip": 1, "mse": 2}
 EXPORTS = ("w4a8_act_quant", "w4a8_mxfp4_linear", "w4a8_workspace_bytes",
            "nvfp4_to_mxfp4_requant", "w4a8_int4g128_linear", "w4a8_int4g128_workspace_bytes",
            "w4a8_status_string", "w4a8_set_gemm_policy", "w4a8_check_device_status",
-           "w4a8_decode_max_m", "w4a8_debug_status_words")
+           "w4a8_decode_max_m", "w4a8_debug_status_words", "w4a8_debug_set_trace")
 
 
 class W4A8Error(RuntimeError):
@@ -60,6 +60,7 @@ def load(build_if_missing: bool = True):
         "w4a8_check_device_status": (I, [P]),
         "w4a8_decode_max_m": (I, []),
         "w4a8_debug_status_words": (I, [P]),
+        "w4a8_debug_set_trace": (None, [P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)

@@ -29,6 +29,10 @@ unsigned int *w4a8_device_status_ptr()
 
 int w4a8_gemm_policy() { return g_policy.load(std::memory_order_relaxed); }
 
+static std::atomic<void *> g_trace{nullptr};
+void *w4a8_debug_trace_ptr() { return g_trace.load(std::memory_order_relaxed); }
+extern "C" void w4a8_debug_set_trace(void *device_buffer) { g_trace.store(device_buffer, std::memory_order_relaxed); }
+
 extern "C" void w4a8_set_gemm_policy(int policy) { g_policy.store(policy, std::memory_order_relaxed); }
 
 extern "C" int w4a8_decode_max_m(void) { return W4A8_DECODE_MAX_M; }

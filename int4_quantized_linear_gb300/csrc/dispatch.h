@@ -10,6 +10,7 @@
 #define W4A8_DECODE_MAX_M 64
 
 int w4a8_gemm_policy();
+void *w4a8_debug_trace_ptr();
 unsigned int *w4a8_device_status_ptr();
 
 w4a8_status w4a8_launch_mxfp4_simt(const uint8_t *xq, const float *x_scale, const uint8_t *wp,

@@ -60,34 +60,46 @@ struct Params {
     int U;                 // 4-k-tile units per tile
     long long TU;          // total units
     int G;                 // CTAs
+    unsigned long long *trace;  // optional pipeline timeline of CTA 0 (diagnostics), or null
 };
 
-// Two rings: A (depth STAGES) holds what TMA writes for a k-tile -- the packed weights and the
-// activation tile; B (depth PSTAGES) holds what the converters write -- the padded weight tile
-// and the widened scales.  A is deep to cover HBM latency; B only covers conversion.
-template <int BN, int STAGES, int PSTAGES, int ACC_BUFS>
+// Pipeline timeline (diagnostics): CTA 0 records clock64() per k-tile i < TRACE_N for each event.
+constexpr int TRACE_N = 256;
+enum { TR_TMA_ISSUED = 0, TR_CONV_DATA, TR_CONV_DONE, TR_MMA_READY, TR_MMA_ISSUED, TR_SLOT_FREED, TR_EVENTS };
+__device__ __forceinline__ void trace_ev(const Params &p, int ev, int i)
+{
+    if (p.trace != nullptr && blockIdx.x == 0 && i < TRACE_N) p.trace[ev * TRACE_N + i] = (unsigned long long)clock64();
+}
+
+// Shared memory.  Ring A (depth STAGES) holds what TMA writes for a k-tile: the activation
+// tile and the weight tile -- already in the padded 4-bit form when TMA does the padding
+// (CONV = false), packed when a converter warpgroup pads it (CONV = true), in which case ring B
+// (depth PSTAGES) holds the padded tiles.  Raw scale tiles (4 k-tiles each) have a ring of 2.
+template <int BN, int STAGES, int PSTAGES, int ACC_BUFS, bool CONV>
 struct Layout {
-    static constexpr int WP_BYTES = BM * 64;    // packed weights: 128 rows x 64 bytes
-    static constexpr int X_BYTES = BN * 128;    // BN tokens x 128 K bytes (128-byte swizzle)
-    static constexpr int W_BYTES = BM * 128;    // padded weights: 128 rows x 8 slots of 16 bytes
-    static constexpr int SF_BYTES = BM * 16;    // 128 rows x (scale word x 4)
-    static constexpr int SFR_SLOTS = 2;         // raw scale tiles, 128 rows x 16 bytes = 4 k-tiles
-    static constexpr int SFR_BYTES = BM * 16;
-    static constexpr int X_OFF = 0;             // 1024-aligned (swizzled)
-    static constexpr int W_OFF = X_OFF + STAGES * X_BYTES;
-    static constexpr int WP_OFF = W_OFF + PSTAGES * W_BYTES;
-    static constexpr int SF_OFF = WP_OFF + STAGES * WP_BYTES;
-    static constexpr int SFR_OFF = SF_OFF + PSTAGES * SF_BYTES;
+    static constexpr int X_BYTES = BN * 128;               // BN tokens x 128 K bytes (swizzled)
+    static constexpr int W_BYTES = BM * 128;               // padded: 128 rows x 8 slots of 16 bytes
+    static constexpr int WP_BYTES = BM * 64;               // packed: 128 rows x 64 bytes
+    static constexpr int A_W_BYTES = CONV ? WP_BYTES : W_BYTES;
+    static constexpr int B_SLOTS = CONV ? PSTAGES : 0;
+    static constexpr int SF_SLOTS = CONV ? PSTAGES : STAGES;  // TMEM scale slots (4 columns each)
+    static constexpr int SFR_SLOTS = 2;
+    static constexpr int SFR_BYTES = BM * 16;              // 128 rows x 16 bytes = 4 k-tiles
+    static constexpr int X_OFF = 0;
+    static constexpr int AW_OFF = X_OFF + STAGES * X_BYTES;   // 1024-aligned for the swizzled form
+    static constexpr int BW_OFF = AW_OFF + STAGES * A_W_BYTES;
+    static constexpr int SFR_OFF = BW_OFF + B_SLOTS * W_BYTES;
     static constexpr int BAR_OFF = SFR_OFF + SFR_SLOTS * SFR_BYTES;
     static constexpr int TOTAL = BAR_OFF + 512 + 1024;  // barriers, flags, alignment slack
+    static constexpr int W_TX_BYTES = BM * 64;          // both forms count the packed bytes
     static constexpr int T_SFB = ACC_BUFS * BN;         // TMEM column of the unit B scales
-    static constexpr int T_SFA = T_SFB + 8;             // TMEM columns of the A scales, 4 per B slot
-    static constexpr int TMEM_NEED = T_SFA + 4 * PSTAGES;
+    static constexpr int T_SFA = T_SFB + 8;             // TMEM columns of the A scales
+    static constexpr int TMEM_NEED = T_SFA + 4 * SF_SLOTS;
     static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64
                                      : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
     static_assert(TMEM_NEED <= 512, "tensor memory");
     static_assert(TOTAL <= 232448, "shared memory");
-    static_assert((X_BYTES % 1024) == 0 && (W_OFF % 1024) == 0, "swizzled tiles are 1024-aligned");
+    static_assert((X_BYTES % 1024) == 0 && (AW_OFF % 1024) == 0 && (BW_OFF % 1024) == 0, "alignment");
 };
 
 // Record a bounded wait that ran out: the role's bit in word 0 of the status block; the first
@@ -107,18 +119,32 @@ __device__ __forceinline__ void fail(unsigned int *status, unsigned int bit, uin
 __device__ __forceinline__ long long unit_start(long long c, long long TU, int G) { return c * TU / G; }
 __device__ __forceinline__ int unit_owner(long long u, long long TU, int G) { return (int)(((u + 1) * G - 1) / TU); }
 
-template <int BN, int STAGES, int PSTAGES, int ACC_BUFS>
+// Warp-uniform bounded wait by lane 0; on a timeout or abort the warp records it and returns
+// nonzero.
+__device__ __forceinline__ int warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                         unsigned int *status, unsigned int bit, int iter, int lane)
+{
+    int w = 0;
+    if (lane == 0) {
+        w = tc::mbar_wait(bar, parity, abort_flag, WAIT_BUDGET);
+        if (w == 1) fail(status, bit, bar, iter);
+        if (w) *abort_flag = 1;
+    }
+    return __shfl_sync(0xffffffffu, w, 0);
+}
+
+template <int BN, int STAGES, int PSTAGES, int ACC_BUFS, bool CONV>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_sf, const Params p)
 {
-    using L = Layout<BN, STAGES, PSTAGES, ACC_BUFS>;
+    using L = Layout<BN, STAGES, PSTAGES, ACC_BUFS, CONV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);  // ring A: TMA landed
-    uint64_t *empty = full + STAGES;                                    // ring A: free again
-    uint64_t *pfull = empty + STAGES;                                   // ring B: converted
-    uint64_t *pempty = pfull + PSTAGES;                                 // ring B: free again
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);  // ring A landed (+ scales)
+    uint64_t *empty = full + STAGES;                                    // ring A free again
+    uint64_t *pfull = empty + STAGES;                                   // ring B converted
+    uint64_t *pempty = pfull + PSTAGES;                                 // ring B free again
     uint64_t *sfr_full = pempty + PSTAGES;
     uint64_t *sfr_empty = sfr_full + L::SFR_SLOTS;
     uint64_t *acc_full = sfr_empty + L::SFR_SLOTS;
@@ -138,16 +164,18 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            tc::mbar_init(&full[s], 1);   // producer expect_tx
-            tc::mbar_init(&empty[s], 5);  // 4 converter warps done with the packed tile + MMA commit
+            // producer expect_tx + 4 scale warps (which also convert, when CONV)
+            tc::mbar_init(&full[s], CONV ? 1 : 5);
+            // MMA commit (+ the 4 converter warps done with the packed tile, when CONV)
+            tc::mbar_init(&empty[s], CONV ? 5 : 1);
         }
         for (int s = 0; s < PSTAGES; ++s) {
-            tc::mbar_init(&pfull[s], 4);  // one arrival per converter warp
-            tc::mbar_init(&pempty[s], 1); // tcgen05.commit of the k-tile's MMAs
+            tc::mbar_init(&pfull[s], 4);   // one arrival per converter warp
+            tc::mbar_init(&pempty[s], 1);  // tcgen05.commit of the k-tile's MMAs
         }
         for (int r = 0; r < L::SFR_SLOTS; ++r) {
             tc::mbar_init(&sfr_full[r], 1);
-            tc::mbar_init(&sfr_empty[r], 4);  // one arrival per converter warp
+            tc::mbar_init(&sfr_empty[r], 4);  // one arrival per scale warp
         }
         for (int b = 0; b < ACC_BUFS; ++b) {
             tc::mbar_init(&acc_full[b], 1);   // tcgen05.commit after a tile's last MMA
@@ -208,11 +236,13 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                         *abort_flag = 1;
                         break;
                     }
-                    tc::mbar_arrive_expect_tx(&full[s], L::WP_BYTES + L::X_BYTES);
+                    tc::mbar_arrive_expect_tx(&full[s], L::W_TX_BYTES + L::X_BYTES);
                     const int k = (4 * ku + j) * BK;
-                    tc::tma_load_2d(smem + L::WP_OFF + s * L::WP_BYTES, &tmap_w, &full[s], k / 2, n0);
+                    // weights: element coordinate k in the 4-bit map, byte coordinate k/2 in the byte map
+                    tc::tma_load_2d(smem + L::AW_OFF + s * L::A_W_BYTES, &tmap_w, &full[s], CONV ? k / 2 : k, n0);
                     tc::tma_load_2d(smem + L::X_OFF + s * L::X_BYTES, &tmap_x, &full[s], k, m0);
                     *issued = i + 1;
+                    trace_ev(p, TR_TMA_ISSUED, i);
                 }
             }
         }
@@ -239,17 +269,19 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 for (long long k4 = 4 * (ue - u); k4 > 0; --k4, ++i) {
                     const int s = i % STAGES, ps = i % PSTAGES;
                     w = tc::mbar_wait(&full[s], (i / STAGES) & 1, abort_flag, WAIT_BUDGET);
-                    if (!w) w = tc::mbar_wait(&pfull[ps], (i / PSTAGES) & 1, abort_flag, WAIT_BUDGET);
+                    if (CONV && !w) w = tc::mbar_wait(&pfull[ps], (i / PSTAGES) & 1, abort_flag, WAIT_BUDGET);
                     if (w) {
-                        if (w == 1) fail(p.status, ST_TIMEOUT_MMA, &pfull[ps], i);
+                        if (w == 1) fail(p.status, ST_TIMEOUT_MMA, &full[s], i);
                         *abort_flag = 1;
                         break;
                     }
                     *consumed = i + 1;
+                    trace_ev(p, TR_MMA_READY, i);
                     tc::tc_fence_after();
-                    const uint32_t sfa = tmem + L::T_SFA + 4 * ps;
-                    tc::tc_cp_128x128b(sfa, tc::smem_desc(tc::smem_u32(smem + L::SF_OFF + ps * L::SF_BYTES), 128, 128, 0));
-                    const uint32_t wa = tc::smem_u32(smem + L::W_OFF + ps * L::W_BYTES);
+                    const int sfs = CONV ? ps : s;
+                    const uint32_t sfa = tmem + L::T_SFA + 4 * sfs;
+                    const uint32_t wa = CONV ? tc::smem_u32(smem + L::BW_OFF + ps * L::W_BYTES)
+                                             : tc::smem_u32(smem + L::AW_OFF + s * L::W_BYTES);
                     const uint32_t xa = tc::smem_u32(smem + L::X_OFF + s * L::X_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
@@ -260,7 +292,8 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                     }
                     first = false;
                     tc::tc_commit(&empty[s]);
-                    tc::tc_commit(&pempty[ps]);
+                    if (CONV) tc::tc_commit(&pempty[ps]);
+                    trace_ev(p, TR_MMA_ISSUED, i);
                 }
                 if (w) break;
                 tc::tc_commit(&acc_full[b]);
@@ -271,56 +304,59 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         }
         __syncwarp();
     } else if (warp < EPI_WARP0) {
-        // ------------------------------------------------------------ converters (warps 2-5)
-        // packed tile: row r, 16-code chunk c at byte 64r + 8c  ->  padded tile: row r at 128r
-        // (rows in 1024-byte groups of 8), chunk c in slot c ^ (r & 7), low 8 bytes, zero pad.
-        const int ct = threadIdx.x - CONV_WARP0 * 32;  // 0..127
+        // ------------------------------------------------------------ scale warps (2-5)
+        // Each warp owns the TMEM lane quarter q = warp & 3 (weight rows 32q..32q+31) and writes
+        // its rows' 4-byte scale word, repeated over the slot's 4 columns, with tcgen05.st.
+        // With CONV they also pad the packed weight tile:
+        //   packed row r, 16-code chunk c at byte 64r + 8c  ->  padded row r at 128r (rows in
+        //   1024-byte groups of 8), chunk c in 16-byte slot c ^ (r & 7), low 8 bytes, zero pad.
+        const int q = warp & 3;
+        const int row = 32 * q + lane;
+        const int ct = threadIdx.x - CONV_WARP0 * 32;  // 0..127 (converter thread)
         int i = 0, g = 0;
         int w = 0;
         for (long long u = u_begin; u < u_end && !w; ++u, ++g) {
             const int rs = g % L::SFR_SLOTS;
-            if (lane == 0) w = tc::mbar_wait(&sfr_full[rs], (g / L::SFR_SLOTS) & 1, abort_flag, WAIT_BUDGET);
-            w = __shfl_sync(0xffffffffu, w, 0);
-            if (w) {
-                if (lane == 0) {
-                    if (w == 1) fail(p.status, ST_TIMEOUT_CONV, &sfr_full[rs], g);
-                    *abort_flag = 1;
-                }
-                break;
-            }
+            w = warp_wait(&sfr_full[rs], (g / L::SFR_SLOTS) & 1, abort_flag, p.status, ST_TIMEOUT_CONV, g, lane);
+            if (w) break;
             const uint8_t *raw = smem + L::SFR_OFF + rs * L::SFR_BYTES;
             for (int j = 0; j < 4; ++j, ++i) {
                 const int s = i % STAGES, ps = i % PSTAGES;
-                if (lane == 0) {
-                    w = tc::mbar_wait(&full[s], (i / STAGES) & 1, abort_flag, WAIT_BUDGET);
-                    if (!w) w = tc::mbar_wait(&pempty[ps], ((i / PSTAGES) & 1) ^ 1, abort_flag, WAIT_BUDGET);
+                if (CONV) {
+                    w = warp_wait(&full[s], (i / STAGES) & 1, abort_flag, p.status, ST_TIMEOUT_CONV, i, lane);
+                    if (!w) w = warp_wait(&pempty[ps], ((i / PSTAGES) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_CONV, i, lane);
+                } else {
+                    // the scale slot is free once the MMAs that last read it (k-tile i - STAGES) are done
+                    w = warp_wait(&empty[s], ((i / STAGES) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_CONV, i, lane);
                 }
-                w = __shfl_sync(0xffffffffu, w, 0);
-                if (w) {
-                    if (lane == 0) {
-                        if (w == 1) fail(p.status, ST_TIMEOUT_CONV, &pempty[ps], i);
-                        *abort_flag = 1;
-                    }
-                    break;
-                }
-                const uint8_t *src = smem + L::WP_OFF + s * L::WP_BYTES;
-                uint8_t *dst = smem + L::W_OFF + ps * L::W_BYTES;
+                if (w) break;
+                if (lane == 0 && warp == CONV_WARP0) trace_ev(p, TR_CONV_DATA, i);
+                if (CONV) {
+                    const uint8_t *src = smem + L::AW_OFF + s * L::WP_BYTES;
+                    uint8_t *dst = smem + L::BW_OFF + ps * L::W_BYTES;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int idx = ct + 128 * q;  // (row, chunk) pair
-                    const int r = idx >> 3, c = idx & 7;
-                    const uint2 v = *reinterpret_cast<const uint2 *>(src + r * 64 + c * 8);
-                    *reinterpret_cast<uint4 *>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = make_uint4(v.x, v.y, 0u, 0u);
+                    for (int qq = 0; qq < 8; ++qq) {
+                        const int idx = ct + 128 * qq;  // (row, chunk) pair
+                        const int r = idx >> 3, c = idx & 7;
+                        const uint2 v = *reinterpret_cast<const uint2 *>(src + r * 64 + c * 8);
+                        *reinterpret_cast<uint4 *>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = make_uint4(v.x, v.y, 0u, 0u);
+                    }
                 }
-                {
-                    const uint32_t sw = *reinterpret_cast<const uint32_t *>(raw + ct * 16 + 4 * j);
-                    *reinterpret_cast<uint4 *>(smem + L::SF_OFF + ps * L::SF_BYTES + ct * 16) = make_uint4(sw, sw, sw, sw);
-                }
-                tc::fence_proxy_async_smem();
+                const uint32_t sw = *reinterpret_cast<const uint32_t *>(raw + row * 16 + 4 * j);
+                const int sfs = CONV ? ps : s;
+                tc::tmem_st4(tmem + L::T_SFA + 4 * sfs + ((32u * q) << 16), sw, sw, sw, sw);
+                tc::tmem_st_wait();
+                if (CONV) tc::fence_proxy_async_smem();
+                tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    tc::mbar_arrive(&pfull[ps]);
-                    tc::mbar_arrive(&empty[s]);  // the packed tile is no longer needed
+                    if (CONV) {
+                        tc::mbar_arrive(&pfull[ps]);
+                        tc::mbar_arrive(&empty[s]);  // the packed tile is no longer needed
+                    } else {
+                        tc::mbar_arrive(&full[s]);
+                    }
+                    if (warp == CONV_WARP0) trace_ev(p, TR_CONV_DONE, i);
                 }
             }
             if (w) break;
@@ -482,19 +518,22 @@ size_t workspace_for(const Cfg &c)
     return partial_bytes(c) + (size_t)c.m_tiles * c.n_tiles * 4;
 }
 
-template <int BN, int STAGES, int PSTAGES, int ACC_BUFS>
+template <int BN, int STAGES, int PSTAGES, int ACC_BUFS, bool CONV>
 w4a8_status launch(const uint8_t *wp, const uint8_t *xq, const Params &prm, cudaStream_t stream)
 {
-    using L = Layout<BN, STAGES, PSTAGES, ACC_BUFS>;
+    using L = Layout<BN, STAGES, PSTAGES, ACC_BUFS, CONV>;
     CUtensorMap tw, tx, tsf;
-    if (!tch::tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wp, prm.N, prm.K / 2, prm.K / 2, BM, 64,
-                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
+    const bool wmap = CONV ? tch::tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wp, prm.N, prm.K / 2, prm.K / 2, BM,
+                                          64, CU_TENSOR_MAP_SWIZZLE_NONE)
+                           : tch::tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wp, prm.N, prm.K, prm.K / 2,
+                                          BM, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!wmap ||
         !tch::tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, prm.M, prm.K, prm.K, BN, 128,
                       CU_TENSOR_MAP_SWIZZLE_128B) ||
         !tch::tmap_2d(&tsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, prm.we, prm.N, prm.K / 32, prm.K / 32, BM, 16,
                       CU_TENSOR_MAP_SWIZZLE_NONE))
         return W4A8_ERR_CUDA;
-    auto kern = mxfp4_tc_kernel<BN, STAGES, PSTAGES, ACC_BUFS>;
+    auto kern = mxfp4_tc_kernel<BN, STAGES, PSTAGES, ACC_BUFS, CONV>;
     static int attr_done[64] = {0};
     if (!tch::set_smem_once(kern, L::TOTAL, attr_done)) return W4A8_ERR_CUDA;
     kern<<<prm.G, NUM_THREADS, L::TOTAL, stream>>>(tw, tx, tsf, prm);
@@ -509,10 +548,11 @@ using namespace w4a8::tcg;
 bool w4a8_tc_mxfp4_supported(const void *xq, const void *wp, const void *we, const void *out, int64_t M,
                              int64_t N, int64_t K)
 {
-    // TMA needs 16-byte-strided scale rows (K a multiple of 512) and 16-byte aligned tensors.
+    // TMA needs 16-byte-strided scale rows (K a multiple of 512), a 32-byte aligned 4-bit tensor
+    // and 16-byte aligned byte tensors.
     if (K % 512 != 0 || K > (1ll << 30) || M < 1 || M > (1ll << 30) || N < 1 || N > (1ll << 30))
         return false;
-    if (!w4a8_aligned(wp, 16) || !w4a8_aligned(xq, 16) || !w4a8_aligned(we, 16) || !w4a8_aligned(out, 2))
+    if (!w4a8_aligned(wp, 32) || !w4a8_aligned(xq, 16) || !w4a8_aligned(we, 16) || !w4a8_aligned(out, 2))
         return false;
     return w4a8::tch::encode_fn() != nullptr;
 }
@@ -544,12 +584,22 @@ w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const 
     prm.U = c.U;
     prm.TU = c.TU;
     prm.G = c.G;
+    prm.trace = static_cast<unsigned long long *>(w4a8_debug_trace_ptr());
+    if (w4a8_gemm_policy() == 3) {  // converter variant (diagnostics)
+        switch (c.BN) {
+        case 16: return launch<16, 12, 3, 2, true>(wp, xq, prm, stream);
+        case 32: return launch<32, 12, 3, 2, true>(wp, xq, prm, stream);
+        case 64: return launch<64, 10, 3, 2, true>(wp, xq, prm, stream);
+        case 128: return launch<128, 6, 3, 2, true>(wp, xq, prm, stream);
+        default: return launch<256, 4, 2, 1, true>(wp, xq, prm, stream);
+        }
+    }
     switch (c.BN) {
-    case 16: return launch<16, 12, 3, 2>(wp, xq, prm, stream);
-    case 32: return launch<32, 12, 3, 2>(wp, xq, prm, stream);
-    case 64: return launch<64, 10, 3, 2>(wp, xq, prm, stream);
-    case 128: return launch<128, 6, 3, 2>(wp, xq, prm, stream);
-    default: return launch<256, 4, 2, 1>(wp, xq, prm, stream);
+    case 16: return launch<16, 12, 1, 2, false>(wp, xq, prm, stream);
+    case 32: return launch<32, 10, 1, 2, false>(wp, xq, prm, stream);
+    case 64: return launch<64, 8, 1, 2, false>(wp, xq, prm, stream);
+    case 128: return launch<128, 6, 1, 2, false>(wp, xq, prm, stream);
+    default: return launch<256, 4, 1, 1, false>(wp, xq, prm, stream);
     }
 }
 

@@ -11,22 +11,22 @@
 //   * tcgen05.mma kind::mxf8f6f4 block_scale.scale_vec::1X: A = e2m1 weights with their ue8m0
 //     scale per 32 along K, B = e4m3 activations with a unit scale (0x7F), fp32 accumulators in
 //     tensor memory; the per-token scale multiplies in the epilogue;
-//   * TMA brings the packed weights (64 bytes per row per k-tile), the activations (128-byte
-//     swizzle) and, once per 4 k-tiles, a [128 x 16-byte] tile of weight scales.  A converter
-//     warpgroup rewrites each packed weight tile into the form the instruction reads for 4-bit
-//     operands -- 16 codes in the low 8 bytes of each 16-byte slot, 128-byte swizzle -- and widens
-//     each row's 4-byte scale word into a 16-byte row, which tcgen05.cp copies to tensor memory
-//     (lane r of each scale column then holds row r's word).  (TMA can do the 4-bit padding itself
-//     with its 16U4_ALIGN16B type, but measured on GB300 that path moves only about 16 GB/s of
-//     packed data per SM, far below an SM's share of HBM bandwidth.);
+//   * TMA: one 3-D box brings KPU consecutive k-tiles (128 K each) of 128 weight rows, already in
+//     the padded form the instruction reads for 4-bit operands (16U4_ALIGN16B: 16 codes in the
+//     low 8 bytes of each 16-byte slot) with the 128-byte swizzle; another brings the matching
+//     activation tiles; the weight scales come as one [128 rows x 16 bytes] tile per 4 k-tiles.
+//     Boxes whose rows read 4 k-tiles (256 contiguous bytes) at once run TMA at the full HBM
+//     rate on GB300, where one-k-tile boxes (64-byte rows) reach only about 60% of it;
+//   * four scale warps (one per TMEM lane quarter) write each row's 4-byte scale word, repeated
+//     over 4 columns, into tensor memory with tcgen05.st; the MMA reads one byte per k-block;
 //   * persistent stream-K: one CTA per SM walks a contiguous range of (tile, 4-k-tile unit)
 //     work, so the TMA ring never drains between tiles and every SM gets the same number of
 //     units; a tile whose K range is split between CTAs is finished by the last contributor,
 //     which adds the fp32 partials in CTA order;
 //   * two accumulator buffers in tensor memory (one for 256-token tiles) let the MMAs of the next
 //     tile run while the epilogue drains the previous one;
-//   * warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2-5 converters, 6-9 epilogue
-//     (each epilogue warp reads the TMEM lane quarter its warp index selects).
+//   * warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2-5 scale warps, 6-9 epilogue
+//     (scale and epilogue warps each use the TMEM lane quarter their warp index selects).
 //
 // Every mbarrier wait is bounded; a wait that runs out sets a bit in the library's device status
 // word and the CTA winds down (draining what it started) instead of hanging.
@@ -39,14 +39,13 @@ namespace w4a8 {
 namespace tcg {
 
 constexpr int BM = 128;            // weight rows per tile (MMA M)
-constexpr int BK = 128;            // K elements per pipeline stage (one k-tile)
 constexpr int NUM_THREADS = 320;   // 10 warps
-constexpr int CONV_WARP0 = 2;      // warps 2-5
+constexpr int SCALE_WARP0 = 2;     // warps 2-5
 constexpr int EPI_WARP0 = 6;       // warps 6-9
 constexpr long long WAIT_BUDGET = 1ll << 29;  // clock cycles (a quarter second or so)
 constexpr long long DRAIN_BUDGET = 1ll << 24;
 
-enum : unsigned { ST_TIMEOUT_PRODUCER = 1, ST_TIMEOUT_MMA = 2, ST_TIMEOUT_CONV = 4, ST_TIMEOUT_EPI = 8 };
+enum : unsigned { ST_TIMEOUT_PRODUCER = 1, ST_TIMEOUT_MMA = 2, ST_TIMEOUT_SCALE = 4, ST_TIMEOUT_EPI = 8 };
 
 struct Params {
     const uint8_t *we;     // [N, K/32] e8m0
@@ -65,41 +64,38 @@ struct Params {
 
 // Pipeline timeline (diagnostics): CTA 0 records clock64() per k-tile i < TRACE_N for each event.
 constexpr int TRACE_N = 256;
-enum { TR_TMA_ISSUED = 0, TR_CONV_DATA, TR_CONV_DONE, TR_MMA_READY, TR_MMA_ISSUED, TR_SLOT_FREED, TR_EVENTS };
+enum { TR_TMA_ISSUED = 0, TR_SCALE_DATA, TR_SCALE_DONE, TR_MMA_READY, TR_MMA_ISSUED, TR_UNUSED, TR_EVENTS };
 __device__ __forceinline__ void trace_ev(const Params &p, int ev, int i)
 {
     if (p.trace != nullptr && blockIdx.x == 0 && i < TRACE_N) p.trace[ev * TRACE_N + i] = (unsigned long long)clock64();
 }
 
-// Shared memory.  Ring A (depth STAGES) holds what TMA writes for a k-tile: the activation
-// tile and the weight tile -- already in the padded 4-bit form when TMA does the padding
-// (CONV = false), packed when a converter warpgroup pads it (CONV = true), in which case ring B
-// (depth PSTAGES) holds the padded tiles.  Raw scale tiles (4 k-tiles each) have a ring of 2.
-template <int BN, int STAGES, int PSTAGES, int ACC_BUFS, bool CONV>
+// Shared memory: a ring of US slots, each holding KPU k-tiles of padded weights (16 KB each)
+// and activations (BN x 128 bytes each), plus a ring of 2 raw scale tiles (4 k-tiles each).
+template <int BN, int KPU, int US, int ACC_BUFS>
 struct Layout {
-    static constexpr int X_BYTES = BN * 128;               // BN tokens x 128 K bytes (swizzled)
-    static constexpr int W_BYTES = BM * 128;               // padded: 128 rows x 8 slots of 16 bytes
-    static constexpr int WP_BYTES = BM * 64;               // packed: 128 rows x 64 bytes
-    static constexpr int A_W_BYTES = CONV ? WP_BYTES : W_BYTES;
-    static constexpr int B_SLOTS = CONV ? PSTAGES : 0;
-    static constexpr int SF_SLOTS = CONV ? PSTAGES : STAGES;  // TMEM scale slots (4 columns each)
+    static constexpr int W_TILE = BM * 128;             // one padded weight k-tile
+    static constexpr int X_TILE = BN * 128;             // one activation k-tile (swizzled)
+    static constexpr int W_SLOT = KPU * W_TILE;
+    static constexpr int X_SLOT = KPU * X_TILE;
     static constexpr int SFR_SLOTS = 2;
-    static constexpr int SFR_BYTES = BM * 16;              // 128 rows x 16 bytes = 4 k-tiles
-    static constexpr int X_OFF = 0;
-    static constexpr int AW_OFF = X_OFF + STAGES * X_BYTES;   // 1024-aligned for the swizzled form
-    static constexpr int BW_OFF = AW_OFF + STAGES * A_W_BYTES;
-    static constexpr int SFR_OFF = BW_OFF + B_SLOTS * W_BYTES;
+    static constexpr int SFR_BYTES = BM * 16;
+    static constexpr int W_OFF = 0;
+    static constexpr int X_OFF = W_OFF + US * W_SLOT;
+    static constexpr int SFR_OFF = X_OFF + US * X_SLOT;
     static constexpr int BAR_OFF = SFR_OFF + SFR_SLOTS * SFR_BYTES;
-    static constexpr int TOTAL = BAR_OFF + 512 + 1024;  // barriers, flags, alignment slack
-    static constexpr int W_TX_BYTES = BM * 64;          // both forms count the packed bytes
+    static constexpr int TOTAL = BAR_OFF + 1024 + 1024;  // barriers, flags, alignment slack
+    static constexpr int TX_BYTES = KPU * (BM * 64 + X_TILE);  // 4-bit boxes count packed bytes
+    static constexpr int SF_SLOTS = KPU * US;           // TMEM scale slots, 4 columns each
     static constexpr int T_SFB = ACC_BUFS * BN;         // TMEM column of the unit B scales
     static constexpr int T_SFA = T_SFB + 8;             // TMEM columns of the A scales
     static constexpr int TMEM_NEED = T_SFA + 4 * SF_SLOTS;
     static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64
                                      : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
+    static_assert(4 % KPU == 0, "a ring slot lies inside one 4-k-tile unit");
     static_assert(TMEM_NEED <= 512, "tensor memory");
     static_assert(TOTAL <= 232448, "shared memory");
-    static_assert((X_BYTES % 1024) == 0 && (AW_OFF % 1024) == 0 && (BW_OFF % 1024) == 0, "alignment");
+    static_assert((X_TILE % 1024) == 0 && (X_OFF % 1024) == 0, "swizzled tiles are 1024-aligned");
 };
 
 // Record a bounded wait that ran out: the role's bit in word 0 of the status block; the first
@@ -119,33 +115,37 @@ __device__ __forceinline__ void fail(unsigned int *status, unsigned int bit, uin
 __device__ __forceinline__ long long unit_start(long long c, long long TU, int G) { return c * TU / G; }
 __device__ __forceinline__ int unit_owner(long long u, long long TU, int G) { return (int)(((u + 1) * G - 1) / TU); }
 
-// Warp-uniform bounded wait by lane 0; on a timeout or abort the warp records it and returns
-// nonzero.
+// Bounded wait by one thread that records a timeout and raises the abort flag; 0 = done.
+__device__ __forceinline__ int wait_or_fail(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                            unsigned int *status, unsigned int bit, int iter)
+{
+    const int w = tc::mbar_wait(bar, parity, abort_flag, WAIT_BUDGET);
+    if (w == 1) fail(status, bit, bar, iter);
+    if (w) *abort_flag = 1;
+    return w;
+}
+
+// Warp-uniform version: lane 0 waits, the result is broadcast.
 __device__ __forceinline__ int warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                          unsigned int *status, unsigned int bit, int iter, int lane)
 {
     int w = 0;
-    if (lane == 0) {
-        w = tc::mbar_wait(bar, parity, abort_flag, WAIT_BUDGET);
-        if (w == 1) fail(status, bit, bar, iter);
-        if (w) *abort_flag = 1;
-    }
+    if (lane == 0) w = wait_or_fail(bar, parity, abort_flag, status, bit, iter);
     return __shfl_sync(0xffffffffu, w, 0);
 }
 
-template <int BN, int STAGES, int PSTAGES, int ACC_BUFS, bool CONV>
+template <int BN, int KPU, int US, int ACC_BUFS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_sf, const Params p)
 {
-    using L = Layout<BN, STAGES, PSTAGES, ACC_BUFS, CONV>;
+    using L = Layout<BN, KPU, US, ACC_BUFS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);  // ring A landed (+ scales)
-    uint64_t *empty = full + STAGES;                                    // ring A free again
-    uint64_t *pfull = empty + STAGES;                                   // ring B converted
-    uint64_t *pempty = pfull + PSTAGES;                                 // ring B free again
-    uint64_t *sfr_full = pempty + PSTAGES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);  // ring slot landed
+    uint64_t *empty = full + US;                                        // ring slot free again
+    uint64_t *sff = empty + US;                                         // TMEM scale slot written
+    uint64_t *sfr_full = sff + L::SF_SLOTS;
     uint64_t *sfr_empty = sfr_full + L::SFR_SLOTS;
     uint64_t *acc_full = sfr_empty + L::SFR_SLOTS;
     uint64_t *acc_empty = acc_full + ACC_BUFS;
@@ -153,29 +153,25 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *last_flag = reinterpret_cast<int *>(tmem_slot + 2);
-    int *consumed = reinterpret_cast<int *>(tmem_slot + 3);
-    int *issued = reinterpret_cast<int *>(tmem_slot + 4);
+    int *consumed = reinterpret_cast<int *>(tmem_slot + 3);   // ring fills the MMA has waited for
+    int *issued = reinterpret_cast<int *>(tmem_slot + 4);     // ring fills issued
     int *sfr_issued = reinterpret_cast<int *>(tmem_slot + 5);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
     const long long u_begin = unit_start(cta, p.TU, p.G);
     const long long u_end = unit_start(cta + 1, p.TU, p.G);
+    const int n_k = (int)(4 * (u_end - u_begin));  // k-tiles this CTA processes
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            // producer expect_tx + 4 scale warps (which also convert, when CONV)
-            tc::mbar_init(&full[s], CONV ? 1 : 5);
-            // MMA commit (+ the 4 converter warps done with the packed tile, when CONV)
-            tc::mbar_init(&empty[s], CONV ? 5 : 1);
+        for (int s = 0; s < US; ++s) {
+            tc::mbar_init(&full[s], 1);   // producer expect_tx
+            tc::mbar_init(&empty[s], 1);  // tcgen05.commit after the slot's last MMAs
         }
-        for (int s = 0; s < PSTAGES; ++s) {
-            tc::mbar_init(&pfull[s], 4);   // one arrival per converter warp
-            tc::mbar_init(&pempty[s], 1);  // tcgen05.commit of the k-tile's MMAs
-        }
+        for (int s = 0; s < L::SF_SLOTS; ++s) tc::mbar_init(&sff[s], 4);  // one arrival per scale warp
         for (int r = 0; r < L::SFR_SLOTS; ++r) {
             tc::mbar_init(&sfr_full[r], 1);
-            tc::mbar_init(&sfr_empty[r], 4);  // one arrival per scale warp
+            tc::mbar_init(&sfr_empty[r], 4);
         }
         for (int b = 0; b < ACC_BUFS; ++b) {
             tc::mbar_init(&acc_full[b], 1);   // tcgen05.commit after a tile's last MMA
@@ -214,36 +210,28 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int i = 0, g = 0;
-            for (long long u = u_begin; u < u_end && !*abort_flag; ++u, ++g) {
-                const int t = (int)(u / p.U), ku = (int)(u - (long long)t * p.U);
+            for (int i = 0; i < n_k && !*abort_flag; i += KPU) {
+                const long long u = u_begin + i / 4;
+                const int t = (int)(u / p.U);
+                const int kt = (int)(u - (long long)t * p.U) * 4 + (i & 3);  // first k-tile of the fill
                 const int n0 = (t / p.m_tiles) * BM, m0 = (t % p.m_tiles) * BN;
-                const int rs = g % L::SFR_SLOTS;
-                int w = tc::mbar_wait(&sfr_empty[rs], ((g / L::SFR_SLOTS) & 1) ^ 1, abort_flag, WAIT_BUDGET);
-                if (w) {
-                    if (w == 1) fail(p.status, ST_TIMEOUT_PRODUCER, &sfr_empty[rs], g);
-                    *abort_flag = 1;
-                    break;
-                }
-                tc::mbar_arrive_expect_tx(&sfr_full[rs], L::SFR_BYTES);
-                tc::tma_load_2d(smem + L::SFR_OFF + rs * L::SFR_BYTES, &tmap_sf, &sfr_full[rs], 16 * ku, n0);
-                *sfr_issued = g + 1;
-                for (int j = 0; j < 4; ++j, ++i) {
-                    const int s = i % STAGES;
-                    w = tc::mbar_wait(&empty[s], ((i / STAGES) & 1) ^ 1, abort_flag, WAIT_BUDGET);
-                    if (w) {
-                        if (w == 1) fail(p.status, ST_TIMEOUT_PRODUCER, &empty[s], i);
-                        *abort_flag = 1;
+                if ((i & 3) == 0) {
+                    const int g = i >> 2, rs = g % L::SFR_SLOTS;
+                    if (wait_or_fail(&sfr_empty[rs], ((g / L::SFR_SLOTS) & 1) ^ 1, abort_flag, p.status,
+                                     ST_TIMEOUT_PRODUCER, g))
                         break;
-                    }
-                    tc::mbar_arrive_expect_tx(&full[s], L::W_TX_BYTES + L::X_BYTES);
-                    const int k = (4 * ku + j) * BK;
-                    // weights: element coordinate k in the 4-bit map, byte coordinate k/2 in the byte map
-                    tc::tma_load_2d(smem + L::AW_OFF + s * L::A_W_BYTES, &tmap_w, &full[s], CONV ? k / 2 : k, n0);
-                    tc::tma_load_2d(smem + L::X_OFF + s * L::X_BYTES, &tmap_x, &full[s], k, m0);
-                    *issued = i + 1;
-                    trace_ev(p, TR_TMA_ISSUED, i);
+                    tc::mbar_arrive_expect_tx(&sfr_full[rs], L::SFR_BYTES);
+                    tc::tma_load_2d(smem + L::SFR_OFF + rs * L::SFR_BYTES, &tmap_sf, &sfr_full[rs], 4 * kt, n0);
+                    *sfr_issued = g + 1;
                 }
+                const int f = i / KPU, sl = f % US;
+                if (wait_or_fail(&empty[sl], ((f / US) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, i))
+                    break;
+                tc::mbar_arrive_expect_tx(&full[sl], L::TX_BYTES);
+                tc::tma_load_3d(smem + L::W_OFF + sl * L::W_SLOT, &tmap_w, &full[sl], 0, n0, kt);
+                tc::tma_load_3d(smem + L::X_OFF + sl * L::X_SLOT, &tmap_x, &full[sl], 0, m0, kt);
+                *issued = f + 1;
+                trace_ev(p, TR_TMA_ISSUED, i);
             }
         }
         __syncwarp();
@@ -251,38 +239,32 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             tc::tc_fence_after();
-            int i = 0, seg = 0;
+            int i = 0, seg = 0, w = 0;
             long long u = u_begin;
-            while (u < u_end && !*abort_flag) {
+            while (u < u_end && !w) {
                 const int t = (int)(u / p.U);
                 const long long ue = min(u_end, (long long)(t + 1) * p.U);
                 const int b = seg % ACC_BUFS;
-                int w = tc::mbar_wait(&acc_empty[b], ((seg / ACC_BUFS) & 1) ^ 1, abort_flag, WAIT_BUDGET);
-                if (w) {
-                    if (w == 1) fail(p.status, ST_TIMEOUT_MMA, &acc_empty[b], seg);
-                    *abort_flag = 1;
+                if ((w = wait_or_fail(&acc_empty[b], ((seg / ACC_BUFS) & 1) ^ 1, abort_flag, p.status,
+                                      ST_TIMEOUT_MMA, seg)))
                     break;
-                }
                 tc::tc_fence_after();
                 const uint32_t t_acc = tmem + b * BN;
-                bool first = true;
-                for (long long k4 = 4 * (ue - u); k4 > 0; --k4, ++i) {
-                    const int s = i % STAGES, ps = i % PSTAGES;
-                    w = tc::mbar_wait(&full[s], (i / STAGES) & 1, abort_flag, WAIT_BUDGET);
-                    if (CONV && !w) w = tc::mbar_wait(&pfull[ps], (i / PSTAGES) & 1, abort_flag, WAIT_BUDGET);
-                    if (w) {
-                        if (w == 1) fail(p.status, ST_TIMEOUT_MMA, &full[s], i);
-                        *abort_flag = 1;
-                        break;
+                const int i_end = i + (int)(4 * (ue - u));
+                for (bool first = true; i < i_end; ++i, first = false) {
+                    const int f = i / KPU, sl = f % US, j = i % KPU, sfs = i % L::SF_SLOTS;
+                    if (j == 0) {
+                        if ((w = wait_or_fail(&full[sl], (f / US) & 1, abort_flag, p.status, ST_TIMEOUT_MMA, i)))
+                            break;
+                        *consumed = f + 1;
                     }
-                    *consumed = i + 1;
+                    if ((w = wait_or_fail(&sff[sfs], (i / L::SF_SLOTS) & 1, abort_flag, p.status, ST_TIMEOUT_MMA, i)))
+                        break;
                     trace_ev(p, TR_MMA_READY, i);
                     tc::tc_fence_after();
-                    const int sfs = CONV ? ps : s;
                     const uint32_t sfa = tmem + L::T_SFA + 4 * sfs;
-                    const uint32_t wa = CONV ? tc::smem_u32(smem + L::BW_OFF + ps * L::W_BYTES)
-                                             : tc::smem_u32(smem + L::AW_OFF + s * L::W_BYTES);
-                    const uint32_t xa = tc::smem_u32(smem + L::X_OFF + s * L::X_BYTES);
+                    const uint32_t wa = tc::smem_u32(smem + L::W_OFF + sl * L::W_SLOT + j * L::W_TILE);
+                    const uint32_t xa = tc::smem_u32(smem + L::X_OFF + sl * L::X_SLOT + j * L::X_TILE);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t ad = tc::smem_desc(wa + 32 * kk, 16, 1024, 2);
@@ -290,9 +272,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                         tc::mma_mxf8f6f4(t_acc, ad, bd, tc::idesc_mxf8f6f4(5, 0, BM, BN, kk, 0), sfa,
                                          tmem + L::T_SFB, (first && kk == 0) ? 0u : 1u);
                     }
-                    first = false;
-                    tc::tc_commit(&empty[s]);
-                    if (CONV) tc::tc_commit(&pempty[ps]);
+                    if (j == KPU - 1) tc::tc_commit(&empty[sl]);
                     trace_ev(p, TR_MMA_ISSUED, i);
                 }
                 if (w) break;
@@ -305,62 +285,34 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         __syncwarp();
     } else if (warp < EPI_WARP0) {
         // ------------------------------------------------------------ scale warps (2-5)
-        // Each warp owns the TMEM lane quarter q = warp & 3 (weight rows 32q..32q+31) and writes
-        // its rows' 4-byte scale word, repeated over the slot's 4 columns, with tcgen05.st.
-        // With CONV they also pad the packed weight tile:
-        //   packed row r, 16-code chunk c at byte 64r + 8c  ->  padded row r at 128r (rows in
-        //   1024-byte groups of 8), chunk c in 16-byte slot c ^ (r & 7), low 8 bytes, zero pad.
+        // Warp w owns TMEM lanes 32q..32q+31, q = w & 3 (weight rows 32q..32q+31).  For k-tile i
+        // it writes its rows' 4-byte scale word (the 4 k-block scales of that k-tile) into the 4
+        // columns of TMEM scale slot i % SF_SLOTS.  That slot was last read by the MMAs of k-tile
+        // i - SF_SLOTS, which sit in the same ring slot one fill earlier; the producer refilled
+        // the ring slot only after those MMAs finished, so waiting for the fill covers it.
         const int q = warp & 3;
         const int row = 32 * q + lane;
-        const int ct = threadIdx.x - CONV_WARP0 * 32;  // 0..127 (converter thread)
-        int i = 0, g = 0;
         int w = 0;
-        for (long long u = u_begin; u < u_end && !w; ++u, ++g) {
-            const int rs = g % L::SFR_SLOTS;
-            w = warp_wait(&sfr_full[rs], (g / L::SFR_SLOTS) & 1, abort_flag, p.status, ST_TIMEOUT_CONV, g, lane);
-            if (w) break;
-            const uint8_t *raw = smem + L::SFR_OFF + rs * L::SFR_BYTES;
-            for (int j = 0; j < 4; ++j, ++i) {
-                const int s = i % STAGES, ps = i % PSTAGES;
-                if (CONV) {
-                    w = warp_wait(&full[s], (i / STAGES) & 1, abort_flag, p.status, ST_TIMEOUT_CONV, i, lane);
-                    if (!w) w = warp_wait(&pempty[ps], ((i / PSTAGES) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_CONV, i, lane);
-                } else {
-                    // the scale slot is free once the MMAs that last read it (k-tile i - STAGES) are done
-                    w = warp_wait(&empty[s], ((i / STAGES) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_CONV, i, lane);
-                }
-                if (w) break;
-                if (lane == 0 && warp == CONV_WARP0) trace_ev(p, TR_CONV_DATA, i);
-                if (CONV) {
-                    const uint8_t *src = smem + L::AW_OFF + s * L::WP_BYTES;
-                    uint8_t *dst = smem + L::BW_OFF + ps * L::W_BYTES;
-#pragma unroll
-                    for (int qq = 0; qq < 8; ++qq) {
-                        const int idx = ct + 128 * qq;  // (row, chunk) pair
-                        const int r = idx >> 3, c = idx & 7;
-                        const uint2 v = *reinterpret_cast<const uint2 *>(src + r * 64 + c * 8);
-                        *reinterpret_cast<uint4 *>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = make_uint4(v.x, v.y, 0u, 0u);
-                    }
-                }
-                const uint32_t sw = *reinterpret_cast<const uint32_t *>(raw + row * 16 + 4 * j);
-                const int sfs = CONV ? ps : s;
-                tc::tmem_st4(tmem + L::T_SFA + 4 * sfs + ((32u * q) << 16), sw, sw, sw, sw);
-                tc::tmem_st_wait();
-                if (CONV) tc::fence_proxy_async_smem();
-                tc::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    if (CONV) {
-                        tc::mbar_arrive(&pfull[ps]);
-                        tc::mbar_arrive(&empty[s]);  // the packed tile is no longer needed
-                    } else {
-                        tc::mbar_arrive(&full[s]);
-                    }
-                    if (warp == CONV_WARP0) trace_ev(p, TR_CONV_DONE, i);
-                }
+        for (int i = 0; i < n_k && !w; ++i) {
+            const int g = i >> 2, rs = g % L::SFR_SLOTS;
+            if ((i & 3) == 0 &&
+                (w = warp_wait(&sfr_full[rs], (g / L::SFR_SLOTS) & 1, abort_flag, p.status, ST_TIMEOUT_SCALE, g, lane)))
+                break;
+            const int f = i / KPU, sl = f % US, sfs = i % L::SF_SLOTS;
+            if (i % KPU == 0 &&
+                (w = warp_wait(&full[sl], (f / US) & 1, abort_flag, p.status, ST_TIMEOUT_SCALE, i, lane)))
+                break;
+            if (lane == 0 && warp == SCALE_WARP0) trace_ev(p, TR_SCALE_DATA, i);
+            const uint32_t sw = *reinterpret_cast<const uint32_t *>(smem + L::SFR_OFF + rs * L::SFR_BYTES + row * 16 + 4 * (i & 3));
+            tc::tmem_st4(tmem + L::T_SFA + 4 * sfs + ((32u * q) << 16), sw, sw, sw, sw);
+            tc::tmem_st_wait();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(&sff[sfs]);
+                if ((i & 3) == 3) tc::mbar_arrive(&sfr_empty[rs]);
+                if (warp == SCALE_WARP0) trace_ev(p, TR_SCALE_DONE, i);
             }
-            if (w) break;
-            if (lane == 0) tc::mbar_arrive(&sfr_empty[rs]);
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -468,14 +420,15 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         }
     }
 
+
     tc::tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0) {
         int zero = 0;
         if (*abort_flag) {
-            // drain: TMA copies issued but not consumed
-            for (int i = *consumed; i < *issued; ++i)
-                if (tc::mbar_wait(&full[i % STAGES], (i / STAGES) & 1, &zero, DRAIN_BUDGET)) break;
+            // drain: TMA copies issued but not waited for
+            for (int f = *consumed; f < *issued; ++f)
+                if (tc::mbar_wait(&full[f % US], (f / US) & 1, &zero, DRAIN_BUDGET)) break;
             for (int g = max(0, *sfr_issued - L::SFR_SLOTS); g < *sfr_issued; ++g)
                 tc::mbar_wait(&sfr_full[g % L::SFR_SLOTS], (g / L::SFR_SLOTS) & 1, &zero, DRAIN_BUDGET);
         }
@@ -518,22 +471,20 @@ size_t workspace_for(const Cfg &c)
     return partial_bytes(c) + (size_t)c.m_tiles * c.n_tiles * 4;
 }
 
-template <int BN, int STAGES, int PSTAGES, int ACC_BUFS, bool CONV>
+template <int BN, int KPU, int US, int ACC_BUFS>
 w4a8_status launch(const uint8_t *wp, const uint8_t *xq, const Params &prm, cudaStream_t stream)
 {
-    using L = Layout<BN, STAGES, PSTAGES, ACC_BUFS, CONV>;
+    using L = Layout<BN, KPU, US, ACC_BUFS>;
     CUtensorMap tw, tx, tsf;
-    const bool wmap = CONV ? tch::tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wp, prm.N, prm.K / 2, prm.K / 2, BM,
-                                          64, CU_TENSOR_MAP_SWIZZLE_NONE)
-                           : tch::tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wp, prm.N, prm.K, prm.K / 2,
-                                          BM, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (!wmap ||
-        !tch::tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, prm.M, prm.K, prm.K, BN, 128,
-                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+    // 3-D views [k-tile][row][128 K]: weights (4-bit codes; a row is K/2 bytes, a k-tile 64) and
+    // activations (bytes; a row is K bytes, a k-tile 128)
+    if (!tch::tmap_3d_ktiles(&tw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wp, prm.N, prm.K / 2, 64, prm.K / 128, BM,
+                             KPU) ||
+        !tch::tmap_3d_ktiles(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, prm.M, prm.K, 128, prm.K / 128, BN, KPU) ||
         !tch::tmap_2d(&tsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, prm.we, prm.N, prm.K / 32, prm.K / 32, BM, 16,
                       CU_TENSOR_MAP_SWIZZLE_NONE))
         return W4A8_ERR_CUDA;
-    auto kern = mxfp4_tc_kernel<BN, STAGES, PSTAGES, ACC_BUFS, CONV>;
+    auto kern = mxfp4_tc_kernel<BN, KPU, US, ACC_BUFS>;
     static int attr_done[64] = {0};
     if (!tch::set_smem_once(kern, L::TOTAL, attr_done)) return W4A8_ERR_CUDA;
     kern<<<prm.G, NUM_THREADS, L::TOTAL, stream>>>(tw, tx, tsf, prm);
@@ -585,21 +536,12 @@ w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const 
     prm.TU = c.TU;
     prm.G = c.G;
     prm.trace = static_cast<unsigned long long *>(w4a8_debug_trace_ptr());
-    if (w4a8_gemm_policy() == 3) {  // converter variant (diagnostics)
-        switch (c.BN) {
-        case 16: return launch<16, 12, 3, 2, true>(wp, xq, prm, stream);
-        case 32: return launch<32, 12, 3, 2, true>(wp, xq, prm, stream);
-        case 64: return launch<64, 10, 3, 2, true>(wp, xq, prm, stream);
-        case 128: return launch<128, 6, 3, 2, true>(wp, xq, prm, stream);
-        default: return launch<256, 4, 2, 1, true>(wp, xq, prm, stream);
-        }
-    }
     switch (c.BN) {
-    case 16: return launch<16, 12, 1, 2, false>(wp, xq, prm, stream);
-    case 32: return launch<32, 10, 1, 2, false>(wp, xq, prm, stream);
-    case 64: return launch<64, 8, 1, 2, false>(wp, xq, prm, stream);
-    case 128: return launch<128, 6, 1, 2, false>(wp, xq, prm, stream);
-    default: return launch<256, 4, 1, 1, false>(wp, xq, prm, stream);
+    case 16: return launch<16, 4, 3, 2>(wp, xq, prm, stream);
+    case 32: return launch<32, 4, 2, 2>(wp, xq, prm, stream);
+    case 64: return launch<64, 4, 2, 2>(wp, xq, prm, stream);
+    case 128: return launch<128, 2, 3, 2>(wp, xq, prm, stream);
+    default: return launch<256, 2, 2, 1>(wp, xq, prm, stream);
     }
 }
 

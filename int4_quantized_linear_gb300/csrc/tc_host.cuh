@@ -38,6 +38,24 @@ inline bool tmap_2d(CUtensorMap *m, CUtensorMapDataType type, const void *base, 
                swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D tensor map over a row-major [rows, row_bytes] array viewed as [k-tile][row][128 elements]:
+// dim 0 = the 128 elements of a k-tile (4- or 8-bit), dim 1 = rows (stride row_bytes), dim 2 =
+// k-tiles (stride ktile_bytes).  Box = 128 elements x box_rows x box_ktiles, 128-byte swizzle.
+inline bool tmap_3d_ktiles(CUtensorMap *m, CUtensorMapDataType type, const void *base, uint64_t rows,
+                           uint64_t row_bytes, uint64_t ktile_bytes, uint64_t ktiles, uint32_t box_rows,
+                           uint32_t box_ktiles)
+{
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {128, (cuuint64_t)rows, (cuuint64_t)ktiles};
+    cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)ktile_bytes};
+    cuuint32_t box[3] = {128, box_rows, box_ktiles};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, type, 3, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline int num_sms()
 {
     static int cache[64] = {0};

@@ -264,8 +264,9 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                         warp_wait(&sff[sfs], (i / L::SF_SLOTS) & 1, abort_flag, p.status, ST_TIMEOUT_GATE, i, lane);
                     if (lane == 0) trace_ev(p, TR_MMA_READY, i);
                 }
-                tc::named_bar_sync(GATE_BARRIER, 64);
-                if (!gate && lane == 0 && !*abort_flag) {
+                // the gate's abort state rides on the barrier: the MMA thread reads no memory here
+                const bool aborted = tc::named_bar_or(GATE_BARRIER, 64, gate && *abort_flag);
+                if (!gate && lane == 0 && !aborted) {
                     tc::tc_fence_after();
                     const uint32_t sfa = tmem + L::T_SFA + 4 * sfs;
                     const uint32_t wa = tc::smem_u32(smem + L::W_OFF + sl * L::W_SLOT + j * L::W_TILE);

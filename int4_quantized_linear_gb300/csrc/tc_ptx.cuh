@@ -217,6 +217,18 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Named barrier that also ORs a predicate over the participating threads (no memory access).
+__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool cond)
+{
+    uint32_t r;
+    asm volatile(
+        "{ .reg .pred p, q; setp.ne.u32 p, %3, 0; barrier.red.or.pred q, %1, %2, p; selp.u32 %0, 1, 0, q; }"
+        : "=r"(r)
+        : "r"(id), "r"(nthreads), "r"((uint32_t)cond)
+        : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -150,8 +150,8 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);  // ring slot landed
     uint64_t *empty = full + US;                                        // ring slot free again
-    uint64_t *sff = empty + US;                                         // TMEM scale slot written
-    uint64_t *sfr_full = sff + L::SF_SLOTS;
+    uint64_t *sff = empty + US;                                         // fill's scales in TMEM
+    uint64_t *sfr_full = sff + US;
     uint64_t *sfr_empty = sfr_full + L::SFR_SLOTS;
     uint64_t *acc_full = sfr_empty + L::SFR_SLOTS;
     uint64_t *acc_empty = acc_full + ACC_BUFS;
@@ -173,7 +173,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             tc::mbar_init(&full[s], 1);   // producer expect_tx
             tc::mbar_init(&empty[s], 1);  // tcgen05.commit after the slot's last MMAs
         }
-        for (int s = 0; s < L::SF_SLOTS; ++s) tc::mbar_init(&sff[s], 4);  // one arrival per scale warp
+        for (int s = 0; s < US; ++s) tc::mbar_init(&sff[s], 4);  // one arrival per scale warp
         for (int r = 0; r < L::SFR_SLOTS; ++r) {
             tc::mbar_init(&sfr_full[r], 1);
             tc::mbar_init(&sfr_empty[r], 4);
@@ -241,45 +241,49 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         __syncwarp();
     } else if (warp == 1 || warp == GATE_WARP) {
         // ------------------------------------------------------------ MMA issuer and its gate
-        // Both warps walk the same k-tile sequence and meet at the named barrier once per k-tile
-        // (also after an abort, so neither can be left waiting there).  The gate first waits for
-        // the k-tile's scales -- written after its data landed -- and, at the first k-tile of a
-        // tile, for the accumulator buffer; the MMA warp then issues without touching memory.
+        // Both warps walk the same sequence of ring fills (KPU k-tiles each) and meet at the named
+        // barrier once per fill (also after an abort, so neither can be left waiting there).  The
+        // gate first waits for the fill's scales -- written after its data landed -- and, at the
+        // first fill of a tile, for the accumulator buffer; the MMA warp then issues the fill's
+        // 4 x KPU MMAs without touching memory.
         const bool gate = (warp == GATE_WARP);
         if (!gate) tc::tc_fence_after();
-        int i = 0, seg = 0;
+        int f = 0, seg = 0;
         long long u = u_begin;
         while (u < u_end) {
             const int t = (int)(u / p.U);
             const long long ue = min(u_end, (long long)(t + 1) * p.U);
             const int b = seg % ACC_BUFS;
             const uint32_t t_acc = tmem + b * BN;
-            const int i_end = i + (int)(4 * (ue - u));
-            for (bool first = true; i < i_end; ++i, first = false) {
-                const int f = i / KPU, sl = f % US, j = i % KPU, sfs = i % L::SF_SLOTS;
+            const int f_end = f + (int)(4 * (ue - u)) / KPU;
+            for (bool first = true; f < f_end; ++f, first = false) {
+                const int sl = f % US;
                 if (gate) {
                     if (!*abort_flag && first)
                         warp_wait(&acc_empty[b], ((seg / ACC_BUFS) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_GATE, seg, lane);
                     if (!*abort_flag)
-                        warp_wait(&sff[sfs], (i / L::SF_SLOTS) & 1, abort_flag, p.status, ST_TIMEOUT_GATE, i, lane);
-                    if (lane == 0) trace_ev(p, TR_MMA_READY, i);
+                        warp_wait(&sff[sl], (f / US) & 1, abort_flag, p.status, ST_TIMEOUT_GATE, f, lane);
+                    if (lane == 0) trace_ev(p, TR_MMA_READY, f);
                 }
                 // the gate's abort state rides on the barrier: the MMA thread reads no memory here
                 const bool aborted = tc::named_bar_or(GATE_BARRIER, 64, gate && *abort_flag);
                 if (!gate && lane == 0 && !aborted) {
                     tc::tc_fence_after();
-                    const uint32_t sfa = tmem + L::T_SFA + 4 * sfs;
-                    const uint32_t wa = tc::smem_u32(smem + L::W_OFF + sl * L::W_SLOT + j * L::W_TILE);
-                    const uint32_t xa = tc::smem_u32(smem + L::X_OFF + sl * L::X_SLOT + j * L::X_TILE);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = tc::smem_desc(wa + 32 * kk, 16, 1024, 2);
-                        const uint64_t bd = tc::smem_desc(xa + 32 * kk, 16, 1024, 2);
-                        tc::mma_mxf8f6f4(t_acc, ad, bd, tc::idesc_mxf8f6f4(5, 0, BM, BN, kk, 0), sfa,
-                                         tmem + L::T_SFB, (first && kk == 0) ? 0u : 1u);
+                    for (int j = 0; j < KPU; ++j) {
+                        const uint32_t sfa = tmem + L::T_SFA + 4 * (sl * KPU + j);
+                        const uint32_t wa = tc::smem_u32(smem + L::W_OFF + sl * L::W_SLOT + j * L::W_TILE);
+                        const uint32_t xa = tc::smem_u32(smem + L::X_OFF + sl * L::X_SLOT + j * L::X_TILE);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t ad = tc::smem_desc(wa + 32 * kk, 16, 1024, 2);
+                            const uint64_t bd = tc::smem_desc(xa + 32 * kk, 16, 1024, 2);
+                            tc::mma_mxf8f6f4(t_acc, ad, bd, tc::idesc_mxf8f6f4(5, 0, BM, BN, kk, 0), sfa,
+                                             tmem + L::T_SFB, (first && j == 0 && kk == 0) ? 0u : 1u);
+                        }
                     }
-                    if (j == KPU - 1) tc::tc_commit(&empty[sl]);
-                    if (i_end - i == 1) tc::tc_commit(&acc_full[b]);
+                    tc::tc_commit(&empty[sl]);
+                    if (f_end - f == 1) tc::tc_commit(&acc_full[b]);
                 }
                 __syncwarp();
             }
@@ -290,33 +294,36 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         __syncwarp();
     } else if (warp < EPI_WARP0) {
         // ------------------------------------------------------------ scale warps (2-5)
-        // Warp w owns TMEM lanes 32q..32q+31, q = w & 3 (weight rows 32q..32q+31).  For k-tile i
-        // it writes its rows' 4-byte scale word (the 4 k-block scales of that k-tile) into the 4
-        // columns of TMEM scale slot i % SF_SLOTS.  That slot was last read by the MMAs of k-tile
-        // i - SF_SLOTS, which sit in the same ring slot one fill earlier; the producer refilled
-        // the ring slot only after those MMAs finished, so waiting for the fill covers it.
+        // Warp w owns TMEM lanes 32q..32q+31, q = w & 3 (weight rows 32q..32q+31).  For each
+        // k-tile of a ring fill it writes its rows' 4-byte scale word (the 4 k-block scales of
+        // that k-tile) into the 4 columns of the fill's TMEM scale slot.  Those columns were last
+        // read by the MMAs of the previous fill of the same ring slot; the producer refilled the
+        // ring slot only after those MMAs finished, so waiting for the fill covers it.
         const int q = warp & 3;
         const int row = 32 * q + lane;
         int w = 0;
-        for (int i = 0; i < n_k && !w; ++i) {
+        for (int i = 0; i < n_k && !w; i += KPU) {
             const int g = i >> 2, rs = g % L::SFR_SLOTS;
             if ((i & 3) == 0 &&
                 (w = warp_wait(&sfr_full[rs], (g / L::SFR_SLOTS) & 1, abort_flag, p.status, ST_TIMEOUT_SCALE, g, lane)))
                 break;
-            const int f = i / KPU, sl = f % US, sfs = i % L::SF_SLOTS;
-            if (i % KPU == 0 &&
-                (w = warp_wait(&full[sl], (f / US) & 1, abort_flag, p.status, ST_TIMEOUT_SCALE, i, lane)))
+            const int f = i / KPU, sl = f % US;
+            if ((w = warp_wait(&full[sl], (f / US) & 1, abort_flag, p.status, ST_TIMEOUT_SCALE, f, lane)))
                 break;
-            if (lane == 0 && warp == SCALE_WARP0) trace_ev(p, TR_SCALE_DATA, i);
-            const uint32_t sw = *reinterpret_cast<const uint32_t *>(smem + L::SFR_OFF + rs * L::SFR_BYTES + row * 16 + 4 * (i & 3));
-            tc::tmem_st4(tmem + L::T_SFA + 4 * sfs + ((32u * q) << 16), sw, sw, sw, sw);
+            if (lane == 0 && warp == SCALE_WARP0) trace_ev(p, TR_SCALE_DATA, f);
+            const uint8_t *raw = smem + L::SFR_OFF + rs * L::SFR_BYTES + row * 16;
+#pragma unroll
+            for (int j = 0; j < KPU; ++j) {
+                const uint32_t sw = *reinterpret_cast<const uint32_t *>(raw + 4 * ((i & 3) + j));
+                tc::tmem_st4(tmem + L::T_SFA + 4 * (sl * KPU + j) + ((32u * q) << 16), sw, sw, sw, sw);
+            }
             tc::tmem_st_wait();
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                tc::mbar_arrive(&sff[sfs]);
-                if ((i & 3) == 3) tc::mbar_arrive(&sfr_empty[rs]);
-                if (warp == SCALE_WARP0) trace_ev(p, TR_SCALE_DONE, i);
+                tc::mbar_arrive(&sff[sl]);
+                if (((i + KPU) & 3) == 0) tc::mbar_arrive(&sfr_empty[rs]);
+                if (warp == SCALE_WARP0) trace_ev(p, TR_SCALE_DONE, f);
             }
         }
     } else {

@@ -57,10 +57,13 @@ __device__ __forceinline__ int mbar_wait(uint64_t *bar, uint32_t parity, volatil
 {
     if (mbar_try_wait(bar, parity)) return 0;
     const long long t0 = clock64();
+    unsigned int nap = 32;  // back off so idle pollers leave shared memory to the tensor core
     while (true) {
         if (mbar_try_wait(bar, parity)) return 0;
         if (*abort) return 2;
         if (clock64() - t0 > budget) return 1;
+        __nanosleep(nap);
+        if (nap < 256) nap <<= 1;
     }
 }
 

@@ -147,10 +147,11 @@ W4A8_API w4a8_status w4a8_check_device_status(cudaStream_t stream);
  * event) and clears it.  Returns a w4a8_status value. */
 W4A8_API int w4a8_debug_status_words(unsigned int *out4);
 
-/* Diagnostic: while device_buffer (device, 6 x 256 uint64, or NULL to stop) is set, the
- * tensor-core MXFP4 GEMM's first CTA records clock64() stamps of its pipeline events for its
- * first 256 k-tiles: TMA issued, packed tile landed, tile converted, MMA ready, MMAs issued,
- * ring slot freed (rows 0-5).  Process-wide; for performance investigation only. */
+/* Diagnostic: while device_buffer (device, 6 x 256 + 4 x 512 uint64, or NULL to stop) is set,
+ * the tensor-core MXFP4 GEMM records, for its first CTA, clock64() stamps of pipeline events
+ * (rows of 256: TMA fill issued, scale data seen, scales written, MMA released), and for every
+ * CTA (up to 512) global-timer stamps of entry, set-up done, epilogue done and exit.
+ * Process-wide; for performance investigation only. */
 W4A8_API void w4a8_debug_set_trace(void *device_buffer);
 
 /* Decode-band threshold: M <= this takes the decode tiling (64). */

@@ -75,6 +75,17 @@ __device__ __forceinline__ void trace_ev(const Params &p, int ev, int i)
 {
     if (p.trace != nullptr && blockIdx.x == 0 && i < TRACE_N) p.trace[ev * TRACE_N + i] = (unsigned long long)clock64();
 }
+// Phase stamps (global timer, ns) of every CTA (up to 512): entry, set-up done, epilogue done,
+// exit (k = 0..3), and for the last tile the epilogue's accumulator ready, partial stored,
+// arrival counted, fix-up done (k = 4..7); at [TR_EVENTS * TRACE_N + 8 * cta + k].
+__device__ __forceinline__ void trace_phase(const Params &p, int k)
+{
+    if (p.trace != nullptr && blockIdx.x < 512) {
+        unsigned long long ns;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(ns));
+        p.trace[TR_EVENTS * TRACE_N + 8 * blockIdx.x + k] = ns;
+    }
+}
 
 // Shared memory: a ring of US slots, each holding KPU k-tiles of padded weights (16 KB each)
 // and activations (BN x 128 bytes each), plus a ring of 2 raw scale tiles (4 k-tiles each).
@@ -167,6 +178,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     const long long u_begin = unit_start(cta, p.TU, p.G);
     const long long u_end = unit_start(cta + 1, p.TU, p.G);
     const int n_k = (int)(4 * (u_end - u_begin));  // k-tiles this CTA processes
+    if (threadIdx.x == 0) trace_phase(p, 0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < US; ++s) {
@@ -210,6 +222,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     }
     tc::tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) trace_phase(p, 1);
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -349,6 +362,8 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 break;
             }
             tc::tc_fence_after();
+            const bool last_seg = (ue == u_end);
+            if (last_seg && threadIdx.x == EPI_WARP0 * 32) trace_phase(p, 4);
             const int n0 = (t / p.m_tiles) * BM, m0 = (t % p.m_tiles) * BN;
             const int row = 32 * q + lane;
             const int n = n0 + row;
@@ -379,6 +394,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 // stream-K fix-up: the last contributor of tile t adds the partials in CTA order
                 const int c_first = unit_owner(t_lo, p.TU, p.G);
                 const int c_last = unit_owner(t_hi - 1, p.TU, p.G);
+                if (last_seg && threadIdx.x == EPI_WARP0 * 32) trace_phase(p, 5);
                 __threadfence();
                 tc::named_bar_sync(1, 128);
                 if (threadIdx.x == EPI_WARP0 * 32) {
@@ -386,6 +402,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                     *last_flag = (old == c_last - c_first);
                 }
                 tc::named_bar_sync(1, 128);
+                if (last_seg && threadIdx.x == EPI_WARP0 * 32) trace_phase(p, 6);
                 if (*last_flag) {
                     __threadfence();
                     // 16 columns at a time, up to 4 contributors' loads in flight together; the
@@ -426,10 +443,12 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                     if (threadIdx.x == EPI_WARP0 * 32) p.counters[t] = 0;
                 }
                 tc::named_bar_sync(1, 128);  // last_flag is reused by the next tile
+                if (last_seg && threadIdx.x == EPI_WARP0 * 32) trace_phase(p, 7);
             }
             ++seg;
             u = ue;
         }
+        if (threadIdx.x == EPI_WARP0 * 32) trace_phase(p, 2);
     }
 
 
@@ -451,6 +470,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, L::TMEM_COLS);
     }
+    if (threadIdx.x == 0) trace_phase(p, 3);
 }
 
 // ------------------------------------------------------------------------------- host side

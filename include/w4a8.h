@@ -87,6 +87,28 @@ W4A8_API w4a8_status w4a8_mxfp4_linear(const uint8_t *xq, const float *x_scale, 
 /* Bytes of workspace w4a8_mxfp4_linear needs for this shape (0 if none). */
 W4A8_API size_t w4a8_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
+/* w4a8_mxfp4_linear for callers that cannot allocate device memory (no counterpart in the
+ * pages; an addition of this library).  Code being captured into a CUDA graph, serving engines
+ * that keep all device memory in their own pool, and plugin interfaces that pass only inputs and
+ * outputs have no way to supply a workspace.  This call keeps the GEMM's scratch (fp32 partial
+ * tiles and arrival counters) in a fixed array of w4a8_noalloc_scratch_bytes() bytes (12 MiB)
+ * inside the library's device image, which every GPU that loads the library holds until the
+ * process exits.  It calls no cudaMalloc or cudaFree.
+ *   Arguments, layouts and the result are those of w4a8_mxfp4_linear, minus the workspace.
+ *   Sizes whose scratch would exceed the array (larger token counts, very wide outputs) are
+ *   rejected with W4A8_ERR_WORKSPACE; w4a8_workspace_bytes(M, N, K) gives the need.
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress); make
+ *   that first call before any stream capture.  The arrival counters are cleared on the stream
+ *   at every call.  All calls share the one array: calls that can run at the same time on the
+ *   GPU (other streams, other threads) race on it and must be serialized by the caller. */
+W4A8_API w4a8_status w4a8_mxfp4_linear_noalloc(const uint8_t *xq, const float *x_scale,
+                                               const uint8_t *w_packed, const uint8_t *w_e8m0,
+                                               uint16_t *out_bf16, int64_t M, int64_t N, int64_t K,
+                                               cudaStream_t stream);
+
+/* Size in bytes of the fixed scratch array used by w4a8_mxfp4_linear_noalloc. */
+W4A8_API size_t w4a8_noalloc_scratch_bytes(void);
+
 /* NVFP4 -> MXFP4 requant of a (merged) linear ("radiance_nvfp4.py": dequant_nvfp4,
  * _block_exponent, e2m1_index, _encode_blocks, quant_mxfp4, requant_rows,
  * RadianceNvfp4ToMxfp4.process_weights_after_loading).  Per 32-block of each row n in

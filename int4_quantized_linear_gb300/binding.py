@@ -23,7 +23,8 @@ MODES = {"ocp": 0, "noclip": 1, "mse": 2}
 EXPORTS = ("w4a8_act_quant", "w4a8_mxfp4_linear", "w4a8_workspace_bytes",
            "nvfp4_to_mxfp4_requant", "w4a8_int4g128_linear", "w4a8_int4g128_workspace_bytes",
            "w4a8_status_string", "w4a8_set_gemm_policy", "w4a8_check_device_status",
-           "w4a8_decode_max_m", "w4a8_debug_status_words", "w4a8_debug_set_trace")
+           "w4a8_decode_max_m", "w4a8_debug_status_words", "w4a8_debug_set_trace",
+           "w4a8_mxfp4_linear_noalloc", "w4a8_noalloc_scratch_bytes")
 
 
 class W4A8Error(RuntimeError):
@@ -61,6 +62,8 @@ def load(build_if_missing: bool = True):
         "w4a8_decode_max_m": (I, []),
         "w4a8_debug_status_words": (I, [P]),
         "w4a8_debug_set_trace": (None, [P]),
+        "w4a8_mxfp4_linear_noalloc": (I, [P, P, P, P, P, I64, I64, I64, P]),
+        "w4a8_noalloc_scratch_bytes": (SZ, []),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -162,6 +165,20 @@ def mxfp4_linear(xq, x_scale, w_packed, w_e8m0, out=None, workspace=None, stream
     _check("w4a8_mxfp4_linear", load().w4a8_mxfp4_linear(
         _ptr(xq), _ptr(x_scale), _ptr(w_packed), _ptr(w_e8m0), _ptr(out), M, N, K,
         _ptr(workspace), wsb, _stream(stream)))
+    return out
+
+
+def mxfp4_linear_noalloc(xq, x_scale, w_packed, w_e8m0, out, stream=None):
+    """w4a8_mxfp4_linear without a workspace: the library's own fixed scratch array is used, so
+    nothing is allocated (for callers that cannot allocate; `out` must be supplied)."""
+    for t, n, d in ((xq, "xq", torch.uint8), (x_scale, "x_scale", torch.float32),
+                    (w_packed, "w_packed", torch.uint8), (w_e8m0, "w_e8m0", torch.uint8),
+                    (out, "out", torch.bfloat16)):
+        _dev(t, n, d)
+    M, K = xq.shape
+    N = w_packed.shape[0]
+    _check("w4a8_mxfp4_linear_noalloc", load().w4a8_mxfp4_linear_noalloc(
+        _ptr(xq), _ptr(x_scale), _ptr(w_packed), _ptr(w_e8m0), _ptr(out), M, N, K, _stream(stream)))
     return out
 
 

@@ -24,6 +24,7 @@ w4a8_status w4a8_launch_int4_simt(const uint8_t *xq, const float *x_scale, const
 bool w4a8_tc_mxfp4_supported(const void *xq, const void *wp, const void *we, const void *out,
                              int64_t M, int64_t N, int64_t K);
 size_t w4a8_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int policy);
+size_t w4a8_tc_workspace_counters_offset(int64_t M, int64_t N, int64_t K);
 w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const uint8_t *wp,
                                  const uint8_t *we, uint16_t *out, int64_t M, int64_t N,
                                  int64_t K, void *workspace, int policy, cudaStream_t stream);

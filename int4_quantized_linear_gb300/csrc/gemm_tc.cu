@@ -540,6 +540,11 @@ bool w4a8_tc_mxfp4_supported(const void *xq, const void *wp, const void *we, con
     return w4a8::tch::encode_fn() != nullptr;
 }
 
+size_t w4a8_tc_workspace_counters_offset(int64_t M, int64_t N, int64_t K)
+{
+    return partial_bytes(choose(M, N, K));
+}
+
 size_t w4a8_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int policy)
 {
     if (policy == 1 || K % 512 != 0 || K <= 0 || M <= 0 || N <= 0) return 0;

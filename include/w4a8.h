@@ -169,10 +169,12 @@ W4A8_API w4a8_status w4a8_check_device_status(cudaStream_t stream);
  * event) and clears it.  Returns a w4a8_status value. */
 W4A8_API int w4a8_debug_status_words(unsigned int *out4);
 
-/* Diagnostic: while device_buffer (device, 6 x 256 + 4 x 512 uint64, or NULL to stop) is set,
- * the tensor-core MXFP4 GEMM records, for its first CTA, clock64() stamps of pipeline events
- * (rows of 256: TMA fill issued, scale data seen, scales written, MMA released), and for every
- * CTA (up to 512) global-timer stamps of entry, set-up done, epilogue done and exit.
+/* Diagnostic: while device_buffer (device, 6 x 256 + 16 x 512 uint64, zero-filled, or NULL to
+ * stop) is set, the tensor-core MXFP4 GEMM records, for its first CTA, clock64() stamps of
+ * pipeline events (6 rows of 256: k-tile issued, scale slot free, scales written, fill released
+ * to the MMA warp, fill issued, fill's scales seen), and for every CTA (up to 512) 16 global-timer
+ * stamps (entry, set-up done, epilogue done, exit, last-tile epilogue steps, first and last fill
+ * released, MMA issue done, first accumulator ready, last-tile partials staged and summed).
  * Process-wide; for performance investigation only. */
 W4A8_API void w4a8_debug_set_trace(void *device_buffer);
 

@@ -19,6 +19,9 @@ __global__ void __launch_bounds__(AQ_THREADS)
 act_quant_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ xq,
                  float *__restrict__ x_scale, int64_t K)
 {
+    // a GEMM launched after this kernel with programmatic dependent launch may start its own
+    // set-up now; it waits for this grid to finish before it reads xq or x_scale
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t m = blockIdx.x;
     const uint4 *row = reinterpret_cast<const uint4 *>(x + m * K);
     const int nchunk = (int)(K / 8);

@@ -18,22 +18,32 @@
 //     Boxes whose rows read 4 k-tiles (256 contiguous bytes) at once run TMA at the full HBM
 //     rate on GB300, where one-k-tile boxes (64-byte rows) reach only about 60% of it;
 //   * four scale warps (one per TMEM lane quarter) write each row's 4-byte scale word, repeated
-//     over 4 columns, into tensor memory with tcgen05.st; the MMA reads one byte per k-block;
+//     over 4 columns, into a ring of tensor-memory scale slots with tcgen05.st; the MMA reads one
+//     byte per k-block.  The raw scale tiles are loaded a few units ahead of the data and a slot
+//     only waits for the MMAs that last read it, so scale work stays off the TMA -> MMA path;
 //   * persistent stream-K: one CTA per SM walks a contiguous range of (tile, 4-k-tile unit)
 //     work, so the TMA ring never drains between tiles and every SM gets the same number of
 //     units; a tile whose K range is split between CTAs is finished by the last contributor,
-//     which adds the fp32 partials in CTA order;
+//     which adds the fp32 partials in CTA order.  Each CTA takes its split tiles first, so their
+//     fix-up overlaps the whole tiles' MMAs; at the CTA's last tile the ring is idle, and bulk
+//     copies bring every contributor's partial into it in one round trip;
 //   * two accumulator buffers in tensor memory (one for 256-token tiles) let the MMAs of the next
-//     tile run while the epilogue drains the previous one;
+//     tile run while the epilogue drains the previous one; output leaves through a small shared
+//     memory staging buffer and TMA tensor stores (per-thread 2-byte stores ran at a fraction of
+//     that rate with most of the L1/shared array given to shared memory);
 //   * the MMA-issuing thread never touches shared memory inside its loop: on GB300 any shared-memory
 //     access by a thread with MMAs in flight (an mbarrier test included) waits for those MMAs to
 //     complete, which drains the tensor pipe every k-tile.  A gate warp does all the mbarrier
-//     waiting and releases the MMA warp one k-tile at a time through a hardware named barrier;
+//     waiting and releases the MMA warp one ring fill at a time through a hardware named barrier;
+//   * programmatic dependent launch: barrier set-up and tensor-memory allocation overlap the
+//     previous kernel in the stream; inputs and outputs are touched only after griddepcontrol.wait;
 //   * warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2-5 scale warps, 6-9 epilogue,
 //     10 gate (scale and epilogue warps each use the TMEM lane quarter their warp index selects).
 //
 // Every mbarrier wait is bounded; a wait that runs out sets a bit in the library's device status
 // word and the CTA winds down (draining what it started) instead of hanging.
+#include <cstring>
+
 #include "common.cuh"
 #include "dispatch.h"
 #include "tc_host.cuh"
@@ -54,6 +64,7 @@ constexpr long long DRAIN_BUDGET = 1ll << 24;
 enum : unsigned { ST_TIMEOUT_PRODUCER = 1, ST_TIMEOUT_GATE = 2, ST_TIMEOUT_SCALE = 4, ST_TIMEOUT_EPI = 8 };
 
 struct Params {
+    const uint8_t *wp;     // [N, K/2] packed e2m1 codes
     const uint8_t *we;     // [N, K/32] e8m0
     const float *xs;       // [M] per-token scale
     uint16_t *out;         // [M, N] bf16
@@ -65,45 +76,56 @@ struct Params {
     int U;                 // 4-k-tile units per tile
     long long TU;          // total units
     int G;                 // CTAs
+    int evict_first;       // weights are read once: load them with the L2 evict-first policy
+    int tma_out;           // output tiles leave through shared memory and TMA stores (else plain stores)
     unsigned long long *trace;  // optional pipeline timeline of CTA 0 (diagnostics), or null
 };
 
 // Pipeline timeline (diagnostics): CTA 0 records clock64() per k-tile i < TRACE_N for each event.
 constexpr int TRACE_N = 256;
-enum { TR_TMA_ISSUED = 0, TR_SCALE_DATA, TR_SCALE_DONE, TR_MMA_READY, TR_MMA_ISSUED, TR_UNUSED, TR_EVENTS };
+enum { TR_TMA_ISSUED = 0, TR_SCALE_DATA, TR_SCALE_DONE, TR_MMA_READY, TR_TMA_FILL, TR_GATE_SFF, TR_EVENTS };
 __device__ __forceinline__ void trace_ev(const Params &p, int ev, int i)
 {
     if (p.trace != nullptr && blockIdx.x == 0 && i < TRACE_N) p.trace[ev * TRACE_N + i] = (unsigned long long)clock64();
 }
-// Phase stamps (global timer, ns) of every CTA (up to 512): entry, set-up done, epilogue done,
-// exit (k = 0..3), and for the last tile the epilogue's accumulator ready, partial stored,
-// arrival counted, fix-up done (k = 4..7); at [TR_EVENTS * TRACE_N + 8 * cta + k].
+// Phase stamps (global timer, ns) of every CTA (up to 512), at [TR_EVENTS * TRACE_N + 16 * cta + k]:
+// k = 0 entry, 1 set-up done, 2 epilogue done, 3 exit; for the CTA's last tile the epilogue's
+// 4 accumulator ready, 5 partial stored, 6 arrival counted, 7 fix-up done; 8 first fill released
+// to the MMA warp, 9 last fill released, 10 MMA warp done issuing, 11 first accumulator ready,
+// 12 last tile's partials staged in shared memory, 13 summed and stored.
+constexpr int TRACE_PHASES = 16;
 __device__ __forceinline__ void trace_phase(const Params &p, int k)
 {
     if (p.trace != nullptr && blockIdx.x < 512) {
         unsigned long long ns;
         asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(ns));
-        p.trace[TR_EVENTS * TRACE_N + 8 * blockIdx.x + k] = ns;
+        p.trace[TR_EVENTS * TRACE_N + TRACE_PHASES * blockIdx.x + k] = ns;
     }
 }
 
 // Shared memory: a ring of US slots, each holding KPU k-tiles of padded weights (16 KB each)
-// and activations (BN x 128 bytes each), plus a ring of 2 raw scale tiles (4 k-tiles each).
-template <int BN, int KPU, int US, int ACC_BUFS>
+// and activations (BN x 128 bytes each), plus a ring of SFR raw scale tiles (4 k-tiles each).
+// Tensor memory: ACC_BUFS accumulators of BN columns, the unit B scales, and a ring of SFQ
+// scale slots (KPU k-tiles of A scales each) that the scale warps fill ahead of the data.
+template <int BN, int KPU, int US, int ACC_BUFS, int SFQ, int SFR>
 struct Layout {
     static constexpr int W_TILE = BM * 128;             // one padded weight k-tile
     static constexpr int X_TILE = BN * 128;             // one activation k-tile (swizzled)
     static constexpr int W_SLOT = KPU * W_TILE;
     static constexpr int X_SLOT = KPU * X_TILE;
-    static constexpr int SFR_SLOTS = 2;
+    static constexpr int SFR_SLOTS = SFR;
     static constexpr int SFR_BYTES = BM * 16;
     static constexpr int W_OFF = 0;
     static constexpr int X_OFF = W_OFF + US * W_SLOT;
     static constexpr int SFR_OFF = X_OFF + US * X_SLOT;
     static constexpr int BAR_OFF = SFR_OFF + SFR_SLOTS * SFR_BYTES;
-    static constexpr int TOTAL = BAR_OFF + 1024 + 1024;  // barriers, flags, alignment slack
+    static constexpr int XS_OFF = BAR_OFF + 512;        // barriers and flags below, then the tile's token scales
+    static constexpr int NSTAGE = BN == 16 ? 1 : 2;     // output staging: [16 tokens][128 rows] bf16 buffers
+    static constexpr int STAGE_BYTES = 16 * BM * 2;
+    static constexpr int STAGE_OFF = (XS_OFF + BN * 4 + 1023) / 1024 * 1024;
+    static constexpr int TOTAL = STAGE_OFF + NSTAGE * STAGE_BYTES + 1024;  // + alignment slack
     static constexpr int TX_BYTES = KPU * (BM * 64 + X_TILE);  // 4-bit boxes count packed bytes
-    static constexpr int SF_SLOTS = KPU * US;           // TMEM scale slots, 4 columns each
+    static constexpr int SF_SLOTS = KPU * SFQ;          // TMEM scale k-tile slots, 4 columns each
     static constexpr int T_SFB = ACC_BUFS * BN;         // TMEM column of the unit B scales
     static constexpr int T_SFA = T_SFB + 8;             // TMEM columns of the A scales
     static constexpr int TMEM_NEED = T_SFA + 4 * SF_SLOTS;
@@ -112,6 +134,7 @@ struct Layout {
     static_assert(4 % KPU == 0, "a ring slot lies inside one 4-k-tile unit");
     static_assert(TMEM_NEED <= 512, "tensor memory");
     static_assert(TOTAL <= 232448, "shared memory");
+    static_assert(8 * (2 * US + 2 * SFQ + 2 * SFR + 2 * ACC_BUFS + 2) + 32 <= 512, "barrier area");
     static_assert((X_TILE % 1024) == 0 && (X_OFF % 1024) == 0, "swizzled tiles are 1024-aligned");
 };
 
@@ -132,6 +155,55 @@ __device__ __forceinline__ void fail(unsigned int *status, unsigned int bit, uin
 __device__ __forceinline__ long long unit_start(long long c, long long TU, int G) { return c * TU / G; }
 __device__ __forceinline__ int unit_owner(long long u, long long TU, int G) { return (int)(((u + 1) * G - 1) / TU); }
 
+// A CTA's work is the unit range [u_begin, u_end), which touches tiles t_first..t_last; the
+// first and last of them may be split with neighbouring CTAs.  Processing order: the split
+// first tile (if split), then the split last tile (if split), then the whole tiles in between.
+// The split tiles' fix-up (partial store, arrival count, last-arrival reduction) then runs in
+// the epilogue while the MMAs of the whole tiles proceed, and the CTA ends on a direct store.
+struct Sched {
+    long long u_begin, u_end, A, L;
+    int U, t_first, t_last, S;
+    bool pf, pl;
+    __device__ Sched(long long ub, long long ue, int U_) : u_begin(ub), u_end(ue), U(U_)
+    {
+        t_first = (int)(ub / U_);
+        t_last = ue > ub ? (int)((ue - 1) / U_) : t_first - 1;
+        S = t_last - t_first + 1;
+        pf = S >= 1 && ((ub % U_) != 0 || (S == 1 && ue - ub < U_));
+        pl = S >= 2 && (ue % U_) != 0;
+        A = pf ? min(ue, (long long)(t_first + 1) * U_) - ub : 0;  // units kept in place up front
+        L = pl ? ue - (long long)t_last * U_ : 0;                   // units moved up
+    }
+    // unit processed at position p (0 <= p < u_end - u_begin)
+    __device__ long long unit_at(long long p) const
+    {
+        if (p < A) return u_begin + p;
+        if (p < A + L) return (long long)t_last * U + (p - A);
+        return u_begin + (p - L);
+    }
+    // weight tile coordinates of the ring fill that starts at k-tile position i
+    __device__ void fill_at(int i, int m_tiles, int &kt, int &n0) const
+    {
+        const long long u = unit_at(i / 4);
+        const int t = (int)(u / U);
+        kt = (int)(u - (long long)t * U) * 4 + (i & 3);
+        n0 = (t / m_tiles) * BM;
+    }
+    // tile of the k-th segment in processing order, and its unit range [a, b)
+    __device__ int seg_tile(int k) const
+    {
+        int s = k;
+        if (pl) s = pf ? (k == 0 ? 0 : (k == 1 ? S - 1 : k - 1)) : (k == 0 ? S - 1 : k - 1);
+        return t_first + s;
+    }
+    __device__ void seg_units(int k, long long &a, long long &b) const
+    {
+        const long long t = seg_tile(k);
+        a = max(u_begin, t * U);
+        b = min(u_end, (t + 1) * U);
+    }
+};
+
 // Bounded wait by one thread that records a timeout and raises the abort flag; 0 = done.
 __device__ __forceinline__ int wait_or_fail(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                             unsigned int *status, unsigned int bit, int iter)
@@ -151,33 +223,39 @@ __device__ __forceinline__ int warp_wait(uint64_t *bar, uint32_t parity, volatil
     return __shfl_sync(0xffffffffu, w, 0);
 }
 
-template <int BN, int KPU, int US, int ACC_BUFS>
+template <int BN, int KPU, int US, int ACC_BUFS, int SFQ, int SFR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
-                const __grid_constant__ CUtensorMap tmap_sf, const Params p)
+                const __grid_constant__ CUtensorMap tmap_sf, const __grid_constant__ CUtensorMap tmap_out,
+                const Params p)
 {
-    using L = Layout<BN, KPU, US, ACC_BUFS>;
+    using L = Layout<BN, KPU, US, ACC_BUFS, SFQ, SFR>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, derived by pointer arithmetic so the compiler keeps it in the shared window
+    uint8_t *smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);  // ring slot landed
     uint64_t *empty = full + US;                                        // ring slot free again
     uint64_t *sff = empty + US;                                         // fill's scales in TMEM
-    uint64_t *sfr_full = sff + US;
+    uint64_t *sfe = sff + SFQ;                                          // TMEM scale slot free again
+    uint64_t *sfr_full = sfe + SFQ;
     uint64_t *sfr_empty = sfr_full + L::SFR_SLOTS;
     uint64_t *acc_full = sfr_empty + L::SFR_SLOTS;
     uint64_t *acc_empty = acc_full + ACC_BUFS;
     uint64_t *mma_done = acc_empty + ACC_BUFS;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    uint64_t *fix_bar = mma_done + 1;  // partials staged for the last tile's fix-up
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fix_bar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *last_flag = reinterpret_cast<int *>(tmem_slot + 2);
     int *issued = reinterpret_cast<int *>(tmem_slot + 4);     // ring fills issued
     int *sfr_issued = reinterpret_cast<int *>(tmem_slot + 5);
+    int *fix_issued = reinterpret_cast<int *>(tmem_slot + 6);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
     const long long u_begin = unit_start(cta, p.TU, p.G);
     const long long u_end = unit_start(cta + 1, p.TU, p.G);
     const int n_k = (int)(4 * (u_end - u_begin));  // k-tiles this CTA processes
+    const Sched sched(u_begin, u_end, p.U);
     if (threadIdx.x == 0) trace_phase(p, 0);
 
     if (threadIdx.x == 0) {
@@ -185,7 +263,10 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             tc::mbar_init(&full[s], 1);   // producer expect_tx
             tc::mbar_init(&empty[s], 1);  // tcgen05.commit after the slot's last MMAs
         }
-        for (int s = 0; s < US; ++s) tc::mbar_init(&sff[s], 4);  // one arrival per scale warp
+        for (int s = 0; s < SFQ; ++s) {
+            tc::mbar_init(&sff[s], 4);  // one arrival per scale warp
+            tc::mbar_init(&sfe[s], 1);  // tcgen05.commit after the slot's MMAs
+        }
         for (int r = 0; r < L::SFR_SLOTS; ++r) {
             tc::mbar_init(&sfr_full[r], 1);
             tc::mbar_init(&sfr_empty[r], 4);
@@ -195,6 +276,8 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             tc::mbar_init(&acc_empty[b], 1);  // epilogue finished reading the buffer
         }
         tc::mbar_init(mma_done, 1);
+        tc::mbar_init(fix_bar, 1);
+        *fix_issued = 0;
         *abort_flag = 0;
         *last_flag = 0;
         *issued = 0;
@@ -203,6 +286,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         tc::tma_prefetch_desc(&tmap_w);
         tc::tma_prefetch_desc(&tmap_x);
         tc::tma_prefetch_desc(&tmap_sf);
+        if (p.tma_out) tc::tma_prefetch_desc(&tmap_out);
     }
     if (warp == 1) {
         tc::tmem_alloc(tmem_slot, L::TMEM_COLS);
@@ -220,6 +304,11 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         tc::tmem_st4(base + 4, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
         tc::tmem_st_wait();
     }
+    // programmatic dependent launch: everything above overlapped the previous kernel in the
+    // stream; wait for it to complete before the first global memory access, and let the next
+    // kernel start its own set-up early (it waits the same way before touching memory)
+    tc::grid_dependency_wait();
+    tc::grid_dependents_launch();
     tc::tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0) trace_phase(p, 1);
@@ -227,28 +316,49 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
+            const int n_units = n_k / 4;
+            const uint64_t w_policy = tc::make_policy_evict_first();
+            int sf_next = 0;  // next unit (in processing order) whose raw scales to load
             for (int i = 0; i < n_k && !*abort_flag; i += KPU) {
-                const long long u = u_begin + i / 4;
+                const long long u = sched.unit_at(i / 4);
                 const int t = (int)(u / p.U);
                 const int kt = (int)(u - (long long)t * p.U) * 4 + (i & 3);  // first k-tile of the fill
                 const int n0 = (t / p.m_tiles) * BM, m0 = (t % p.m_tiles) * BN;
                 if ((i & 3) == 0) {
-                    const int g = i >> 2, rs = g % L::SFR_SLOTS;
-                    if (wait_or_fail(&sfr_empty[rs], ((g / L::SFR_SLOTS) & 1) ^ 1, abort_flag, p.status,
-                                     ST_TIMEOUT_PRODUCER, g))
-                        break;
-                    tc::mbar_arrive_expect_tx(&sfr_full[rs], L::SFR_BYTES);
-                    tc::tma_load_2d(smem + L::SFR_OFF + rs * L::SFR_BYTES, &tmap_sf, &sfr_full[rs], 4 * kt, n0);
-                    *sfr_issued = g + 1;
+                    // raw scales: this unit's must be on their way before its data (blocking);
+                    // up to SFR - 1 later units' are loaded too when their slot is already free,
+                    // so the scale warps can fill tensor memory before a fill's data lands
+                    bool stop = false;
+                    const int g = i >> 2;
+                    for (const int g_hi = min(n_units, g + SFR); sf_next < g_hi; ++sf_next) {
+                        const int rs = sf_next % SFR;
+                        const uint32_t par = ((sf_next / SFR) & 1) ^ 1;
+                        if (sf_next > g && !tc::mbar_try_wait(&sfr_empty[rs], par)) break;
+                        if (wait_or_fail(&sfr_empty[rs], par, abort_flag, p.status, ST_TIMEOUT_PRODUCER, sf_next)) {
+                            stop = true;
+                            break;
+                        }
+                        int kts, ns;
+                        sched.fill_at(4 * sf_next, p.m_tiles, kts, ns);
+                        tc::mbar_arrive_expect_tx(&sfr_full[rs], L::SFR_BYTES);
+                        tc::tma_load_2d(smem + L::SFR_OFF + rs * L::SFR_BYTES, &tmap_sf, &sfr_full[rs], 4 * kts, ns);
+                        *sfr_issued = sf_next + 1;
+                    }
+                    if (stop) break;
                 }
                 const int f = i / KPU, sl = f % US;
                 if (wait_or_fail(&empty[sl], ((f / US) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, i))
                     break;
                 tc::mbar_arrive_expect_tx(&full[sl], L::TX_BYTES);
-                tc::tma_load_3d(smem + L::W_OFF + sl * L::W_SLOT, &tmap_w, &full[sl], 0, n0, kt);
+                if (p.evict_first)
+                    tc::tma_load_3d_hint(smem + L::W_OFF + sl * L::W_SLOT, &tmap_w, &full[sl], 0, n0, kt, w_policy);
+                else
+                    tc::tma_load_3d(smem + L::W_OFF + sl * L::W_SLOT, &tmap_w, &full[sl], 0, n0, kt);
+
                 tc::tma_load_3d(smem + L::X_OFF + sl * L::X_SLOT, &tmap_x, &full[sl], 0, m0, kt);
                 *issued = f + 1;
                 trace_ev(p, TR_TMA_ISSUED, i);
+                trace_ev(p, TR_TMA_FILL, f);
             }
         }
         __syncwarp();
@@ -261,22 +371,29 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         // 4 x KPU MMAs without touching memory.
         const bool gate = (warp == GATE_WARP);
         if (!gate) tc::tc_fence_after();
-        int f = 0, seg = 0;
-        long long u = u_begin;
-        while (u < u_end) {
-            const int t = (int)(u / p.U);
-            const long long ue = min(u_end, (long long)(t + 1) * p.U);
+        int f = 0;
+        for (int seg = 0; seg < sched.S; ++seg) {
+            long long u, ue;
+            sched.seg_units(seg, u, ue);
             const int b = seg % ACC_BUFS;
             const uint32_t t_acc = tmem + b * BN;
             const int f_end = f + (int)(4 * (ue - u)) / KPU;
             for (bool first = true; f < f_end; ++f, first = false) {
                 const int sl = f % US;
+                const int sq = f % SFQ;
                 if (gate) {
                     if (!*abort_flag && first)
                         warp_wait(&acc_empty[b], ((seg / ACC_BUFS) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_GATE, seg, lane);
                     if (!*abort_flag)
-                        warp_wait(&sff[sl], (f / US) & 1, abort_flag, p.status, ST_TIMEOUT_GATE, f, lane);
-                    if (lane == 0) trace_ev(p, TR_MMA_READY, f);
+                        warp_wait(&sff[sq], (f / SFQ) & 1, abort_flag, p.status, ST_TIMEOUT_GATE, f, lane);
+                    if (lane == 0) trace_ev(p, TR_GATE_SFF, f);
+                    if (!*abort_flag)
+                        warp_wait(&full[sl], (f / US) & 1, abort_flag, p.status, ST_TIMEOUT_GATE, f, lane);
+                    if (lane == 0) {
+                        trace_ev(p, TR_MMA_READY, f);
+                        if (f == 0) trace_phase(p, 8);
+                        if (f == n_k / KPU - 1) trace_phase(p, 9);
+                    }
                 }
                 // the gate's abort state rides on the barrier: the MMA thread reads no memory here
                 const bool aborted = tc::named_bar_or(GATE_BARRIER, 64, gate && *abort_flag);
@@ -284,7 +401,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                     tc::tc_fence_after();
 #pragma unroll
                     for (int j = 0; j < KPU; ++j) {
-                        const uint32_t sfa = tmem + L::T_SFA + 4 * (sl * KPU + j);
+                        const uint32_t sfa = tmem + L::T_SFA + 4 * (sq * KPU + j);
                         const uint32_t wa = tc::smem_u32(smem + L::W_OFF + sl * L::W_SLOT + j * L::W_TILE);
                         const uint32_t xa = tc::smem_u32(smem + L::X_OFF + sl * L::X_SLOT + j * L::X_TILE);
 #pragma unroll
@@ -296,77 +413,111 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                         }
                     }
                     tc::tc_commit(&empty[sl]);
+                    tc::tc_commit(&sfe[sq]);
                     if (f_end - f == 1) tc::tc_commit(&acc_full[b]);
                 }
                 __syncwarp();
             }
-            ++seg;
-            u = ue;
         }
-        if (!gate && lane == 0) tc::tc_commit(mma_done);  // teardown waits on it before freeing TMEM
+        if (!gate && lane == 0) {
+            tc::tc_commit(mma_done);  // teardown waits on it before freeing TMEM
+            trace_phase(p, 10);
+        }
         __syncwarp();
     } else if (warp < EPI_WARP0) {
         // ------------------------------------------------------------ scale warps (2-5)
         // Warp w owns TMEM lanes 32q..32q+31, q = w & 3 (weight rows 32q..32q+31).  For each
         // k-tile of a ring fill it writes its rows' 4-byte scale word (the 4 k-block scales of
-        // that k-tile) into the 4 columns of the fill's TMEM scale slot.  Those columns were last
-        // read by the MMAs of the previous fill of the same ring slot; the producer refilled the
-        // ring slot only after those MMAs finished, so waiting for the fill covers it.
+        // that k-tile) into the 4 columns of the fill's TMEM scale slot, once the raw scale tile
+        // has landed and the MMAs that last read the slot have finished; the data of the fill
+        // need not have arrived, so this work stays off the path from TMA to MMA.
         const int q = warp & 3;
         const int row = 32 * q + lane;
         int w = 0;
         for (int i = 0; i < n_k && !w; i += KPU) {
-            const int g = i >> 2, rs = g % L::SFR_SLOTS;
+            const int g = i >> 2, rs = g % SFR;
             if ((i & 3) == 0 &&
-                (w = warp_wait(&sfr_full[rs], (g / L::SFR_SLOTS) & 1, abort_flag, p.status, ST_TIMEOUT_SCALE, g, lane)))
+                (w = warp_wait(&sfr_full[rs], (g / SFR) & 1, abort_flag, p.status, ST_TIMEOUT_SCALE, g, lane)))
                 break;
-            const int f = i / KPU, sl = f % US;
-            if ((w = warp_wait(&full[sl], (f / US) & 1, abort_flag, p.status, ST_TIMEOUT_SCALE, f, lane)))
+            const int f = i / KPU, sq = f % SFQ;
+            if ((w = warp_wait(&sfe[sq], ((f / SFQ) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_SCALE, f, lane)))
                 break;
+            tc::tc_fence_after();
             if (lane == 0 && warp == SCALE_WARP0) trace_ev(p, TR_SCALE_DATA, f);
             const uint8_t *raw = smem + L::SFR_OFF + rs * L::SFR_BYTES + row * 16;
 #pragma unroll
             for (int j = 0; j < KPU; ++j) {
                 const uint32_t sw = *reinterpret_cast<const uint32_t *>(raw + 4 * ((i & 3) + j));
-                tc::tmem_st4(tmem + L::T_SFA + 4 * (sl * KPU + j) + ((32u * q) << 16), sw, sw, sw, sw);
+                tc::tmem_st4(tmem + L::T_SFA + 4 * (sq * KPU + j) + ((32u * q) << 16), sw, sw, sw, sw);
             }
             tc::tmem_st_wait();
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                tc::mbar_arrive(&sff[sl]);
+                tc::mbar_arrive(&sff[sq]);
                 if (((i + KPU) & 3) == 0) tc::mbar_arrive(&sfr_empty[rs]);
                 if (warp == SCALE_WARP0) trace_ev(p, TR_SCALE_DONE, f);
             }
+
         }
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
-        const int first_tile = (int)(u_begin / p.U);
-        int seg = 0;
-        long long u = u_begin;
-        while (u < u_end) {
+        const int first_tile = sched.t_first;
+        const int row = 32 * q + lane;
+        const bool issuer = (threadIdx.x == EPI_WARP0 * 32);
+        int ck = 0;  // output chunks emitted (staging buffer rotation)
+        // Write 16 token columns (c0..c0+15 of the tile at m0, n0) of this thread's weight row.
+        // With TMA stores the 128 threads stage a [16 tokens][128 rows] bf16 block in shared memory
+        // and one thread stores it (out-of-range rows and tokens are clipped by the tensor map);
+        // all 128 threads must call this together.
+        auto emit = [&](const float (&o)[16], int c0, int m0, int n0) {
+            const int n = n0 + row;
+            if (p.tma_out) {
+                uint16_t *stg = reinterpret_cast<uint16_t *>(smem + L::STAGE_OFF + (ck % L::NSTAGE) * L::STAGE_BYTES);
+                if (ck >= L::NSTAGE) {  // the store that last used this buffer has read it
+                    if (issuer) tc::bulk_wait_group_read<L::NSTAGE - 1>();
+                    tc::named_bar_sync(1, 128);
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) stg[j * BM + row] = float_to_bf16_bits(o[j]);
+                tc::fence_proxy_async_smem();
+                tc::named_bar_sync(1, 128);
+                if (issuer) {
+                    tc::tma_store_2d(&tmap_out, stg, n0, m0 + c0);
+                    tc::bulk_commit_group();
+                }
+                ++ck;
+            } else if (n < p.N) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (m0 + c0 + j < p.M) tc::st_cg_u16(p.out + (size_t)(m0 + c0 + j) * p.N + n, float_to_bf16_bits(o[j]));
+            }
+        };
+        for (int seg = 0; seg < sched.S; ++seg) {
+            long long u, ue;
+            sched.seg_units(seg, u, ue);
             const int t = (int)(u / p.U);
             const long long t_lo = (long long)t * p.U, t_hi = t_lo + p.U;
-            const long long ue = min(u_end, t_hi);
             const bool whole = (u == t_lo) && (ue == t_hi);
             const int b = seg % ACC_BUFS;
+            const int n0 = (t / p.m_tiles) * BM, m0 = (t % p.m_tiles) * BN;
+            // the tile's per-token scales, staged once in shared memory (the load overlaps the wait)
+            float *xs_s = reinterpret_cast<float *>(smem + L::XS_OFF);
+            for (int i = row; i < BN; i += BM) xs_s[i] = (m0 + i < p.M) ? __ldg(p.xs + m0 + i) : 0.0f;
             int w = 0;
             if (lane == 0) w = tc::mbar_wait(&acc_full[b], (seg / ACC_BUFS) & 1, abort_flag, WAIT_BUDGET);
             w = __shfl_sync(0xffffffffu, w, 0);
-            if (w) {
-                if (lane == 0) {
-                    if (w == 1) fail(p.status, ST_TIMEOUT_EPI, &acc_full[b], seg);
-                    *abort_flag = 1;
-                }
-                break;
+            if (w && lane == 0) {
+                if (w == 1) fail(p.status, ST_TIMEOUT_EPI, &acc_full[b], seg);
+                *abort_flag = 1;
             }
+            // all four warps leave together if any of them gave up (this also publishes xs_s)
+            if (tc::named_bar_or(1, 128, w != 0)) break;
             tc::tc_fence_after();
-            const bool last_seg = (ue == u_end);
+            if (seg == 0 && threadIdx.x == EPI_WARP0 * 32) trace_phase(p, 11);
+            const bool last_seg = (seg == sched.S - 1);
             if (last_seg && threadIdx.x == EPI_WARP0 * 32) trace_phase(p, 4);
-            const int n0 = (t / p.m_tiles) * BM, m0 = (t % p.m_tiles) * BN;
-            const int row = 32 * q + lane;
-            const int n = n0 + row;
             const uint32_t t_acc = tmem + b * BN + ((32u * q) << 16);
             float *slot = p.partials + ((size_t)cta * 2 + (t == first_tile ? 0 : 1)) * (size_t)(BM * BN);
 #pragma unroll 1
@@ -375,15 +526,15 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 tc::tmem_ld16(t_acc + c0, r);
                 tc::tmem_ld_wait();
                 if (whole) {
+                    if (m0 + c0 < p.M) {
+                        float o[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int m = m0 + c0 + j;
-                        if (m < p.M && n < p.N)
-                            p.out[(size_t)m * p.N + n] = float_to_bf16_bits(__uint_as_float(r[j]) * __ldg(p.xs + m));
+                        for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(r[j]) * xs_s[c0 + j];
+                        emit(o, c0, m0, n0);
                     }
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) slot[(c0 + j) * BM + row] = __uint_as_float(r[j]);
+                    for (int j = 0; j < 16; ++j) tc::st_cg_f32(slot + (c0 + j) * BM + row, __uint_as_float(r[j]));
                 }
             }
             // release the accumulator buffer to the MMA issuer
@@ -395,49 +546,90 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 const int c_first = unit_owner(t_lo, p.TU, p.G);
                 const int c_last = unit_owner(t_hi - 1, p.TU, p.G);
                 if (last_seg && threadIdx.x == EPI_WARP0 * 32) trace_phase(p, 5);
-                __threadfence();
+                // the CTA's partial stores happen before one thread's acq_rel arrival (release);
+                // the last arrival's acquire makes every contributor's partial visible to it
                 tc::named_bar_sync(1, 128);
                 if (threadIdx.x == EPI_WARP0 * 32) {
-                    const int old = atomicAdd(p.counters + t, 1);
+                    const int old = tc::atomic_add_acq_rel_gpu(p.counters + t, 1);
                     *last_flag = (old == c_last - c_first);
                 }
                 tc::named_bar_sync(1, 128);
                 if (last_seg && threadIdx.x == EPI_WARP0 * 32) trace_phase(p, 6);
                 if (*last_flag) {
-                    __threadfence();
-                    // 16 columns at a time, up to 4 contributors' loads in flight together; the
-                    // additions still run in CTA order, so the result does not depend on timing
+                    const int n_contrib = c_last - c_first + 1;
                     const int m_cnt = min(BN, p.M - m0);
-                    for (int c0 = 0; c0 < m_cnt; c0 += 16) {
-                        float acc[16];
+                    const int m16 = (m_cnt + 15) & ~15;  // columns staged: whole 16-column groups
+                    const uint32_t part_bytes = (uint32_t)m16 * BM * 4;  // first m16 columns of a slot
+                    // The CTA's last tile: every ring fill has been consumed (its accumulator is
+                    // complete), so the ring's shared memory is idle.  Bulk copies bring all the
+                    // contributors' partials in one round trip instead of one per 16 columns.
+                    if (last_seg && (size_t)n_contrib * part_bytes <= (size_t)L::SFR_OFF) {
+                        if (threadIdx.x == EPI_WARP0 * 32) {
+                            tc::fence_proxy_async_global();  // partials were written by generic stores
+                            tc::mbar_arrive_expect_tx(fix_bar, (uint32_t)n_contrib * part_bytes);
+                            *fix_issued = 1;
+                            for (int c = c_first; c <= c_last; ++c) {
+                                const int sl = (t == (int)(unit_start(c, p.TU, p.G) / p.U)) ? 0 : 1;
+                                tc::bulk_load(smem + (size_t)(c - c_first) * part_bytes,
+                                              p.partials + ((size_t)c * 2 + sl) * (size_t)(BM * BN), part_bytes, fix_bar);
+                            }
+                        }
+                        int w = 0;
+                        if (lane == 0) w = tc::mbar_wait(fix_bar, 0, abort_flag, WAIT_BUDGET);
+                        w = __shfl_sync(0xffffffffu, w, 0);
+                        if (threadIdx.x == EPI_WARP0 * 32) trace_phase(p, 12);
+                        if (w) {
+                            if (lane == 0) {
+                                if (w == 1) fail(p.status, ST_TIMEOUT_EPI, fix_bar, seg);
+                                *abort_flag = 1;
+                            }
+                        } else {
+                            // same order of additions as below: zero, then the contributors in CTA
+                            // order; 16 independent columns per step keep the loads pipelined
+                            const float *st = reinterpret_cast<const float *>(smem) + row;
+                            const int stride = m16 * BM;
+                            for (int c0 = 0; c0 < m_cnt; c0 += 16) {
+                                float a[16];
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
-                        for (int cb = c_first; cb <= c_last; cb += 4) {
-                            float v[4][16];
+                                for (int j = 0; j < 16; ++j) a[j] = 0.0f;
+                                for (int c = 0; c < n_contrib; ++c) {
+                                    const float *sc = st + c * stride + c0 * BM;
 #pragma unroll
-                            for (int cc = 0; cc < 4; ++cc) {
-                                const int c = cb + cc;
-                                if (c <= c_last) {
+                                    for (int j = 0; j < 16; ++j) a[j] += sc[j * BM];
+                                }
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) a[j] *= xs_s[c0 + j];
+                                emit(a, c0, m0, n0);
+                            }
+                        }
+                        if (threadIdx.x == EPI_WARP0 * 32) trace_phase(p, 13);
+                    } else {
+                        // 16 columns at a time, up to 6 contributors' loads in flight together; the
+                        // additions still run in CTA order, so the result does not depend on timing
+                        for (int c0 = 0; c0 < m_cnt; c0 += 16) {
+                            float acc[16];
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+                            for (int cb = c_first; cb <= c_last; cb += 6) {
+                                float v[6][16];
+#pragma unroll
+                                for (int cc = 0; cc < 6; ++cc) {
+                                    const int c = min(cb + cc, c_last);  // past the end: reload the last, unused
                                     const int sl = (t == (int)(unit_start(c, p.TU, p.G) / p.U)) ? 0 : 1;
                                     const float *src = p.partials + ((size_t)c * 2 + sl) * (size_t)(BM * BN) + c0 * BM + row;
 #pragma unroll
                                     for (int j = 0; j < 16; ++j) v[cc][j] = __ldcg(src + j * BM);
                                 }
+#pragma unroll
+                                for (int cc = 0; cc < 6; ++cc)
+                                    if (cb + cc <= c_last) {
+#pragma unroll
+                                        for (int j = 0; j < 16; ++j) acc[j] += v[cc][j];
+                                    }
                             }
 #pragma unroll
-                            for (int cc = 0; cc < 4; ++cc)
-                                if (cb + cc <= c_last) {
-#pragma unroll
-                                    for (int j = 0; j < 16; ++j) acc[j] += v[cc][j];
-                                }
-                        }
-                        if (n < p.N) {
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int m = m0 + c0 + j;
-                                if (c0 + j < m_cnt)
-                                    p.out[(size_t)m * p.N + n] = float_to_bf16_bits(acc[j] * __ldg(p.xs + m));
-                            }
+                            for (int j = 0; j < 16; ++j) acc[j] *= xs_s[c0 + j];
+                            emit(acc, c0, m0, n0);
                         }
                     }
                     if (threadIdx.x == EPI_WARP0 * 32) p.counters[t] = 0;
@@ -445,10 +637,11 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 tc::named_bar_sync(1, 128);  // last_flag is reused by the next tile
                 if (last_seg && threadIdx.x == EPI_WARP0 * 32) trace_phase(p, 7);
             }
-            ++seg;
-            u = ue;
         }
-        if (threadIdx.x == EPI_WARP0 * 32) trace_phase(p, 2);
+        if (issuer) {
+            tc::bulk_wait_group_all();  // output stores done before the CTA's shared memory goes away
+            trace_phase(p, 2);
+        }
     }
 
 
@@ -460,8 +653,9 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             // drain: TMA copies issued but not waited for
             for (int f = max(0, *issued - US); f < *issued; ++f)
                 if (tc::mbar_wait(&full[f % US], (f / US) & 1, &zero, DRAIN_BUDGET)) break;
-            for (int g = max(0, *sfr_issued - L::SFR_SLOTS); g < *sfr_issued; ++g)
-                tc::mbar_wait(&sfr_full[g % L::SFR_SLOTS], (g / L::SFR_SLOTS) & 1, &zero, DRAIN_BUDGET);
+            for (int g = max(0, *sfr_issued - SFR); g < *sfr_issued; ++g)
+                tc::mbar_wait(&sfr_full[g % SFR], (g / SFR) & 1, &zero, DRAIN_BUDGET);
+            if (*fix_issued) tc::mbar_wait(fix_bar, 0, &zero, DRAIN_BUDGET);
         }
         tc::mbar_wait(mma_done, 0, &zero, WAIT_BUDGET);  // every MMA finished before TMEM is freed
     }
@@ -503,11 +697,16 @@ size_t workspace_for(const Cfg &c)
     return partial_bytes(c) + (size_t)c.m_tiles * c.n_tiles * 4;
 }
 
-template <int BN, int KPU, int US, int ACC_BUFS>
-w4a8_status launch(const uint8_t *wp, const uint8_t *xq, const Params &prm, cudaStream_t stream)
+template <int BN, int KPU, int US, int ACC_BUFS, int SFQ, int SFR>
+w4a8_status launch(const uint8_t *wp, const uint8_t *xq, Params prm, cudaStream_t stream)
 {
-    using L = Layout<BN, KPU, US, ACC_BUFS>;
-    CUtensorMap tw, tx, tsf;
+    using L = Layout<BN, KPU, US, ACC_BUFS, SFQ, SFR>;
+    CUtensorMap tw, tx, tsf, tout;
+    // output through TMA when its rows are 16-byte strided and the base 16-byte aligned
+    memset(&tout, 0, sizeof(tout));
+    prm.tma_out = (prm.N % 8 == 0) && w4a8_aligned(prm.out, 16) &&
+                  tch::tmap_2d(&tout, CU_TENSOR_MAP_DATA_TYPE_UINT16, prm.out, prm.M, prm.N, (uint64_t)prm.N * 2, 16,
+                               BM, CU_TENSOR_MAP_SWIZZLE_NONE);
     // 3-D views [k-tile][row][128 K]: weights (4-bit codes; a row is K/2 bytes, a k-tile 64) and
     // activations (bytes; a row is K bytes, a k-tile 128)
     if (!tch::tmap_3d_ktiles(&tw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wp, prm.N, prm.K / 2, 64, prm.K / 128, BM,
@@ -516,10 +715,23 @@ w4a8_status launch(const uint8_t *wp, const uint8_t *xq, const Params &prm, cuda
         !tch::tmap_2d(&tsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, prm.we, prm.N, prm.K / 32, prm.K / 32, BM, 16,
                       CU_TENSOR_MAP_SWIZZLE_NONE))
         return W4A8_ERR_CUDA;
-    auto kern = mxfp4_tc_kernel<BN, KPU, US, ACC_BUFS>;
+    auto kern = mxfp4_tc_kernel<BN, KPU, US, ACC_BUFS, SFQ, SFR>;
     static int attr_done[64] = {0};
     if (!tch::set_smem_once(kern, L::TOTAL, attr_done)) return W4A8_ERR_CUDA;
-    kern<<<prm.G, NUM_THREADS, L::TOTAL, stream>>>(tw, tx, tsf, prm);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(prm.G);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = L::TOTAL;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tw, tx, tsf, tout, prm) != cudaSuccess) {
+        cudaGetLastError();
+        return W4A8_ERR_CUDA;
+    }
     return w4a8_launch_status();
 }
 
@@ -557,6 +769,7 @@ w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const 
 {
     const Cfg c = choose(M, N, K);
     Params prm;
+    prm.wp = wp;
     prm.we = we;
     prm.xs = x_scale;
     prm.out = out;
@@ -573,12 +786,14 @@ w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const 
     prm.TU = c.TU;
     prm.G = c.G;
     prm.trace = static_cast<unsigned long long *>(w4a8_debug_trace_ptr());
+    // a single token tile reads every weight once: keep it from displacing other lines in L2
+    prm.evict_first = c.m_tiles == 1;
     switch (c.BN) {
-    case 16: return launch<16, 4, 3, 2>(wp, xq, prm, stream);
-    case 32: return launch<32, 4, 2, 2>(wp, xq, prm, stream);
-    case 64: return launch<64, 4, 2, 2>(wp, xq, prm, stream);
-    case 128: return launch<128, 2, 3, 2>(wp, xq, prm, stream);
-    default: return launch<256, 2, 2, 1>(wp, xq, prm, stream);
+    case 16: return launch<16, 4, 3, 2, 6, 2>(wp, xq, prm, stream);
+    case 32: return launch<32, 4, 2, 2, 4, 4>(wp, xq, prm, stream);
+    case 64: return launch<64, 4, 2, 2, 4, 4>(wp, xq, prm, stream);
+    case 128: return launch<128, 2, 3, 2, 6, 4>(wp, xq, prm, stream);
+    default: return launch<256, 2, 2, 1, 4, 4>(wp, xq, prm, stream);
     }
 }
 

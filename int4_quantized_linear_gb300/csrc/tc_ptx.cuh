@@ -57,13 +57,12 @@ __device__ __forceinline__ int mbar_wait(uint64_t *bar, uint32_t parity, volatil
 {
     if (mbar_try_wait(bar, parity)) return 0;
     const long long t0 = clock64();
-    unsigned int nap = 32;  // back off so idle pollers leave shared memory to the tensor core
+    // try_wait suspends the thread in hardware until the phase completes or a short time limit
+    // passes, so the loop wakes as soon as the barrier flips; no software back-off on top
     while (true) {
         if (mbar_try_wait(bar, parity)) return 0;
         if (*abort) return 2;
         if (clock64() - t0 > budget) return 1;
-        __nanosleep(nap);
-        if (nap < 256) nap <<= 1;
     }
 }
 
@@ -100,6 +99,68 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
+
+// Same with an L2 cache policy (from make_policy_evict_first and the like).
+__device__ __forceinline__ void tma_load_3d_hint(void *dst, const CUtensorMap *map, uint64_t *bar, int c0,
+                                                 int c1, int c2, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
+}
+
+// L2 policy for data read once: its lines are the first to be replaced.
+__device__ __forceinline__ uint64_t make_policy_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Plain bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16), completing
+// on an mbarrier's transaction count.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Global stores that bypass L1 (with most of the unified L1/shared array given to shared memory,
+// L1-allocating stores throttle the epilogue).
+__device__ __forceinline__ void st_cg_u16(uint16_t *p, uint16_t v)
+{
+    asm volatile("st.global.cg.u16 [%0], %1;" ::"l"(p), "h"(v) : "memory");
+}
+__device__ __forceinline__ void st_cg_f32(float *p, float v)
+{
+    asm volatile("st.global.cg.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+// Tensor store shared -> global (2-D tile), tracked by the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int c0, int c1)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's bulk groups still read their shared memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until all of this thread's bulk groups have completed (writes performed).
+__device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Orders this thread's view of global memory (generic proxy) before its later async-proxy
+// (TMA / bulk copy) accesses to global memory.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
@@ -219,6 +280,17 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v
 }
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Programmatic dependent launch controls (no-ops when the kernel was not launched with it).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *addr, int v)
+{
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
 
 // Named barrier that also ORs a predicate over the participating threads (no memory access).
 __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool cond)

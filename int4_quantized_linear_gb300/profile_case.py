@@ -1,0 +1,47 @@
+"""One small, self-checking invocation of the decode/prefill MXFP4 path, for profilers.
+
+    python -m int4_quantized_linear_gb300.profile_case --m 1 --n 34816 --k 5120 --calls 3
+
+Builds synthetic inputs of the given shape (the same recipe as the benchmark), runs the
+per-token activation quant once and the MXFP4 GEMM ``--calls`` times on ``cuda:0``, then checks
+the library's device status word; exits non-zero if a bounded wait ran out.  Meant as the
+target of ``ncu -k regex:mxfp4_tc -c <calls>``: it launches nothing else of note.
+"""
+from __future__ import annotations
+
+import argparse
+
+import numpy as np
+import torch
+
+from . import binding as lib
+from . import synth
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--m", type=int, default=1)
+    ap.add_argument("--n", type=int, default=synth.GATE_UP[0])
+    ap.add_argument("--k", type=int, default=synth.GATE_UP[1])
+    ap.add_argument("--calls", type=int, default=3)
+    args = ap.parse_args(argv)
+    M, N, K = args.m, args.n, args.k
+    lib.load()
+    dev = torch.device("cuda", 0)
+    w, e = synth.mxfp4_weights(N, K, 0, 118, 121)
+    wd = torch.from_numpy(w).to(dev)
+    ed = torch.from_numpy(e).to(dev)
+    x = torch.from_numpy(np.ascontiguousarray(synth.activations(M, K, seed=M)).view(np.int16)).to(dev)
+    xq, xs = lib.act_quant(x.view(torch.bfloat16))
+    ws = lib.make_workspace(lib.workspace_bytes(M, N, K), dev)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    for _ in range(args.calls):
+        lib.mxfp4_linear(xq, xs, wd, ed, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    lib.check_device_status()
+    print(f"ok M={M} N={N} K={K} calls={args.calls} workspace={lib.workspace_bytes(M, N, K)}")
+    return 0
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())

@@ -2,7 +2,8 @@
 
 Workload (one step): for each of the two served shapes -- gate_up N=34816 K=5120 and down
 N=5120 K=17408 -- and each decode batch M in {1, 8, 32, 64}: per-token fp8 activation quant
-of x [M, K] followed by the MXFP4 W4A8 GEMM, 16 kernel launches in all.  Each (shape, M)
+of x [M, K] followed by the MXFP4 W4A8 GEMM (one w4a8_mxfp4_linear_bf16 call, two kernels
+chained by programmatic dependent launch), 16 kernel launches in all.  Each (shape, M)
 pair owns its own weight copy, so one step streams 568 MB of weights (more than the 129 MB
 L2): every GEMM reads its weights from HBM.  The step is captured once in a CUDA graph and
 replayed.
@@ -43,7 +44,7 @@ SHAPES = [("gate_up", synth.GATE_UP), ("down", synth.DOWN)]
 DECODE_M = [1, 8, 32, 64]
 METRIC = "W4A8 GEMM: decode weight GB/s and prefill TFLOP/s, % of GB300 roofline"
 WORKLOAD = ("decode band MXFP4 W4A8: M in {1,8,32,64} x {gate_up N=34816 K=5120, down N=5120 "
-            "K=17408}; act quant + GEMM per (shape, M)")
+            "K=17408}; act quant + GEMM per (shape, M), one w4a8_mxfp4_linear_bf16 call each")
 
 
 def weight_bytes(N, K):
@@ -224,23 +225,21 @@ def run_ours(args, rank, world, local_rank):
             xs = torch.empty((M,), dtype=torch.float32, device=dev)
             out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             ws = lib.make_workspace(lib.workspace_bytes(M, N, K), dev)
+            lws = lib.make_linear_workspace(M, N, K, dev)
             calls.append(dict(name=name, N=N, K=K, M=M, w=w, e=e, x=x, x_host=x_host, xq=xq, xs=xs,
-                              out=out, ws=ws, bytes=weight_bytes(N, K)))
+                              out=out, ws=ws, lws=lws, bytes=weight_bytes(N, K)))
     step_bytes = sum(c["bytes"] for c in calls)
     clib = lib.load()
     stream = torch.cuda.Stream(device=dev)
 
     def launch(c, s):
-        st = clib.w4a8_act_quant(c["x"].data_ptr(), c["xq"].data_ptr(), c["xs"].data_ptr(), c["M"], c["K"], s)
+        # one native call per (shape, M): activation quant, then the GEMM (chained on the stream)
+        lws = c["lws"]
+        st = clib.w4a8_mxfp4_linear_bf16(c["x"].data_ptr(), c["w"].data_ptr(), c["e"].data_ptr(),
+                                         c["out"].data_ptr(), c["M"], c["N"], c["K"], lws.data_ptr(),
+                                         lws.numel(), s)
         if st:
-            raise lib.W4A8Error("w4a8_act_quant", st)
-        ws = c["ws"]
-        st = clib.w4a8_mxfp4_linear(c["xq"].data_ptr(), c["xs"].data_ptr(), c["w"].data_ptr(),
-                                    c["e"].data_ptr(), c["out"].data_ptr(), c["M"], c["N"], c["K"],
-                                    None if ws is None else ws.data_ptr(),
-                                    0 if ws is None else ws.numel(), s)
-        if st:
-            raise lib.W4A8Error("w4a8_mxfp4_linear", st)
+            raise lib.W4A8Error("w4a8_mxfp4_linear_bf16", st)
 
     # eager warm-up (also makes the library's lazy per-device set-up happen outside capture)
     with torch.cuda.stream(stream):
@@ -344,7 +343,7 @@ def run_ours(args, rank, world, local_rank):
         with torch.cuda.stream(stream):
             for c, hx, ho in zip(calls, pinned_x, pinned_o):
                 xd = hx.to(dev, non_blocking=True)
-                o = lib.linear(xd, c["w"], c["e"], workspace=c["ws"], stream=stream)
+                o = lib.linear(xd, c["w"], c["e"], workspace=c["lws"], stream=stream)
                 ho.copy_(o, non_blocking=True)
     for _ in range(2):
         e2e_step()

@@ -87,6 +87,28 @@ W4A8_API w4a8_status w4a8_mxfp4_linear(const uint8_t *xq, const float *x_scale, 
 /* Bytes of workspace w4a8_mxfp4_linear needs for this shape (0 if none). */
 W4A8_API size_t w4a8_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
+/* The whole MXFP4 W4A8 linear from bf16 activations: the per-token fp8 activation quant
+ * followed by the MXFP4 GEMM, in one call ("radiance_autoround.py", autoround_linear: the
+ * activation cast and the GEMM form one linear step; "vllm-radiance (MXFP4)": fp8 activations
+ * into the W4A8 kernel).  The result is bit-identical to w4a8_act_quant followed by
+ * w4a8_mxfp4_linear.
+ *   x_bf16    [M, K] bf16 (16-byte aligned)
+ *   w_packed, w_e8m0, out_bf16: as for w4a8_mxfp4_linear
+ *   workspace: device scratch of at least w4a8_mxfp4_linear_bf16_workspace_bytes(M, N, K)
+ *              bytes, 256-byte aligned.  It receives the quantized activations [M, K] and their
+ *              scales [M], then holds the GEMM's scratch, with the zero-counter contract of
+ *              w4a8_mxfp4_linear (zero before first use, left at zero by every call).
+ * The two kernels are chained with programmatic dependent launch: the activation quant waits
+ * for the work before it on the stream before touching memory, and the GEMM begins fetching
+ * its weights while the quant runs.  K must be a multiple of 32. */
+W4A8_API w4a8_status w4a8_mxfp4_linear_bf16(const uint16_t *x_bf16, const uint8_t *w_packed,
+                                            const uint8_t *w_e8m0, uint16_t *out_bf16, int64_t M,
+                                            int64_t N, int64_t K, void *workspace,
+                                            size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of workspace w4a8_mxfp4_linear_bf16 needs for this shape. */
+W4A8_API size_t w4a8_mxfp4_linear_bf16_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
 /* w4a8_mxfp4_linear for callers that cannot allocate device memory (no counterpart in the
  * pages; an addition of this library).  Code being captured into a CUDA graph, serving engines
  * that keep all device memory in their own pool, and plugin interfaces that pass only inputs and

@@ -24,7 +24,8 @@ EXPORTS = ("w4a8_act_quant", "w4a8_mxfp4_linear", "w4a8_workspace_bytes",
            "nvfp4_to_mxfp4_requant", "w4a8_int4g128_linear", "w4a8_int4g128_workspace_bytes",
            "w4a8_status_string", "w4a8_set_gemm_policy", "w4a8_check_device_status",
            "w4a8_decode_max_m", "w4a8_debug_status_words", "w4a8_debug_set_trace",
-           "w4a8_mxfp4_linear_noalloc", "w4a8_noalloc_scratch_bytes")
+           "w4a8_mxfp4_linear_noalloc", "w4a8_noalloc_scratch_bytes",
+           "w4a8_mxfp4_linear_bf16", "w4a8_mxfp4_linear_bf16_workspace_bytes")
 
 
 class W4A8Error(RuntimeError):
@@ -64,6 +65,8 @@ def load(build_if_missing: bool = True):
         "w4a8_debug_set_trace": (None, [P]),
         "w4a8_mxfp4_linear_noalloc": (I, [P, P, P, P, P, I64, I64, I64, P]),
         "w4a8_noalloc_scratch_bytes": (SZ, []),
+        "w4a8_mxfp4_linear_bf16": (I, [P, P, P, P, I64, I64, I64, P, SZ, P]),
+        "w4a8_mxfp4_linear_bf16_workspace_bytes": (SZ, [I64, I64, I64]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -252,8 +255,35 @@ def requant(nv_packed, nv_scale, divisors, partition_rows, mode="mse", out_packe
     return out_packed, out_e8m0, es
 
 
-def linear(x: torch.Tensor, w_packed: torch.Tensor, w_e8m0: torch.Tensor, workspace=None,
-           stream=None) -> torch.Tensor:
-    """The whole W4A8 MXFP4 linear: per-token fp8 activation quant, then the GEMM."""
-    xq, xs = act_quant(x, stream=stream)
-    return mxfp4_linear(xq, xs, w_packed, w_e8m0, workspace=workspace, stream=stream)
+def linear_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load().w4a8_mxfp4_linear_bf16_workspace_bytes(M, N, K))
+
+
+def make_linear_workspace(M: int, N: int, K: int, device) -> torch.Tensor:
+    """Zero-initialised, 256-byte aligned workspace for linear() / w4a8_mxfp4_linear_bf16."""
+    nbytes = linear_workspace_bytes(M, N, K)
+    buf = torch.zeros(nbytes + 256, dtype=torch.uint8, device=device)
+    off = (-buf.data_ptr()) % 256
+    return buf[off:off + nbytes]
+
+
+def linear(x: torch.Tensor, w_packed: torch.Tensor, w_e8m0: torch.Tensor, out=None,
+           workspace=None, stream=None) -> torch.Tensor:
+    """The whole W4A8 MXFP4 linear from bf16 activations in one native call: per-token fp8
+    activation quant, then the GEMM (w4a8_mxfp4_linear_bf16)."""
+    _dev(x, "x", torch.bfloat16)
+    _dev(w_packed, "w_packed", torch.uint8)
+    _dev(w_e8m0, "w_e8m0", torch.uint8)
+    M, K = x.shape
+    N = w_packed.shape[0]
+    if w_packed.shape != (N, K // 2) or w_e8m0.shape != (N, K // 32):
+        raise ValueError("weight shapes do not match K")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = make_linear_workspace(M, N, K, x.device)
+    wsb = workspace.numel() * workspace.element_size()
+    _check("w4a8_mxfp4_linear_bf16", load().w4a8_mxfp4_linear_bf16(
+        _ptr(x), _ptr(w_packed), _ptr(w_e8m0), _ptr(out), M, N, K, _ptr(workspace), wsb,
+        _stream(stream)))
+    return out

@@ -4,35 +4,64 @@
 // dynamic per-token scale before the GEMM; the scale is amax / 448 so the row maximum maps to
 // the largest e4m3 magnitude, and codes are rounded to nearest even.
 //
-// One CTA per row.  Pass 1 streams the row with 16-byte loads and takes the amax on the bf16
-// bit patterns (|x| ordering equals the ordering of the 15 low bits for finite values), warp
-// shuffles then shared memory reduce it; pass 2 re-reads the row (now in L1/L2, so HBM sees it
-// once), divides each element by the scale with a correctly rounded fp32 division and packs
-// eight e4m3 codes per 8-byte store.  HBM-bound: 2 bytes read + 1 byte written per element.
+// Grid (M, S): S CTAs per row.  Every CTA of a row reads the whole row once (each thread keeps
+// its 16-byte chunks in registers for rows up to AQ_THREADS * AQ_CACHE * 8 elements; longer rows
+// are re-read from L1/L2 for the second pass) and takes the amax on the bf16 bit patterns (|x|
+// ordering equals the ordering of the 15 low bits for finite values), reduced by warp shuffles
+// and shared memory; it then quantizes only its 1/S slice of the row: each element divided by the
+// scale with a correctly rounded fp32 division, eight e4m3 codes per 8-byte store.  Splitting a
+// row over S CTAs costs S reads of the row from L2 but spreads the divisions over S SMs, which
+// for decode batches (a few rows) is what bounds the kernel's latency.
+//
+// Launched with programmatic dependent launch: the kernel first waits for the previous kernel
+// in the stream (which may produce x, or still read xq / x_scale), and only then lets the next
+// kernel start early.  So when that next kernel is the library's GEMM, everything before this
+// kernel has completed by the time the GEMM starts, and it may fetch its weights before waiting
+// for this kernel.
+#include <algorithm>
+
 #include "common.cuh"
+#include "dispatch.h"
 
 namespace w4a8 {
 
 constexpr int AQ_THREADS = 256;
+constexpr int AQ_CACHE = 16;  // chunks of 8 elements kept per thread: rows up to 32768 read once
 
 __global__ void __launch_bounds__(AQ_THREADS)
 act_quant_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ xq,
                  float *__restrict__ x_scale, int64_t K)
 {
-    // a GEMM launched after this kernel with programmatic dependent launch may start its own
-    // set-up now; it waits for this grid to finish before it reads xq or x_scale
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t m = blockIdx.x;
     const uint4 *row = reinterpret_cast<const uint4 *>(x + m * K);
     const int nchunk = (int)(K / 8);
+    const bool cached = nchunk <= AQ_THREADS * AQ_CACHE;
+    // this CTA's slice of the row's chunks
+    const int c_lo = (int)((long long)nchunk * blockIdx.y / gridDim.y);
+    const int c_hi = (int)((long long)nchunk * (blockIdx.y + 1) / gridDim.y);
 
+    uint4 v[AQ_CACHE];
     uint32_t amax2 = 0;  // two 15-bit magnitudes packed, per-halfword max
-    for (int c = threadIdx.x; c < nchunk; c += AQ_THREADS) {
-        uint4 v = __ldg(row + c);
-        amax2 = __vmaxu2(amax2, v.x & 0x7fff7fffu);
-        amax2 = __vmaxu2(amax2, v.y & 0x7fff7fffu);
-        amax2 = __vmaxu2(amax2, v.z & 0x7fff7fffu);
-        amax2 = __vmaxu2(amax2, v.w & 0x7fff7fffu);
+    if (cached) {
+#pragma unroll
+        for (int i = 0; i < AQ_CACHE; ++i) {
+            const int c = threadIdx.x + i * AQ_THREADS;
+            v[i] = c < nchunk ? __ldg(row + c) : make_uint4(0u, 0u, 0u, 0u);
+            amax2 = __vmaxu2(amax2, v[i].x & 0x7fff7fffu);
+            amax2 = __vmaxu2(amax2, v[i].y & 0x7fff7fffu);
+            amax2 = __vmaxu2(amax2, v[i].z & 0x7fff7fffu);
+            amax2 = __vmaxu2(amax2, v[i].w & 0x7fff7fffu);
+        }
+    } else {
+        for (int c = threadIdx.x; c < nchunk; c += AQ_THREADS) {
+            const uint4 w = __ldg(row + c);
+            amax2 = __vmaxu2(amax2, w.x & 0x7fff7fffu);
+            amax2 = __vmaxu2(amax2, w.y & 0x7fff7fffu);
+            amax2 = __vmaxu2(amax2, w.z & 0x7fff7fffu);
+            amax2 = __vmaxu2(amax2, w.w & 0x7fff7fffu);
+        }
     }
     uint32_t hb = max(amax2 & 0xffffu, amax2 >> 16);
     float amax = bf16_bits_to_float(hb);
@@ -41,31 +70,61 @@ act_quant_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ xq,
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
     __syncthreads();
     if (threadIdx.x < 32) {
-        float v = threadIdx.x < AQ_THREADS / 32 ? red[threadIdx.x] : 0.0f;
-        v = warp_max(v);
-        if (threadIdx.x == 0) red[0] = v;
+        float t = threadIdx.x < AQ_THREADS / 32 ? red[threadIdx.x] : 0.0f;
+        t = warp_max(t);
+        if (threadIdx.x == 0) red[0] = t;
     }
     __syncthreads();
     amax = red[0];
     const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-    if (threadIdx.x == 0) x_scale[m] = s;
+    if (threadIdx.x == 0 && blockIdx.y == 0) x_scale[m] = s;
 
     uint2 *out = reinterpret_cast<uint2 *>(xq + m * K);
-    for (int c = threadIdx.x; c < nchunk; c += AQ_THREADS) {
-        uint4 v = row[c];
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    auto quant8 = [&](const uint4 &w) {
+        const uint32_t h[4] = {w.x, w.y, w.z, w.w};
         uint32_t q[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            float lo = __fdiv_rn(bf16_bits_to_float(w[j] & 0xffffu), s);
-            float hi = __fdiv_rn(bf16_bits_to_float(w[j] >> 16), s);
+            const float lo = __fdiv_rn(bf16_bits_to_float(h[j] & 0xffffu), s);
+            const float hi = __fdiv_rn(bf16_bits_to_float(h[j] >> 16), s);
             q[j] = float2_to_e4m3x2(lo, hi);
         }
-        out[c] = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+        return make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+    };
+    if (cached) {
+#pragma unroll
+        for (int i = 0; i < AQ_CACHE; ++i) {
+            const int c = threadIdx.x + i * AQ_THREADS;
+            if (c >= c_lo && c < c_hi) out[c] = quant8(v[i]);
+        }
+    } else {
+        for (int c = c_lo + (int)threadIdx.x; c < c_hi; c += AQ_THREADS) out[c] = quant8(row[c]);
     }
 }
 
 }  // namespace w4a8
+
+w4a8_status w4a8_launch_act_quant(const uint16_t *x_bf16, uint8_t *xq, float *x_scale, int64_t M,
+                                  int64_t K, cudaStream_t stream)
+{
+    // about 256 CTAs in all, at most 16 per row
+    const int per_row = M >= 256 ? 1 : (int)std::min<int64_t>(16, (256 + M - 1) / M);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)M, (unsigned)per_row);
+    cfg.blockDim = dim3(w4a8::AQ_THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, w4a8::act_quant_kernel, x_bf16, xq, x_scale, K) != cudaSuccess) {
+        cudaGetLastError();
+        return W4A8_ERR_CUDA;
+    }
+    return w4a8_launch_status();
+}
 
 extern "C" w4a8_status w4a8_act_quant(const uint16_t *x_bf16, uint8_t *xq, float *x_scale,
                                       int64_t M, int64_t K, cudaStream_t stream)
@@ -77,6 +136,5 @@ extern "C" w4a8_status w4a8_act_quant(const uint16_t *x_bf16, uint8_t *xq, float
     if (!w4a8_aligned(x_bf16, 16) || !w4a8_aligned(xq, 8) || !w4a8_aligned(x_scale, 4))
         return W4A8_ERR_MISALIGNED;
     if (M > 0x7fffffffLL) return W4A8_ERR_UNSUPPORTED_SHAPE;
-    w4a8::act_quant_kernel<<<(unsigned)M, w4a8::AQ_THREADS, 0, stream>>>(x_bf16, xq, x_scale, K);
-    return w4a8_launch_status();
+    return w4a8_launch_act_quant(x_bf16, xq, x_scale, M, K, stream);
 }

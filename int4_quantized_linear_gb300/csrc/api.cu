@@ -105,9 +105,50 @@ extern "C" w4a8_status w4a8_mxfp4_linear(const uint8_t *xq, const float *x_scale
         if (need && (!workspace || workspace_bytes < need)) return W4A8_ERR_WORKSPACE;
         if (need && !w4a8_aligned(workspace, 16)) return W4A8_ERR_MISALIGNED;
         return w4a8_launch_mxfp4_tc(xq, x_scale, w_packed, w_e8m0, out_bf16, M, N, K, workspace,
-                                    policy, stream);
+                                    policy, false, stream);
     }
     return w4a8_launch_mxfp4_simt(xq, x_scale, w_packed, w_e8m0, out_bf16, M, N, K, stream);
+}
+
+// Workspace of the fused entry: quantized activations, their scales, then the GEMM's scratch
+// (each part starting on a 256-byte boundary).
+static size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
+
+extern "C" size_t w4a8_mxfp4_linear_bf16_workspace_bytes(int64_t M, int64_t N, int64_t K)
+{
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    return round256((size_t)M * (size_t)K) + round256((size_t)M * 4) + w4a8_workspace_bytes(M, N, K);
+}
+
+extern "C" w4a8_status w4a8_mxfp4_linear_bf16(const uint16_t *x_bf16, const uint8_t *w_packed,
+                                              const uint8_t *w_e8m0, uint16_t *out_bf16, int64_t M,
+                                              int64_t N, int64_t K, void *workspace,
+                                              size_t workspace_bytes, cudaStream_t stream)
+{
+    if (M < 0 || N < 0 || K < 0) return W4A8_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return W4A8_OK;
+    if (K == 0 || !x_bf16 || !w_packed || !w_e8m0 || !out_bf16) return W4A8_ERR_INVALID_ARG;
+    if (K % 32 != 0 || M > 0x7fffffffLL) return W4A8_ERR_UNSUPPORTED_SHAPE;
+    if (!w4a8_aligned(x_bf16, 16) || !w4a8_aligned(w_packed, 16) || !w4a8_aligned(out_bf16, 2))
+        return W4A8_ERR_MISALIGNED;
+    const size_t need = w4a8_mxfp4_linear_bf16_workspace_bytes(M, N, K);
+    if (!workspace || workspace_bytes < need) return W4A8_ERR_WORKSPACE;
+    if (!w4a8_aligned(workspace, 256)) return W4A8_ERR_MISALIGNED;
+    uint8_t *xq = static_cast<uint8_t *>(workspace);
+    float *xs = reinterpret_cast<float *>(xq + round256((size_t)M * (size_t)K));
+    uint8_t *gws = reinterpret_cast<uint8_t *>(xs) + round256((size_t)M * 4);
+    const size_t gws_bytes = workspace_bytes - (size_t)(gws - xq);
+
+    w4a8_status st = w4a8_launch_act_quant(x_bf16, xq, xs, M, K, stream);
+    if (st != W4A8_OK) return st;
+    const int policy = w4a8_gemm_policy();
+    if (policy != 1 && w4a8_tc_mxfp4_supported(xq, w_packed, w_e8m0, out_bf16, M, N, K)) {
+        const size_t g_need = w4a8_tc_workspace_bytes(M, N, K, policy);
+        if (g_need > gws_bytes) return W4A8_ERR_WORKSPACE;
+        // the GEMM directly follows the activation quant: it may fetch weights before waiting
+        return w4a8_launch_mxfp4_tc(xq, xs, w_packed, w_e8m0, out_bf16, M, N, K, gws, policy, true, stream);
+    }
+    return w4a8_launch_mxfp4_simt(xq, xs, w_packed, w_e8m0, out_bf16, M, N, K, stream);
 }
 
 extern "C" w4a8_status w4a8_int4g128_linear(const uint8_t *xq, const float *x_scale,

@@ -25,9 +25,16 @@ bool w4a8_tc_mxfp4_supported(const void *xq, const void *wp, const void *we, con
                              int64_t M, int64_t N, int64_t K);
 size_t w4a8_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int policy);
 size_t w4a8_tc_workspace_counters_offset(int64_t M, int64_t N, int64_t K);
+// w_early: the kernel just before this one on the stream is the library's activation quant
+// (chained by programmatic dependent launch), so weights may be read before waiting on it.
 w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const uint8_t *wp,
                                  const uint8_t *we, uint16_t *out, int64_t M, int64_t N,
-                                 int64_t K, void *workspace, int policy, cudaStream_t stream);
+                                 int64_t K, void *workspace, int policy, bool w_early,
+                                 cudaStream_t stream);
+// Per-token activation quant launched with programmatic dependent launch (waits for the
+// previous kernel before reading x, then lets the next kernel start).
+w4a8_status w4a8_launch_act_quant(const uint16_t *x_bf16, uint8_t *xq, float *x_scale, int64_t M,
+                                  int64_t K, cudaStream_t stream);
 
 bool w4a8_tc_int4_supported(const void *xq, const void *qw, const void *s16, const void *out,
                             int64_t M, int64_t N, int64_t K);

@@ -74,10 +74,13 @@ struct Params {
     int M, N, K;
     int m_tiles, n_tiles;
     int U;                 // 4-k-tile units per tile
-    long long TU;          // total units
-    int G;                 // CTAs
+    long long RU;          // stream-K units (those of the first R tiles)
+    int R, D;              // stream-K tiles; whole tiles per CTA after them
+    int G, Gsk;            // CTAs; CTAs sharing the stream-K units
     int evict_first;       // weights are read once: load them with the L2 evict-first policy
     int tma_out;           // output tiles leave through shared memory and TMA stores (else plain stores)
+    int w_early;           // the first ring fills' weights and scales may be loaded before the
+                           // wait on the previous kernel (it is known not to write them)
     unsigned long long *trace;  // optional pipeline timeline of CTA 0 (diagnostics), or null
 };
 
@@ -151,35 +154,52 @@ __device__ __forceinline__ void fail(unsigned int *status, unsigned int bit, uin
     }
 }
 
-// First unit of CTA c, and the CTA that owns unit u, for the even split of TU units over G CTAs.
-__device__ __forceinline__ long long unit_start(long long c, long long TU, int G) { return c * TU / G; }
-__device__ __forceinline__ int unit_owner(long long u, long long TU, int G) { return (int)(((u + 1) * G - 1) / TU); }
+// First stream-K unit of CTA c, and the CTA that owns stream-K unit u, for the even split of RU
+// units over the first G CTAs (RU >= G).
+__device__ __forceinline__ long long unit_start(long long c, long long RU, int G) { return c * RU / G; }
+__device__ __forceinline__ int unit_owner(long long u, long long RU, int G) { return (int)(((u + 1) * G - 1) / RU); }
 
-// A CTA's work is the unit range [u_begin, u_end), which touches tiles t_first..t_last; the
-// first and last of them may be split with neighbouring CTAs.  Processing order: the split
-// first tile (if split), then the split last tile (if split), then the whole tiles in between.
-// The split tiles' fix-up (partial store, arrival count, last-arrival reduction) then runs in
-// the epilogue while the MMAs of the whole tiles proceed, and the CTA ends on a direct store.
+// Work split (data-parallel + stream-K hybrid).  With T tiles of U units on G CTAs, every CTA
+// owns D = T / G whole tiles (tiles R + c*D ... R + c*D + D - 1, R = T - D*G), and the first R
+// tiles' RU = R*U units are split evenly over the first Gsk = min(G, RU) CTAs: CTA c < Gsk takes
+// stream-K units [c*RU/Gsk, (c+1)*RU/Gsk) (at least one, so a split tile's contributors are
+// consecutive CTAs), which touch tiles t_first..t_last; the first and last of those may be
+// shared with neighbouring CTAs.
+// Processing order: the split first stream-K tile (if split), then the split last one, then the
+// remaining stream-K tiles, then the whole data-parallel tiles.  The split tiles' fix-up
+// (partial store, arrival count, last-arrival reduction) then runs in the epilogue while the
+// MMAs of whole tiles proceed, and a CTA that owns whole tiles ends on a direct store.
 struct Sched {
-    long long u_begin, u_end, A, L;
-    int U, t_first, t_last, S;
+    long long u_begin, u_end, A, L;  // stream-K unit range, units kept in place / moved up front
+    int U, t_first, t_last, S_sk, S, dp_t0, D, n_sk, n_units;
     bool pf, pl;
-    __device__ Sched(long long ub, long long ue, int U_) : u_begin(ub), u_end(ue), U(U_)
+    __device__ Sched(int cta, int Gsk, long long RU, int D_, int R, int U_) : U(U_), D(D_)
     {
+        u_begin = cta < Gsk ? (long long)cta * RU / Gsk : RU;
+        u_end = cta < Gsk ? (long long)(cta + 1) * RU / Gsk : RU;
+        const long long ub = u_begin, ue = u_end;
         t_first = (int)(ub / U_);
         t_last = ue > ub ? (int)((ue - 1) / U_) : t_first - 1;
-        S = t_last - t_first + 1;
-        pf = S >= 1 && ((ub % U_) != 0 || (S == 1 && ue - ub < U_));
-        pl = S >= 2 && (ue % U_) != 0;
-        A = pf ? min(ue, (long long)(t_first + 1) * U_) - ub : 0;  // units kept in place up front
-        L = pl ? ue - (long long)t_last * U_ : 0;                   // units moved up
+        S_sk = t_last - t_first + 1;
+        pf = S_sk >= 1 && ((ub % U_) != 0 || (S_sk == 1 && ue - ub < U_));
+        pl = S_sk >= 2 && (ue % U_) != 0;
+        A = pf ? min(ue, (long long)(t_first + 1) * U_) - ub : 0;
+        L = pl ? ue - (long long)t_last * U_ : 0;
+        dp_t0 = R + cta * D_;
+        S = S_sk + D_;
+        n_sk = (int)(ue - ub);
+        n_units = n_sk + D_ * U_;
     }
-    // unit processed at position p (0 <= p < u_end - u_begin)
+    // global unit (tile * U + unit within the tile) processed at position p (0 <= p < n_units)
     __device__ long long unit_at(long long p) const
     {
-        if (p < A) return u_begin + p;
-        if (p < A + L) return (long long)t_last * U + (p - A);
-        return u_begin + (p - L);
+        if (p < n_sk) {
+            if (p < A) return u_begin + p;
+            if (p < A + L) return (long long)t_last * U + (p - A);
+            return u_begin + (p - L);
+        }
+        const long long q = p - n_sk;
+        return (long long)(dp_t0 + q / U) * U + q % U;
     }
     // weight tile coordinates of the ring fill that starts at k-tile position i
     __device__ void fill_at(int i, int m_tiles, int &kt, int &n0) const
@@ -192,13 +212,19 @@ struct Sched {
     // tile of the k-th segment in processing order, and its unit range [a, b)
     __device__ int seg_tile(int k) const
     {
+        if (k >= S_sk) return dp_t0 + (k - S_sk);
         int s = k;
-        if (pl) s = pf ? (k == 0 ? 0 : (k == 1 ? S - 1 : k - 1)) : (k == 0 ? S - 1 : k - 1);
+        if (pl) s = pf ? (k == 0 ? 0 : (k == 1 ? S_sk - 1 : k - 1)) : (k == 0 ? S_sk - 1 : k - 1);
         return t_first + s;
     }
     __device__ void seg_units(int k, long long &a, long long &b) const
     {
         const long long t = seg_tile(k);
+        if (k >= S_sk) {
+            a = t * U;
+            b = a + U;
+            return;
+        }
         a = max(u_begin, t * U);
         b = min(u_end, (t + 1) * U);
     }
@@ -252,10 +278,8 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
-    const long long u_begin = unit_start(cta, p.TU, p.G);
-    const long long u_end = unit_start(cta + 1, p.TU, p.G);
-    const int n_k = (int)(4 * (u_end - u_begin));  // k-tiles this CTA processes
-    const Sched sched(u_begin, u_end, p.U);
+    const Sched sched(cta, p.Gsk, p.RU, p.D, p.R, p.U);
+    const int n_k = 4 * sched.n_units;  // k-tiles this CTA processes
     if (threadIdx.x == 0) trace_phase(p, 0);
 
     if (threadIdx.x == 0) {
@@ -304,6 +328,31 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         tc::tmem_st4(base + 4, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
         tc::tmem_st_wait();
     }
+    // Early weights: when the kernel before this one in the stream is known to leave the weights
+    // alone (the library's own activation quant, which itself waited for everything before it),
+    // the first US ring fills' weights and the first SFR scale tiles are requested now, while that
+    // kernel still runs; the fills' activation halves follow after the wait below.
+    int pre = 0;  // ring fills whose weights went out early (producer thread)
+    if (p.w_early && threadIdx.x == 0) {
+        for (int g = 0; g < min(n_k / 4, SFR); ++g) {
+            int kts, ns;
+            sched.fill_at(4 * g, p.m_tiles, kts, ns);
+            tc::mbar_arrive_expect_tx(&sfr_full[g], L::SFR_BYTES);
+            tc::tma_load_2d(smem + L::SFR_OFF + g * L::SFR_BYTES, &tmap_sf, &sfr_full[g], 4 * kts, ns);
+            *sfr_issued = g + 1;
+        }
+        const uint64_t w_policy = tc::make_policy_evict_first();
+        for (; pre < min(n_k / KPU, US); ++pre) {
+            int kt, n0;
+            sched.fill_at(pre * KPU, p.m_tiles, kt, n0);
+            tc::mbar_arrive_expect_tx(&full[pre], L::TX_BYTES);  // weights now, activations later
+            if (p.evict_first)
+                tc::tma_load_3d_hint(smem + L::W_OFF + pre * L::W_SLOT, &tmap_w, &full[pre], 0, n0, kt, w_policy);
+            else
+                tc::tma_load_3d(smem + L::W_OFF + pre * L::W_SLOT, &tmap_w, &full[pre], 0, n0, kt);
+            *issued = pre + 1;
+        }
+    }
     // programmatic dependent launch: everything above overlapped the previous kernel in the
     // stream; wait for it to complete before the first global memory access, and let the next
     // kernel start its own set-up early (it waits the same way before touching memory)
@@ -318,7 +367,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         if (lane == 0) {
             const int n_units = n_k / 4;
             const uint64_t w_policy = tc::make_policy_evict_first();
-            int sf_next = 0;  // next unit (in processing order) whose raw scales to load
+            int sf_next = *sfr_issued;  // next unit (in processing order) whose raw scales to load
             for (int i = 0; i < n_k && !*abort_flag; i += KPU) {
                 const long long u = sched.unit_at(i / 4);
                 const int t = (int)(u / p.U);
@@ -347,13 +396,15 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                     if (stop) break;
                 }
                 const int f = i / KPU, sl = f % US;
-                if (wait_or_fail(&empty[sl], ((f / US) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, i))
-                    break;
-                tc::mbar_arrive_expect_tx(&full[sl], L::TX_BYTES);
-                if (p.evict_first)
-                    tc::tma_load_3d_hint(smem + L::W_OFF + sl * L::W_SLOT, &tmap_w, &full[sl], 0, n0, kt, w_policy);
-                else
-                    tc::tma_load_3d(smem + L::W_OFF + sl * L::W_SLOT, &tmap_w, &full[sl], 0, n0, kt);
+                if (f >= pre) {
+                    if (wait_or_fail(&empty[sl], ((f / US) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, i))
+                        break;
+                    tc::mbar_arrive_expect_tx(&full[sl], L::TX_BYTES);
+                    if (p.evict_first)
+                        tc::tma_load_3d_hint(smem + L::W_OFF + sl * L::W_SLOT, &tmap_w, &full[sl], 0, n0, kt, w_policy);
+                    else
+                        tc::tma_load_3d(smem + L::W_OFF + sl * L::W_SLOT, &tmap_w, &full[sl], 0, n0, kt);
+                }
 
                 tc::tma_load_3d(smem + L::X_OFF + sl * L::X_SLOT, &tmap_x, &full[sl], 0, m0, kt);
                 *issued = f + 1;
@@ -543,8 +594,8 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             if (threadIdx.x == EPI_WARP0 * 32) tc::mbar_arrive(&acc_empty[b]);
             if (!whole) {
                 // stream-K fix-up: the last contributor of tile t adds the partials in CTA order
-                const int c_first = unit_owner(t_lo, p.TU, p.G);
-                const int c_last = unit_owner(t_hi - 1, p.TU, p.G);
+                const int c_first = unit_owner(t_lo, p.RU, p.Gsk);
+                const int c_last = unit_owner(t_hi - 1, p.RU, p.Gsk);
                 if (last_seg && threadIdx.x == EPI_WARP0 * 32) trace_phase(p, 5);
                 // the CTA's partial stores happen before one thread's acq_rel arrival (release);
                 // the last arrival's acquire makes every contributor's partial visible to it
@@ -569,7 +620,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                             tc::mbar_arrive_expect_tx(fix_bar, (uint32_t)n_contrib * part_bytes);
                             *fix_issued = 1;
                             for (int c = c_first; c <= c_last; ++c) {
-                                const int sl = (t == (int)(unit_start(c, p.TU, p.G) / p.U)) ? 0 : 1;
+                                const int sl = (t == (int)(unit_start(c, p.RU, p.Gsk) / p.U)) ? 0 : 1;
                                 tc::bulk_load(smem + (size_t)(c - c_first) * part_bytes,
                                               p.partials + ((size_t)c * 2 + sl) * (size_t)(BM * BN), part_bytes, fix_bar);
                             }
@@ -615,7 +666,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 #pragma unroll
                                 for (int cc = 0; cc < 6; ++cc) {
                                     const int c = min(cb + cc, c_last);  // past the end: reload the last, unused
-                                    const int sl = (t == (int)(unit_start(c, p.TU, p.G) / p.U)) ? 0 : 1;
+                                    const int sl = (t == (int)(unit_start(c, p.RU, p.Gsk) / p.U)) ? 0 : 1;
                                     const float *src = p.partials + ((size_t)c * 2 + sl) * (size_t)(BM * BN) + c0 * BM + row;
 #pragma unroll
                                     for (int j = 0; j < 16; ++j) v[cc][j] = __ldcg(src + j * BM);
@@ -671,7 +722,8 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 
 struct Cfg {
     int BN, m_tiles, n_tiles, U, G;
-    long long TU;
+    long long TU, RU;
+    int R, D, Gsk;
 };
 
 Cfg choose(int64_t M, int64_t N, int64_t K)
@@ -683,6 +735,11 @@ Cfg choose(int64_t M, int64_t N, int64_t K)
     c.U = (int)(K / 512);
     c.TU = (long long)c.n_tiles * c.m_tiles * c.U;
     c.G = (int)std::min<long long>(tch::num_sms(), c.TU);
+    const int T = c.n_tiles * c.m_tiles;
+    c.D = T / c.G;        // whole tiles per CTA
+    c.R = T - c.D * c.G;  // tiles split stream-K over all CTAs
+    c.RU = (long long)c.R * c.U;
+    c.Gsk = (int)std::max<long long>(1, std::min<long long>(c.G, c.RU));
     return c;
 }
 
@@ -765,7 +822,7 @@ size_t w4a8_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int policy)
 
 w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const uint8_t *wp, const uint8_t *we,
                                  uint16_t *out, int64_t M, int64_t N, int64_t K, void *workspace, int,
-                                 cudaStream_t stream)
+                                 bool w_early, cudaStream_t stream)
 {
     const Cfg c = choose(M, N, K);
     Params prm;
@@ -783,11 +840,15 @@ w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const 
     prm.m_tiles = c.m_tiles;
     prm.n_tiles = c.n_tiles;
     prm.U = c.U;
-    prm.TU = c.TU;
+    prm.RU = c.RU;
+    prm.R = c.R;
+    prm.D = c.D;
+    prm.Gsk = c.Gsk;
     prm.G = c.G;
     prm.trace = static_cast<unsigned long long *>(w4a8_debug_trace_ptr());
     // a single token tile reads every weight once: keep it from displacing other lines in L2
     prm.evict_first = c.m_tiles == 1;
+    prm.w_early = w_early ? 1 : 0;
     switch (c.BN) {
     case 16: return launch<16, 4, 3, 2, 6, 2>(wp, xq, prm, stream);
     case 32: return launch<32, 4, 2, 2, 4, 4>(wp, xq, prm, stream);

@@ -60,5 +60,6 @@ extern "C" w4a8_status w4a8_mxfp4_linear_noalloc(const uint8_t *xq, const float 
         cudaMemsetAsync(static_cast<unsigned char *>(scratch) + counters_off, 0, need - counters_off, stream) !=
             cudaSuccess)
         return W4A8_ERR_CUDA;
-    return w4a8_launch_mxfp4_tc(xq, x_scale, w_packed, w_e8m0, out_bf16, M, N, K, scratch, policy, stream);
+    return w4a8_launch_mxfp4_tc(xq, x_scale, w_packed, w_e8m0, out_bf16, M, N, K, scratch, policy, false,
+                                stream);
 }

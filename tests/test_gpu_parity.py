@@ -211,6 +211,76 @@ def test_mxfp4_rejects(lib):
         lib.mxfp4_linear(xq, xs, w, e)  # K = 48 is not a multiple of 32
 
 
+# ------------------------------------------------------- fused act quant + GEMM (one call)
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (7, 384, 640), (1, 128, 512), (5, 384, 1024),
+                                   (33, 520, 1536), (64, 1000, 2048), (130, 520, 1024)])
+def test_linear_fused_matches_two_calls(lib, orc, policy, M, N, K):
+    """w4a8_mxfp4_linear_bf16 is bit-identical to act quant + w4a8_mxfp4_linear, and within the
+    GEMM bound of the oracle."""
+    x, w, e = synth.prefill_case(M, N, K, seed=M * 11 + N)
+    xd, wd, ed = to_dev_bf16(x), to_dev(w), to_dev(e)
+    fused = lib.linear(xd, wd, ed)
+    xq, xs = lib.act_quant(xd)
+    two = lib.mxfp4_linear(xq, xs, wd, ed)
+    lib.check_device_status()
+    assert torch.equal(fused.view(torch.int16), two.view(torch.int16))
+    gemm_check(bf16_to_f64(fused), orc.mxfp4_linear(host(xq), host(xs), w, e), f"fused M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("shape", [GATE_UP, DOWN], ids=["gate_up", "down"])
+@pytest.mark.parametrize("M", [1, 64])
+def test_linear_fused_decode_full_sampled(lib, orc, shape, M):
+    N, K = shape
+    x, w, e = synth.decode_case(M, N, K, seed=3)
+    out = lib.linear(to_dev_bf16(x), to_dev(w), to_dev(e))
+    lib.check_device_status()
+    hq, hs = orc.act_quant(x)
+    im, inn = _sample_pairs(M, N, seed=4)
+    gemm_check(bf16_to_f64(out)[im, inn], orc.mxfp4_linear_pairs(hq, hs, w, e, im, inn),
+               f"fused decode M={M} N={N} K={K}")
+
+
+def test_linear_fused_chained_layers(lib, orc):
+    """Layer 2 quantizes layer 1's output: the activation quant must wait for the GEMM before
+    it on the stream (both launched with programmatic dependent launch).  One workspace per
+    layer, reused over repeated passes."""
+    M, K1, N1, N2 = 8, 512, 1536, 1024
+    x, w1, e1 = synth.prefill_case(M, N1, K1, seed=21)
+    _, w2, e2 = synth.prefill_case(M, N2, N1, seed=22)
+    xd = to_dev_bf16(x)
+    w1d, e1d, w2d, e2d = to_dev(w1), to_dev(e1), to_dev(w2), to_dev(e2)
+    ws1 = lib.make_linear_workspace(M, N1, K1, "cuda")
+    ws2 = lib.make_linear_workspace(M, N2, N1, "cuda")
+    outs = []
+    for _ in range(3):
+        h = lib.linear(xd, w1d, e1d, workspace=ws1)
+        outs.append(lib.linear(h, w2d, e2d, workspace=ws2))
+    lib.check_device_status()
+    h_ref = lib.linear(xd, w1d, e1d)
+    torch.cuda.synchronize()
+    hq, hs = lib.act_quant(h_ref)
+    ref2 = lib.mxfp4_linear(hq, hs, w2d, e2d)
+    for o in outs:
+        assert torch.equal(o.view(torch.int16), ref2.view(torch.int16))
+    gemm_check(bf16_to_f64(ref2), orc.mxfp4_linear(host(hq), host(hs), w2, e2), "layer 2")
+
+
+def test_linear_fused_rejects(lib):
+    M, N, K = 2, 128, 512
+    x = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((N, K // 2), dtype=torch.uint8, device="cuda")
+    e = torch.zeros((N, K // 32), dtype=torch.uint8, device="cuda")
+    small = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(lib.W4A8Error):
+        lib.linear(x, w, e, workspace=small)
+    ws = lib.make_linear_workspace(M, N, K, "cuda")
+    big = torch.zeros(ws.numel() + 512, dtype=torch.uint8, device="cuda")
+    off = (-big.data_ptr()) % 256 + 16  # 16-byte but not 256-byte aligned
+    with pytest.raises(lib.W4A8Error):
+        lib.linear(x, w, e, workspace=big[off:off + ws.numel()])
+
+
 def _i4_gemm(lib, orc, x, qw, s16, qz, pairs=None):
     xq, xs = lib.act_quant(to_dev_bf16(x))
     out = lib.int4g128_linear(xq, xs, to_dev(qw), to_dev_fp16(s16), qzeros=to_dev(qz))

@@ -369,7 +369,7 @@ def run_ours(args, rank, world, local_rank):
                 "path": "binding.linear per (shape, M), eager, pinned host x in / bf16 out"},
         "gpu_launches": 2 * len(calls) * args.steps,
     }
-    if args.extras and rank == 0:
+    if not args.no_extras and rank == 0:
         line["extras"] = run_extras(lib, dev, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle as orc
@@ -417,6 +417,92 @@ def run_extras(lib, dev, peaks):
                                   "frac_of_fp8_peak": round(tf / fp8_peak, 4)}
     out["prefill"] = {"fp8_peak_tflops": fp8_peak,
                       "peak_note": "2 x measured bf16 burst (fp8 dense rate is twice bf16)", "cases": pf}
+    hbm = peaks["hbm_gbs"]
+
+    def timeit_rot(fns, reps=24):
+        """Average time of one call, cycling over calls that touch different buffers (so the
+        working set exceeds L2); the calls are captured in a CUDA graph, so host-side launch
+        cost does not enter the figure."""
+        s = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(s):
+            for f in fns:
+                f()
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(reps):
+                fns[i % len(fns)]()
+        g.replay()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        with torch.cuda.stream(s):
+            g.replay()
+        b.record(s)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    # ---- per-token activation quant: 2MK bytes read, MK + 4M written
+    aq = {}
+    for M, K in ((1, 17408), (64, 17408), (4096, 5120), (4096, 17408)):
+        n_copies = max(2, int(3 * 129e6 // (3 * M * K)) + 1) if M * K * 3 > 4e6 else 8
+        xs_ = [torch.randn((M, K), device=dev).to(torch.bfloat16) for _ in range(min(n_copies, 8))]
+        qs_ = [(torch.empty((M, K), dtype=torch.uint8, device=dev), torch.empty((M,), dtype=torch.float32, device=dev))
+               for _ in xs_]
+        fns = [lambda x=x, q=q: lib.act_quant(x, q[0], q[1]) for x, q in zip(xs_, qs_)]
+        ms = timeit_rot(fns)
+        gbs = (3 * M * K + 4 * M) / (ms * 1e-3) / 1e9
+        aq[f"M{M}_K{K}"] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4)}
+        del xs_, qs_
+    out["act_quant"] = {"bound": "hbm", "peak_gbs": hbm, "cases": aq}
+
+    # ---- NVFP4 -> MXFP4 requant of the merged gate_up weight (two partitions)
+    N, K = synth.GATE_UP
+    nv_p, nv_s = synth.nvfp4_tensor_bytes(N, K, 0)
+    nvp, nvs = to_dev(nv_p), to_dev(nv_s)
+    div = torch.tensor([2688.0, 10752.0], dtype=torch.float32, device=dev)
+    o_p = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+    o_e = torch.empty((N, K // 32), dtype=torch.uint8, device=dev)
+    rq_bytes = N * K // 2 + N * K // 16 + N * K // 2 + N * K // 32
+    rq = {}
+    for mode in ("ocp", "noclip", "mse"):
+        ms = timeit(lambda: lib.requant(nvp, nvs, div, list(synth.GATE_UP_PARTITIONS), mode, o_p, o_e, err_ssq=True))
+        gbs = rq_bytes / (ms * 1e-3) / 1e9
+        rq[mode] = {"us": round(ms * 1e3, 1), "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4)}
+    out["requant"] = {"bound": "hbm", "peak_gbs": hbm, "bytes": rq_bytes,
+                      "config": "gate_up N=34816 K=5120, partitions 17408+17408, with per-partition error sums",
+                      "cases": rq}
+    del nvp, nvs, o_p, o_e
+
+    # ---- AutoRound int4 g128: decode weight GB/s, prefill TFLOP/s
+    i4 = {}
+    for name, (N, K) in SHAPES:
+        qw, sc, _ = synth.int4_weights(N, K, 0)
+        wb = N * K // 2 + N * K // 64
+        n_copies = 3
+        qws = [to_dev(qw) for _ in range(n_copies)]
+        scs = [to_dev(sc).view(torch.float16) for _ in range(n_copies)]
+        for M in (1, 8, 64):
+            x = torch.randn((M, K), device=dev).to(torch.bfloat16)
+            xq, xs = lib.act_quant(x)
+            o = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ws = lib.make_workspace(lib.int4_workspace_bytes(M, N, K), dev)
+            fns = [lambda a=a, b=b: lib.int4g128_linear(xq, xs, a, b, out=o, workspace=ws) for a, b in zip(qws, scs)]
+            ms = timeit_rot(fns)
+            gbs = wb / (ms * 1e-3) / 1e9
+            i4[f"{name}_M{M}"] = {"us": round(ms * 1e3, 2), "weight GB/s": round(gbs, 1),
+                                  "frac_of_hbm": round(gbs / hbm, 4)}
+        M = 4096
+        x = torch.randn((M, K), device=dev).to(torch.bfloat16)
+        xq, xs = lib.act_quant(x)
+        o = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        ws = lib.make_workspace(lib.int4_workspace_bytes(M, N, K), dev)
+        ms = timeit(lambda: lib.int4g128_linear(xq, xs, qws[0], scs[0], out=o, workspace=ws), reps=2)
+        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        i4[f"{name}_M{M}"] = {"ms": round(ms, 3), "tflops": round(tf, 1), "frac_of_fp8_peak": round(tf / fp8_peak, 4)}
+        del qws, scs
+    out["int4g128"] = {"decode_bound": "hbm", "prefill_bound": "tensor (fp8 peak)", "cases": i4}
     return out
 
 
@@ -426,7 +512,9 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--extras", action="store_true", help="also time prefill / int4 / requant")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other hot-path kernels (prefill, act quant, requant, int4)")
+    ap.add_argument("--extras", action="store_true", help="(default) kept for compatibility")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -147,7 +147,9 @@ W4A8_API size_t w4a8_noalloc_scratch_bytes(void);
  *   partition_rows [P] HOST array of row counts, in order, summing to N; 1 <= P <= 16
  *   out_packed [N, K/2] (16-byte aligned), out_e8m0 [N, K/32], written
  *   err_ssq    [P][2] fp64 or NULL; written with {sum of squared requant error, sum of
- *              squared dequantized weights} per partition (relRMS = sqrt(err/ssq))
+ *              squared dequantized weights} per partition (relRMS = sqrt(err/ssq)); each
+ *              32-block's terms are rounded and summed in fp32, the blocks summed in fp64
+ *              (a float-precision statistic, about 1e-7 relative)
  * K must be a multiple of 32. */
 W4A8_API w4a8_status nvfp4_to_mxfp4_requant(const uint8_t *nv_packed, const uint8_t *nv_scale_e4m3,
                                    const float *global_divisor, const int64_t *partition_rows,

@@ -8,11 +8,13 @@
 //
 // One thread per 32-block: a 16-byte load of 32 NVFP4 codes plus two e4m3 scale bytes in,
 // a 16-byte store of 32 MXFP4 codes plus one e8m0 byte out, so a warp moves 512 contiguous
-// bytes each way.  The whole block lives in registers; the page's fp32 transient and its row
+// bytes each way; a persistent grid strides over the blocks of each partition.  The whole block lives in registers; the page's fp32 transient and its row
 // chunking are not needed.  Every fp32 operation is written with an explicit rounding
 // intrinsic so that no multiply-add is contracted and the results match the oracle bit for
 // bit: the exponent comes from the float's bits (exact), the scaling by 2^-e is an exact
 // power-of-two product, and the squared errors are summed in ascending k.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace w4a8 {
@@ -80,84 +82,112 @@ W4A8_DEVICE float encode_block(const float (&w)[32], int e, uint32_t (&codes)[4]
     return S;
 }
 
+// One 32-block: dequantize (R1), choose the exponent (R2), encode (R3) and pack (R4).  Returns
+// the block exponent e; S receives the squared error in scale units and ssq the block's sum of
+// squared dequantized weights.
+W4A8_DEVICE int requant_block(const uint4 &pk, uint16_t sc, float dv, int mode, uint4 &out, float &S, float &ssq)
+{
+    const float2 s2 = e4m3x2_to_float2(sc);
+    const float sd0 = __fdiv_rn(s2.x, dv), sd1 = __fdiv_rn(s2.y, dv);
+    // R1: dequantize (one rounded product per element)
+    float w[32];
+    const uint32_t words[4] = {pk.x, pk.y, pk.z, pk.w};
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        float2 gv = e2m1x2_to_float2((words[j >> 2] >> (8 * (j & 3))) & 0xffu);
+        float sd = j < 8 ? sd0 : sd1;
+        w[2 * j] = __fmul_rn(gv.x, sd);
+        w[2 * j + 1] = __fmul_rn(gv.y, sd);
+        amax = fmaxf(amax, fmaxf(fabsf(w[2 * j]), fabsf(w[2 * j + 1])));
+    }
+    // R2 + R3: exponent rule and encode
+    uint32_t codes[4];
+    int e;
+    if (mode == 2) {
+        const int e0 = block_exponent(amax, 1);
+        uint32_t c0[4];
+        const float S0 = encode_block(w, e0, c0);
+        bool take1 = false;
+        uint32_t c1[4] = {0, 0, 0, 0};
+        float S1 = 0.0f;
+        if (e0 > -127) {
+            S1 = encode_block(w, e0 - 1, c1);
+            take1 = S1 < __fmul_rn(4.0f, S0);
+        }
+        e = take1 ? e0 - 1 : e0;
+        S = take1 ? S1 : S0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) codes[j] = take1 ? c1[j] : c0[j];
+    } else {
+        e = block_exponent(amax, mode);
+        S = encode_block(w, e, codes);
+    }
+    // R4: nibble k of word j is element 8j + k (the even k lands in the low nibble)
+    out = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+    // sum of squares for the relRMS report (a float-precision statistic): the block's 32
+    // squares rounded and added in fp32, ascending k; blocks are then summed in fp64.  fp64
+    // arithmetic per element would cost more than the rest of the kernel on GB300.
+    float q = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) q = __fadd_rn(q, __fmul_rn(w[k], w[k]));
+    ssq = q;
+    return e;
+}
+
+// Persistent grid: the partitions one after another; inside a partition every thread walks the
+// 32-blocks with a grid stride, so a warp handles 32 consecutive blocks of a row (512 bytes of
+// codes each way).  The error sums are kept per thread, reduced per CTA and added to the output
+// with one atomic per CTA and partition.
 __global__ void __launch_bounds__(RQ_THREADS)
 requant_kernel(const uint8_t *__restrict__ nv_packed, const uint8_t *__restrict__ nv_scale,
                const float *__restrict__ divisor, Partitions parts, int64_t N, int64_t K,
                int mode, uint8_t *__restrict__ out_packed, uint8_t *__restrict__ out_e8m0,
                double *__restrict__ err_ssq)
 {
+    __shared__ double red[2][RQ_THREADS / 32];
     const int64_t KB = K / 32;
-    const int64_t g = (int64_t)blockIdx.x * RQ_THREADS + threadIdx.x;
-    const bool valid = g < N * KB;
-    int p = -1;
-    double err = 0.0, ssq = 0.0;
-    if (valid) {
-        const int64_t n = g / KB, b = g - n * KB;
-        p = 0;
-        while (p < parts.P - 1 && n >= parts.row_end[p]) ++p;
-        const uint4 pk = *reinterpret_cast<const uint4 *>(nv_packed + n * (K / 2) + b * 16);
-        const uint16_t sc = *reinterpret_cast<const uint16_t *>(nv_scale + n * (K / 16) + b * 2);
+    const int64_t stride = (int64_t)gridDim.x * RQ_THREADS;
+    int64_t row_beg = 0;
+    for (int p = 0; p < parts.P; ++p) {
+        const int64_t row_end = parts.row_end[p];
         const float dv = divisor[p];
-        const float2 s2 = e4m3x2_to_float2(sc);
-        const float sd0 = __fdiv_rn(s2.x, dv), sd1 = __fdiv_rn(s2.y, dv);
-        // R1: dequantize (one rounded product per element)
-        float w[32];
-        const uint32_t words[4] = {pk.x, pk.y, pk.z, pk.w};
-        float amax = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            float2 gv = e2m1x2_to_float2((words[j >> 2] >> (8 * (j & 3))) & 0xffu);
-            float sd = j < 8 ? sd0 : sd1;
-            w[2 * j] = __fmul_rn(gv.x, sd);
-            w[2 * j + 1] = __fmul_rn(gv.y, sd);
-            amax = fmaxf(amax, fmaxf(fabsf(w[2 * j]), fabsf(w[2 * j + 1])));
-        }
-        // R2 + R3: exponent rule and encode
-        uint32_t codes[4];
-        int e;
-        float S;
-        if (mode == 2) {
-            const int e0 = block_exponent(amax, 1);
-            uint32_t c0[4];
-            const float S0 = encode_block(w, e0, c0);
-            bool take1 = false;
-            uint32_t c1[4] = {0, 0, 0, 0};
-            float S1 = 0.0f;
-            if (e0 > -127) {
-                S1 = encode_block(w, e0 - 1, c1);
-                take1 = S1 < __fmul_rn(4.0f, S0);
+        double err = 0.0, ssq = 0.0;
+        for (int64_t g = row_beg * KB + (int64_t)blockIdx.x * RQ_THREADS + threadIdx.x; g < row_end * KB; g += stride) {
+            const uint4 pk = *reinterpret_cast<const uint4 *>(nv_packed + g * 16);
+            const uint16_t sc = *reinterpret_cast<const uint16_t *>(nv_scale + g * 2);
+            uint4 codes;
+            float S, q;
+            const int e = requant_block(pk, sc, dv, mode, codes, S, q);
+            *reinterpret_cast<uint4 *>(out_packed + g * 16) = codes;
+            out_e8m0[g] = (uint8_t)(e + 127);
+            if (err_ssq) {
+                err += ldexp((double)S, 2 * e);
+                ssq += (double)q;
             }
-            e = take1 ? e0 - 1 : e0;
-            S = take1 ? S1 : S0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) codes[j] = take1 ? c1[j] : c0[j];
-        } else {
-            e = block_exponent(amax, mode);
-            S = encode_block(w, e, codes);
         }
-        // R4: pack (nibble k of word j is element 8j + k: the even k lands in the low nibble)
-        *reinterpret_cast<uint4 *>(out_packed + n * (K / 2) + b * 16) =
-            make_uint4(codes[0], codes[1], codes[2], codes[3]);
-        out_e8m0[n * KB + b] = (uint8_t)(e + 127);
         if (err_ssq) {
-            err = ldexp((double)S, 2 * e);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) ssq = fma((double)w[k], (double)w[k], ssq);
-        }
-    }
-    if (err_ssq) {
-        const int p0 = __shfl_sync(0xffffffffu, p, 0);
-        if (__all_sync(0xffffffffu, p == p0) && p0 >= 0) {
             err = warp_sum_d(err);
             ssq = warp_sum_d(ssq);
             if ((threadIdx.x & 31) == 0) {
-                atomicAdd(&err_ssq[2 * p0], err);
-                atomicAdd(&err_ssq[2 * p0 + 1], ssq);
+                red[0][threadIdx.x >> 5] = err;
+                red[1][threadIdx.x >> 5] = ssq;
             }
-        } else if (valid) {
-            atomicAdd(&err_ssq[2 * p], err);
-            atomicAdd(&err_ssq[2 * p + 1], ssq);
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                double a = 0.0, b2 = 0.0;
+                for (int i = 0; i < RQ_THREADS / 32; ++i) {
+                    a += red[0][i];
+                    b2 += red[1][i];
+                }
+                if (a != 0.0 || b2 != 0.0) {
+                    atomicAdd(&err_ssq[2 * p], a);
+                    atomicAdd(&err_ssq[2 * p + 1], b2);
+                }
+            }
+            __syncthreads();
         }
+        row_beg = row_end;
     }
 }
 
@@ -192,9 +222,17 @@ extern "C" w4a8_status nvfp4_to_mxfp4_requant(const uint8_t *nv_packed, const ui
         return W4A8_ERR_MISALIGNED;
     if (err_ssq && cudaMemsetAsync(err_ssq, 0, sizeof(double) * 2 * P, stream) != cudaSuccess)
         return W4A8_ERR_CUDA;
+    // a row's 32-blocks are contiguous in both arrays: block g of the whole tensor sits at
+    // packed byte 16 g and scale byte 2 g, so the kernel indexes blocks linearly
     const int64_t blocks = N * (K / 32);
-    const int64_t grid = (blocks + w4a8::RQ_THREADS - 1) / w4a8::RQ_THREADS;
-    if (grid > 0x7fffffffLL) return W4A8_ERR_UNSUPPORTED_SHAPE;
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, w4a8::requant_kernel, w4a8::RQ_THREADS, 0) !=
+            cudaSuccess)
+        return W4A8_ERR_CUDA;
+    const int64_t need = (blocks + w4a8::RQ_THREADS - 1) / w4a8::RQ_THREADS;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sms * std::max(per_sm, 1)));
     w4a8::requant_kernel<<<(unsigned)grid, w4a8::RQ_THREADS, 0, stream>>>(
         nv_packed, nv_scale_e4m3, global_divisor, parts, N, K, mode, out_packed, out_e8m0,
         err_ssq);

@@ -26,7 +26,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
 # Tensor ids: one independent stream per tensor role.
-T_X, T_OUTLIER, T_OUTLIER_PICK, T_W, T_E, T_ROWSCALE, T_QW, T_QS, T_WREQ = range(1, 10)
+T_X, T_OUTLIER, T_OUTLIER_PICK, T_W, T_E, T_ROWSCALE, T_QW, T_QS, T_WREQ, T_NVS = range(1, 11)
 
 GATE_UP = (34816, 5120)
 DOWN = (5120, 17408)
@@ -142,6 +142,16 @@ def int4_case(M: int, N: int, K: int, seed: int = 0):
     x = activations(M, K, seed)
     qw, sc, qz = int4_weights(N, K, seed)
     return x, qw, sc, qz
+
+
+def nvfp4_tensor_bytes(N: int, K: int, seed: int = 0, s_lo: int = 0x28, s_hi: int = 0x50):
+    """Throughput-test stand-in for an NVFP4 checkpoint tensor, in its storage layout:
+    (packed [N, K/2] uniform bytes, e4m3 scale codes [N, K/16] uniform in [s_lo, s_hi] (positive
+    normals, 2^-2 .. 2^3 for the defaults)).  Shapes and byte volumes match a real checkpoint;
+    the values are not the output of a quantizer (parity tests use the oracle's quantizer)."""
+    packed = uniform_bytes(N, K // 2, seed, T_W)
+    scale = uniform_ints(N * (K // 16), s_lo, s_hi, seed, T_NVS).astype(np.uint8)
+    return packed, scale.reshape(N, K // 16)
 
 
 def gaussian_weights(N: int, K: int, sigma: float = 0.02, seed: int = 0,

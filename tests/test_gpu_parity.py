@@ -76,7 +76,17 @@ def test_requant_bit_exact(lib, orc, mode, N, K, parts, gain2):
     rp, re_, rs = orc.requant(packed, scale, div, parts, mode)
     assert np.array_equal(host(ge), re_)
     assert np.array_equal(host(gp), rp)
-    assert np.allclose(host(gs), rs, rtol=1e-9)
+    _check_err_ssq(host(gs), rs)
+
+
+def _check_err_ssq(got, ref):
+    """Requant error report: the error column sums the same fp32 block errors on both sides
+    (fp64 across blocks, order aside); the weight-energy column is a float-precision statistic
+    (fp32 per 32-block on the GPU, fp64 in the oracle), checked to 2e-6 relative -- the relRMS
+    it feeds is specified to 1e-5 relative ("radiance_nvfp4.py",
+    process_weights_after_loading)."""
+    assert np.allclose(got[:, 0], ref[:, 0], rtol=1e-9, atol=0)
+    assert np.allclose(got[:, 1], ref[:, 1], rtol=2e-6, atol=0)
 
 
 def test_requant_degenerate_blocks(lib, orc):
@@ -106,7 +116,7 @@ def test_requant_full_gate_up(lib, orc):
         rp, re_, rs = orc.requant(packed, scale, div, parts, mode)
         assert np.array_equal(host(ge), re_), mode
         assert np.array_equal(host(gp), rp), mode
-        assert np.allclose(host(gs), rs, rtol=1e-6), mode
+        _check_err_ssq(host(gs), rs)
         rel_g = orc.rel_rms(host(gs))
         assert abs(rel_g - orc.rel_rms(rs)) <= 1e-5 * orc.rel_rms(rs)
 
@@ -294,7 +304,11 @@ def _i4_gemm(lib, orc, x, qw, s16, qz, pairs=None):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 128, 128), (8, 256, 512), (33, 136, 384), (64, 512, 1024),
-                                   (100, 264, 256), (200, 128, 640)])
+                                   (100, 264, 256), (200, 128, 640),
+                                   # K a multiple of 512: the tensor-core path (stream-K splits,
+                                   # ragged token and column tails, every token tile width)
+                                   (1, 132, 512), (5, 384, 1024), (17, 200, 1536), (33, 520, 2048),
+                                   (64, 1000, 512), (65, 260, 1024), (130, 384, 512), (300, 640, 1536)])
 def test_int4_linear_small(lib, orc, policy, M, N, K):
     x, qw, s16, qz = synth.int4_case(M, N, K, seed=M + N)
     got, ref = _i4_gemm(lib, orc, x, qw, s16, qz)

@@ -127,6 +127,17 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------------- CPU side
 
+def aggregate(elapsed_ms, step_bytes, steps, world, dist=None, device="cpu"):
+    """Whole-job throughput of independent replicas: every rank did step_bytes per step; the
+    job time is the slowest rank's (max over ranks).  Returns (GB/s, max elapsed ms)."""
+    if dist is not None and world > 1:
+        import torch
+        t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    return world * step_bytes * steps / (elapsed_ms * 1e-3) / 1e9, elapsed_ms
+
+
 def oracle_sample(orc, cases, budget_s):
     """Time the oracle GEMM (act quant of the sample rows + dequantize-and-matmul) over a
     column sample of every (shape, M) case; returns (weight bytes processed, seconds)."""
@@ -301,13 +312,8 @@ def run_ours(args, rank, world, local_rank):
     t_wall1 = time.time()
     if dist:
         dist.barrier()
-    elapsed_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    value, elapsed_ms = aggregate(e0.elapsed_time(e1), step_bytes, args.steps, world, dist, dev)
     ms_per_step = elapsed_ms / args.steps
-    value = world * step_bytes * args.steps / (elapsed_ms * 1e-3) / 1e9
 
     # ---- per-kernel durations of the decode GEMM (same graph, event-bracketed GEMMs)
     gemm_ms = [0.0] * len(calls)

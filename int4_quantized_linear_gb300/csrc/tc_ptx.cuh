@@ -50,17 +50,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint (ns): the thread sleeps in hardware until the phase completes
+// (it wakes within a couple of hundred cycles of the flip) or the hint runs out.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Returns 0 when it did, 1 when
 // `budget` clock cycles passed first (a genuine timeout), 2 when another role set *abort.
+// After a first plain test the thread sleeps in try_wait with a 1 us hint per round, so idle
+// waiters take no issue slots from the warps that do the work.
 __device__ __forceinline__ int mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                          long long budget)
 {
     if (mbar_try_wait(bar, parity)) return 0;
     const long long t0 = clock64();
-    // try_wait suspends the thread in hardware until the phase completes or a short time limit
-    // passes, so the loop wakes as soon as the barrier flips; no software back-off on top
     while (true) {
-        if (mbar_try_wait(bar, parity)) return 0;
+        if (mbar_try_wait_sleep(bar, parity, 1000u)) return 0;
         if (*abort) return 2;
         if (clock64() - t0 > budget) return 1;
     }

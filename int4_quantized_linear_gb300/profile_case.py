@@ -5,7 +5,8 @@
 Builds synthetic inputs of the given shape (the same recipe as the benchmark), runs the
 per-token activation quant once and the MXFP4 GEMM ``--calls`` times on ``cuda:0``, then checks
 the library's device status word; exits non-zero if a bounded wait ran out.  Meant as the
-target of ``ncu -k regex:mxfp4_tc -c <calls>``: it launches nothing else of note.
+target of ``ncu -k regex:mxfp4_tc -c <calls>`` (``regex:int4_tc`` with ``--int4``): it launches
+nothing else of note.
 """
 from __future__ import annotations
 
@@ -24,22 +25,31 @@ def main(argv=None) -> int:
     ap.add_argument("--n", type=int, default=synth.GATE_UP[0])
     ap.add_argument("--k", type=int, default=synth.GATE_UP[1])
     ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--int4", action="store_true", help="the AutoRound int4 g128 GEMM instead of MXFP4")
     args = ap.parse_args(argv)
     M, N, K = args.m, args.n, args.k
     lib.load()
     dev = torch.device("cuda", 0)
-    w, e = synth.mxfp4_weights(N, K, 0, 118, 121)
-    wd = torch.from_numpy(w).to(dev)
-    ed = torch.from_numpy(e).to(dev)
     x = torch.from_numpy(np.ascontiguousarray(synth.activations(M, K, seed=M)).view(np.int16)).to(dev)
     xq, xs = lib.act_quant(x.view(torch.bfloat16))
-    ws = lib.make_workspace(lib.workspace_bytes(M, N, K), dev)
     out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    for _ in range(args.calls):
-        lib.mxfp4_linear(xq, xs, wd, ed, out=out, workspace=ws)
+    if args.int4:
+        qw, sc, _ = synth.int4_weights(N, K, 0)
+        qd = torch.from_numpy(qw).to(dev)
+        sd = torch.from_numpy(sc).to(dev).view(torch.float16)
+        ws = lib.make_workspace(lib.int4_workspace_bytes(M, N, K), dev)
+        for _ in range(args.calls):
+            lib.int4g128_linear(xq, xs, qd, sd, out=out, workspace=ws)
+    else:
+        w, e = synth.mxfp4_weights(N, K, 0, 118, 121)
+        wd = torch.from_numpy(w).to(dev)
+        ed = torch.from_numpy(e).to(dev)
+        ws = lib.make_workspace(lib.workspace_bytes(M, N, K), dev)
+        for _ in range(args.calls):
+            lib.mxfp4_linear(xq, xs, wd, ed, out=out, workspace=ws)
     torch.cuda.synchronize()
     lib.check_device_status()
-    print(f"ok M={M} N={N} K={K} calls={args.calls} workspace={lib.workspace_bytes(M, N, K)}")
+    print(f"ok {'int4' if args.int4 else 'mxfp4'} M={M} N={N} K={K} calls={args.calls}")
     return 0
 
 

@@ -51,6 +51,22 @@ def weight_bytes(N, K):
     return N * K // 2 + N * K // 32
 
 
+def decode_traffic():
+    """DRAM bytes per decode-GEMM launch (mean over the step's 8 launches) from the committed ncu
+    capture, or None when the kernel's sources changed since that capture."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "decode_gemm_traffic.json")) as fh:
+            rec = json.load(fh)
+        h = hashlib.sha256()
+        for s in rec["sources"]:
+            with open(os.path.join(ROOT, s), "rb") as fh:
+                h.update(fh.read())
+        return rec["dram_bytes_per_launch_mean"] if h.hexdigest() == rec["sources_sha256"] else None
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
@@ -329,11 +345,13 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.summary(t_wall0, t_wall1)
 
     peaks, peak_src = load_peaks()
+    traffic = decode_traffic()
     roofline = None
     if ev_graph is not None:
         ach = sum(c["bytes"] for c in calls) / (sum(gemm_ms) * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                    "frac": ach / peaks["hbm_gbs"], "traffic": traffic,
+                    "algorithmic_bytes_per_launch": sum(c["bytes"] for c in calls) / len(calls),
                     "kernel": "decode-band MXFP4 GEMM (w4a8_mxfp4_linear, M<=64)",
                     "peak_source": peak_src,
                     "per_case_us": {f"{c['name']}_M{c['M']}": round(1e3 * g, 2) for c, g in zip(calls, gemm_ms)}}

@@ -202,7 +202,7 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                 int kt, n0;
                 sched.fill_at(i, p.m_tiles, kt, n0);
                 const long long u = sched.unit_at(i / 4);
-                const int m0 = ((int)(u / p.U) % p.m_tiles) * BN;
+                const int m0 = ((int)div_nonneg(u, p.U) % p.m_tiles) * BN;
                 const int f = i / KPU, sl = f % US;
                 if (wait_or_fail(&empty[sl], ((f / US) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, f))
                     break;
@@ -319,7 +319,7 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         auto unit_scales = [&](int pu, float (&dst)[4]) {
             if (pu >= sched.n_units) return;
             const long long u = sched.unit_at(pu);
-            const int t = (int)(u / p.U);
+            const int t = (int)div_nonneg(u, p.U);
             const int n = (t / p.m_tiles) * BM + r;
             const int g0 = (int)(u - (long long)t * p.U) * 4;
 #pragma unroll
@@ -332,7 +332,7 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         for (int seg = 0; seg < sched.S; ++seg) {
             long long u, ue;
             sched.seg_units(seg, u, ue);
-            const int t = (int)(u / p.U);
+            const int t = (int)div_nonneg(u, p.U);
             const long long t_lo = (long long)t * p.U, t_hi = t_lo + p.U;
             const bool whole = (u == t_lo) && (ue == t_hi);
             const int n0 = (t / p.m_tiles) * BM, m0 = (t % p.m_tiles) * BN;

@@ -262,7 +262,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             int sf_next = *sfr_issued;  // next unit (in processing order) whose raw scales to load
             for (int i = 0; i < n_k && !*abort_flag; i += KPU) {
                 const long long u = sched.unit_at(i / 4);
-                const int t = (int)(u / p.U);
+                const int t = (int)div_nonneg(u, p.U);
                 const int kt = (int)(u - (long long)t * p.U) * 4 + (i & 3);  // first k-tile of the fill
                 const int n0 = (t / p.m_tiles) * BM, m0 = (t % p.m_tiles) * BN;
                 if ((i & 3) == 0) {
@@ -440,7 +440,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         for (int seg = 0; seg < sched.S; ++seg) {
             long long u, ue;
             sched.seg_units(seg, u, ue);
-            const int t = (int)(u / p.U);
+            const int t = (int)div_nonneg(u, p.U);
             const long long t_lo = (long long)t * p.U, t_hi = t_lo + p.U;
             const bool whole = (u == t_lo) && (ue == t_hi);
             const int b = seg % ACC_BUFS;

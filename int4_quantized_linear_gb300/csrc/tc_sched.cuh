@@ -41,6 +41,12 @@ __device__ __forceinline__ int unit_owner(long long u, long long RU, int G) { re
 // remaining stream-K tiles, then the whole data-parallel tiles.  The split tiles' fix-up
 // (partial store, arrival count, last-arrival reduction) then runs in the epilogue while the
 // MMAs of whole tiles proceed, and a CTA that owns whole tiles ends on a direct store.
+// a / b for a >= 0, b > 0: a 32-bit division when a fits (the common case), else 64-bit.
+__device__ __forceinline__ long long div_nonneg(long long a, int b)
+{
+    return a <= 0x7fffffffLL ? (long long)((unsigned)a / (unsigned)b) : a / b;
+}
+
 struct Sched {
     long long u_begin, u_end, A, L;  // stream-K unit range, units kept in place / moved up front
     int U, t_first, t_last, S_sk, S, dp_t0, D, n_sk, n_units;
@@ -70,16 +76,17 @@ struct Sched {
             if (p < A + L) return (long long)t_last * U + (p - A);
             return u_begin + (p - L);
         }
-        const long long q = p - n_sk;
-        return (long long)(dp_t0 + q / U) * U + q % U;
+        const unsigned q = (unsigned)(p - n_sk);  // < D * U: fits in 32 bits
+        const unsigned qt = q / (unsigned)U;
+        return (long long)(dp_t0 + (int)qt) * U + (long long)(q - qt * (unsigned)U);
     }
     // weight tile coordinates of the ring fill that starts at k-tile position i
     __device__ void fill_at(int i, int m_tiles, int &kt, int &n0) const
     {
         const long long u = unit_at(i / 4);
-        const int t = (int)(u / U);
+        const int t = (int)div_nonneg(u, U);
         kt = (int)(u - (long long)t * U) * 4 + (i & 3);
-        n0 = (t / m_tiles) * BM;
+        n0 = (int)((unsigned)t / (unsigned)m_tiles) * BM;
     }
     // tile of the k-th segment in processing order, and its unit range [a, b)
     __device__ int seg_tile(int k) const

@@ -5,19 +5,25 @@
 // activations, fp32 accumulation:
 //   out[m,n] = bf16( x_scale[m] * sum_g s[g,n] * sum_{k in g} e4m3(xq[m,k]) * (c[k,n] - 8) ).
 //
-// Every integer c - 8 in [-8, 7] is exact in e4m3, so each group's inner sum is an exact-input
-// e4m3 x e4m3 product, which tcgen05.mma kind::f8f6f4 computes into fp32 tensor memory; the
-// group scale is not a power of two and cannot ride on the instruction's block scale, so each
-// group's partial is read back and promoted into fp32 registers as acc += s[g,n] * partial.
+// The 4-bit code c itself, zero-extended to a byte, is the e4m3 encoding of c * 2^-9: codes 0-7
+// are the subnormals m * 2^-9 and codes 8-15 the first normal binade (1 + m/8) * 2^-6, which
+// continue the same linear scale.  So the operand tile is the codes spread to bytes (two masks
+// and two byte permutes per eight codes), and the zero point rides on four more MMAs per k-tile
+// whose A operand is the constant e4m3 -2^-6 (= -8 * 2^-9) in every element:
+//   sum_k c_k 2^-9 x_k + sum_k (-8 * 2^-9) x_k = 2^-9 * sum_k (c_k - 8) x_k,
+// all inputs exact, accumulated in fp32 tensor memory.  The group scale is not a power of two
+// and cannot ride on the instruction's block scale, so each group's partial is read back and
+// promoted into fp32 registers as acc += (512 * s[g,n]) * partial.
 //
 //   * swap-AB as in the MXFP4 kernel: the weights are the MMA "M" operand (128 output columns n
 //     per tile, one per tensor-memory lane) and the tokens the "N" operand (16, 32 or 64);
 //   * TMA brings the checkpoint words as stored ([K/8, N] int32, 8 consecutive k of one column
 //     per word, 512 contiguous bytes per box row) plus the activation tiles;
 //   * eight converter warps turn each k-tile (128 k x 128 columns) into the e4m3 operand tile the
-//     instruction reads (K-major, 128-byte swizzle), four codes at a time through byte-permute
-//     lookup tables (no conversion instructions);
-//   * a k-tile is one group, so every k-tile's four MMAs go to a fresh accumulator buffer in
+//     instruction reads (K-major, 128-byte swizzle), eight codes per five integer instructions;
+//     the constant zero-point operand is one 1 KB swizzle atom that every 8-row group of the
+//     instruction reads (stride between groups 0);
+//   * a k-tile is one group, so every k-tile's eight MMAs go to a fresh accumulator buffer in
 //     tensor memory (four buffers rotate); four promotion warps read it, scale by s[g,n] (read
 //     from global memory a unit ahead) and add into registers; at the end of a tile the same
 //     warps write bf16 through a shared-memory stage and TMA stores, or the fp32 partial of a
@@ -92,8 +98,9 @@ __device__ __forceinline__ void trace_ev(const Params &p, int ev, int i)
     if (p.trace != nullptr && blockIdx.x == 0 && i < 256) p.trace[ev * 256 + i] = (unsigned long long)clock64();
 }
 
-// Shared memory: NA converted operand tiles, then a ring of US fills, each holding KPU k-tiles of
-// activations (BN x 128 bytes, swizzled) and of checkpoint words ([16 word rows][128 columns]).
+// Shared memory: the zero-point operand atom (1 KB), NA converted operand tiles, then a ring of US
+// fills, each holding KPU k-tiles of activations (BN x 128 bytes, swizzled) and of checkpoint
+// words ([16 word rows][128 columns]).
 template <int BN, int US, int NA, int NB>
 struct Layout {
     static constexpr int RAW_TILE = 16 * BM * 4;  // 8 KB of words: 128 k x 128 columns
@@ -101,7 +108,8 @@ struct Layout {
     static constexpr int A_TILE = BM * 128;       // e4m3 [128 columns][128 k], 128-byte swizzle
     static constexpr int RAW_SLOT = KPU * RAW_TILE;
     static constexpr int X_SLOT = KPU * X_TILE;
-    static constexpr int A_OFF = 0;
+    static constexpr int Z_OFF = 0;                // 8 rows x 128 bytes of e4m3 -2^-6
+    static constexpr int A_OFF = Z_OFF + 1024;
     static constexpr int X_OFF = A_OFF + NA * A_TILE;
     static constexpr int RAW_OFF = X_OFF + US * X_SLOT;
     static constexpr int BAR_OFF = RAW_OFF + US * RAW_SLOT;
@@ -120,24 +128,16 @@ struct Layout {
     static_assert(NA <= NB, "a converted tile's release rides on the group-accumulator barrier");
 };
 
-// Eight int4 codes of one word (k = 8i..8i+7, low nibble first) -> eight e4m3 codes of c - 8,
-// low byte first, in two words.  Byte permutes serve as 8-entry lookup tables (a permute reads
-// four 4-bit selectors from the low half of its selector word): one table holds e4m3(c - 8) for
-// c = 0..7 (the values -8..-1), the other for c = 8..15 (0..7), both indexed by c & 7; bit 3 of
-// each code picks between them through a byte mask built by a third permute (selector 4 reads
-// 0xFF, selector 5 reads 0x00).  Every value is an exact e4m3 code, so nothing is rounded.
-__device__ __forceinline__ uint2 i4x8_to_e4m3x8(uint32_t w)
+// Eight int4 codes of one word (k = 8i..8i+7, low nibble first) -> the eight codes as bytes,
+// low byte first, in two words: each byte read as e4m3 is c * 2^-9.
+__device__ __forceinline__ uint2 i4x8_to_bytes(uint32_t w)
 {
-    const uint32_t idx = w & 0x77777777u;
-    const uint32_t sel = 0x55555555u - ((w >> 3) & 0x11111111u);  // 4 where c >= 8, else 5
-    const uint32_t idx_h = idx >> 16, sel_h = sel >> 16;
-    const uint32_t m_l = __byte_perm(0u, 0xFFu, sel), m_h = __byte_perm(0u, 0xFFu, sel_h);
-    const uint32_t n_l = __byte_perm(0xCACCCED0u, 0xB8C0C4C8u, idx);  // -8 -7 -6 -5 | -4 -3 -2 -1
-    const uint32_t n_h = __byte_perm(0xCACCCED0u, 0xB8C0C4C8u, idx_h);
-    const uint32_t p_l = __byte_perm(0x44403800u, 0x4E4C4A48u, idx);  //  0  1  2  3 |  4  5  6  7
-    const uint32_t p_h = __byte_perm(0x44403800u, 0x4E4C4A48u, idx_h);
-    return make_uint2((p_l & m_l) | (n_l & ~m_l), (p_h & m_h) | (n_h & ~m_h));
+    const uint32_t ev = w & 0x0F0F0F0Fu;          // codes 0, 2, 4, 6
+    const uint32_t od = (w >> 4) & 0x0F0F0F0Fu;   // codes 1, 3, 5, 7
+    return make_uint2(__byte_perm(ev, od, 0x5140), __byte_perm(ev, od, 0x7362));
 }
+
+constexpr uint32_t E4M3_MINUS_2POW_M6 = 0x88u;  // sign 1, exponent field 1, mantissa 0: -2^-6
 
 template <int BN, int US, int NA, int NB>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -186,6 +186,13 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     if (warp == 1) {
         tc::tmem_alloc(tmem_slot, L::TMEM_COLS);
         tc::tmem_relinquish();
+    }
+    // the zero-point operand atom (a swizzle only permutes its equal bytes), made visible to the
+    // tensor core before the barrier below
+    if (threadIdx.x < 64) {
+        const uint32_t z = E4M3_MINUS_2POW_M6 * 0x01010101u;
+        reinterpret_cast<uint4 *>(smem + L::Z_OFF)[threadIdx.x] = make_uint4(z, z, z, z);
+        tc::fence_proxy_async_smem();
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -242,8 +249,8 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {  // 16-byte chunk c = k 16c .. 16c+15 = words 2c, 2c+1
                 const int c = 4 * h + cc;
-                const uint2 lo = i4x8_to_e4m3x8(wv[2 * cc]);
-                const uint2 hi = i4x8_to_e4m3x8(wv[2 * cc + 1]);
+                const uint2 lo = i4x8_to_bytes(wv[2 * cc]);
+                const uint2 hi = i4x8_to_bytes(wv[2 * cc + 1]);
                 *reinterpret_cast<uint4 *>(dst + ((c ^ (r & 7)) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
             }
             tc::fence_proxy_async_smem();  // generic writes -> visible to the tensor core
@@ -272,11 +279,17 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             if (!gate && lane == 0 && !aborted) {
                 tc::tc_fence_after();
                 const uint32_t aa = tc::smem_u32(smem + L::A_OFF + a * L::A_TILE);
+                const uint32_t za = tc::smem_u32(smem + L::Z_OFF);
                 const uint32_t xa = tc::smem_u32(smem + L::X_OFF + sl * L::X_SLOT + j * L::X_TILE);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     tc::mma_f8f6f4(tmem + b * BN, tc::smem_desc(aa + 32 * kk, 16, 1024, 2),
                                    tc::smem_desc(xa + 32 * kk, 16, 1024, 2), idesc, kk > 0 ? 1u : 0u);
+                // zero point: the constant atom for every 8-row group (stride 0)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc::mma_f8f6f4(tmem + b * BN, tc::smem_desc(za + 32 * kk, 16, 0, 2),
+                                   tc::smem_desc(xa + 32 * kk, 16, 1024, 2), idesc, 1u);
                 tc::tc_commit(&g_full[b]);
                 if (j == KPU - 1) tc::tc_commit(&empty[sl]);
             }
@@ -315,7 +328,8 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                     if (m0 + c0 + j < p.M) tc::st_cg_u16(p.out + (size_t)(m0 + c0 + j) * p.N + n, float_to_bf16_bits(o[j]));
             }
         };
-        // group scales of one unit (4 k-tiles) for this thread's column, fetched a unit ahead
+        // group scales of one unit (4 k-tiles) for this thread's column, times 2^9 (the operand
+        // codes are c * 2^-9), fetched a unit ahead
         auto unit_scales = [&](int pu, float (&dst)[4]) {
             if (pu >= sched.n_units) return;
             const long long u = sched.unit_at(pu);
@@ -324,7 +338,7 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             const int g0 = (int)(u - (long long)t * p.U) * 4;
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj)
-                dst[jj] = n < p.N ? __half2float(__ushort_as_half(__ldg(p.s16 + (size_t)(g0 + jj) * p.N + n))) : 0.0f;
+                dst[jj] = n < p.N ? 512.0f * __half2float(__ushort_as_half(__ldg(p.s16 + (size_t)(g0 + jj) * p.N + n))) : 0.0f;
         };
         float sc_cur[4] = {0.0f, 0.0f, 0.0f, 0.0f}, sc_nxt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         unit_scales(0, sc_nxt);

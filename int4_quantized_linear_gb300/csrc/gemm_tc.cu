@@ -19,8 +19,10 @@
 //     rate on GB300, where one-k-tile boxes (64-byte rows) reach only about 60% of it;
 //   * four scale warps (one per TMEM lane quarter) write each row's 4-byte scale word, repeated
 //     over 4 columns, into a ring of tensor-memory scale slots with tcgen05.st; the MMA reads one
-//     byte per k-block.  The raw scale tiles are loaded a few units ahead of the data and a slot
-//     only waits for the MMAs that last read it, so scale work stays off the TMA -> MMA path;
+//     byte per k-block.  The raw scale tiles are loaded a few units ahead of the data (the first
+//     ones by the producer, each later one by a scale warp as soon as the tile it replaces has been
+//     read, so a scale load never holds up a data load) and a TMEM slot only waits for the MMAs
+//     that last read it, so scale work stays off the TMA -> MMA path;
 //   * persistent stream-K: one CTA per SM walks a contiguous range of (tile, 4-k-tile unit)
 //     work, so the TMA ring never drains between tiles and every SM gets the same number of
 //     units; a tile whose K range is split between CTAs is finished by the last contributor,
@@ -231,7 +233,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             sched.fill_at(4 * g, p.m_tiles, kts, ns);
             tc::mbar_arrive_expect_tx(&sfr_full[g], L::SFR_BYTES);
             tc::tma_load_2d(smem + L::SFR_OFF + g * L::SFR_BYTES, &tmap_sf, &sfr_full[g], 4 * kts, ns);
-            *sfr_issued = g + 1;
+            atomicMax(sfr_issued, g + 1);
         }
         const uint64_t w_policy = tc::make_policy_evict_first();
         for (; pre < min(n_k / KPU, US); ++pre) {
@@ -259,34 +261,21 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         if (lane == 0) {
             const int n_units = n_k / 4;
             const uint64_t w_policy = tc::make_policy_evict_first();
-            int sf_next = *sfr_issued;  // next unit (in processing order) whose raw scales to load
+            if (!p.w_early) {
+                // the first SFR units' raw scale tiles (later ones come from the scale warps)
+                for (int g = 0; g < min(n_units, SFR); ++g) {
+                    int kts, ns;
+                    sched.fill_at(4 * g, p.m_tiles, kts, ns);
+                    tc::mbar_arrive_expect_tx(&sfr_full[g], L::SFR_BYTES);
+                    tc::tma_load_2d(smem + L::SFR_OFF + g * L::SFR_BYTES, &tmap_sf, &sfr_full[g], 4 * kts, ns);
+                    atomicMax(sfr_issued, g + 1);
+                }
+            }
             for (int i = 0; i < n_k && !*abort_flag; i += KPU) {
                 const long long u = sched.unit_at(i / 4);
                 const int t = (int)div_nonneg(u, p.U);
                 const int kt = (int)(u - (long long)t * p.U) * 4 + (i & 3);  // first k-tile of the fill
                 const int n0 = (t / p.m_tiles) * BM, m0 = (t % p.m_tiles) * BN;
-                if ((i & 3) == 0) {
-                    // raw scales: this unit's must be on their way before its data (blocking);
-                    // up to SFR - 1 later units' are loaded too when their slot is already free,
-                    // so the scale warps can fill tensor memory before a fill's data lands
-                    bool stop = false;
-                    const int g = i >> 2;
-                    for (const int g_hi = min(n_units, g + SFR); sf_next < g_hi; ++sf_next) {
-                        const int rs = sf_next % SFR;
-                        const uint32_t par = ((sf_next / SFR) & 1) ^ 1;
-                        if (sf_next > g && !tc::mbar_try_wait(&sfr_empty[rs], par)) break;
-                        if (wait_or_fail(&sfr_empty[rs], par, abort_flag, p.status, ST_TIMEOUT_PRODUCER, sf_next)) {
-                            stop = true;
-                            break;
-                        }
-                        int kts, ns;
-                        sched.fill_at(4 * sf_next, p.m_tiles, kts, ns);
-                        tc::mbar_arrive_expect_tx(&sfr_full[rs], L::SFR_BYTES);
-                        tc::tma_load_2d(smem + L::SFR_OFF + rs * L::SFR_BYTES, &tmap_sf, &sfr_full[rs], 4 * kts, ns);
-                        *sfr_issued = sf_next + 1;
-                    }
-                    if (stop) break;
-                }
                 const int f = i / KPU, sl = f % US;
                 if (f >= pre) {
                     if (wait_or_fail(&empty[sl], ((f / US) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER, i))
@@ -401,6 +390,18 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 if (((i + KPU) & 3) == 0) tc::mbar_arrive(&sfr_empty[rs]);
                 if (warp == SCALE_WARP0) trace_ev(p, TR_SCALE_DONE, f);
             }
+            // the unit's raw tile is consumed by all four warps: one thread loads unit g + SFR's
+            // tile into the same slot, so scale loads never hold up the producer's data loads
+            if (((i + KPU) & 3) == 0 && warp == SCALE_WARP0 && lane == 0 && g + SFR < n_k / 4) {
+                if ((w = wait_or_fail(&sfr_empty[rs], (g / SFR) & 1, abort_flag, p.status, ST_TIMEOUT_SCALE, g)) == 0) {
+                    int kts, ns;
+                    sched.fill_at(4 * (g + SFR), p.m_tiles, kts, ns);
+                    tc::mbar_arrive_expect_tx(&sfr_full[rs], L::SFR_BYTES);
+                    tc::tma_load_2d(smem + L::SFR_OFF + rs * L::SFR_BYTES, &tmap_sf, &sfr_full[rs], 4 * kts, ns);
+                    atomicMax(sfr_issued, g + SFR + 1);
+                }
+            }
+            w = __shfl_sync(0xffffffffu, w, 0);
 
         }
     } else {

@@ -111,7 +111,9 @@ __device__ __forceinline__ void trace_phase(const Params &p, int k)
 // Shared memory: a ring of US slots, each holding KPU k-tiles of padded weights (16 KB each)
 // and activations (BN x 128 bytes each), plus a ring of SFR raw scale tiles (4 k-tiles each).
 // Tensor memory: ACC_BUFS accumulators of BN columns, the unit B scales, and a ring of SFQ
-// scale slots (KPU k-tiles of A scales each) that the scale warps fill ahead of the data.
+// scale slots (KPU k-tiles of A scales each) that the scale warps fill ahead of the data.  With
+// SFQ == US (the decode tilings) a scale slot is tied to its ring slot and freed by the same
+// commit, one commit per fill fewer.
 template <int BN, int KPU, int US, int ACC_BUFS, int SFQ, int SFR>
 struct Layout {
     static constexpr int W_TILE = BM * 128;             // one padded weight k-tile
@@ -345,7 +347,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                         }
                     }
                     tc::tc_commit(&empty[sl]);
-                    tc::tc_commit(&sfe[sq]);
+                    if (SFQ != US) tc::tc_commit(&sfe[sq]);
                     if (f_end - f == 1) tc::tc_commit(&acc_full[b]);
                 }
                 __syncwarp();
@@ -372,7 +374,9 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 (w = warp_wait(&sfr_full[rs], (g / SFR) & 1, abort_flag, p.status, ST_TIMEOUT_SCALE, g, lane)))
                 break;
             const int f = i / KPU, sq = f % SFQ;
-            if ((w = warp_wait(&sfe[sq], ((f / SFQ) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_SCALE, f, lane)))
+            // with one scale slot per ring slot, the slot is free when the fill's ring slot is
+            if ((w = warp_wait(SFQ == US ? &empty[f % US] : &sfe[sq], ((f / SFQ) & 1) ^ 1, abort_flag, p.status,
+                               ST_TIMEOUT_SCALE, f, lane)))
                 break;
             tc::tc_fence_after();
             if (lane == 0 && warp == SCALE_WARP0) trace_ev(p, TR_SCALE_DATA, f);
@@ -743,9 +747,9 @@ w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const 
     prm.evict_first = c.m_tiles == 1;
     prm.w_early = w_early ? 1 : 0;
     switch (c.BN) {
-    case 16: return launch<16, 4, 3, 2, 6, 2>(wp, xq, prm, stream);
-    case 32: return launch<32, 4, 2, 2, 4, 4>(wp, xq, prm, stream);
-    case 64: return launch<64, 4, 2, 2, 4, 4>(wp, xq, prm, stream);
+    case 16: return launch<16, 4, 3, 2, 3, 2>(wp, xq, prm, stream);
+    case 32: return launch<32, 4, 2, 2, 2, 4>(wp, xq, prm, stream);
+    case 64: return launch<64, 4, 2, 2, 2, 4>(wp, xq, prm, stream);
     case 128: return launch<128, 2, 3, 2, 6, 4>(wp, xq, prm, stream);
     default: return launch<256, 2, 2, 1, 4, 4>(wp, xq, prm, stream);
     }

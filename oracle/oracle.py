@@ -65,6 +65,8 @@ def _load():
             "orc_requant": (ctypes.c_int, [P, P, P, P, ctypes.c_int, I64, I64, ctypes.c_int,
                                            P, P, P]),
             "orc_dequant_mxfp4": (None, [P, P, I64, I64, P]),
+            "orc_requant_fp8_channel": (ctypes.c_int, [P, P, I64, I64, ctypes.c_int, P, P, P]),
+            "orc_requant_bf16": (ctypes.c_int, [P, I64, I64, ctypes.c_int, P, P, P]),
             "orc_nvfp4_quantize": (None, [P, P, ctypes.c_int, I64, P, P, P]),
             "orc_mxfp4_linear": (None, [P, P, P, P, I64, I64, I64, P]),
             "orc_mxfp4_linear_pairs": (None, [P, P, P, P, I64, P, P, I64, P]),
@@ -176,6 +178,32 @@ def requant(nv_packed, nv_scale, divisors, partition_rows, mode: str):
     rc = _load().orc_requant(pkp, scp, dvp, prp, P, N, K, MODES[mode], _p(out_p), _p(out_e),
                              _p(es))
     if rc != 0:
+        raise ValueError("oracle requant: invalid arguments")
+    return out_p, out_e, es
+
+
+def requant_fp8_channel(w8, row_scale, mode: str):
+    """FP8 per-channel [N, K] e4m3 codes x fp32 scale [N] -> MXFP4.  Returns (packed [N, K/2],
+    e8m0 [N, K/32], err_ssq [1, 2])."""
+    w, wp = _c(w8, np.uint8)
+    s, sp = _c(row_scale, np.float32)
+    N, K = w.shape
+    out_p = np.empty((N, K // 2), np.uint8)
+    out_e = np.empty((N, K // 32), np.uint8)
+    es = np.zeros((1, 2), np.float64)
+    if _load().orc_requant_fp8_channel(wp, sp, N, K, MODES[mode], _p(out_p), _p(out_e), _p(es)) != 0:
+        raise ValueError("oracle requant: invalid arguments")
+    return out_p, out_e, es
+
+
+def requant_bf16(w_bf16, mode: str):
+    """bf16 [N, K] (uint16 bits) -> MXFP4.  Returns (packed, e8m0, err_ssq [1, 2])."""
+    w, wp = _c(w_bf16, np.uint16)
+    N, K = w.shape
+    out_p = np.empty((N, K // 2), np.uint8)
+    out_e = np.empty((N, K // 32), np.uint8)
+    es = np.zeros((1, 2), np.float64)
+    if _load().orc_requant_bf16(wp, N, K, MODES[mode], _p(out_p), _p(out_e), _p(es)) != 0:
         raise ValueError("oracle requant: invalid arguments")
     return out_p, out_e, es
 

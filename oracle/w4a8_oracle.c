@@ -7,8 +7,9 @@
  *
  * Sources (web pages; each function names the passage it follows):
  *   [nvfp4]  "radiance_nvfp4.py" -- unpack_e2m1, dequant_nvfp4, e2m1_index, _block_exponent,
- *            _encode_blocks, quant_mxfp4, dequant_mxfp4, requant_rows and
- *            RadianceNvfp4ToMxfp4.process_weights_after_loading.
+ *            _encode_blocks, quant_mxfp4, dequant_mxfp4, requant_rows and the
+ *            process_weights_after_loading of RadianceNvfp4ToMxfp4, RadianceFp8ChannelToMxfp4
+ *            and RadianceBf16ToMxfp4.
  *   [readme] "vllm-radiance (MXFP4)" -- section "How the MXFP4 path works", subsection
  *            "The W4A8 fp8-WMMA kernel" (fp8 activations x e2m1 weights with folded e8m0).
  *   [ar]     "radiance_autoround.py" -- module docstring (format), autoround_linear (per-token
@@ -24,6 +25,7 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
@@ -290,6 +292,72 @@ int orc_requant(const uint8_t *nv_packed, const uint8_t *nv_scale, const float *
         if (err_ssq) { err_ssq[2 * p] = err_sum; err_ssq[2 * p + 1] = ssq_sum; }
         row0 += partition_rows[p];
     }
+    return 0;
+}
+
+/* One layer of already-dequantized rows -> MXFP4 (quant_mxfp4 per 32-block, packing as in
+ * orc_requant).  row(n, w) fills w[0..K) with row n's fp32 weights.  err_ssq, when non-NULL,
+ * receives {sum of squared requant error, sum of squared weights} for the whole layer. */
+typedef void (*orc_row_fn)(const void *ctx, int64_t n, int64_t K, float *w);
+
+static void orc_requant_rows(orc_row_fn row, const void *ctx, int64_t N, int64_t K, int mode,
+                             uint8_t *out_packed, uint8_t *out_e8m0, double *err_ssq)
+{
+    double err_sum = 0.0, ssq_sum = 0.0;
+#pragma omp parallel for schedule(static) reduction(+ : err_sum, ssq_sum)
+    for (int64_t n = 0; n < N; ++n) {
+        float *w = (float *)malloc(sizeof(float) * (size_t)K);
+        uint8_t codes[32];
+        row(ctx, n, K, w);
+        for (int64_t b = 0; b < K / 32; ++b) {
+            double err;
+            int e = orc_quant_block(w + 32 * b, mode, codes, &err);
+            for (int j = 0; j < 16; ++j)
+                out_packed[n * (K / 2) + b * 16 + j] = (uint8_t)(codes[2 * j] | (codes[2 * j + 1] << 4));
+            out_e8m0[n * (K / 32) + b] = (uint8_t)(e + 127);
+            err_sum += err;
+        }
+        for (int64_t k = 0; k < K; ++k) ssq_sum += (double)w[k] * (double)w[k];
+        free(w);
+    }
+    if (err_ssq) { err_ssq[0] = err_sum; err_ssq[1] = ssq_sum; }
+}
+
+/* [nvfp4] RadianceFp8ChannelToMxfp4.process_weights_after_loading: W[n, k] = fp32(w8[n, k]) *
+ * scale[n], the e4m3 code cast to fp32 (exact) times the row's fp32 channel scale, one rounded
+ * fp32 product per element; then quant_mxfp4 and the layer's relRMS sums, as for NVFP4 with the
+ * whole layer as one partition. */
+struct orc_fp8ch { const uint8_t *w8; const float *scale; };
+
+static void orc_fp8ch_row(const void *ctx, int64_t n, int64_t K, float *w)
+{
+    const struct orc_fp8ch *c = (const struct orc_fp8ch *)ctx;
+    const float s = c->scale[n];
+    for (int64_t k = 0; k < K; ++k) w[k] = (float)orc_e4m3_decode(c->w8[n * K + k]) * s;
+}
+
+int orc_requant_fp8_channel(const uint8_t *w8, const float *scale, int64_t N, int64_t K, int mode,
+                            uint8_t *out_packed, uint8_t *out_e8m0, double *err_ssq)
+{
+    if (K % 32 != 0 || mode < 0 || mode > 2 || N < 0) return 1;
+    struct orc_fp8ch c = {w8, scale};
+    orc_requant_rows(orc_fp8ch_row, &c, N, K, mode, out_packed, out_e8m0, err_ssq);
+    return 0;
+}
+
+/* [nvfp4] RadianceBf16ToMxfp4.process_weights_after_loading: requant_rows on the bf16 weight;
+ * the fp32 cast of a bf16 value is exact, so W[n, k] = fp32(w[n, k]). */
+static void orc_bf16_row(const void *ctx, int64_t n, int64_t K, float *w)
+{
+    const uint16_t *wb = (const uint16_t *)ctx;
+    for (int64_t k = 0; k < K; ++k) w[k] = orc_bf16_decode(wb[n * K + k]);
+}
+
+int orc_requant_bf16(const uint16_t *w_bf16, int64_t N, int64_t K, int mode, uint8_t *out_packed,
+                     uint8_t *out_e8m0, double *err_ssq)
+{
+    if (K % 32 != 0 || mode < 0 || mode > 2 || N < 0) return 1;
+    orc_requant_rows(orc_bf16_row, w_bf16, N, K, mode, out_packed, out_e8m0, err_ssq);
     return 0;
 }
 

@@ -226,3 +226,83 @@ def test_nvfp4_producer_roundtrip(orc):
     step = np.where(v < 2, 0.5, np.where(v < 4, 1.0, 2.0))
     q = np.abs(wd.astype(np.float64)) * float(div[0]) / np.repeat(s, 16, axis=1)
     assert np.all(np.abs(np.minimum(v, 6.0) - q) <= step / 2 + 1e-6)
+
+
+# --- other requant sources ("radiance_nvfp4.py": RadianceFp8ChannelToMxfp4, RadianceBf16ToMxfp4)
+
+def _fp8_checkpoint(N, K, seed):
+    """An FP8 per-channel checkpoint built with torch's own e4m3 cast: scale[n] = amax_n / 448,
+    codes = e4m3(w / scale)."""
+    w = synth.gaussian_weights(N, K, 0.02, seed).astype(np.float32)
+    s = (np.max(np.abs(w), axis=1) / np.float32(448.0)).astype(np.float32)
+    q = torch.from_numpy(w / s[:, None]).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).numpy().copy(), s
+
+
+def _check_against_brute(wd, out_p, out_e, es, mode):
+    N, K = wd.shape
+    codes = np.stack([out_p & 0x0F, out_p >> 4], -1).reshape(N, K)
+    err = 0.0
+    for n in range(N):
+        for b in range(K // 32):
+            blk = wd[n, 32 * b:32 * b + 32]
+            e = int(out_e[n, b]) - 127
+            amax = float(np.max(np.abs(blk)))
+            if mode != "mse":
+                assert e == brute_exponent(amax, mode)
+            else:
+                assert e in (brute_exponent(amax, "noclip"), brute_exponent(amax, "noclip") - 1)
+            bc, berr = brute_encode(blk, e)
+            assert np.array_equal(codes[n, 32 * b:32 * b + 32], bc)
+            err += berr
+    assert es[0, 0] == pytest.approx(err, rel=1e-5)
+    assert es[0, 1] == pytest.approx(float(np.sum(wd.astype(np.float64) ** 2)), rel=1e-9)
+
+
+@pytest.mark.parametrize("mode", ["ocp", "noclip", "mse"])
+def test_requant_fp8_channel_vs_independent(orc, mode):
+    N, K = 24, 256
+    w8, s = _fp8_checkpoint(N, K, 11)
+    out_p, out_e, es = orc.requant_fp8_channel(w8, s, mode)
+    # independent dequant: torch's e4m3 decode, then one fp32 product per element
+    wd = (torch.from_numpy(w8).view(torch.float8_e4m3fn).to(torch.float32).numpy() * s[:, None]).astype(np.float32)
+    _check_against_brute(wd, out_p, out_e, es, mode)
+
+
+@pytest.mark.parametrize("mode", ["ocp", "noclip", "mse"])
+def test_requant_bf16_vs_independent(orc, mode):
+    N, K = 16, 320
+    wb = synth.to_bf16_bits(synth.gaussian_weights(N, K, 0.02, 12).astype(np.float64))
+    out_p, out_e, es = orc.requant_bf16(wb, mode)
+    wd = (wb.astype(np.uint32) << 16).view(np.float32)
+    _check_against_brute(wd, out_p, out_e, es, mode)
+
+
+@pytest.mark.parametrize("mode", ["ocp", "noclip", "mse"])
+def test_requant_sources_agree_on_exact_weights(orc, mode):
+    # NVFP4 with a power-of-two divisor dequantizes exactly to values with at most six
+    # significant bits, exact in bf16: the bf16 source must give the NVFP4 result bit for bit
+    N, K = 12, 128
+    packed = synth.uniform_bytes(N, K // 2, 13, 1)
+    scale = synth.uniform_ints(N * K // 16, 0x28, 0x48, 13, 2).astype(np.uint8).reshape(N, K // 16)
+    ref = orc.requant(packed, scale, np.array([1024.0], np.float32), [N], mode)
+    wd = independent_dequant_nvfp4(packed, scale, 1024.0)
+    wb = ((wd.view(np.uint32) >> 16)).astype(np.uint16)
+    assert np.array_equal((wb.astype(np.uint32) << 16).view(np.float32), wd)
+    got = orc.requant_bf16(wb, mode)
+    assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
+    assert got[2][0, 0] == ref[2][0, 0] and got[2][0, 1] == ref[2][0, 1]
+
+
+def test_requant_fp8_channel_closed_forms(orc):
+    # codes 0x38 (1.0) and 0xB8 (-1.0) with scale 2: every block is +-2 -> noclip e = -1,
+    # index 6 (value 4), no error; an all-zero row gives e = 0 and code 0
+    w8 = np.full((3, 64), 0x38, np.uint8)
+    w8[1, ::2] = 0xB8
+    w8[2] = 0
+    out_p, out_e, es = orc.requant_fp8_channel(w8, np.array([2.0, 2.0, 5.0], np.float32), "noclip")
+    assert np.all(out_e[:2] == 126) and np.all(out_e[2] == 127)
+    assert np.all(out_p[0] == 0x66) and np.all(out_p[1] == 0x6E) and np.all(out_p[2] == 0)
+    assert es[0, 0] == 0.0 and es[0, 1] == 2 * 64 * 4.0
+    with pytest.raises(ValueError):
+        orc.requant_fp8_channel(np.zeros((2, 48), np.uint8), np.ones(2, np.float32), "ocp")

@@ -537,7 +537,26 @@ def run_extras(lib, dev, peaks):
     out["requant"] = {"bound": "hbm", "peak_gbs": hbm, "bytes": rq_bytes,
                       "config": "gate_up N=34816 K=5120, partitions 17408+17408, with per-partition error sums",
                       "cases": rq}
-    del nvp, nvs, o_p, o_e
+    del nvp, nvs
+
+    # ---- FP8-per-channel and bf16 -> MXFP4 requant, same shape, mse rule, with error sums
+    w8_h, s8_h = synth.fp8_channel_weights(N, K, 0)
+    w8, s8 = to_dev(w8_h), to_dev(s8_h)
+    ms = timeit(lambda: lib.requant_fp8_channel(w8, s8, "mse", o_p, o_e, err_ssq=True))
+    by = N * K + 4 * N + N * K // 2 + N * K // 32
+    gbs = by / (ms * 1e-3) / 1e9
+    other = {"fp8_channel_mse": {"us": round(ms * 1e3, 1), "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4),
+                                 "bytes": by}}
+    del w8, s8, w8_h
+    wb = torch.from_numpy(synth.bf16_weights(N, K, 0).view(np.int16)).to(dev).view(torch.bfloat16)
+    ms = timeit(lambda: lib.requant_bf16(wb, "mse", o_p, o_e, err_ssq=True))
+    by = 2 * N * K + N * K // 2 + N * K // 32
+    gbs = by / (ms * 1e-3) / 1e9
+    other["bf16_mse"] = {"us": round(ms * 1e3, 1), "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4), "bytes": by}
+    out["requant_other_sources"] = {"bound": "alu (as the NVFP4 requant)", "peak_gbs": hbm,
+                                    "config": "gate_up N=34816 K=5120, one partition, mse rule, with error sums",
+                                    "cases": other}
+    del wb, o_p, o_e
 
     # ---- AutoRound int4 g128: decode weight GB/s, prefill TFLOP/s
     i4 = {}

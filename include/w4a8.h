@@ -156,6 +156,28 @@ W4A8_API w4a8_status nvfp4_to_mxfp4_requant(const uint8_t *nv_packed, const uint
                                    int P, int64_t N, int64_t K, int mode, uint8_t *out_packed,
                                    uint8_t *out_e8m0, double *err_ssq, cudaStream_t stream);
 
+/* FP8-per-channel -> MXFP4 requant ("radiance_nvfp4.py": RadianceFp8ChannelToMxfp4.
+ * process_weights_after_loading, then quant_mxfp4 as above).  Per 32-block of row n:
+ *   R1  w = fl( fp32(e4m3 code) * row_scale[n] ), one rounded fp32 product per element;
+ *   R2-R4 as for nvfp4_to_mxfp4_requant, the whole layer being one partition.
+ *   w_e4m3     [N, K] e4m3 codes, row-major (16-byte aligned)
+ *   row_scale  [N] fp32 per-output-channel scale (4-byte aligned)
+ *   out_packed [N, K/2] (16-byte aligned), out_e8m0 [N, K/32], written
+ *   err_ssq    [1][2] fp64 or NULL: {sum of squared requant error, sum of squared weights}
+ * K must be a multiple of 32; mode as above.  Device pointers, stream-ordered. */
+W4A8_API w4a8_status fp8_channel_to_mxfp4_requant(const uint8_t *w_e4m3, const float *row_scale,
+                                                  int64_t N, int64_t K, int mode,
+                                                  uint8_t *out_packed, uint8_t *out_e8m0,
+                                                  double *err_ssq, cudaStream_t stream);
+
+/* bf16 -> MXFP4 requant ("radiance_nvfp4.py": RadianceBf16ToMxfp4.process_weights_after_loading,
+ * requant_rows, quant_mxfp4).  R1 is the exact fp32 value of each bf16 weight; R2-R4 and the
+ * outputs as for fp8_channel_to_mxfp4_requant.
+ *   w_bf16 [N, K] bf16 bits, row-major (16-byte aligned). */
+W4A8_API w4a8_status bf16_to_mxfp4_requant(const uint16_t *w_bf16, int64_t N, int64_t K, int mode,
+                                           uint8_t *out_packed, uint8_t *out_e8m0, double *err_ssq,
+                                           cudaStream_t stream);
+
 /* AutoRound int4 group-128 symmetric W4A8 linear ("radiance_autoround.py": module docstring,
  * _exact_ref; the symmetric zero point 8 is folded in, so code c means c - 8):
  *   out[m,n] = bf16( x_scale[m] * sum_k e4m3(xq[m,k]) * (c[k,n] - 8) * fp16(s[k/128, n]) )

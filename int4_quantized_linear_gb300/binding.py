@@ -21,7 +21,8 @@ STATUS = {0: "W4A8_OK", 1: "W4A8_ERR_INVALID_ARG", 2: "W4A8_ERR_UNSUPPORTED_SHAP
           6: "W4A8_ERR_TIMEOUT"}
 MODES = {"ocp": 0, "noclip": 1, "mse": 2}
 EXPORTS = ("w4a8_act_quant", "w4a8_mxfp4_linear", "w4a8_workspace_bytes",
-           "nvfp4_to_mxfp4_requant", "w4a8_int4g128_linear", "w4a8_int4g128_workspace_bytes",
+           "nvfp4_to_mxfp4_requant", "fp8_channel_to_mxfp4_requant", "bf16_to_mxfp4_requant",
+           "w4a8_int4g128_linear", "w4a8_int4g128_workspace_bytes",
            "w4a8_status_string", "w4a8_set_gemm_policy", "w4a8_check_device_status",
            "w4a8_decode_max_m", "w4a8_debug_status_words", "w4a8_debug_set_trace",
            "w4a8_mxfp4_linear_noalloc", "w4a8_noalloc_scratch_bytes",
@@ -55,6 +56,8 @@ def load(build_if_missing: bool = True):
         "w4a8_mxfp4_linear": (I, [P, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "w4a8_workspace_bytes": (SZ, [I64, I64, I64]),
         "nvfp4_to_mxfp4_requant": (I, [P, P, P, P, I, I64, I64, I, P, P, P, P]),
+        "fp8_channel_to_mxfp4_requant": (I, [P, P, I64, I64, I, P, P, P, P]),
+        "bf16_to_mxfp4_requant": (I, [P, I64, I64, I, P, P, P, P]),
         "w4a8_int4g128_linear": (I, [P, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "w4a8_int4g128_workspace_bytes": (SZ, [I64, I64, I64]),
         "w4a8_status_string": (ctypes.c_char_p, [I]),
@@ -252,6 +255,44 @@ def requant(nv_packed, nv_scale, divisors, partition_rows, mode="mse", out_packe
         _ptr(nv_packed), _ptr(nv_scale), _ptr(divisors), ctypes.cast(rows, ctypes.c_void_p), P, N,
         K, MODES[mode] if isinstance(mode, str) else int(mode), _ptr(out_packed), _ptr(out_e8m0),
         _ptr(es), _stream(stream)))
+    return out_packed, out_e8m0, es
+
+
+def _requant_outputs(N, K, device, out_packed, out_e8m0, err_ssq):
+    if out_packed is None:
+        out_packed = torch.empty((N, K // 2), dtype=torch.uint8, device=device)
+    if out_e8m0 is None:
+        out_e8m0 = torch.empty((N, K // 32), dtype=torch.uint8, device=device)
+    es = torch.empty((1, 2), dtype=torch.float64, device=device) if err_ssq else None
+    return out_packed, out_e8m0, es
+
+
+def requant_fp8_channel(w_e4m3, row_scale, mode="mse", out_packed=None, out_e8m0=None, err_ssq=True,
+                        stream=None):
+    """FP8 per-channel weight [N, K] (e4m3 codes or float8_e4m3fn) x fp32 scale [N] -> MXFP4.
+    Returns (packed [N, K/2], e8m0 [N, K/32], err_ssq float64 [1, 2] or None)."""
+    if w_e4m3.dtype == torch.float8_e4m3fn:
+        w_e4m3 = w_e4m3.view(torch.uint8)
+    _dev(w_e4m3, "w_e4m3", torch.uint8)
+    row_scale = row_scale.reshape(-1)
+    _dev(row_scale, "row_scale", torch.float32)
+    N, K = w_e4m3.shape
+    out_packed, out_e8m0, es = _requant_outputs(N, K, w_e4m3.device, out_packed, out_e8m0, err_ssq)
+    _check("fp8_channel_to_mxfp4_requant", load().fp8_channel_to_mxfp4_requant(
+        _ptr(w_e4m3), _ptr(row_scale), N, K, MODES[mode] if isinstance(mode, str) else int(mode),
+        _ptr(out_packed), _ptr(out_e8m0), _ptr(es), _stream(stream)))
+    return out_packed, out_e8m0, es
+
+
+def requant_bf16(w_bf16, mode="mse", out_packed=None, out_e8m0=None, err_ssq=True, stream=None):
+    """bf16 weight [N, K] -> MXFP4.  Returns (packed [N, K/2], e8m0 [N, K/32], err_ssq float64
+    [1, 2] or None)."""
+    _dev(w_bf16, "w_bf16", torch.bfloat16)
+    N, K = w_bf16.shape
+    out_packed, out_e8m0, es = _requant_outputs(N, K, w_bf16.device, out_packed, out_e8m0, err_ssq)
+    _check("bf16_to_mxfp4_requant", load().bf16_to_mxfp4_requant(
+        _ptr(w_bf16), N, K, MODES[mode] if isinstance(mode, str) else int(mode), _ptr(out_packed),
+        _ptr(out_e8m0), _ptr(es), _stream(stream)))
     return out_packed, out_e8m0, es
 
 

@@ -1,15 +1,18 @@
-// requant.cu -- NVFP4 -> MXFP4 requant of a (merged) linear at load time.
+// requant.cu -- NVFP4 / FP8-per-channel / bf16 -> MXFP4 requant of a linear at load time.
 //
 // "radiance_nvfp4.py": dequant_nvfp4 (W = e2m1 * fp32(e4m3 scale per 16) / global divisor,
 // per partition of a merged linear), _block_exponent (ocp / noclip), quant_mxfp4 (mse: the
 // no-clip exponent or one binade finer, whichever has the lower squared error), e2m1_index
 // (nearest grid point, ties to the even code), _encode_blocks, and the packing of item 3 of
-// the module docstring (low nibble = even k, e8m0 = e + 127).
+// the module docstring (low nibble = even k, e8m0 = e + 127).  The FP8-per-channel and bf16
+// sources (RadianceFp8ChannelToMxfp4, RadianceBf16ToMxfp4) differ only in the dequantize step
+// and treat the layer as one partition.
 //
-// One thread per 32-block: a 16-byte load of 32 NVFP4 codes plus two e4m3 scale bytes in,
-// a 16-byte store of 32 MXFP4 codes plus one e8m0 byte out, so a warp moves 512 contiguous
-// bytes each way; a persistent grid strides over the blocks of each partition.  The whole block lives in registers; the page's fp32 transient and its row
-// chunking are not needed.  Every fp32 operation is written with an explicit rounding
+// One thread per 32-block: a 16-byte load of 32 NVFP4 codes plus two e4m3 scale bytes in (32
+// bytes of FP8 codes, or 64 of bf16), a 16-byte store of 32 MXFP4 codes plus one e8m0 byte out,
+// so a warp moves 512 contiguous bytes of codes each way; a persistent grid strides over the
+// blocks of each partition.  The whole block lives in registers; the page's fp32 transient and
+// its row chunking are not needed.  Every fp32 operation is written with an explicit rounding
 // intrinsic so that no multiply-add is contracted and the results match the oracle bit for
 // bit: the exponent comes from the float's bits (exact), the scaling by 2^-e is an exact
 // power-of-two product, and the squared errors are summed in ascending k.
@@ -82,26 +85,14 @@ W4A8_DEVICE float encode_block(const float (&w)[32], int e, uint32_t (&codes)[4]
     return S;
 }
 
-// One 32-block: dequantize (R1), choose the exponent (R2), encode (R3) and pack (R4).  Returns
-// the block exponent e; S receives the squared error in scale units and ssq the block's sum of
-// squared dequantized weights.
-W4A8_DEVICE int requant_block(const uint4 &pk, uint16_t sc, float dv, int mode, uint4 &out, float &S, float &ssq)
+// R2-R4 on one 32-block of fp32 weights: choose the exponent (R2), encode (R3) and pack (R4).
+// Returns the block exponent e; S receives the squared error in scale units and ssq the
+// block's sum of squared weights.
+W4A8_DEVICE int quantize_block(const float (&w)[32], int mode, uint4 &out, float &S, float &ssq)
 {
-    const float2 s2 = e4m3x2_to_float2(sc);
-    const float sd0 = __fdiv_rn(s2.x, dv), sd1 = __fdiv_rn(s2.y, dv);
-    // R1: dequantize (one rounded product per element)
-    float w[32];
-    const uint32_t words[4] = {pk.x, pk.y, pk.z, pk.w};
     float amax = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        float2 gv = e2m1x2_to_float2((words[j >> 2] >> (8 * (j & 3))) & 0xffu);
-        float sd = j < 8 ? sd0 : sd1;
-        w[2 * j] = __fmul_rn(gv.x, sd);
-        w[2 * j + 1] = __fmul_rn(gv.y, sd);
-        amax = fmaxf(amax, fmaxf(fabsf(w[2 * j]), fabsf(w[2 * j + 1])));
-    }
-    // R2 + R3: exponent rule and encode
+    for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(w[k]));
     uint32_t codes[4];
     int e;
     if (mode == 2) {
@@ -135,14 +126,76 @@ W4A8_DEVICE int requant_block(const uint4 &pk, uint16_t sc, float dv, int mode, 
     return e;
 }
 
+// R1 sources.  Each yields block g's 32 fp32 weights (row n = g / (K / 32)).
+// NVFP4 ("radiance_nvfp4.py", dequant_nvfp4): w = fl(e2m1 * fl(fp32(e4m3 scale per 16) / divisor))
+// for partition p's divisor: 16 packed bytes and two scale bytes per block.
+struct SrcNvfp4 {
+    const uint8_t *packed, *scale;
+    const float *divisor;
+    W4A8_DEVICE void load(int64_t g, int64_t, int p, float (&w)[32]) const
+    {
+        const uint4 pk = *reinterpret_cast<const uint4 *>(packed + g * 16);
+        const uint16_t sc = *reinterpret_cast<const uint16_t *>(scale + g * 2);
+        const float dv = divisor[p];
+        const float2 s2 = e4m3x2_to_float2(sc);
+        const float sd0 = __fdiv_rn(s2.x, dv), sd1 = __fdiv_rn(s2.y, dv);
+        const uint32_t words[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            float2 gv = e2m1x2_to_float2((words[j >> 2] >> (8 * (j & 3))) & 0xffu);
+            float sd = j < 8 ? sd0 : sd1;
+            w[2 * j] = __fmul_rn(gv.x, sd);
+            w[2 * j + 1] = __fmul_rn(gv.y, sd);
+        }
+    }
+};
+// FP8 per channel ("radiance_nvfp4.py", RadianceFp8ChannelToMxfp4): w = fl(fp32(e4m3 code) *
+// scale[n]), 32 code bytes per block.
+struct SrcFp8Channel {
+    const uint8_t *w8;
+    const float *scale;
+    W4A8_DEVICE void load(int64_t g, int64_t n, int, float (&w)[32]) const
+    {
+        const uint4 a = *reinterpret_cast<const uint4 *>(w8 + g * 32);
+        const uint4 b = *reinterpret_cast<const uint4 *>(w8 + g * 32 + 16);
+        const uint32_t words[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        const float s = scale[n];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float2 v = e4m3x2_to_float2((uint16_t)(words[j >> 1] >> (16 * (j & 1))));
+            w[2 * j] = __fmul_rn(v.x, s);
+            w[2 * j + 1] = __fmul_rn(v.y, s);
+        }
+    }
+};
+// bf16 ("radiance_nvfp4.py", RadianceBf16ToMxfp4): the fp32 value of each bf16 weight (exact),
+// 64 bytes per block.
+struct SrcBf16 {
+    const uint16_t *wb;
+    W4A8_DEVICE void load(int64_t g, int64_t, int, float (&w)[32]) const
+    {
+        const uint4 *src = reinterpret_cast<const uint4 *>(wb + g * 32);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 v = src[q];
+            const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                w[8 * q + 2 * j] = __uint_as_float(words[j] << 16);
+                w[8 * q + 2 * j + 1] = __uint_as_float(words[j] & 0xffff0000u);
+            }
+        }
+    }
+};
+
 // Persistent grid: the partitions one after another; inside a partition every thread walks the
 // 32-blocks with a grid stride, so a warp handles 32 consecutive blocks of a row (512 bytes of
 // codes each way).  The error sums are kept per thread, reduced per CTA and added to the output
 // with one atomic per CTA and partition.
+template <class Src>
 __global__ void __launch_bounds__(RQ_THREADS)
-requant_kernel(const uint8_t *__restrict__ nv_packed, const uint8_t *__restrict__ nv_scale,
-               const float *__restrict__ divisor, Partitions parts, int64_t N, int64_t K,
-               int mode, uint8_t *__restrict__ out_packed, uint8_t *__restrict__ out_e8m0,
+requant_kernel(const Src src, Partitions parts, int64_t N, int64_t K, int mode,
+               uint8_t *__restrict__ out_packed, uint8_t *__restrict__ out_e8m0,
                double *__restrict__ err_ssq)
 {
     __shared__ double red[2][RQ_THREADS / 32];
@@ -151,14 +204,13 @@ requant_kernel(const uint8_t *__restrict__ nv_packed, const uint8_t *__restrict_
     int64_t row_beg = 0;
     for (int p = 0; p < parts.P; ++p) {
         const int64_t row_end = parts.row_end[p];
-        const float dv = divisor[p];
         double err = 0.0, ssq = 0.0;
         for (int64_t g = row_beg * KB + (int64_t)blockIdx.x * RQ_THREADS + threadIdx.x; g < row_end * KB; g += stride) {
-            const uint4 pk = *reinterpret_cast<const uint4 *>(nv_packed + g * 16);
-            const uint16_t sc = *reinterpret_cast<const uint16_t *>(nv_scale + g * 2);
+            float w[32];
+            src.load(g, g / KB, p, w);
             uint4 codes;
             float S, q;
-            const int e = requant_block(pk, sc, dv, mode, codes, S, q);
+            const int e = quantize_block(w, mode, codes, S, q);
             *reinterpret_cast<uint4 *>(out_packed + g * 16) = codes;
             out_e8m0[g] = (uint8_t)(e + 127);
             if (err_ssq) {
@@ -193,6 +245,40 @@ requant_kernel(const uint8_t *__restrict__ nv_packed, const uint8_t *__restrict_
 
 }  // namespace w4a8
 
+namespace w4a8 {
+
+// Persistent grid over all of the layer's 32-blocks: as many CTAs as fit on the GPU at once (or
+// fewer for small layers); err_ssq is zeroed first and receives one atomic pair per CTA and
+// partition.
+template <class Src>
+static w4a8_status launch_requant(const Src &src, const Partitions &parts, int64_t N, int64_t K, int mode,
+                                  uint8_t *out_packed, uint8_t *out_e8m0, double *err_ssq, cudaStream_t stream)
+{
+    if (err_ssq && cudaMemsetAsync(err_ssq, 0, sizeof(double) * 2 * parts.P, stream) != cudaSuccess)
+        return W4A8_ERR_CUDA;
+    const int64_t blocks = N * (K / 32);
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_kernel<Src>, RQ_THREADS, 0) != cudaSuccess)
+        return W4A8_ERR_CUDA;
+    const int64_t need = (blocks + RQ_THREADS - 1) / RQ_THREADS;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sms * std::max(per_sm, 1)));
+    requant_kernel<Src><<<(unsigned)grid, RQ_THREADS, 0, stream>>>(src, parts, N, K, mode, out_packed, out_e8m0,
+                                                                    err_ssq);
+    return w4a8_launch_status();
+}
+
+static Partitions one_partition(int64_t N)
+{
+    Partitions parts;
+    parts.P = 1;
+    for (int p = 0; p < RQ_MAX_PARTS; ++p) parts.row_end[p] = N;
+    return parts;
+}
+
+}  // namespace w4a8
+
 extern "C" w4a8_status nvfp4_to_mxfp4_requant(const uint8_t *nv_packed, const uint8_t *nv_scale_e4m3,
                                               const float *global_divisor,
                                               const int64_t *partition_rows, int P, int64_t N,
@@ -220,21 +306,37 @@ extern "C" w4a8_status nvfp4_to_mxfp4_requant(const uint8_t *nv_packed, const ui
         !w4a8_aligned(nv_scale_e4m3, 2) || !w4a8_aligned(global_divisor, 4) ||
         (err_ssq && !w4a8_aligned(err_ssq, 8)))
         return W4A8_ERR_MISALIGNED;
-    if (err_ssq && cudaMemsetAsync(err_ssq, 0, sizeof(double) * 2 * P, stream) != cudaSuccess)
-        return W4A8_ERR_CUDA;
     // a row's 32-blocks are contiguous in both arrays: block g of the whole tensor sits at
     // packed byte 16 g and scale byte 2 g, so the kernel indexes blocks linearly
-    const int64_t blocks = N * (K / 32);
-    int dev = 0, sms = 0, per_sm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, w4a8::requant_kernel, w4a8::RQ_THREADS, 0) !=
-            cudaSuccess)
-        return W4A8_ERR_CUDA;
-    const int64_t need = (blocks + w4a8::RQ_THREADS - 1) / w4a8::RQ_THREADS;
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sms * std::max(per_sm, 1)));
-    w4a8::requant_kernel<<<(unsigned)grid, w4a8::RQ_THREADS, 0, stream>>>(
-        nv_packed, nv_scale_e4m3, global_divisor, parts, N, K, mode, out_packed, out_e8m0,
-        err_ssq);
-    return w4a8_launch_status();
+    return w4a8::launch_requant(w4a8::SrcNvfp4{nv_packed, nv_scale_e4m3, global_divisor}, parts, N, K, mode,
+                                out_packed, out_e8m0, err_ssq, stream);
+}
+
+extern "C" w4a8_status fp8_channel_to_mxfp4_requant(const uint8_t *w_e4m3, const float *row_scale, int64_t N,
+                                                    int64_t K, int mode, uint8_t *out_packed,
+                                                    uint8_t *out_e8m0, double *err_ssq, cudaStream_t stream)
+{
+    if (N < 0 || K < 0 || mode < 0 || mode > 2) return W4A8_ERR_INVALID_ARG;
+    if (K % 32 != 0) return W4A8_ERR_UNSUPPORTED_SHAPE;
+    if (N == 0 || K == 0) return W4A8_OK;
+    if (!w_e4m3 || !row_scale || !out_packed || !out_e8m0) return W4A8_ERR_INVALID_ARG;
+    if (!w4a8_aligned(w_e4m3, 16) || !w4a8_aligned(out_packed, 16) || !w4a8_aligned(row_scale, 4) ||
+        (err_ssq && !w4a8_aligned(err_ssq, 8)))
+        return W4A8_ERR_MISALIGNED;
+    return w4a8::launch_requant(w4a8::SrcFp8Channel{w_e4m3, row_scale}, w4a8::one_partition(N), N, K, mode,
+                                out_packed, out_e8m0, err_ssq, stream);
+}
+
+extern "C" w4a8_status bf16_to_mxfp4_requant(const uint16_t *w_bf16, int64_t N, int64_t K, int mode,
+                                             uint8_t *out_packed, uint8_t *out_e8m0, double *err_ssq,
+                                             cudaStream_t stream)
+{
+    if (N < 0 || K < 0 || mode < 0 || mode > 2) return W4A8_ERR_INVALID_ARG;
+    if (K % 32 != 0) return W4A8_ERR_UNSUPPORTED_SHAPE;
+    if (N == 0 || K == 0) return W4A8_OK;
+    if (!w_bf16 || !out_packed || !out_e8m0) return W4A8_ERR_INVALID_ARG;
+    if (!w4a8_aligned(w_bf16, 16) || !w4a8_aligned(out_packed, 16) || (err_ssq && !w4a8_aligned(err_ssq, 8)))
+        return W4A8_ERR_MISALIGNED;
+    return w4a8::launch_requant(w4a8::SrcBf16{w_bf16}, w4a8::one_partition(N), N, K, mode, out_packed, out_e8m0,
+                                err_ssq, stream);
 }

@@ -16,6 +16,9 @@ Workload recipes (the served model's linear shapes: hidden 5120, MLP 17408, merg
 * int4:     qweight int32 of uniform nibbles [K/8, N]; scales fp16(|N(0, 0.003)|) [K/128, N];
             qzeros 0x77777777 [K/128, N/8]; x bf16 ~ N(0, 1).
 * requant:  W fp32 ~ N(0, 0.02) [N, K], split into row partitions.
+* fp8 per-channel requant source: e4m3 codes uniform over the 254 finite codes [N, K];
+            row scale fp32 2^u, u uniform in [-12, -6], per row.
+* bf16 requant source: bf16(N(0, 0.02)) [N, K].
 """
 from __future__ import annotations
 
@@ -26,7 +29,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
 # Tensor ids: one independent stream per tensor role.
-T_X, T_OUTLIER, T_OUTLIER_PICK, T_W, T_E, T_ROWSCALE, T_QW, T_QS, T_WREQ, T_NVS = range(1, 11)
+T_X, T_OUTLIER, T_OUTLIER_PICK, T_W, T_E, T_ROWSCALE, T_QW, T_QS, T_WREQ, T_NVS, T_W8, T_W8S, T_WB = range(1, 14)
 
 GATE_UP = (34816, 5120)
 DOWN = (5120, 17408)
@@ -161,3 +164,18 @@ def gaussian_weights(N: int, K: int, sigma: float = 0.02, seed: int = 0,
     if row_gain is not None:
         w = w * np.asarray(row_gain, np.float64)[:, None]
     return w.astype(np.float32)
+
+
+def fp8_channel_weights(N: int, K: int, seed: int = 0):
+    """FP8 per-channel checkpoint stand-in: (codes uint8 [N, K] uniform over the finite e4m3
+    codes, i.e. every byte but 0x7F and 0xFF; row scale float32 [N] = 2^u, u uniform in
+    [-12, -6])."""
+    idx = uniform_ints(N * K, 0, 253, seed, T_W8)
+    codes = (idx + (idx >= 0x7F)).astype(np.uint8)  # skip 0x7F (and so end below 0xFF)
+    u = uniform(seed, T_W8S, N) * 6.0 - 12.0
+    return codes.reshape(N, K), np.exp2(u).astype(np.float32)
+
+
+def bf16_weights(N: int, K: int, seed: int = 0, sigma: float = 0.02) -> np.ndarray:
+    """bf16 bits [N, K] of N(0, sigma) weights."""
+    return to_bf16_bits(normal(seed, T_WB, N * K).reshape(N, K) * sigma)

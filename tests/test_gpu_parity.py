@@ -121,6 +121,77 @@ def test_requant_full_gate_up(lib, orc):
         assert abs(rel_g - orc.rel_rms(rs)) <= 1e-5 * orc.rel_rms(rs)
 
 
+@pytest.mark.parametrize("mode", ["ocp", "noclip", "mse"])
+@pytest.mark.parametrize("N,K", [(1, 32), (70, 384), (257, 1024)])
+def test_requant_fp8_channel_bit_exact(lib, orc, mode, N, K):
+    w8, s = synth.fp8_channel_weights(N, K, seed=N)
+    gp, ge, gs = lib.requant_fp8_channel(to_dev(w8), to_dev(s), mode)
+    rp, re_, rs = orc.requant_fp8_channel(w8, s, mode)
+    assert np.array_equal(host(ge), re_)
+    assert np.array_equal(host(gp), rp)
+    _check_err_ssq(host(gs), rs)
+
+
+@pytest.mark.parametrize("mode", ["ocp", "noclip", "mse"])
+@pytest.mark.parametrize("N,K", [(1, 32), (70, 384), (257, 1024)])
+def test_requant_bf16_bit_exact(lib, orc, mode, N, K):
+    wb = synth.bf16_weights(N, K, seed=N)
+    gp, ge, gs = lib.requant_bf16(to_dev_bf16(wb), mode)
+    rp, re_, rs = orc.requant_bf16(wb, mode)
+    assert np.array_equal(host(ge), re_)
+    assert np.array_equal(host(gp), rp)
+    _check_err_ssq(host(gs), rs)
+
+
+def test_requant_other_sources_degenerate(lib, orc):
+    # zero rows, the largest and smallest e4m3 magnitudes, a zero channel scale, bf16 zeros,
+    # signed zeros and values whose exponent clamps at the e8m0 range
+    w8, s = synth.fp8_channel_weights(6, 64, seed=7)
+    w8[0] = 0
+    w8[1, :32] = 0x7E                    # 448
+    w8[1, 32:] = 0x01                    # 2^-9
+    w8[2] = 0x80                         # -0
+    s[3] = 0.0
+    s[4] = np.float32(2.0 ** -120)
+    wb = synth.bf16_weights(6, 64, seed=8)
+    wb[0] = 0
+    wb[1] = 0x8000                       # -0
+    wb[2, :32] = 0x7F7F                  # largest finite bf16
+    wb[3, :32] = 0x0001                  # smallest subnormal bf16
+    for mode in ("ocp", "noclip", "mse"):
+        gp, ge, _ = lib.requant_fp8_channel(to_dev(w8), to_dev(s), mode)
+        rp, re_, _ = orc.requant_fp8_channel(w8, s, mode)
+        assert np.array_equal(host(ge), re_) and np.array_equal(host(gp), rp), mode
+        gp, ge, _ = lib.requant_bf16(to_dev_bf16(wb), mode)
+        rp, re_, _ = orc.requant_bf16(wb, mode)
+        assert np.array_equal(host(ge), re_) and np.array_equal(host(gp), rp), mode
+
+
+@pytest.mark.slow
+def test_requant_other_sources_full_gate_up(lib, orc):
+    N, K = GATE_UP
+    w8, s = synth.fp8_channel_weights(N, K, seed=1)
+    gp, ge, gs = lib.requant_fp8_channel(to_dev(w8), to_dev(s), "mse")
+    rp, re_, rs = orc.requant_fp8_channel(w8, s, "mse")
+    assert np.array_equal(host(ge), re_) and np.array_equal(host(gp), rp)
+    _check_err_ssq(host(gs), rs)
+    del w8, gp, ge
+    wb = synth.bf16_weights(N, K, seed=2)
+    gp, ge, gs = lib.requant_bf16(to_dev_bf16(wb), "mse")
+    rp, re_, rs = orc.requant_bf16(wb, "mse")
+    assert np.array_equal(host(ge), re_) and np.array_equal(host(gp), rp)
+    _check_err_ssq(host(gs), rs)
+
+
+def test_requant_other_sources_reject(lib):
+    w = torch.zeros((4, 48), dtype=torch.uint8, device="cuda")
+    with pytest.raises(lib.W4A8Error):
+        lib.requant_fp8_channel(w, torch.ones(4, dtype=torch.float32, device="cuda"), "mse")  # K % 32
+    wb = torch.zeros((4, 40), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(lib.W4A8Error):
+        lib.requant_bf16(wb, "ocp")
+
+
 def test_requant_rejects(lib):
     p = torch.zeros((4, 16), dtype=torch.uint8, device="cuda")
     s = torch.zeros((4, 2), dtype=torch.uint8, device="cuda")

@@ -19,6 +19,7 @@ Workload recipes (the served model's linear shapes: hidden 5120, MLP 17408, merg
 * fp8 per-channel requant source: e4m3 codes uniform over the 254 finite codes [N, K];
             row scale fp32 2^u, u uniform in [-12, -6], per row.
 * bf16 requant source: bf16(N(0, 0.02)) [N, K].
+* int4 asymmetric: as int4, with qzeros [K/128, ceil(N/8)] of uniform nibbles (zero points 1..16).
 """
 from __future__ import annotations
 
@@ -29,7 +30,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
 # Tensor ids: one independent stream per tensor role.
-T_X, T_OUTLIER, T_OUTLIER_PICK, T_W, T_E, T_ROWSCALE, T_QW, T_QS, T_WREQ, T_NVS, T_W8, T_W8S, T_WB = range(1, 14)
+T_X, T_OUTLIER, T_OUTLIER_PICK, T_W, T_E, T_ROWSCALE, T_QW, T_QS, T_WREQ, T_NVS, T_W8, T_W8S, T_WB, T_QZ = range(1, 15)
 
 GATE_UP = (34816, 5120)
 DOWN = (5120, 17408)
@@ -179,3 +180,10 @@ def fp8_channel_weights(N: int, K: int, seed: int = 0):
 def bf16_weights(N: int, K: int, seed: int = 0, sigma: float = 0.02) -> np.ndarray:
     """bf16 bits [N, K] of N(0, sigma) weights."""
     return to_bf16_bits(normal(seed, T_WB, N * K).reshape(N, K) * sigma)
+
+
+def int4_asym_zeros(N: int, K: int, seed: int = 0) -> np.ndarray:
+    """qzeros int32 [K/128, ceil(N/8)] of uniform nibbles."""
+    nz = (N + 7) // 8
+    words = (u64(seed, T_QZ, (K // 128) * nz) & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+    return words.reshape(K // 128, nz).view(np.int32)

@@ -72,6 +72,8 @@ def _load():
             "orc_mxfp4_linear_pairs": (None, [P, P, P, P, I64, P, P, I64, P]),
             "orc_int4g128_linear": (None, [P, P, P, P, I64, I64, I64, P]),
             "orc_int4g128_linear_pairs": (None, [P, P, P, P, I64, I64, P, P, I64, P]),
+            "orc_int4g128_asym_linear": (None, [P, P, P, P, P, I64, I64, I64, P]),
+            "orc_int4g128_asym_linear_pairs": (None, [P, P, P, P, P, I64, I64, P, P, I64, P]),
             "orc_e4m3_encode_many": (None, [P, I64, P]),
             "orc_e4m3_decode_many": (None, [P, I64, P]),
             "orc_fp16_decode_many": (None, [P, I64, P]),
@@ -284,4 +286,33 @@ def int4g128_linear_pairs(xq, x_scale, qweight, scales_fp16, idx_m, idx_n) -> np
     N = q.shape[1]
     out = np.empty(im.size, np.float64)
     _load().orc_int4g128_linear_pairs(xp, sp, qp, scp, N, K, imp, inp, im.size, _p(out))
+    return out
+
+
+def int4g128_asym_linear(xq, x_scale, qweight, scales_fp16, qzeros) -> np.ndarray:
+    """Asymmetric int4 g128: zero point 1 + nibble of qzeros [K/128, ceil(N/8)] per (group, column)."""
+    x, xp = _c(xq, np.uint8)
+    s, sp = _c(x_scale, np.float32)
+    q, qp = _c(qweight, np.int32)
+    sc, scp = _c(scales_fp16, np.uint16)
+    z, zp = _c(qzeros, np.int32)
+    M, K = x.shape
+    N = q.shape[1]
+    out = np.empty((M, N), np.float64)
+    _load().orc_int4g128_asym_linear(xp, sp, qp, scp, zp, M, N, K, _p(out))
+    return out
+
+
+def int4g128_asym_linear_pairs(xq, x_scale, qweight, scales_fp16, qzeros, idx_m, idx_n) -> np.ndarray:
+    x, xp = _c(xq, np.uint8)
+    s, sp = _c(x_scale, np.float32)
+    q, qp = _c(qweight, np.int32)
+    sc, scp = _c(scales_fp16, np.uint16)
+    z, zp = _c(qzeros, np.int32)
+    im, imp = _c(idx_m, np.int64)
+    inn, inp = _c(idx_n, np.int64)
+    K = x.shape[1]
+    N = q.shape[1]
+    out = np.empty(im.size, np.float64)
+    _load().orc_int4g128_asym_linear_pairs(xp, sp, qp, scp, zp, N, K, imp, inp, im.size, _p(out))
     return out

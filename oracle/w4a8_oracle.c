@@ -510,6 +510,48 @@ void orc_int4g128_linear(const uint8_t *xq, const float *x_scale, const int32_t 
         }
 }
 
+/* Asymmetric int4 group-128 ("vllm-radiance (MXFP4)", section "ParoQuant (int4 W4A8 and int5 W5A8)":
+ * int4 group-128 asymmetric, the zero point folded into the GEMM as a row-sum correction).  The
+ * zero point of group g and column n is z = 1 + nibble (n % 8) of qzeros[g, n / 8] -- reading:
+ * the packed-qzeros convention under which the symmetric checkpoint's 0x77777777 means the
+ * zero point 8 that "radiance_autoround.py" states -- and the weight is (c - z) * s:
+ *   out[m, n] = scale[m] * sum_k e4m3(xq[m, k]) * (c[k, n] - z[k/128, n]) * fp16(s[k/128, n]). */
+static double orc_int4_asym_dot(const uint8_t *xq, const int32_t *qweight, const uint16_t *scales_fp16,
+                                const int32_t *qzeros, int64_t N, int64_t K, int64_t m, int64_t n)
+{
+    const int64_t NZ = (N + 7) / 8;
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        uint32_t word = (uint32_t)qweight[(k / 8) * N + n];
+        int c = (int)((word >> (4 * (k % 8))) & 0xF);
+        uint32_t zw = (uint32_t)qzeros[(k / 128) * NZ + n / 8];
+        int z = 1 + (int)((zw >> (4 * (n % 8))) & 0xF);
+        double wv = (double)(c - z) * orc_fp16_decode(scales_fp16[(k / 128) * N + n]);
+        acc += orc_e4m3_decode(xq[m * K + k]) * wv;
+    }
+    return acc;
+}
+
+void orc_int4g128_asym_linear(const uint8_t *xq, const float *x_scale, const int32_t *qweight,
+                              const uint16_t *scales_fp16, const int32_t *qzeros, int64_t M, int64_t N,
+                              int64_t K, double *out)
+{
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            out[m * N + n] = (double)x_scale[m] * orc_int4_asym_dot(xq, qweight, scales_fp16, qzeros, N, K, m, n);
+}
+
+void orc_int4g128_asym_linear_pairs(const uint8_t *xq, const float *x_scale, const int32_t *qweight,
+                                    const uint16_t *scales_fp16, const int32_t *qzeros, int64_t N, int64_t K,
+                                    const int64_t *idx_m, const int64_t *idx_n, int64_t count, double *out)
+{
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t i = 0; i < count; ++i)
+        out[i] = (double)x_scale[idx_m[i]] *
+                 orc_int4_asym_dot(xq, qweight, scales_fp16, qzeros, N, K, idx_m[i], idx_n[i]);
+}
+
 /* Number of threads the parallel loops above use (1 without OpenMP). */
 int orc_num_threads(void)
 {

@@ -124,3 +124,59 @@ def test_int4_linear_closed_forms(orc):
     out = orc.int4g128_linear(xq, sc, qw.view(np.int32), s16)
     assert out[0, 0] == 2.0 * 256
     assert out[0, 1] == 2.0 * (64 * -8.0 * 1.0 + 64 * -8.0 * 0.5)
+
+
+# --- asymmetric int4 g128 ("vllm-radiance (MXFP4)", ParoQuant: asymmetric zero point)
+
+def independent_int4_asym_ref(xq, sc, qw, s16, qz):
+    """Numpy restatement: w[k, n] = (c - (1 + z nibble)) * s, then the dot in float64."""
+    K = xq.shape[1]
+    N = qw.shape[1]
+    words = qw.view(np.uint32)
+    c = np.stack([(words >> np.uint32(4 * j)) & np.uint32(0xF) for j in range(8)], 1).reshape(K, N).astype(np.float64)
+    zw = qz.view(np.uint32)
+    z = np.empty((K // 128, N))
+    for n in range(N):
+        z[:, n] = 1 + ((zw[:, n // 8] >> np.uint32(4 * (n % 8))) & np.uint32(0xF)).astype(np.float64)
+    s = torch.from_numpy(s16.view(np.float16)).to(torch.float64).numpy()
+    w = (c - np.repeat(z, 128, axis=0)) * np.repeat(s, 128, axis=0)
+    xv = torch.from_numpy(xq).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return sc.astype(np.float64)[:, None] * (xv @ w)
+
+
+def test_int4_asym_vs_independent(orc):
+    M, N, K = 3, 40, 384
+    x, qw, s16, _ = synth.int4_case(M, N, K, seed=6)
+    qz = synth.int4_asym_zeros(N, K, seed=6)
+    xq, sc = orc.act_quant(x)
+    out = orc.int4g128_asym_linear(xq, sc, qw, s16, qz)
+    ref = independent_int4_asym_ref(xq, sc, qw, s16, qz)
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    im = np.array([2, 0, 1]); inn = np.array([39, 8, 17])
+    assert np.array_equal(orc.int4g128_asym_linear_pairs(xq, sc, qw, s16, qz, im, inn), out[im, inn])
+
+
+def test_int4_asym_reduces_to_symmetric(orc):
+    # qzeros 0x77777777 is the zero point 8 of the symmetric format
+    M, N, K = 2, 24, 256
+    x, qw, s16, qz = synth.int4_case(M, N, K, seed=7)
+    assert np.all(qz.view(np.uint32) == 0x77777777)
+    xq, sc = orc.act_quant(x)
+    assert np.array_equal(orc.int4g128_asym_linear(xq, sc, qw, s16, qz[:, :3]), orc.int4g128_linear(xq, sc, qw, s16))
+
+
+def test_int4_asym_closed_forms(orc):
+    # x = 1, scale 1: column 0 codes 5 with zero point 3 (nibble 2) -> +2 per k; column 1 codes
+    # 0 with zero point 16 (nibble 15) -> -16 per k; column 9 codes 15 with zero point 1 -> +14
+    M, N, K = 1, 10, 128
+    xq = np.full((M, K), 0x38, np.uint8)
+    sc = np.array([1.0], np.float32)
+    qw = np.zeros((K // 8, N), np.uint32)
+    qw[:, 0] = 0x55555555
+    qw[:, 9] = 0xFFFFFFFF
+    s16 = np.full((K // 128, N), 0x3C00, np.uint16)
+    qz = np.zeros((1, 2), np.uint32)
+    qz[0, 0] = 0x000000F2           # column 0: nibble 2, column 1: nibble 15
+    qz[0, 1] = 0x00000000           # column 9 (word 1, nibble 1): nibble 0
+    out = orc.int4g128_asym_linear(xq, sc, qw.view(np.int32), s16, qz.view(np.int32))
+    assert out[0, 0] == 2.0 * K and out[0, 1] == -16.0 * K and out[0, 9] == 14.0 * K

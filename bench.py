@@ -586,6 +586,28 @@ def run_extras(lib, dev, peaks):
         i4[f"{name}_M{M}"] = {"ms": round(ms, 3), "tflops": round(tf, 1), "frac_of_fp8_peak": round(tf / fp8_peak, 4)}
         del qws, scs
     out["int4g128"] = {"decode_bound": "hbm", "prefill_bound": "tensor (fp8 peak)", "cases": i4}
+
+    # ---- asymmetric int4 g128 (per-group, per-column zero points): decode GB/s, M = 1 and 64
+    i4a = {}
+    for name, (N, K) in SHAPES:
+        qw, sc, _ = synth.int4_weights(N, K, 0)
+        qz = to_dev(synth.int4_asym_zeros(N, K, 0))
+        wb = N * K // 2 + N * K // 64 + (K // 128) * ((N + 7) // 8) * 4
+        qws = [to_dev(qw) for _ in range(3)]
+        scs = [to_dev(sc).view(torch.float16) for _ in range(3)]
+        for M in (1, 64):
+            x = torch.randn((M, K), device=dev).to(torch.bfloat16)
+            xq, xs = lib.act_quant(x)
+            o = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ws = lib.make_workspace(lib.int4_workspace_bytes(M, N, K), dev)
+            fns = [lambda a=a, b=b: lib.int4g128_asym_linear(xq, xs, a, b, qz, out=o, workspace=ws)
+                   for a, b in zip(qws, scs)]
+            ms = timeit_rot(fns)
+            gbs = wb / (ms * 1e-3) / 1e9
+            i4a[f"{name}_M{M}"] = {"us": round(ms * 1e3, 2), "weight GB/s": round(gbs, 1),
+                                   "frac_of_hbm": round(gbs / hbm, 4)}
+        del qws, scs, qz
+    out["int4g128_asym"] = {"decode_bound": "hbm", "cases": i4a}
     return out
 
 

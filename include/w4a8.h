@@ -195,6 +195,22 @@ W4A8_API w4a8_status w4a8_int4g128_linear(const uint8_t *xq, const float *x_scal
 
 W4A8_API size_t w4a8_int4g128_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
+/* Asymmetric int4 group-128 W4A8 linear ("vllm-radiance (MXFP4)", section "ParoQuant (int4 W4A8
+ * and int5 W5A8)": int4 group-128 asymmetric, the zero point folded into the GEMM as a row-sum
+ * correction rather than dequantized into the operand).
+ *   out[m, n] = bf16( x_scale[m] * sum_g s[g, n] * sum_{k in g} e4m3(xq[m, k]) * (c[k, n] - z[g, n]) )
+ * with z[g, n] = 1 + nibble (n % 8) of qzeros[g, n / 8] (the packed convention under which the
+ * symmetric format's 0x77777777 is the zero point 8), so z is in [1, 16].
+ *   qzeros [K/128, ceil(N/8)] int32 (4-byte aligned, non-NULL); every other argument, the
+ *   workspace (w4a8_int4g128_workspace_bytes) and the errors as for w4a8_int4g128_linear.
+ * The tensor-core kernel keeps the activations' per-group sums (times -8 * 2^-9) in a second
+ * tensor-memory accumulator and applies each column's z in the fp32 promotion. */
+W4A8_API w4a8_status w4a8_int4g128_asym_linear(const uint8_t *xq, const float *x_scale,
+                                               const int32_t *qweight, const uint16_t *scales_fp16,
+                                               const int32_t *qzeros, uint16_t *out_bf16, int64_t M,
+                                               int64_t N, int64_t K, void *workspace,
+                                               size_t workspace_bytes, cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 W4A8_API const char *w4a8_status_string(w4a8_status s);
 

@@ -18,7 +18,8 @@ w4a8_status w4a8_launch_mxfp4_simt(const uint8_t *xq, const float *x_scale, cons
                                    int64_t K, cudaStream_t stream);
 w4a8_status w4a8_launch_int4_simt(const uint8_t *xq, const float *x_scale, const int32_t *qw,
                                   const uint16_t *s16, uint16_t *out, int64_t M, int64_t N,
-                                  int64_t K, cudaStream_t stream);
+                                  int64_t K, cudaStream_t stream,
+                                  const int32_t *qzeros = nullptr);
 
 // Tensor-core (tcgen05) paths.
 bool w4a8_tc_mxfp4_supported(const void *xq, const void *wp, const void *we, const void *out,
@@ -41,4 +42,5 @@ bool w4a8_tc_int4_supported(const void *xq, const void *qw, const void *s16, con
 size_t w4a8_tc_int4_workspace_bytes(int64_t M, int64_t N, int64_t K, int policy);
 w4a8_status w4a8_launch_int4_tc(const uint8_t *xq, const float *x_scale, const int32_t *qw,
                                 const uint16_t *s16, uint16_t *out, int64_t M, int64_t N,
-                                int64_t K, void *workspace, int policy, cudaStream_t stream);
+                                int64_t K, void *workspace, int policy, cudaStream_t stream,
+                                const int32_t *qzeros = nullptr);

@@ -77,6 +77,7 @@ enum : unsigned { ST_TIMEOUT_PRODUCER = 1, ST_TIMEOUT_GATE = 2, ST_TIMEOUT_CONV 
 struct Params {
     const uint16_t *s16;   // [K/128, N] fp16 group scales
     const float *xs;       // [M] per-token scale
+    const int32_t *qz;     // asymmetric only: [K/128, ceil(N/8)] packed zero points minus one
     uint16_t *out;         // [M, N] bf16
     float *partials;       // [G][2][BN][128] fp32 stream-K partial tiles
     int *counters;         // [tiles] arrival counters, zero between calls
@@ -101,7 +102,7 @@ __device__ __forceinline__ void trace_ev(const Params &p, int ev, int i)
 // Shared memory: the zero-point operand atom (1 KB), NA converted operand tiles, then a ring of US
 // fills, each holding KPU k-tiles of activations (BN x 128 bytes, swizzled) and of checkpoint
 // words ([16 word rows][128 columns]).
-template <int BN, int US, int NA, int NB>
+template <int BN, int US, int NA, int NB, bool ASYM = false>
 struct Layout {
     static constexpr int RAW_TILE = 16 * BM * 4;  // 8 KB of words: 128 k x 128 columns
     static constexpr int X_TILE = BN * 128;
@@ -119,9 +120,10 @@ struct Layout {
     static constexpr int STAGE_OFF = (XS_OFF + BN * 4 + 1023) / 1024 * 1024;
     static constexpr int TOTAL = STAGE_OFF + NSTAGE * STAGE_BYTES + 1024;  // + alignment slack
     static constexpr int TX_BYTES = KPU * (RAW_TILE + X_TILE);
-    static constexpr int TMEM_NEED = NB * BN;
-    static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128 : 256;
-    static_assert(TMEM_NEED <= 256, "tensor memory");
+    static constexpr int TMEM_NEED = NB * BN * (ASYM ? 2 : 1);  // + the zero-point sums (asymmetric)
+    static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128
+                                     : TMEM_NEED <= 256 ? 256 : 512;
+    static_assert(TMEM_NEED <= 512, "tensor memory");
     static_assert(TOTAL <= 232448, "shared memory");
     static_assert((X_TILE % 1024) == 0 && (X_OFF % 1024) == 0 && (A_TILE % 1024) == 0, "swizzled tiles");
     static_assert(8 * (2 * US + NA + 2 * NB + 1) + 32 <= 512, "barrier area");
@@ -139,12 +141,12 @@ __device__ __forceinline__ uint2 i4x8_to_bytes(uint32_t w)
 
 constexpr uint32_t E4M3_MINUS_2POW_M6 = 0x88u;  // sign 1, exponent field 1, mantissa 0: -2^-6
 
-template <int BN, int US, int NA, int NB>
+template <int BN, int US, int NA, int NB, bool ASYM>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_x,
                const __grid_constant__ CUtensorMap tmap_out, const Params p)
 {
-    using L = Layout<BN, US, NA, NB>;
+    using L = Layout<BN, US, NA, NB, ASYM>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);  // ring fill landed
@@ -285,11 +287,13 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                 for (int kk = 0; kk < 4; ++kk)
                     tc::mma_f8f6f4(tmem + b * BN, tc::smem_desc(aa + 32 * kk, 16, 1024, 2),
                                    tc::smem_desc(xa + 32 * kk, 16, 1024, 2), idesc, kk > 0 ? 1u : 0u);
-                // zero point: the constant atom for every 8-row group (stride 0)
+                // zero point: the constant atom for every 8-row group (stride 0); with per-column
+                // zero points (asymmetric) into a buffer of its own, scaled per column in promotion
+                const uint32_t zacc = tmem + (ASYM ? NB + b : b) * BN;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    tc::mma_f8f6f4(tmem + b * BN, tc::smem_desc(za + 32 * kk, 16, 0, 2),
-                                   tc::smem_desc(xa + 32 * kk, 16, 1024, 2), idesc, 1u);
+                    tc::mma_f8f6f4(zacc, tc::smem_desc(za + 32 * kk, 16, 0, 2),
+                                   tc::smem_desc(xa + 32 * kk, 16, 1024, 2), idesc, (ASYM && kk == 0) ? 0u : 1u);
                 tc::tc_commit(&g_full[b]);
                 if (j == KPU - 1) tc::tc_commit(&empty[sl]);
             }
@@ -340,8 +344,24 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             for (int jj = 0; jj < 4; ++jj)
                 dst[jj] = n < p.N ? 512.0f * __half2float(__ushort_as_half(__ldg(p.s16 + (size_t)(g0 + jj) * p.N + n))) : 0.0f;
         };
+        // asymmetric: the unit's zero points z of this thread's column, as z / 8 (exact)
+        auto unit_zeros = [&](int pu, float (&dst)[4]) {
+            if (pu >= sched.n_units) return;
+            const long long u = sched.unit_at(pu);
+            const int t = (int)div_nonneg(u, p.U);
+            const int n = (t / p.m_tiles) * BM + r;
+            const int g0 = (int)(u - (long long)t * p.U) * 4;
+            const int nz = (p.N + 7) / 8;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const uint32_t w = n < p.N ? (uint32_t)__ldg(p.qz + (size_t)(g0 + jj) * nz + n / 8) : 0x77777777u;
+                dst[jj] = 0.125f * (float)(1 + ((w >> (4 * (n & 7))) & 0xfu));
+            }
+        };
         float sc_cur[4] = {0.0f, 0.0f, 0.0f, 0.0f}, sc_nxt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float zf_cur[4] = {1.0f, 1.0f, 1.0f, 1.0f}, zf_nxt[4] = {1.0f, 1.0f, 1.0f, 1.0f};
         unit_scales(0, sc_nxt);
+        if (ASYM) unit_zeros(0, zf_nxt);
         int i = 0;  // k-tile position, in the order the MMAs run
         for (int seg = 0; seg < sched.S; ++seg) {
             long long u, ue;
@@ -362,6 +382,11 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
 #pragma unroll
                     for (int z = 0; z < 4; ++z) sc_cur[z] = sc_nxt[z];
                     unit_scales(i / 4 + 1, sc_nxt);
+                    if (ASYM) {
+#pragma unroll
+                        for (int z = 0; z < 4; ++z) zf_cur[z] = zf_nxt[z];
+                        unit_zeros(i / 4 + 1, zf_nxt);
+                    }
                 }
                 int w = 0;
                 if (lane == 0) w = tc::mbar_wait(&g_full[b], (i / NB) & 1, abort_flag, WAIT_BUDGET);
@@ -383,8 +408,19 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                     uint32_t v[16];
                     tc::tmem_ld16(tb + c0, v);
                     tc::tmem_ld_wait();
+                    if constexpr (ASYM) {
+                        // 512 s (P + (z/8) Z) = s (sum c x - z sum x), Z = -2^-6 sum x
+                        const float zf = jj == 0 ? zf_cur[0] : jj == 1 ? zf_cur[1] : jj == 2 ? zf_cur[2] : zf_cur[3];
+                        uint32_t vz[16];
+                        tc::tmem_ld16(tb + NB * BN + c0, vz);
+                        tc::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) acc[c0 + j] = fmaf(s, __uint_as_float(v[j]), acc[c0 + j]);
+                        for (int j = 0; j < 16; ++j)
+                            acc[c0 + j] = fmaf(s, fmaf(zf, __uint_as_float(vz[j]), __uint_as_float(v[j])), acc[c0 + j]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) acc[c0 + j] = fmaf(s, __uint_as_float(v[j]), acc[c0 + j]);
+                    }
                 }
                 tc::tc_fence_before();
                 __syncwarp();
@@ -491,10 +527,10 @@ static size_t partial_bytes(const Cfg &c)
     return (b + 255) / 256 * 256;
 }
 
-template <int BN, int US, int NA, int NB>
+template <int BN, int US, int NA, int NB, bool ASYM>
 static w4a8_status launch(const int32_t *qw, const uint8_t *xq, Params prm, cudaStream_t stream)
 {
-    using L = Layout<BN, US, NA, NB>;
+    using L = Layout<BN, US, NA, NB, ASYM>;
     CUtensorMap tq, tx, tout;
     memset(&tout, 0, sizeof(tout));
     prm.tma_out = (prm.N % 8 == 0) && w4a8_aligned(prm.out, 16) &&
@@ -506,7 +542,7 @@ static w4a8_status launch(const int32_t *qw, const uint8_t *xq, Params prm, cuda
                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !tch::tmap_3d_ktiles(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, prm.M, prm.K, 128, prm.K / 128, BN, KPU))
         return W4A8_ERR_CUDA;
-    auto kern = int4_tc_kernel<BN, US, NA, NB>;
+    auto kern = int4_tc_kernel<BN, US, NA, NB, ASYM>;
     static int attr_done[64] = {0};
     if (!tch::set_smem_once(kern, L::TOTAL, attr_done)) return W4A8_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -551,12 +587,13 @@ size_t w4a8_tc_int4_workspace_bytes(int64_t M, int64_t N, int64_t K, int policy)
 
 w4a8_status w4a8_launch_int4_tc(const uint8_t *xq, const float *x_scale, const int32_t *qw, const uint16_t *s16,
                                 uint16_t *out, int64_t M, int64_t N, int64_t K, void *workspace, int,
-                                cudaStream_t stream)
+                                cudaStream_t stream, const int32_t *qzeros)
 {
     const Cfg c = w4a8::tci::choose(M, N, K);
     Params prm;
     prm.s16 = s16;
     prm.xs = x_scale;
+    prm.qz = qzeros;
     prm.out = out;
     prm.partials = static_cast<float *>(workspace);
     prm.counters = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) + partial_bytes(c));
@@ -575,9 +612,16 @@ w4a8_status w4a8_launch_int4_tc(const uint8_t *xq, const float *x_scale, const i
     prm.Gsk = c.k.Gsk;
     prm.tma_out = 0;
     prm.trace = static_cast<unsigned long long *>(w4a8_debug_trace_ptr());
+    if (qzeros != nullptr) {
+        switch (c.BN) {
+        case 16: return launch<16, 4, 3, 4, true>(qw, xq, prm, stream);
+        case 32: return launch<32, 3, 3, 4, true>(qw, xq, prm, stream);
+        default: return launch<64, 2, 3, 4, true>(qw, xq, prm, stream);
+        }
+    }
     switch (c.BN) {
-    case 16: return launch<16, 4, 3, 4>(qw, xq, prm, stream);
-    case 32: return launch<32, 3, 3, 4>(qw, xq, prm, stream);
-    default: return launch<64, 2, 3, 4>(qw, xq, prm, stream);
+    case 16: return launch<16, 4, 3, 4, false>(qw, xq, prm, stream);
+    case 32: return launch<32, 3, 3, 4, false>(qw, xq, prm, stream);
+    default: return launch<64, 2, 3, 4, false>(qw, xq, prm, stream);
     }
 }

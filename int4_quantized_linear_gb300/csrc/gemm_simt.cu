@@ -11,8 +11,9 @@
 //
 // int4 ("radiance_autoround.py", module docstring / _exact_ref): one thread per output column
 // n and up to MT tokens; a warp reads 32 consecutive qweight words of one K/8 row (128
-// coalesced bytes of the checkpoint's [K/8, N] layout).  Per 128-group the (c - 8) x e4m3
-// products are summed in fp32 and multiplied by the group's fp16 scale.
+// coalesced bytes of the checkpoint's [K/8, N] layout).  Per 128-group the (c - z) x e4m3
+// products are summed in fp32 and multiplied by the group's fp16 scale; z = 8, or for the
+// asymmetric format ("vllm-radiance (MXFP4)", ParoQuant) 1 + the column's qzeros nibble.
 #include "common.cuh"
 
 namespace w4a8 {
@@ -75,7 +76,8 @@ template <int MT>
 __global__ void __launch_bounds__(128)
 int4_simt_kernel(const uint8_t *__restrict__ xq, const float *__restrict__ x_scale,
                  const uint32_t *__restrict__ qw, const uint16_t *__restrict__ s16,
-                 uint16_t *__restrict__ out, int64_t M, int64_t N, int64_t K)
+                 const uint32_t *__restrict__ qz, uint16_t *__restrict__ out, int64_t M, int64_t N,
+                 int64_t K)
 {
     const int64_t n = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t m0 = (int64_t)blockIdx.y * MT;
@@ -87,11 +89,13 @@ int4_simt_kernel(const uint8_t *__restrict__ xq, const float *__restrict__ x_sca
         float part[MT];
 #pragma unroll
         for (int t = 0; t < MT; ++t) part[t] = 0.0f;
+        // zero point 8, or (asymmetric) 1 + the column's nibble of the group's qzeros word
+        const int z = qz ? 1 + (int)((__ldg(qz + g * ((N + 7) / 8) + n / 8) >> (4 * (n & 7))) & 0xfu) : 8;
         for (int i = 0; i < 16; ++i) {
             const uint32_t word = __ldg(qw + (g * 16 + i) * N + n);
             float w[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) w[j] = (float)((int)((word >> (4 * j)) & 0xfu) - 8);
+            for (int j = 0; j < 8; ++j) w[j] = (float)((int)((word >> (4 * j)) & 0xfu) - z);
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
                 if (m0 + t < M) {
@@ -132,11 +136,12 @@ w4a8_status w4a8_launch_mxfp4_simt(const uint8_t *xq, const float *x_scale, cons
 
 w4a8_status w4a8_launch_int4_simt(const uint8_t *xq, const float *x_scale, const int32_t *qw,
                                   const uint16_t *s16, uint16_t *out, int64_t M, int64_t N,
-                                  int64_t K, cudaStream_t stream)
+                                  int64_t K, cudaStream_t stream, const int32_t *qzeros)
 {
     dim3 grid((unsigned)((N + 127) / 128), (unsigned)((M + w4a8::SIMT_MT - 1) / w4a8::SIMT_MT));
     if (grid.y > 65535u) return W4A8_ERR_UNSUPPORTED_SHAPE;
     w4a8::int4_simt_kernel<w4a8::SIMT_MT><<<grid, 128, 0, stream>>>(
-        xq, x_scale, reinterpret_cast<const uint32_t *>(qw), s16, out, M, N, K);
+        xq, x_scale, reinterpret_cast<const uint32_t *>(qw), s16, reinterpret_cast<const uint32_t *>(qzeros), out, M, N,
+        K);
     return w4a8_launch_status();
 }

@@ -401,6 +401,46 @@ def test_int4_full_sampled(lib, orc, shape, M):
     gemm_check(got, ref, f"int4 M={M} N={N} K={K}")
 
 
+def _i4_asym_gemm(lib, orc, x, qw, s16, qz, pairs=None):
+    xq, xs = lib.act_quant(to_dev_bf16(x))
+    out = lib.int4g128_asym_linear(xq, xs, to_dev(qw), to_dev_fp16(s16), to_dev(qz))
+    lib.check_device_status()
+    hq, hs = host(xq), host(xs)
+    got = bf16_to_f64(out)
+    if pairs is None:
+        return got, orc.int4g128_asym_linear(hq, hs, qw, s16, qz)
+    im, inn = pairs
+    return got[im, inn], orc.int4g128_asym_linear_pairs(hq, hs, qw, s16, qz, im, inn)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (8, 260, 512), (33, 136, 384), (100, 264, 256),
+                                   (1, 132, 512), (5, 384, 1024), (17, 200, 1536), (33, 520, 2048),
+                                   (64, 1000, 512), (65, 260, 1024), (130, 384, 512)])
+def test_int4_asym_linear_small(lib, orc, policy, M, N, K):
+    x, qw, s16, _ = synth.int4_case(M, N, K, seed=M + N + 1)
+    qz = synth.int4_asym_zeros(N, K, seed=M + N + 1)
+    got, ref = _i4_asym_gemm(lib, orc, x, qw, s16, qz)
+    gemm_check(got, ref, f"int4 asym M={M} N={N} K={K} policy={policy}")
+
+
+@pytest.mark.parametrize("M", [1, 64])
+def test_int4_asym_full_sampled(lib, orc, M):
+    N, K = GATE_UP
+    x, qw, s16, _ = synth.int4_case(M, N, K, seed=3)
+    qz = synth.int4_asym_zeros(N, K, seed=3)
+    got, ref = _i4_asym_gemm(lib, orc, x, qw, s16, qz, pairs=_sample_pairs(M, N, 96))
+    gemm_check(got, ref, f"int4 asym M={M} N={N} K={K}")
+
+
+def test_int4_asym_symmetric_zeros_match(lib, orc):
+    # qzeros 0x77777777 through the asymmetric entry reproduces the symmetric definition
+    M, N, K = 4, 256, 1024
+    x, qw, s16, qz = synth.int4_case(M, N, K, seed=9)
+    got, ref = _i4_asym_gemm(lib, orc, x, qw, s16, qz[:, :N // 8])
+    gemm_check(got, orc.int4g128_linear(*[host(t) for t in lib.act_quant(to_dev_bf16(x))], qw, s16),
+               "int4 asym with symmetric zeros")
+
+
 def test_int4_rejects_asymmetric(lib):
     xq = torch.zeros((1, 128), dtype=torch.uint8, device="cuda")
     xs = torch.ones(1, dtype=torch.float32, device="cuda")

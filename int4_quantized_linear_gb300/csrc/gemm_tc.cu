@@ -289,7 +289,13 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                         tc::tma_load_3d(smem + L::W_OFF + sl * L::W_SLOT, &tmap_w, &full[sl], 0, n0, kt);
                 }
 
-                tc::tma_load_3d(smem + L::X_OFF + sl * L::X_SLOT, &tmap_x, &full[sl], 0, m0, kt);
+                // prefill tilings: every activation tile is read again by the CTAs working on
+                // other weight tiles, so it is kept in L2 over the streaming weights and outputs
+                if constexpr (BN >= 128)
+                    tc::tma_load_3d_hint(smem + L::X_OFF + sl * L::X_SLOT, &tmap_x, &full[sl], 0, m0, kt,
+                                         tc::make_policy_evict_last());
+                else
+                    tc::tma_load_3d(smem + L::X_OFF + sl * L::X_SLOT, &tmap_x, &full[sl], 0, m0, kt);
                 *issued = f + 1;
                 trace_ev(p, TR_TMA_ISSUED, i);
                 trace_ev(p, TR_TMA_FILL, f);
@@ -432,7 +438,10 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 tc::fence_proxy_async_smem();
                 tc::named_bar_sync(1, 128);
                 if (issuer) {
-                    tc::tma_store_2d(&tmap_out, stg, n0, m0 + c0);
+                    if constexpr (BN >= 128)  // prefill: the output is not read again, keep L2 for operands
+                        tc::tma_store_2d_hint(&tmap_out, stg, n0, m0 + c0, tc::make_policy_evict_first());
+                    else
+                        tc::tma_store_2d(&tmap_out, stg, n0, m0 + c0);
                     tc::bulk_commit_group();
                 }
                 ++ck;

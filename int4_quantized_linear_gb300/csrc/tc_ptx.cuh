@@ -132,6 +132,14 @@ __device__ __forceinline__ uint64_t make_policy_evict_first()
     return pol;
 }
 
+// L2 policy for data read again soon by other CTAs (prefill activation tiles): kept over others.
+__device__ __forceinline__ uint64_t make_policy_evict_last()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // Plain bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16), completing
 // on an mbarrier's transaction count.
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
@@ -159,6 +167,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void 
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),
                  "r"(smem_u32(src)), "r"(c0), "r"(c1)
+                 : "memory");
+}
+// Same with an L2 cache policy (output written once: evict first).
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap *map, const void *src, int c0, int c1,
+                                                  uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(c0), "r"(c1), "l"(policy)
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }

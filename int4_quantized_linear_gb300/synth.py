@@ -30,7 +30,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
 # Tensor ids: one independent stream per tensor role.
-T_X, T_OUTLIER, T_OUTLIER_PICK, T_W, T_E, T_ROWSCALE, T_QW, T_QS, T_WREQ, T_NVS, T_W8, T_W8S, T_WB, T_QZ = range(1, 15)
+T_X, T_OUTLIER, T_OUTLIER_PICK, T_W, T_E, T_ROWSCALE, T_QW, T_QS, T_WREQ, T_NVS, T_W8, T_W8S, T_WB, T_QZ, T_QH, T_Z5 = range(1, 17)
 
 GATE_UP = (34816, 5120)
 DOWN = (5120, 17408)
@@ -187,3 +187,22 @@ def int4_asym_zeros(N: int, K: int, seed: int = 0) -> np.ndarray:
     nz = (N + 7) // 8
     words = (u64(seed, T_QZ, (K // 128) * nz) & np.uint64(0xFFFFFFFF)).astype(np.uint32)
     return words.reshape(K // 128, nz).view(np.int32)
+
+
+def int5_weights(N: int, K: int, seed: int = 0):
+    """int5 group-128 stand-in: uniform 5-bit codes as (qweight int32 [K/8, N] of the low
+    nibbles, qhigh uint8 [K/8, N] of the fifth bits, bit j of byte (i, n) for k = 8i + j,
+    scales fp16 bits uint16 [K/128, N] ~ |N(0, 0.0015)|, half the int4 spread for the doubled
+    code range)."""
+    n_words = (K // 8) * N
+    q = u64(seed, T_QW, (n_words + 1) // 2).view(np.uint32)[:n_words]
+    qweight = q.view(np.int32).reshape(K // 8, N).copy()
+    qhigh = uniform_bytes(K // 8, N, seed, T_QH)
+    s = np.abs(normal(seed, T_QS, (K // 128) * N) * 0.0015).astype(np.float16)
+    scales = s.view(np.uint16).reshape(K // 128, N).copy()
+    return qweight, qhigh, scales
+
+
+def int5_zeros(N: int, K: int, seed: int = 0) -> np.ndarray:
+    """Per (group, column) zero points, uint8 [K/128, N], uniform in 0..31."""
+    return uniform_ints((K // 128) * N, 0, 31, seed, T_Z5).astype(np.uint8).reshape(K // 128, N)

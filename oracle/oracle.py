@@ -8,6 +8,8 @@ arithmetic lives in the C file, each routine citing the page passage it follows:
   _encode_blocks, quant_mxfp4, dequant_mxfp4, requant_rows, process_weights_after_loading.
 * "vllm-radiance (MXFP4)", section "How the MXFP4 path works" / "The W4A8 fp8-WMMA kernel".
 * "radiance_autoround.py": module docstring, autoround_linear, _exact_ref.
+* "vllm-radiance (MXFP4)", section "ParoQuant (int4 W4A8 and int5 W5A8)" and "int5 (W5A8)":
+  the asymmetric int4 zero point and the 5-bit codes.
 
 Parity pins: every routine is pinned by the ``-m "not gpu"`` tests in ``tests/test_oracle_*.py``
 (closed forms, brute force on tiny inputs, hand-built exact blocks, invariants).  Two
@@ -74,6 +76,8 @@ def _load():
             "orc_int4g128_linear_pairs": (None, [P, P, P, P, I64, I64, P, P, I64, P]),
             "orc_int4g128_asym_linear": (None, [P, P, P, P, P, I64, I64, I64, P]),
             "orc_int4g128_asym_linear_pairs": (None, [P, P, P, P, P, I64, I64, P, P, I64, P]),
+            "orc_int5g128_linear": (None, [P, P, P, P, P, P, I64, I64, I64, P]),
+            "orc_int5g128_linear_pairs": (None, [P, P, P, P, P, P, I64, I64, P, P, I64, P]),
             "orc_e4m3_encode_many": (None, [P, I64, P]),
             "orc_e4m3_decode_many": (None, [P, I64, P]),
             "orc_fp16_decode_many": (None, [P, I64, P]),
@@ -315,4 +319,36 @@ def int4g128_asym_linear_pairs(xq, x_scale, qweight, scales_fp16, qzeros, idx_m,
     N = q.shape[1]
     out = np.empty(im.size, np.float64)
     _load().orc_int4g128_asym_linear_pairs(xp, sp, qp, scp, zp, N, K, imp, inp, im.size, _p(out))
+    return out
+
+
+def int5g128_linear(xq, x_scale, qweight, qhigh, scales_fp16, zeros=None) -> np.ndarray:
+    """int5 g128: low nibbles in qweight [K/8, N], fifth bits in qhigh [K/8, N] (bit j of byte
+    (i, n) for k = 8i + j); zero point 16, or zeros [K/128, N] uint8 per (group, column)."""
+    x, xp = _c(xq, np.uint8)
+    s, sp = _c(x_scale, np.float32)
+    q, qp = _c(qweight, np.int32)
+    h, hp = _c(qhigh, np.uint8)
+    sc, scp = _c(scales_fp16, np.uint16)
+    z, zp = (None, None) if zeros is None else _c(zeros, np.uint8)
+    M, K = x.shape
+    N = q.shape[1]
+    out = np.empty((M, N), np.float64)
+    _load().orc_int5g128_linear(xp, sp, qp, hp, scp, zp, M, N, K, _p(out))
+    return out
+
+
+def int5g128_linear_pairs(xq, x_scale, qweight, qhigh, scales_fp16, zeros, idx_m, idx_n) -> np.ndarray:
+    x, xp = _c(xq, np.uint8)
+    s, sp = _c(x_scale, np.float32)
+    q, qp = _c(qweight, np.int32)
+    h, hp = _c(qhigh, np.uint8)
+    sc, scp = _c(scales_fp16, np.uint16)
+    z, zp = (None, None) if zeros is None else _c(zeros, np.uint8)
+    im, imp = _c(idx_m, np.int64)
+    inn, inp = _c(idx_n, np.int64)
+    K = x.shape[1]
+    N = q.shape[1]
+    out = np.empty(im.size, np.float64)
+    _load().orc_int5g128_linear_pairs(xp, sp, qp, hp, scp, zp, N, K, imp, inp, im.size, _p(out))
     return out

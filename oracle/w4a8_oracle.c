@@ -552,6 +552,53 @@ void orc_int4g128_asym_linear_pairs(const uint8_t *xq, const float *x_scale, con
                  orc_int4_asym_dot(xq, qweight, scales_fp16, qzeros, N, K, idx_m[i], idx_n[i]);
 }
 
+/* int5 group-128 ("vllm-radiance (MXFP4)", section "int5 (W5A8)": the int4 path with 5-bit
+ * codes, c - 16 spanning -16..15; the low nibbles keep the int4 word layout and the fifth bit
+ * sits in a plane of one byte per word).  Reading of the plane: qhigh [K/8, N] uint8, bit j of
+ * byte (i, n) is bit 4 of the code of k = 8i + j, the byte beside word (i, n) of qweight.  So
+ *   c[k, n] = nibble (k % 8) of qweight[k/8, n]  +  16 * bit (k % 8) of qhigh[k/8, n].
+ * Zero point: 16 (symmetric), or z[k/128, n] from a byte per group and column when zeros is
+ * given (the page folds a zero point in for int5 as for int4 but does not give its storage; a
+ * byte per (group, column) holding z itself is the reading taken):
+ *   out[m, n] = scale[m] * sum_k e4m3(xq[m, k]) * (c[k, n] - z[k/128, n]) * fp16(s[k/128, n]). */
+static double orc_int5_dot(const uint8_t *xq, const int32_t *qweight, const uint8_t *qhigh,
+                           const uint16_t *scales_fp16, const uint8_t *zeros, int64_t N, int64_t K,
+                           int64_t m, int64_t n)
+{
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        uint32_t word = (uint32_t)qweight[(k / 8) * N + n];
+        int lo = (int)((word >> (4 * (k % 8))) & 0xF);
+        int hi = (int)((qhigh[(k / 8) * N + n] >> (k % 8)) & 1);
+        int c = lo + 16 * hi;
+        int z = zeros ? (int)zeros[(k / 128) * N + n] : 16;
+        double wv = (double)(c - z) * orc_fp16_decode(scales_fp16[(k / 128) * N + n]);
+        acc += orc_e4m3_decode(xq[m * K + k]) * wv;
+    }
+    return acc;
+}
+
+void orc_int5g128_linear(const uint8_t *xq, const float *x_scale, const int32_t *qweight,
+                         const uint8_t *qhigh, const uint16_t *scales_fp16, const uint8_t *zeros,
+                         int64_t M, int64_t N, int64_t K, double *out)
+{
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            out[m * N + n] = (double)x_scale[m] * orc_int5_dot(xq, qweight, qhigh, scales_fp16, zeros, N, K, m, n);
+}
+
+void orc_int5g128_linear_pairs(const uint8_t *xq, const float *x_scale, const int32_t *qweight,
+                               const uint8_t *qhigh, const uint16_t *scales_fp16, const uint8_t *zeros,
+                               int64_t N, int64_t K, const int64_t *idx_m, const int64_t *idx_n,
+                               int64_t count, double *out)
+{
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t i = 0; i < count; ++i)
+        out[i] = (double)x_scale[idx_m[i]] *
+                 orc_int5_dot(xq, qweight, qhigh, scales_fp16, zeros, N, K, idx_m[i], idx_n[i]);
+}
+
 /* Number of threads the parallel loops above use (1 without OpenMP). */
 int orc_num_threads(void)
 {

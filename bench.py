@@ -608,6 +608,41 @@ def run_extras(lib, dev, peaks):
                                    "frac_of_hbm": round(gbs / hbm, 4)}
         del qws, scs, qz
     out["int4g128_asym"] = {"decode_bound": "hbm", "cases": i4a}
+
+    # ---- int5 g128 (fifth-bit plane; zero point 16, or a byte per group and column): decode
+    # weight GB/s at M = 1 and 64, prefill TFLOP/s at M = 4096
+    i5 = {}
+    for name, (N, K) in SHAPES:
+        qw, qh, sc = synth.int5_weights(N, K, 0)
+        z5 = to_dev(synth.int5_zeros(N, K, 0))
+        wb = N * K // 2 + N * K // 8 + N * K // 64
+        qws = [to_dev(qw) for _ in range(3)]
+        qhs = [to_dev(qh) for _ in range(3)]
+        scs = [to_dev(sc).view(torch.float16) for _ in range(3)]
+        for M in (1, 64):
+            x = torch.randn((M, K), device=dev).to(torch.bfloat16)
+            xq, xs = lib.act_quant(x)
+            o = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ws = lib.make_workspace(lib.int5_workspace_bytes(M, N, K), dev)
+            for tag, z in (("", None), ("_asym", z5)):
+                fns = [lambda a=a, h=h, b=b, z=z: lib.int5g128_linear(xq, xs, a, h, b, z, out=o, workspace=ws)
+                       for a, h, b in zip(qws, qhs, scs)]
+                ms = timeit_rot(fns)
+                by = wb + (0 if z is None else (K // 128) * N)
+                gbs = by / (ms * 1e-3) / 1e9
+                i5[f"{name}_M{M}{tag}"] = {"us": round(ms * 1e3, 2), "weight GB/s": round(gbs, 1),
+                                           "frac_of_hbm": round(gbs / hbm, 4)}
+        M = 4096
+        x = torch.randn((M, K), device=dev).to(torch.bfloat16)
+        xq, xs = lib.act_quant(x)
+        o = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        ws = lib.make_workspace(lib.int5_workspace_bytes(M, N, K), dev)
+        ms = timeit(lambda: lib.int5g128_linear(xq, xs, qws[0], qhs[0], scs[0], out=o, workspace=ws), reps=2)
+        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        i5[f"{name}_M{M}"] = {"ms": round(ms, 3), "tflops": round(tf, 1), "frac_of_fp8_peak": round(tf / fp8_peak, 4)}
+        del qws, qhs, scs, z5
+    out["int5g128"] = {"decode_bound": "hbm", "prefill_bound": "tensor (fp8 peak)",
+                       "weight_bytes": "N*K*(1/2 + 1/8 + 2/128) (+ K/128*N zero bytes for asym)", "cases": i5}
     return out
 
 

@@ -211,6 +211,31 @@ W4A8_API w4a8_status w4a8_int4g128_asym_linear(const uint8_t *xq, const float *x
                                                int64_t N, int64_t K, void *workspace,
                                                size_t workspace_bytes, cudaStream_t stream);
 
+/* int5 group-128 W5A8 linear ("vllm-radiance (MXFP4)", section "int5 (W5A8)": 5-bit codes c
+ * whose value c - 16 spans -16..15, the low nibbles kept in the int4 word layout and the fifth
+ * bit in a plane of one byte per word; the zero point folded in as for int4).
+ *   c[k, n]   = nibble (k % 8) of qweight[k/8, n] + 16 * bit (k % 8) of qhigh[k/8, n]
+ *   out[m, n] = bf16( x_scale[m] * sum_g s[g, n] * sum_{k in g} e4m3(xq[m, k]) * (c[k, n] - z[g, n]) )
+ * with z = 16 when zeros is NULL, else z[g, n] = zeros[g, n].
+ *   qweight [K/8, N] int32, nibble j of word (i, n) = the low four bits of the code of k = 8i + j
+ *   qhigh   [K/8, N] uint8, bit j of byte (i, n) = the fifth bit of the code of k = 8i + j
+ *           (device, non-NULL; the tensor-core kernel needs it 16-byte aligned and N % 16 == 0,
+ *           other shapes run on the CUDA-core kernel)
+ *   scales_fp16 [K/128, N] fp16 bits
+ *   zeros   [K/128, N] uint8 holding z in 0..31, or NULL (symmetric)
+ *   workspace: sized by w4a8_int5g128_workspace_bytes; errors as for w4a8_int4g128_linear.
+ * K must be a multiple of 128.  The tensor-core kernel converts the fifth bits into a second
+ * e4m3 operand (-16 * 2^-9 where the bit is 0) whose MMAs add into the same accumulator as the
+ * nibble operand's; with zeros it also keeps the activations' group sums in a second
+ * accumulator and applies (z - 16) per column in the fp32 promotion. */
+W4A8_API w4a8_status w4a8_int5g128_linear(const uint8_t *xq, const float *x_scale, const int32_t *qweight,
+                                          const uint8_t *qhigh, const uint16_t *scales_fp16,
+                                          const uint8_t *zeros, uint16_t *out_bf16, int64_t M, int64_t N,
+                                          int64_t K, void *workspace, size_t workspace_bytes,
+                                          cudaStream_t stream);
+
+W4A8_API size_t w4a8_int5g128_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
 /* Human-readable name of a status code (static storage). */
 W4A8_API const char *w4a8_status_string(w4a8_status s);
 

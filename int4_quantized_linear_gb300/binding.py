@@ -23,6 +23,7 @@ MODES = {"ocp": 0, "noclip": 1, "mse": 2}
 EXPORTS = ("w4a8_act_quant", "w4a8_mxfp4_linear", "w4a8_workspace_bytes",
            "nvfp4_to_mxfp4_requant", "fp8_channel_to_mxfp4_requant", "bf16_to_mxfp4_requant",
            "w4a8_int4g128_linear", "w4a8_int4g128_asym_linear", "w4a8_int4g128_workspace_bytes",
+           "w4a8_int5g128_linear", "w4a8_int5g128_workspace_bytes",
            "w4a8_status_string", "w4a8_set_gemm_policy", "w4a8_check_device_status",
            "w4a8_decode_max_m", "w4a8_debug_status_words", "w4a8_debug_set_trace",
            "w4a8_mxfp4_linear_noalloc", "w4a8_noalloc_scratch_bytes",
@@ -61,6 +62,8 @@ def load(build_if_missing: bool = True):
         "w4a8_int4g128_linear": (I, [P, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "w4a8_int4g128_asym_linear": (I, [P, P, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "w4a8_int4g128_workspace_bytes": (SZ, [I64, I64, I64]),
+        "w4a8_int5g128_linear": (I, [P, P, P, P, P, P, P, I64, I64, I64, P, SZ, P]),
+        "w4a8_int5g128_workspace_bytes": (SZ, [I64, I64, I64]),
         "w4a8_status_string": (ctypes.c_char_p, [I]),
         "w4a8_set_gemm_policy": (None, [I]),
         "w4a8_check_device_status": (I, [P]),
@@ -145,6 +148,10 @@ def workspace_bytes(M: int, N: int, K: int) -> int:
 
 def int4_workspace_bytes(M: int, N: int, K: int) -> int:
     return int(load().w4a8_int4g128_workspace_bytes(M, N, K))
+
+
+def int5_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load().w4a8_int5g128_workspace_bytes(M, N, K))
 
 
 def make_workspace(nbytes: int, device) -> torch.Tensor | None:
@@ -255,6 +262,36 @@ def int4g128_asym_linear(xq, x_scale, qweight, scales_fp16, qzeros, out=None, wo
     _check("w4a8_int4g128_asym_linear", load().w4a8_int4g128_asym_linear(
         _ptr(xq), _ptr(x_scale), _ptr(qweight), _ptr(scales_fp16), _ptr(qzeros), _ptr(out), M, N, K,
         _ptr(workspace), wsb, _stream(stream)))
+    return out
+
+
+def int5g128_linear(xq, x_scale, qweight, qhigh, scales_fp16, zeros=None, out=None, workspace=None,
+                    stream=None):
+    """out[m, n] = bf16(x_scale[m] * sum_k e4m3(xq) * (c - z) * fp16(s[k/128, n])) with the 5-bit
+    code c = nibble of qweight [K/8, N] + 16 * bit of qhigh [K/8, N] (bit j of byte (i, n) for
+    k = 8i + j), z = 16 or zeros [K/128, N] uint8 (w4a8_int5g128_linear)."""
+    _dev(xq, "xq", torch.uint8)
+    _dev(x_scale, "x_scale", torch.float32)
+    _dev(qweight, "qweight", torch.int32)
+    _dev(qhigh, "qhigh", torch.uint8)
+    _dev(scales_fp16, "scales", torch.float16)
+    M, K = xq.shape
+    N = qweight.shape[1]
+    if qweight.shape != (K // 8, N) or qhigh.shape != (K // 8, N) or scales_fp16.shape != (K // 128, N):
+        raise ValueError("int5 weight shapes do not match K")
+    if zeros is not None:
+        _dev(zeros, "zeros", torch.uint8)
+        if zeros.shape != (K // 128, N):
+            raise ValueError("int5 zeros must be [K/128, N]")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    need = int5_workspace_bytes(M, N, K)
+    if need and workspace is None:
+        workspace = make_workspace(need, xq.device)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("w4a8_int5g128_linear", load().w4a8_int5g128_linear(
+        _ptr(xq), _ptr(x_scale), _ptr(qweight), _ptr(qhigh), _ptr(scales_fp16), _ptr(zeros), _ptr(out),
+        M, N, K, _ptr(workspace), wsb, _stream(stream)))
     return out
 
 

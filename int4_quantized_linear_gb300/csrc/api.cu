@@ -194,3 +194,34 @@ extern "C" w4a8_status w4a8_int4g128_asym_linear(const uint8_t *xq, const float 
     return int4g128_linear_impl(xq, x_scale, qweight, scales_fp16, qzeros, out_bf16, M, N, K, workspace,
                                 workspace_bytes, stream);
 }
+
+extern "C" size_t w4a8_int5g128_workspace_bytes(int64_t M, int64_t N, int64_t K)
+{
+    // the int5 kernel shares the int4 kernel's work split and partial-tile scratch
+    return w4a8_int4g128_workspace_bytes(M, N, K);
+}
+
+extern "C" w4a8_status w4a8_int5g128_linear(const uint8_t *xq, const float *x_scale, const int32_t *qweight,
+                                            const uint8_t *qhigh, const uint16_t *scales_fp16,
+                                            const uint8_t *zeros, uint16_t *out_bf16, int64_t M, int64_t N,
+                                            int64_t K, void *workspace, size_t workspace_bytes,
+                                            cudaStream_t stream)
+{
+    if (M < 0 || N < 0 || K < 0) return W4A8_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return W4A8_OK;
+    if (K == 0 || !xq || !x_scale || !qweight || !qhigh || !scales_fp16 || !out_bf16) return W4A8_ERR_INVALID_ARG;
+    if (K % 128 != 0) return W4A8_ERR_UNSUPPORTED_SHAPE;
+    if (!w4a8_aligned(xq, 16) || !w4a8_aligned(qweight, 4) || !w4a8_aligned(scales_fp16, 2) ||
+        !w4a8_aligned(x_scale, 4) || !w4a8_aligned(out_bf16, 2))
+        return W4A8_ERR_MISALIGNED;
+    const int policy = w4a8_gemm_policy();
+    if (policy != 1 && w4a8_tc_int5_supported(xq, qweight, qhigh, scales_fp16, out_bf16, M, N, K)) {
+        const size_t need = w4a8_tc_int4_workspace_bytes(M, N, K, policy);
+        if (need && (!workspace || workspace_bytes < need)) return W4A8_ERR_WORKSPACE;
+        if (need && !w4a8_aligned(workspace, 16)) return W4A8_ERR_MISALIGNED;
+        return w4a8_launch_int5_tc(xq, x_scale, qweight, qhigh, scales_fp16, zeros, out_bf16, M, N, K, workspace,
+                                   policy, stream);
+    }
+    return w4a8_launch_int4_simt(xq, x_scale, qweight, scales_fp16, out_bf16, M, N, K, stream, nullptr, qhigh,
+                                 zeros);
+}

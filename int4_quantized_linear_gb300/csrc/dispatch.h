@@ -19,7 +19,8 @@ w4a8_status w4a8_launch_mxfp4_simt(const uint8_t *xq, const float *x_scale, cons
 w4a8_status w4a8_launch_int4_simt(const uint8_t *xq, const float *x_scale, const int32_t *qw,
                                   const uint16_t *s16, uint16_t *out, int64_t M, int64_t N,
                                   int64_t K, cudaStream_t stream,
-                                  const int32_t *qzeros = nullptr);
+                                  const int32_t *qzeros = nullptr, const uint8_t *qhigh = nullptr,
+                                  const uint8_t *zeros5 = nullptr);
 
 // Tensor-core (tcgen05) paths.
 bool w4a8_tc_mxfp4_supported(const void *xq, const void *wp, const void *we, const void *out,
@@ -44,3 +45,11 @@ w4a8_status w4a8_launch_int4_tc(const uint8_t *xq, const float *x_scale, const i
                                 const uint16_t *s16, uint16_t *out, int64_t M, int64_t N,
                                 int64_t K, void *workspace, int policy, cudaStream_t stream,
                                 const int32_t *qzeros = nullptr);
+
+// int5 g128: qh is the fifth-bit plane [K/8, N], zeros the per-(group, column) zero points
+// [K/128, N] or null (zero point 16).
+bool w4a8_tc_int5_supported(const void *xq, const void *qw, const void *qh, const void *s16, const void *out,
+                            int64_t M, int64_t N, int64_t K);
+w4a8_status w4a8_launch_int5_tc(const uint8_t *xq, const float *x_scale, const int32_t *qw, const uint8_t *qh,
+                                const uint16_t *s16, const uint8_t *zeros, uint16_t *out, int64_t M, int64_t N,
+                                int64_t K, void *workspace, int policy, cudaStream_t stream);

@@ -30,6 +30,15 @@
 //     split tile for the stream-K fix-up (last contributor adds partials in CTA order);
 //   * the work split, bounded waits, gate warp and abort handling follow the MXFP4 kernel.
 //
+// int5 ("vllm-radiance (MXFP4)", section "int5 (W5A8)": 5-bit codes c, value c - 16, the low
+// nibbles in the same word layout and the fifth bit in a plane of one byte per word, bit j of
+// byte (i, n) for k = 8i + j).  Codes 16-31 are not linear in the e4m3 byte, so the fifth bit
+// gets an operand tile of its own: e4m3 -2^-5 (= -16 * 2^-9) where the bit is 0 and 0 where it
+// is 1.  Its four MMAs take the place of the constant zero-point MMAs:
+//   sum_k lo_k 2^-9 x_k + sum_k (-16 * 2^-9)(1 - hi_k) x_k = 2^-9 * sum_k (c_k - 16) x_k.
+// With a zero point z per (group, column) the constant-atom MMAs come back, into the second
+// accumulator as for asymmetric int4, and promotion adds ((z - 16) / 8) times it.
+//
 // Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 5 gate, 2-4, 6-8, 10, 11 converters,
 // 12-15 promotion and epilogue (9 idle).
 #include <cstring>
@@ -77,7 +86,8 @@ enum : unsigned { ST_TIMEOUT_PRODUCER = 1, ST_TIMEOUT_GATE = 2, ST_TIMEOUT_CONV 
 struct Params {
     const uint16_t *s16;   // [K/128, N] fp16 group scales
     const float *xs;       // [M] per-token scale
-    const int32_t *qz;     // asymmetric only: [K/128, ceil(N/8)] packed zero points minus one
+    const int32_t *qz;     // asymmetric int4 only: [K/128, ceil(N/8)] packed zero points minus one
+    const uint8_t *z5;     // asymmetric int5 only: [K/128, N] zero points
     uint16_t *out;         // [M, N] bf16
     float *partials;       // [G][2][BN][128] fp32 stream-K partial tiles
     int *counters;         // [tiles] arrival counters, zero between calls
@@ -99,19 +109,23 @@ __device__ __forceinline__ void trace_ev(const Params &p, int ev, int i)
     if (p.trace != nullptr && blockIdx.x == 0 && i < 256) p.trace[ev * 256 + i] = (unsigned long long)clock64();
 }
 
-// Shared memory: the zero-point operand atom (1 KB), NA converted operand tiles, then a ring of US
-// fills, each holding KPU k-tiles of activations (BN x 128 bytes, swizzled) and of checkpoint
-// words ([16 word rows][128 columns]).
-template <int BN, int US, int NA, int NB, bool ASYM = false>
+// Shared memory: the zero-point operand atom (1 KB), NA converted operand tiles (and, for int5,
+// NA fifth-bit operand tiles), then a ring of US fills, each holding KPU k-tiles of activations
+// (BN x 128 bytes, swizzled) and of checkpoint words ([16 word rows][128 columns]), then (int5)
+// KPU k-tiles of the fifth-bit plane ([16 byte rows][128 columns]).
+template <int BN, int US, int NA, int NB, bool ASYM = false, bool I5 = false>
 struct Layout {
     static constexpr int RAW_TILE = 16 * BM * 4;  // 8 KB of words: 128 k x 128 columns
+    static constexpr int PLANE_TILE = I5 ? 16 * BM : 0;  // 2 KB of fifth bits: 128 k x 128 columns
     static constexpr int X_TILE = BN * 128;
     static constexpr int A_TILE = BM * 128;       // e4m3 [128 columns][128 k], 128-byte swizzle
-    static constexpr int RAW_SLOT = KPU * RAW_TILE;
+    static constexpr int RAW_SLOT = KPU * (RAW_TILE + PLANE_TILE);
+    static constexpr int PLANE_OFF = KPU * RAW_TILE;  // within a raw slot
     static constexpr int X_SLOT = KPU * X_TILE;
     static constexpr int Z_OFF = 0;                // 8 rows x 128 bytes of e4m3 -2^-6
     static constexpr int A_OFF = Z_OFF + 1024;
-    static constexpr int X_OFF = A_OFF + NA * A_TILE;
+    static constexpr int H_OFF = A_OFF + NA * A_TILE;  // int5: the fifth-bit operand tiles
+    static constexpr int X_OFF = H_OFF + (I5 ? NA * A_TILE : 0);
     static constexpr int RAW_OFF = X_OFF + US * X_SLOT;
     static constexpr int BAR_OFF = RAW_OFF + US * RAW_SLOT;
     static constexpr int XS_OFF = BAR_OFF + 512;
@@ -119,7 +133,7 @@ struct Layout {
     static constexpr int STAGE_BYTES = 16 * BM * 2;
     static constexpr int STAGE_OFF = (XS_OFF + BN * 4 + 1023) / 1024 * 1024;
     static constexpr int TOTAL = STAGE_OFF + NSTAGE * STAGE_BYTES + 1024;  // + alignment slack
-    static constexpr int TX_BYTES = KPU * (RAW_TILE + X_TILE);
+    static constexpr int TX_BYTES = KPU * (RAW_TILE + PLANE_TILE + X_TILE);
     static constexpr int TMEM_NEED = NB * BN * (ASYM ? 2 : 1);  // + the zero-point sums (asymmetric)
     static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128
                                      : TMEM_NEED <= 256 ? 256 : 512;
@@ -141,12 +155,26 @@ __device__ __forceinline__ uint2 i4x8_to_bytes(uint32_t w)
 
 constexpr uint32_t E4M3_MINUS_2POW_M6 = 0x88u;  // sign 1, exponent field 1, mantissa 0: -2^-6
 
-template <int BN, int US, int NA, int NB, bool ASYM>
+// The fifth bits of eight int5 codes (bit j for k = 8i + j) -> one operand byte per code, low
+// byte first, in two words: e4m3 -2^-5 (0x90: sign 1, exponent field 2, mantissa 0) where the
+// bit is 0 and 0x00 where it is 1.  A multiply by 1 + 2^7 + 2^14 + 2^21 moves bit j of a nibble
+// to bit 8j (the four shifted copies do not overlap, so nothing carries); the mask keeps those
+// bits and the multiply by 0x90 turns each 0/1 byte into 0x00/0x90.
+__device__ __forceinline__ uint2 i5_high_to_bytes(uint32_t b)
+{
+    const uint32_t nb = ~b;
+    const uint32_t lo = ((nb & 0xFu) * 0x00204081u) & 0x01010101u;
+    const uint32_t hi = (((nb >> 4) & 0xFu) * 0x00204081u) & 0x01010101u;
+    return make_uint2(lo * 0x90u, hi * 0x90u);
+}
+
+template <int BN, int US, int NA, int NB, bool ASYM, bool I5>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_x,
-               const __grid_constant__ CUtensorMap tmap_out, const Params p)
+               const __grid_constant__ CUtensorMap tmap_out, const __grid_constant__ CUtensorMap tmap_h,
+               const Params p)
 {
-    using L = Layout<BN, US, NA, NB, ASYM>;
+    using L = Layout<BN, US, NA, NB, ASYM, I5>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);  // ring fill landed
@@ -183,6 +211,7 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         tc::fence_mbar_init();
         tc::tma_prefetch_desc(&tmap_q);
         tc::tma_prefetch_desc(&tmap_x);
+        if (I5) tc::tma_prefetch_desc(&tmap_h);
         if (p.tma_out) tc::tma_prefetch_desc(&tmap_out);
     }
     if (warp == 1) {
@@ -218,6 +247,8 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                 tc::mbar_arrive_expect_tx(&full[sl], L::TX_BYTES);
                 tc::tma_load_2d(smem + L::RAW_OFF + sl * L::RAW_SLOT, &tmap_q, &full[sl], n0, 16 * kt);
                 tc::tma_load_3d(smem + L::X_OFF + sl * L::X_SLOT, &tmap_x, &full[sl], 0, m0, kt);
+                if constexpr (I5)
+                    tc::tma_load_2d(smem + L::RAW_OFF + sl * L::RAW_SLOT + L::PLANE_OFF, &tmap_h, &full[sl], n0, 16 * kt);
                 *issued = f + 1;
                 trace_ev(p, 0, f);
             }
@@ -255,6 +286,22 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                 const uint2 hi = i4x8_to_bytes(wv[2 * cc + 1]);
                 *reinterpret_cast<uint4 *>(dst + ((c ^ (r & 7)) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
             }
+            if constexpr (I5) {
+                // the fifth bits of the same 64 codes: plane bytes of the same word rows, to the
+                // same swizzled places of this k-tile's fifth-bit operand tile
+                const uint8_t *pl = smem + L::RAW_OFF + sl * L::RAW_SLOT + L::PLANE_OFF + (j * 16 + 8 * h) * BM + r;
+                uint8_t *hdst = smem + L::H_OFF + a * L::A_TILE + r * 128;
+                uint32_t hb[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) hb[k] = pl[k * BM];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int c = 4 * h + cc;
+                    const uint2 lo = i5_high_to_bytes(hb[2 * cc]);
+                    const uint2 hi = i5_high_to_bytes(hb[2 * cc + 1]);
+                    *reinterpret_cast<uint4 *>(hdst + ((c ^ (r & 7)) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+                }
+            }
             tc::fence_proxy_async_smem();  // generic writes -> visible to the tensor core
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&a_full[a]);
@@ -287,13 +334,24 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                 for (int kk = 0; kk < 4; ++kk)
                     tc::mma_f8f6f4(tmem + b * BN, tc::smem_desc(aa + 32 * kk, 16, 1024, 2),
                                    tc::smem_desc(xa + 32 * kk, 16, 1024, 2), idesc, kk > 0 ? 1u : 0u);
+                if constexpr (I5) {
+                    // int5: the fifth-bit operand (-16 * 2^-9 where the bit is 0) into the same
+                    // accumulator, which then holds 2^-9 * sum (c - 16) x
+                    const uint32_t ha = tc::smem_u32(smem + L::H_OFF + a * L::A_TILE);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_f8f6f4(tmem + b * BN, tc::smem_desc(ha + 32 * kk, 16, 1024, 2),
+                                       tc::smem_desc(xa + 32 * kk, 16, 1024, 2), idesc, 1u);
+                }
                 // zero point: the constant atom for every 8-row group (stride 0); with per-column
                 // zero points (asymmetric) into a buffer of its own, scaled per column in promotion
-                const uint32_t zacc = tmem + (ASYM ? NB + b : b) * BN;
+                if constexpr (!I5 || ASYM) {
+                    const uint32_t zacc = tmem + (ASYM ? NB + b : b) * BN;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    tc::mma_f8f6f4(zacc, tc::smem_desc(za + 32 * kk, 16, 0, 2),
-                                   tc::smem_desc(xa + 32 * kk, 16, 1024, 2), idesc, (ASYM && kk == 0) ? 0u : 1u);
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_f8f6f4(zacc, tc::smem_desc(za + 32 * kk, 16, 0, 2),
+                                       tc::smem_desc(xa + 32 * kk, 16, 1024, 2), idesc, (ASYM && kk == 0) ? 0u : 1u);
+                }
                 tc::tc_commit(&g_full[b]);
                 if (j == KPU - 1) tc::tc_commit(&empty[sl]);
             }
@@ -344,7 +402,8 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             for (int jj = 0; jj < 4; ++jj)
                 dst[jj] = n < p.N ? 512.0f * __half2float(__ushort_as_half(__ldg(p.s16 + (size_t)(g0 + jj) * p.N + n))) : 0.0f;
         };
-        // asymmetric: the unit's zero points z of this thread's column, as z / 8 (exact)
+        // asymmetric: the unit's zero points z of this thread's column, as z / 8 for int4 (the
+        // accumulator holds the codes alone) or (z - 16) / 8 for int5 (it holds c - 16); exact
         auto unit_zeros = [&](int pu, float (&dst)[4]) {
             if (pu >= sched.n_units) return;
             const long long u = sched.unit_at(pu);
@@ -354,8 +413,13 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             const int nz = (p.N + 7) / 8;
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
-                const uint32_t w = n < p.N ? (uint32_t)__ldg(p.qz + (size_t)(g0 + jj) * nz + n / 8) : 0x77777777u;
-                dst[jj] = 0.125f * (float)(1 + ((w >> (4 * (n & 7))) & 0xfu));
+                if constexpr (I5) {
+                    const int z = n < p.N ? (int)__ldg(p.z5 + (size_t)(g0 + jj) * p.N + n) : 16;
+                    dst[jj] = 0.125f * (float)(z - 16);
+                } else {
+                    const uint32_t w = n < p.N ? (uint32_t)__ldg(p.qz + (size_t)(g0 + jj) * nz + n / 8) : 0x77777777u;
+                    dst[jj] = 0.125f * (float)(1 + ((w >> (4 * (n & 7))) & 0xfu));
+                }
             }
         };
         float sc_cur[4] = {0.0f, 0.0f, 0.0f, 0.0f}, sc_nxt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -409,7 +473,8 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                     tc::tmem_ld16(tb + c0, v);
                     tc::tmem_ld_wait();
                     if constexpr (ASYM) {
-                        // 512 s (P + (z/8) Z) = s (sum c x - z sum x), Z = -2^-6 sum x
+                        // 512 s (P + (z/8) Z) = s (sum c x - z sum x), Z = -2^-6 sum x (int4); for
+                        // int5 P holds c - 16 and the factor is (z - 16) / 8
                         const float zf = jj == 0 ? zf_cur[0] : jj == 1 ? zf_cur[1] : jj == 2 ? zf_cur[2] : zf_cur[3];
                         uint32_t vz[16];
                         tc::tmem_ld16(tb + NB * BN + c0, vz);
@@ -527,12 +592,18 @@ static size_t partial_bytes(const Cfg &c)
     return (b + 255) / 256 * 256;
 }
 
-template <int BN, int US, int NA, int NB, bool ASYM>
-static w4a8_status launch(const int32_t *qw, const uint8_t *xq, Params prm, cudaStream_t stream)
+template <int BN, int US, int NA, int NB, bool ASYM, bool I5 = false>
+static w4a8_status launch(const int32_t *qw, const uint8_t *xq, Params prm, cudaStream_t stream,
+                          const uint8_t *qh = nullptr)
 {
-    using L = Layout<BN, US, NA, NB, ASYM>;
-    CUtensorMap tq, tx, tout;
+    using L = Layout<BN, US, NA, NB, ASYM, I5>;
+    CUtensorMap tq, tx, tout, th;
     memset(&tout, 0, sizeof(tout));
+    memset(&th, 0, sizeof(th));
+    // int5 fifth-bit plane [K/8 rows][N columns] uint8: boxes of 16 * KPU byte rows x 128 columns
+    if (I5 && !tch::tmap_2d(&th, CU_TENSOR_MAP_DATA_TYPE_UINT8, qh, prm.K / 8, prm.N, (uint64_t)prm.N, 16 * KPU,
+                            BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return W4A8_ERR_CUDA;
     prm.tma_out = (prm.N % 8 == 0) && w4a8_aligned(prm.out, 16) &&
                   tch::tmap_2d(&tout, CU_TENSOR_MAP_DATA_TYPE_UINT16, prm.out, prm.M, prm.N, (uint64_t)prm.N * 2, 16,
                                BM, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -542,7 +613,7 @@ static w4a8_status launch(const int32_t *qw, const uint8_t *xq, Params prm, cuda
                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !tch::tmap_3d_ktiles(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, prm.M, prm.K, 128, prm.K / 128, BN, KPU))
         return W4A8_ERR_CUDA;
-    auto kern = int4_tc_kernel<BN, US, NA, NB, ASYM>;
+    auto kern = int4_tc_kernel<BN, US, NA, NB, ASYM, I5>;
     static int attr_done[64] = {0};
     if (!tch::set_smem_once(kern, L::TOTAL, attr_done)) return W4A8_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -555,7 +626,7 @@ static w4a8_status launch(const int32_t *qw, const uint8_t *xq, Params prm, cuda
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, tq, tx, tout, prm) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kern, tq, tx, tout, th, prm) != cudaSuccess) {
         cudaGetLastError();
         return W4A8_ERR_CUDA;
     }
@@ -585,20 +656,17 @@ size_t w4a8_tc_int4_workspace_bytes(int64_t M, int64_t N, int64_t K, int policy)
     return partial_bytes(c) + (size_t)c.m_tiles * c.n_tiles * 4;
 }
 
-w4a8_status w4a8_launch_int4_tc(const uint8_t *xq, const float *x_scale, const int32_t *qw, const uint16_t *s16,
-                                uint16_t *out, int64_t M, int64_t N, int64_t K, void *workspace, int,
-                                cudaStream_t stream, const int32_t *qzeros)
+static bool make_params(Params &prm, const Cfg &c, const float *x_scale, const uint16_t *s16, uint16_t *out,
+                        int64_t M, int64_t N, int64_t K, void *workspace)
 {
-    const Cfg c = w4a8::tci::choose(M, N, K);
-    Params prm;
     prm.s16 = s16;
     prm.xs = x_scale;
-    prm.qz = qzeros;
+    prm.qz = nullptr;
+    prm.z5 = nullptr;
     prm.out = out;
     prm.partials = static_cast<float *>(workspace);
     prm.counters = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) + partial_bytes(c));
     prm.status = w4a8_device_status_ptr();
-    if (!prm.status) return W4A8_ERR_CUDA;
     prm.M = (int)M;
     prm.N = (int)N;
     prm.K = (int)K;
@@ -612,6 +680,17 @@ w4a8_status w4a8_launch_int4_tc(const uint8_t *xq, const float *x_scale, const i
     prm.Gsk = c.k.Gsk;
     prm.tma_out = 0;
     prm.trace = static_cast<unsigned long long *>(w4a8_debug_trace_ptr());
+    return prm.status != nullptr;
+}
+
+w4a8_status w4a8_launch_int4_tc(const uint8_t *xq, const float *x_scale, const int32_t *qw, const uint16_t *s16,
+                                uint16_t *out, int64_t M, int64_t N, int64_t K, void *workspace, int,
+                                cudaStream_t stream, const int32_t *qzeros)
+{
+    const Cfg c = w4a8::tci::choose(M, N, K);
+    Params prm;
+    if (!make_params(prm, c, x_scale, s16, out, M, N, K, workspace)) return W4A8_ERR_CUDA;
+    prm.qz = qzeros;
     if (qzeros != nullptr) {
         switch (c.BN) {
         case 16: return launch<16, 4, 3, 4, true>(qw, xq, prm, stream);
@@ -623,5 +702,35 @@ w4a8_status w4a8_launch_int4_tc(const uint8_t *xq, const float *x_scale, const i
     case 16: return launch<16, 4, 3, 4, false>(qw, xq, prm, stream);
     case 32: return launch<32, 3, 3, 4, false>(qw, xq, prm, stream);
     default: return launch<64, 2, 3, 4, false>(qw, xq, prm, stream);
+    }
+}
+
+bool w4a8_tc_int5_supported(const void *xq, const void *qw, const void *qh, const void *s16, const void *out,
+                            int64_t M, int64_t N, int64_t K)
+{
+    // the fifth-bit plane's rows are N bytes: TMA wants them 16-byte aligned
+    return w4a8_tc_int4_supported(xq, qw, s16, out, M, N, K) && N % 16 == 0 && w4a8_aligned(qh, 16);
+}
+
+w4a8_status w4a8_launch_int5_tc(const uint8_t *xq, const float *x_scale, const int32_t *qw, const uint8_t *qh,
+                                const uint16_t *s16, const uint8_t *zeros, uint16_t *out, int64_t M, int64_t N,
+                                int64_t K, void *workspace, int, cudaStream_t stream)
+{
+    const Cfg c = w4a8::tci::choose(M, N, K);
+    Params prm;
+    if (!make_params(prm, c, x_scale, s16, out, M, N, K, workspace)) return W4A8_ERR_CUDA;
+    prm.z5 = zeros;
+    // the fifth-bit tiles double the converted operand area: two of each, ring depth 3 / 2 / 2
+    if (zeros != nullptr) {
+        switch (c.BN) {
+        case 16: return launch<16, 3, 2, 4, true, true>(qw, xq, prm, stream, qh);
+        case 32: return launch<32, 2, 2, 4, true, true>(qw, xq, prm, stream, qh);
+        default: return launch<64, 2, 2, 4, true, true>(qw, xq, prm, stream, qh);
+        }
+    }
+    switch (c.BN) {
+    case 16: return launch<16, 3, 2, 4, false, true>(qw, xq, prm, stream, qh);
+    case 32: return launch<32, 2, 2, 4, false, true>(qw, xq, prm, stream, qh);
+    default: return launch<64, 2, 2, 4, false, true>(qw, xq, prm, stream, qh);
     }
 }

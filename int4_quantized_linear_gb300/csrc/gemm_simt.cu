@@ -76,8 +76,8 @@ template <int MT>
 __global__ void __launch_bounds__(128)
 int4_simt_kernel(const uint8_t *__restrict__ xq, const float *__restrict__ x_scale,
                  const uint32_t *__restrict__ qw, const uint16_t *__restrict__ s16,
-                 const uint32_t *__restrict__ qz, uint16_t *__restrict__ out, int64_t M, int64_t N,
-                 int64_t K)
+                 const uint32_t *__restrict__ qz, const uint8_t *__restrict__ qh,
+                 const uint8_t *__restrict__ z5, uint16_t *__restrict__ out, int64_t M, int64_t N, int64_t K)
 {
     const int64_t n = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t m0 = (int64_t)blockIdx.y * MT;
@@ -89,13 +89,17 @@ int4_simt_kernel(const uint8_t *__restrict__ xq, const float *__restrict__ x_sca
         float part[MT];
 #pragma unroll
         for (int t = 0; t < MT; ++t) part[t] = 0.0f;
-        // zero point 8, or (asymmetric) 1 + the column's nibble of the group's qzeros word
-        const int z = qz ? 1 + (int)((__ldg(qz + g * ((N + 7) / 8) + n / 8) >> (4 * (n & 7))) & 0xfu) : 8;
+        // int4: zero point 8, or (asymmetric) 1 + the column's nibble of the group's qzeros word;
+        // int5 (fifth-bit plane qh): zero point 16, or the column's byte of the group's zeros
+        const int z = qh ? (z5 ? (int)__ldg(z5 + g * N + n) : 16)
+                         : qz ? 1 + (int)((__ldg(qz + g * ((N + 7) / 8) + n / 8) >> (4 * (n & 7))) & 0xfu) : 8;
         for (int i = 0; i < 16; ++i) {
             const uint32_t word = __ldg(qw + (g * 16 + i) * N + n);
+            const uint32_t hb = qh ? (uint32_t)__ldg(qh + (g * 16 + i) * N + n) : 0u;
             float w[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) w[j] = (float)((int)((word >> (4 * j)) & 0xfu) - z);
+            for (int j = 0; j < 8; ++j)
+                w[j] = (float)((int)((word >> (4 * j)) & 0xfu) + 16 * (int)((hb >> j) & 1u) - z);
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
                 if (m0 + t < M) {
@@ -136,12 +140,13 @@ w4a8_status w4a8_launch_mxfp4_simt(const uint8_t *xq, const float *x_scale, cons
 
 w4a8_status w4a8_launch_int4_simt(const uint8_t *xq, const float *x_scale, const int32_t *qw,
                                   const uint16_t *s16, uint16_t *out, int64_t M, int64_t N,
-                                  int64_t K, cudaStream_t stream, const int32_t *qzeros)
+                                  int64_t K, cudaStream_t stream, const int32_t *qzeros,
+                                  const uint8_t *qhigh, const uint8_t *zeros5)
 {
     dim3 grid((unsigned)((N + 127) / 128), (unsigned)((M + w4a8::SIMT_MT - 1) / w4a8::SIMT_MT));
     if (grid.y > 65535u) return W4A8_ERR_UNSUPPORTED_SHAPE;
     w4a8::int4_simt_kernel<w4a8::SIMT_MT><<<grid, 128, 0, stream>>>(
-        xq, x_scale, reinterpret_cast<const uint32_t *>(qw), s16, reinterpret_cast<const uint32_t *>(qzeros), out, M, N,
-        K);
+        xq, x_scale, reinterpret_cast<const uint32_t *>(qw), s16, reinterpret_cast<const uint32_t *>(qzeros), qhigh, zeros5,
+        out, M, N, K);
     return w4a8_launch_status();
 }

@@ -449,3 +449,84 @@ def test_int4_rejects_asymmetric(lib):
     qz = torch.full((1, 1), 0x77777776, dtype=torch.int32, device="cuda")
     with pytest.raises(ValueError):
         lib.int4g128_linear(xq, xs, qw, s, qzeros=qz)
+
+
+# --- int5 g128 ("vllm-radiance (MXFP4)", section "int5 (W5A8)")
+
+def _i5_gemm(lib, orc, x, qw, qh, s16, z=None, pairs=None):
+    xq, xs = lib.act_quant(to_dev_bf16(x))
+    out = lib.int5g128_linear(xq, xs, to_dev(qw), to_dev(qh), to_dev_fp16(s16),
+                              None if z is None else to_dev(z))
+    lib.check_device_status()
+    hq, hs = host(xq), host(xs)
+    got = bf16_to_f64(out)
+    if pairs is None:
+        return got, orc.int5g128_linear(hq, hs, qw, qh, s16, z)
+    im, inn = pairs
+    return got[im, inn], orc.int5g128_linear_pairs(hq, hs, qw, qh, s16, z, im, inn)
+
+
+@pytest.mark.parametrize("asym", [False, True], ids=["sym", "asym"])
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (8, 256, 512), (33, 144, 384), (100, 264, 256),
+                                   # N % 16 == 0 and K % 512 == 0: the tensor-core path (stream-K
+                                   # splits, ragged token and column tails, every token tile width)
+                                   (1, 144, 512), (5, 384, 1024), (17, 208, 1536), (33, 528, 2048),
+                                   (64, 1008, 512), (65, 272, 1024), (130, 384, 512), (300, 640, 1536),
+                                   # N % 16 != 0: CUDA-core kernel under every policy
+                                   (3, 200, 1024)])
+def test_int5_linear_small(lib, orc, policy, asym, M, N, K):
+    x = synth.activations(M, K, seed=M + N + 2)
+    qw, qh, s16 = synth.int5_weights(N, K, seed=M + N + 2)
+    z = synth.int5_zeros(N, K, seed=M + N + 2) if asym else None
+    got, ref = _i5_gemm(lib, orc, x, qw, qh, s16, z)
+    gemm_check(got, ref, f"int5 asym={asym} M={M} N={N} K={K} policy={policy}")
+
+
+@pytest.mark.parametrize("asym", [False, True], ids=["sym", "asym"])
+@pytest.mark.parametrize("shape", [GATE_UP, DOWN], ids=["gate_up", "down"])
+@pytest.mark.parametrize("M", [1, 64, 4096])
+def test_int5_full_sampled(lib, orc, shape, M, asym):
+    N, K = shape
+    x = synth.activations(M, K, seed=4)
+    qw, qh, s16 = synth.int5_weights(N, K, seed=4)
+    z = synth.int5_zeros(N, K, seed=4) if asym else None
+    if M > 64:
+        rows = np.unique(np.concatenate([[0, 63, 64, M - 1], synth.uniform_ints(6, 0, M - 1, 4, 5)]))
+        cols = np.unique(np.concatenate([[0, 127, 128, N - 1], synth.uniform_ints(32, 0, N - 1, 4, 6)]))
+        pairs = (np.repeat(rows, cols.size), np.tile(cols, rows.size))
+    else:
+        pairs = _sample_pairs(M, N, 96)
+    got, ref = _i5_gemm(lib, orc, x, qw, qh, s16, z, pairs=pairs)
+    gemm_check(got, ref, f"int5 asym={asym} M={M} N={N} K={K}")
+
+
+def test_int5_degenerate_codes(lib, orc):
+    # every fifth bit set with zero point 16 (values = nibbles), none set (nibble - 16), and
+    # zero points at both ends of 0..31
+    M, N, K = 4, 256, 1024
+    x = synth.activations(M, K, seed=13)
+    qw, _, s16 = synth.int5_weights(N, K, seed=13)
+    for qh in (np.full((K // 8, N), 0xFF, np.uint8), np.zeros((K // 8, N), np.uint8)):
+        got, ref = _i5_gemm(lib, orc, x, qw, qh, s16)
+        gemm_check(got, ref, "int5 constant fifth bits")
+    _, qh, _ = synth.int5_weights(N, K, seed=14)
+    z = np.zeros((K // 128, N), np.uint8)
+    z[:, 1::2] = 31
+    got, ref = _i5_gemm(lib, orc, x, qw, qh, s16, z)
+    gemm_check(got, ref, "int5 zero points 0 and 31")
+
+
+def test_int5_rejects(lib):
+    xq = torch.zeros((1, 128), dtype=torch.uint8, device="cuda")
+    xs = torch.ones(1, dtype=torch.float32, device="cuda")
+    qw = torch.zeros((16, 16), dtype=torch.int32, device="cuda")
+    qh = torch.zeros((16, 16), dtype=torch.uint8, device="cuda")
+    s = torch.ones((1, 16), dtype=torch.float16, device="cuda")
+    with pytest.raises(ValueError):
+        lib.int5g128_linear(xq, xs, qw, qh[:8], s)
+    with pytest.raises(ValueError):
+        lib.int5g128_linear(xq, xs, qw, qh, s, torch.zeros((2, 16), dtype=torch.uint8, device="cuda"))
+    out = torch.empty((1, 16), dtype=torch.bfloat16, device="cuda")
+    st = lib.load().w4a8_int5g128_linear(xq.data_ptr(), xs.data_ptr(), qw.data_ptr(), None, s.data_ptr(), None,
+                                         out.data_ptr(), 1, 16, 128, None, 0, None)
+    assert st == 1  # W4A8_ERR_INVALID_ARG: no fifth-bit plane

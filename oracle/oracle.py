@@ -9,7 +9,8 @@ arithmetic lives in the C file, each routine citing the page passage it follows:
 * "vllm-radiance (MXFP4)", section "How the MXFP4 path works" / "The W4A8 fp8-WMMA kernel".
 * "radiance_autoround.py": module docstring, autoround_linear, _exact_ref.
 * "vllm-radiance (MXFP4)", section "ParoQuant (int4 W4A8 and int5 W5A8)" and "int5 (W5A8)":
-  the asymmetric int4 zero point and the 5-bit codes.
+  the asymmetric int4 zero point and the 5-bit codes; section "Native MXFP4": the W4A4 path
+  (MXFP4 activations, OCP rule per 32).
 
 Parity pins: every routine is pinned by the ``-m "not gpu"`` tests in ``tests/test_oracle_*.py``
 (closed forms, brute force on tiny inputs, hand-built exact blocks, invariants).  Two
@@ -78,6 +79,9 @@ def _load():
             "orc_int4g128_asym_linear_pairs": (None, [P, P, P, P, P, I64, I64, P, P, I64, P]),
             "orc_int5g128_linear": (None, [P, P, P, P, P, P, I64, I64, I64, P]),
             "orc_int5g128_linear_pairs": (None, [P, P, P, P, P, P, I64, I64, P, P, I64, P]),
+            "orc_act_quant_mxfp4": (None, [P, I64, I64, P, P]),
+            "orc_mxfp4_a4_linear": (None, [P, P, P, P, I64, I64, I64, P]),
+            "orc_mxfp4_a4_linear_pairs": (None, [P, P, P, P, I64, P, P, I64, P]),
             "orc_e4m3_encode_many": (None, [P, I64, P]),
             "orc_e4m3_decode_many": (None, [P, I64, P]),
             "orc_fp16_decode_many": (None, [P, I64, P]),
@@ -351,4 +355,42 @@ def int5g128_linear_pairs(xq, x_scale, qweight, qhigh, scales_fp16, zeros, idx_m
     N = q.shape[1]
     out = np.empty(im.size, np.float64)
     _load().orc_int5g128_linear_pairs(xp, sp, qp, hp, scp, zp, N, K, imp, inp, im.size, _p(out))
+    return out
+
+
+def act_quant_mxfp4(x_bf16):
+    """W4A4 activations: bf16 [M, K] (uint16 bits) -> (packed e2m1 [M, K/2], e8m0 [M, K/32]) by the
+    OCP rule per 32 along each row."""
+    x, xp = _c(x_bf16, np.uint16)
+    M, K = x.shape
+    out_p = np.empty((M, K // 2), np.uint8)
+    out_e = np.empty((M, K // 32), np.uint8)
+    _load().orc_act_quant_mxfp4(xp, M, K, _p(out_p), _p(out_e))
+    return out_p, out_e
+
+
+def mxfp4_a4_linear(xa, xe, w_packed, w_e8m0) -> np.ndarray:
+    """W4A4: out[m, n] = sum_k dequant(xa)[m, k] * dequant(w)[n, k], fp64."""
+    a, ap = _c(xa, np.uint8)
+    e, ep = _c(xe, np.uint8)
+    w, wp = _c(w_packed, np.uint8)
+    we, wep = _c(w_e8m0, np.uint8)
+    M = a.shape[0]
+    K = 2 * a.shape[1]
+    N = w.shape[0]
+    out = np.empty((M, N), np.float64)
+    _load().orc_mxfp4_a4_linear(ap, ep, wp, wep, M, N, K, _p(out))
+    return out
+
+
+def mxfp4_a4_linear_pairs(xa, xe, w_packed, w_e8m0, idx_m, idx_n) -> np.ndarray:
+    a, ap = _c(xa, np.uint8)
+    e, ep = _c(xe, np.uint8)
+    w, wp = _c(w_packed, np.uint8)
+    we, wep = _c(w_e8m0, np.uint8)
+    im, imp = _c(idx_m, np.int64)
+    inn, inp = _c(idx_n, np.int64)
+    K = 2 * a.shape[1]
+    out = np.empty(im.size, np.float64)
+    _load().orc_mxfp4_a4_linear_pairs(ap, ep, wp, wep, K, imp, inp, im.size, _p(out))
     return out

@@ -599,6 +599,52 @@ void orc_int5g128_linear_pairs(const uint8_t *xq, const float *x_scale, const in
                  orc_int5_dot(xq, qweight, qhigh, scales_fp16, zeros, N, K, idx_m[i], idx_n[i]);
 }
 
+/* W4A4 ("vllm-radiance (MXFP4)", section "Native MXFP4": Quark OCP micro-scaling checkpoints with
+ * MXFP4 weights AND activations, group 32, e8m0 scales; and "The W4A8 fp8-WMMA kernel", which
+ * names that W4A4 path as the less accurate alternative to fp8 activations).
+ *
+ * Activation quant: the pages do not spell out the activation quantizer; the reading taken is
+ * the OCP micro-scaling rule, which "radiance_nvfp4.py" names "ocp" (_block_exponent: e =
+ * floor(log2 amax) - 2, then e2m1_index of x * 2^-e with the sign rule), applied per 32 along
+ * each token row -- quant_mxfp4 in ocp mode on the bf16 row, the same routine as the bf16
+ * requant source above.  No per-token scale: each block carries its own e8m0. */
+void orc_act_quant_mxfp4(const uint16_t *x_bf16, int64_t M, int64_t K, uint8_t *xa_packed, uint8_t *xa_e8m0)
+{
+    orc_requant_rows(orc_bf16_row, x_bf16, M, K, 0 /* ocp */, xa_packed, xa_e8m0, NULL);
+}
+
+/* W4A4 GEMM: both operands dequantized exactly (e2m1 * 2^(e8m0 - 127)), fp64 sum, k ascending:
+ *   out[m, n] = sum_k e2m1(xa[m, k]) 2^(xe[m, k/32] - 127) * e2m1(w[n, k]) 2^(we[n, k/32] - 127). */
+static double orc_a4_dot(const uint8_t *xa, const uint8_t *xe, const uint8_t *w_packed, const uint8_t *w_e8m0,
+                         int64_t K, int64_t m, int64_t n)
+{
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        uint8_t xb = xa[m * (K / 2) + k / 2], wb = w_packed[n * (K / 2) + k / 2];
+        uint8_t xc = (k & 1) ? (xb >> 4) : (xb & 0x0F), wc = (k & 1) ? (wb >> 4) : (wb & 0x0F);
+        double xv = orc_e2m1_decode(xc) * orc_e8m0_decode(xe[m * (K / 32) + k / 32]);
+        double wv = orc_e2m1_decode(wc) * orc_e8m0_decode(w_e8m0[n * (K / 32) + k / 32]);
+        acc += xv * wv;
+    }
+    return acc;
+}
+
+void orc_mxfp4_a4_linear(const uint8_t *xa, const uint8_t *xe, const uint8_t *w_packed, const uint8_t *w_e8m0,
+                         int64_t M, int64_t N, int64_t K, double *out)
+{
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) out[m * N + n] = orc_a4_dot(xa, xe, w_packed, w_e8m0, K, m, n);
+}
+
+void orc_mxfp4_a4_linear_pairs(const uint8_t *xa, const uint8_t *xe, const uint8_t *w_packed,
+                               const uint8_t *w_e8m0, int64_t K, const int64_t *idx_m, const int64_t *idx_n,
+                               int64_t count, double *out)
+{
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t i = 0; i < count; ++i) out[i] = orc_a4_dot(xa, xe, w_packed, w_e8m0, K, idx_m[i], idx_n[i]);
+}
+
 /* Number of threads the parallel loops above use (1 without OpenMP). */
 int orc_num_threads(void)
 {

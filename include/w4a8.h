@@ -236,6 +236,29 @@ W4A8_API w4a8_status w4a8_int5g128_linear(const uint8_t *xq, const float *x_scal
 
 W4A8_API size_t w4a8_int5g128_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
+/* W4A4 activation quant ("vllm-radiance (MXFP4)", section "Native MXFP4": Quark OCP
+ * micro-scaling checkpoints quantize activations to MXFP4 too, group 32, e8m0 scales).  Each
+ * token row of x, per 32 along K, by the OCP rule ("radiance_nvfp4.py", _block_exponent "ocp":
+ * e = floor(log2 amax) - 2, amax = 0 gives e = 0; _encode_blocks: e2m1 code of |x| * 2^-e with
+ * ties to the even code, clamped to 6, sign bit only on a nonzero code):
+ *   x_bf16    [M, K] bf16 bits (device, 16-byte aligned), K a multiple of 32
+ *   xa_packed [M, K/2] uint8 (out; 16-byte aligned), code of k = 2j in the low nibble of byte j
+ *   xa_e8m0   [M, K/32] uint8 (out), e + 127
+ * Asynchronous on `stream`; bit-exact against the oracle.  Errors as for bf16_to_mxfp4_requant. */
+W4A8_API w4a8_status w4a4_act_quant(const uint16_t *x_bf16, uint8_t *xa_packed, uint8_t *xa_e8m0, int64_t M,
+                                    int64_t K, cudaStream_t stream);
+
+/* W4A4 MXFP4 linear: both operands MXFP4, no per-token scale.
+ *   out[m, n] = bf16( sum_k e2m1(xa[m, k]) 2^(xe[m, k/32] - 127) * e2m1(w[n, k]) 2^(we[n, k/32] - 127) )
+ *   xa_packed [M, K/2], xa_e8m0 [M, K/32] as written by w4a4_act_quant; w_packed / w_e8m0 and the
+ *   workspace (w4a8_workspace_bytes) as for w4a8_mxfp4_linear.
+ * The tensor-core kernel takes K % 512 == 0 with xa_packed and w_packed 32-byte aligned and
+ * xa_e8m0 / w_e8m0 16-byte aligned (other shapes run on the CUDA-core kernel); both operands
+ * go to tcgen05.mma kind::mxf8f6f4 as e2m1 with their block scales in tensor memory. */
+W4A8_API w4a8_status w4a4_mxfp4_linear(const uint8_t *xa_packed, const uint8_t *xa_e8m0, const uint8_t *w_packed,
+                                       const uint8_t *w_e8m0, uint16_t *out_bf16, int64_t M, int64_t N, int64_t K,
+                                       void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 W4A8_API const char *w4a8_status_string(w4a8_status s);
 

@@ -23,7 +23,7 @@ MODES = {"ocp": 0, "noclip": 1, "mse": 2}
 EXPORTS = ("w4a8_act_quant", "w4a8_mxfp4_linear", "w4a8_workspace_bytes",
            "nvfp4_to_mxfp4_requant", "fp8_channel_to_mxfp4_requant", "bf16_to_mxfp4_requant",
            "w4a8_int4g128_linear", "w4a8_int4g128_asym_linear", "w4a8_int4g128_workspace_bytes",
-           "w4a8_int5g128_linear", "w4a8_int5g128_workspace_bytes",
+           "w4a8_int5g128_linear", "w4a8_int5g128_workspace_bytes", "w4a4_act_quant", "w4a4_mxfp4_linear",
            "w4a8_status_string", "w4a8_set_gemm_policy", "w4a8_check_device_status",
            "w4a8_decode_max_m", "w4a8_debug_status_words", "w4a8_debug_set_trace",
            "w4a8_mxfp4_linear_noalloc", "w4a8_noalloc_scratch_bytes",
@@ -64,6 +64,8 @@ def load(build_if_missing: bool = True):
         "w4a8_int4g128_workspace_bytes": (SZ, [I64, I64, I64]),
         "w4a8_int5g128_linear": (I, [P, P, P, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "w4a8_int5g128_workspace_bytes": (SZ, [I64, I64, I64]),
+        "w4a4_act_quant": (I, [P, P, P, I64, I64, P]),
+        "w4a4_mxfp4_linear": (I, [P, P, P, P, P, I64, I64, I64, P, SZ, P]),
         "w4a8_status_string": (ctypes.c_char_p, [I]),
         "w4a8_set_gemm_policy": (None, [I]),
         "w4a8_check_device_status": (I, [P]),
@@ -292,6 +294,40 @@ def int5g128_linear(xq, x_scale, qweight, qhigh, scales_fp16, zeros=None, out=No
     _check("w4a8_int5g128_linear", load().w4a8_int5g128_linear(
         _ptr(xq), _ptr(x_scale), _ptr(qweight), _ptr(qhigh), _ptr(scales_fp16), _ptr(zeros), _ptr(out),
         M, N, K, _ptr(workspace), wsb, _stream(stream)))
+    return out
+
+
+def act_quant_mxfp4(x, xa=None, xe=None, stream=None):
+    """W4A4 activations: bf16 [M, K] -> (e2m1 codes uint8 [M, K/2], e8m0 uint8 [M, K/32]) by the
+    OCP rule per 32 (w4a4_act_quant)."""
+    _dev(x, "x", torch.bfloat16)
+    M, K = x.shape
+    if xa is None:
+        xa = torch.empty((M, K // 2), dtype=torch.uint8, device=x.device)
+    if xe is None:
+        xe = torch.empty((M, K // 32), dtype=torch.uint8, device=x.device)
+    _check("w4a4_act_quant", load().w4a4_act_quant(_ptr(x), _ptr(xa), _ptr(xe), M, K, _stream(stream)))
+    return xa, xe
+
+
+def mxfp4_a4_linear(xa, xe, w_packed, w_e8m0, out=None, workspace=None, stream=None):
+    """W4A4: out[m, n] = bf16(sum_k dequant(xa)[m, k] * dequant(w)[n, k]) (w4a4_mxfp4_linear)."""
+    for t, name in ((xa, "xa"), (xe, "xe"), (w_packed, "w_packed"), (w_e8m0, "w_e8m0")):
+        _dev(t, name, torch.uint8)
+    M, K2 = xa.shape
+    K = 2 * K2
+    N = w_packed.shape[0]
+    if xe.shape != (M, K // 32) or w_packed.shape != (N, K // 2) or w_e8m0.shape != (N, K // 32):
+        raise ValueError("W4A4 operand shapes do not match")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=xa.device)
+    need = workspace_bytes(M, N, K)
+    if need and workspace is None:
+        workspace = make_workspace(need, xa.device)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("w4a4_mxfp4_linear", load().w4a4_mxfp4_linear(
+        _ptr(xa), _ptr(xe), _ptr(w_packed), _ptr(w_e8m0), _ptr(out), M, N, K, _ptr(workspace), wsb,
+        _stream(stream)))
     return out
 
 

@@ -225,3 +225,24 @@ extern "C" w4a8_status w4a8_int5g128_linear(const uint8_t *xq, const float *x_sc
     return w4a8_launch_int4_simt(xq, x_scale, qweight, scales_fp16, out_bf16, M, N, K, stream, nullptr, qhigh,
                                  zeros);
 }
+
+extern "C" w4a8_status w4a4_mxfp4_linear(const uint8_t *xa_packed, const uint8_t *xa_e8m0, const uint8_t *w_packed,
+                                         const uint8_t *w_e8m0, uint16_t *out_bf16, int64_t M, int64_t N, int64_t K,
+                                         void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    if (M < 0 || N < 0 || K < 0) return W4A8_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return W4A8_OK;
+    if (K == 0 || !xa_packed || !xa_e8m0 || !w_packed || !w_e8m0 || !out_bf16) return W4A8_ERR_INVALID_ARG;
+    if (K % 32 != 0) return W4A8_ERR_UNSUPPORTED_SHAPE;
+    if (!w4a8_aligned(xa_packed, 16) || !w4a8_aligned(w_packed, 16) || !w4a8_aligned(out_bf16, 2))
+        return W4A8_ERR_MISALIGNED;
+    const int policy = w4a8_gemm_policy();
+    if (policy != 1 && w4a8_tc_mxfp4_a4_supported(xa_packed, xa_e8m0, w_packed, w_e8m0, out_bf16, M, N, K)) {
+        const size_t need = w4a8_tc_workspace_bytes(M, N, K, policy);
+        if (need && (!workspace || workspace_bytes < need)) return W4A8_ERR_WORKSPACE;
+        if (need && !w4a8_aligned(workspace, 16)) return W4A8_ERR_MISALIGNED;
+        return w4a8_launch_mxfp4_a4_tc(xa_packed, xa_e8m0, w_packed, w_e8m0, out_bf16, M, N, K, workspace, policy,
+                                       stream);
+    }
+    return w4a8_launch_mxfp4_a4_simt(xa_packed, xa_e8m0, w_packed, w_e8m0, out_bf16, M, N, K, stream);
+}

@@ -53,3 +53,12 @@ bool w4a8_tc_int5_supported(const void *xq, const void *qw, const void *qh, cons
 w4a8_status w4a8_launch_int5_tc(const uint8_t *xq, const float *x_scale, const int32_t *qw, const uint8_t *qh,
                                 const uint16_t *s16, const uint8_t *zeros, uint16_t *out, int64_t M, int64_t N,
                                 int64_t K, void *workspace, int policy, cudaStream_t stream);
+
+// W4A4: MXFP4 activations (xa [M, K/2] e2m1 codes, xe [M, K/32] e8m0), no per-token scale.
+bool w4a8_tc_mxfp4_a4_supported(const void *xa, const void *xe, const void *wp, const void *we, const void *out,
+                                int64_t M, int64_t N, int64_t K);
+w4a8_status w4a8_launch_mxfp4_a4_tc(const uint8_t *xa, const uint8_t *xe, const uint8_t *wp, const uint8_t *we,
+                                    uint16_t *out, int64_t M, int64_t N, int64_t K, void *workspace, int policy,
+                                    cudaStream_t stream);
+w4a8_status w4a8_launch_mxfp4_a4_simt(const uint8_t *xa, const uint8_t *xe, const uint8_t *wp, const uint8_t *we,
+                                      uint16_t *out, int64_t M, int64_t N, int64_t K, cudaStream_t stream);

@@ -72,6 +72,57 @@ mxfp4_simt_kernel(const uint8_t *__restrict__ xq, const float *__restrict__ x_sc
     }
 }
 
+// W4A4 ("vllm-radiance (MXFP4)", section "Native MXFP4"): the same walk with MXFP4 activations
+// (e2m1 codes [M, K/2] and e8m0 [M, K/32]); per 32-block the e2m1 x e2m1 products are summed in
+// fp32 and both blocks' power-of-two scales applied once.
+template <int MT>
+__global__ void __launch_bounds__(256)
+mxfp4_a4_simt_kernel(const uint8_t *__restrict__ xa, const uint8_t *__restrict__ xe,
+                     const uint8_t *__restrict__ wp, const uint8_t *__restrict__ we,
+                     uint16_t *__restrict__ out, int64_t M, int64_t N, int64_t K)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t n = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int64_t m0 = (int64_t)blockIdx.y * MT;
+    if (n >= N) return;
+    const int64_t KB = K / 32;
+    float acc[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) acc[t] = 0.0f;
+    for (int64_t b = lane; b < KB; b += 32) {
+        const uint4 wv = __ldg(reinterpret_cast<const uint4 *>(wp + n * (K / 2) + b * 16));
+        const float sw = exp2i((int)we[n * KB + b] - 127);
+        float w[32];
+        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            float2 f = e2m1x2_to_float2((ww[j >> 2] >> (8 * (j & 3))) & 0xffu);
+            w[2 * j] = f.x;
+            w[2 * j + 1] = f.y;
+        }
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            if (m0 + t < M) {
+                const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(xa + (m0 + t) * (K / 2) + b * 16));
+                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                float part = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float2 a = e2m1x2_to_float2((xw[j >> 2] >> (8 * (j & 3))) & 0xffu);
+                    part = fmaf(a.x, w[2 * j], part);
+                    part = fmaf(a.y, w[2 * j + 1], part);
+                }
+                acc[t] = fmaf(part, sw * exp2i((int)xe[(m0 + t) * KB + b] - 127), acc[t]);
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+        float v = warp_sum(acc[t]);
+        if (lane == 0 && m0 + t < M) out[(m0 + t) * N + n] = float_to_bf16_bits(v);
+    }
+}
+
 template <int MT>
 __global__ void __launch_bounds__(128)
 int4_simt_kernel(const uint8_t *__restrict__ xq, const float *__restrict__ x_scale,
@@ -148,5 +199,14 @@ w4a8_status w4a8_launch_int4_simt(const uint8_t *xq, const float *x_scale, const
     w4a8::int4_simt_kernel<w4a8::SIMT_MT><<<grid, 128, 0, stream>>>(
         xq, x_scale, reinterpret_cast<const uint32_t *>(qw), s16, reinterpret_cast<const uint32_t *>(qzeros), qhigh, zeros5,
         out, M, N, K);
+    return w4a8_launch_status();
+}
+
+w4a8_status w4a8_launch_mxfp4_a4_simt(const uint8_t *xa, const uint8_t *xe, const uint8_t *wp, const uint8_t *we,
+                                      uint16_t *out, int64_t M, int64_t N, int64_t K, cudaStream_t stream)
+{
+    dim3 grid((unsigned)((N + 7) / 8), (unsigned)((M + w4a8::SIMT_MT - 1) / w4a8::SIMT_MT));
+    if (grid.y > 65535u) return W4A8_ERR_UNSUPPORTED_SHAPE;
+    w4a8::mxfp4_a4_simt_kernel<w4a8::SIMT_MT><<<grid, 256, 0, stream>>>(xa, xe, wp, we, out, M, N, K);
     return w4a8_launch_status();
 }

@@ -42,6 +42,14 @@
 //   * warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2-5 scale warps, 6-9 epilogue,
 //     10 gate (scale and epilogue warps each use the TMEM lane quarter their warp index selects).
 //
+// W4A4 ("vllm-radiance (MXFP4)", section "Native MXFP4": MXFP4 activations too, group 32, e8m0):
+// the A4 instantiations read the activations as 4-bit codes through the same padded TMA form
+// as the weights and give the instruction both operands as e2m1 (the same kind::mxf8f6f4
+// instruction, B format e2m1).  The activation scales come as [BN tokens x 16 bytes] tiles
+// beside each weight scale tile and the scale warps write them into a ring of B-scale slots:
+// token t's 4-byte word (its 4 k-block scales of a k-tile) in lane t % 32 of every lane
+// quarter, column t / 32 of the slot.  There is no per-token scale.
+//
 // Every mbarrier wait is bounded; a wait that runs out sets a bit in the library's device status
 // word and the CTA winds down (draining what it started) instead of hanging.
 #include <cstring>
@@ -114,14 +122,15 @@ __device__ __forceinline__ void trace_phase(const Params &p, int k)
 // scale slots (KPU k-tiles of A scales each) that the scale warps fill ahead of the data.  With
 // SFQ == US (the decode tilings) a scale slot is tied to its ring slot and freed by the same
 // commit, one commit per fill fewer.
-template <int BN, int KPU, int US, int ACC_BUFS, int SFQ, int SFR>
+template <int BN, int KPU, int US, int ACC_BUFS, int SFQ, int SFR, bool A4 = false>
 struct Layout {
     static constexpr int W_TILE = BM * 128;             // one padded weight k-tile
     static constexpr int X_TILE = BN * 128;             // one activation k-tile (swizzled)
     static constexpr int W_SLOT = KPU * W_TILE;
     static constexpr int X_SLOT = KPU * X_TILE;
     static constexpr int SFR_SLOTS = SFR;
-    static constexpr int SFR_BYTES = BM * 16;
+    static constexpr int SFR_BYTES = BM * 16 + (A4 ? BN * 16 : 0);  // weight (+ activation) scale tiles
+    static constexpr int SFR_B_OFF = BM * 16;           // the activation scale tile in a raw slot
     static constexpr int W_OFF = 0;
     static constexpr int X_OFF = W_OFF + US * W_SLOT;
     static constexpr int SFR_OFF = X_OFF + US * X_SLOT;
@@ -131,10 +140,11 @@ struct Layout {
     static constexpr int STAGE_BYTES = 16 * BM * 2;
     static constexpr int STAGE_OFF = (XS_OFF + BN * 4 + 1023) / 1024 * 1024;
     static constexpr int TOTAL = STAGE_OFF + NSTAGE * STAGE_BYTES + 1024;  // + alignment slack
-    static constexpr int TX_BYTES = KPU * (BM * 64 + X_TILE);  // 4-bit boxes count packed bytes
+    static constexpr int TX_BYTES = KPU * (BM * 64 + (A4 ? BN * 64 : X_TILE));  // 4-bit boxes count packed bytes
     static constexpr int SF_SLOTS = KPU * SFQ;          // TMEM scale k-tile slots, 4 columns each
-    static constexpr int T_SFB = ACC_BUFS * BN;         // TMEM column of the unit B scales
-    static constexpr int T_SFA = T_SFB + 8;             // TMEM columns of the A scales
+    static constexpr int SFBW = BN <= 128 ? 4 : 8;      // W4A4: TMEM columns per B-scale k-tile slot
+    static constexpr int T_SFB = ACC_BUFS * BN;         // TMEM column of the B scales (unit, or W4A4's ring)
+    static constexpr int T_SFA = T_SFB + (A4 ? SFBW * SF_SLOTS : 8);  // TMEM columns of the A scales
     static constexpr int TMEM_NEED = T_SFA + 4 * SF_SLOTS;
     static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64
                                      : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
@@ -145,13 +155,13 @@ struct Layout {
     static_assert((X_TILE % 1024) == 0 && (X_OFF % 1024) == 0, "swizzled tiles are 1024-aligned");
 };
 
-template <int BN, int KPU, int US, int ACC_BUFS, int SFQ, int SFR>
+template <int BN, int KPU, int US, int ACC_BUFS, int SFQ, int SFR, bool A4>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_sf, const __grid_constant__ CUtensorMap tmap_out,
-                const Params p)
+                const __grid_constant__ CUtensorMap tmap_sfb, const Params p)
 {
-    using L = Layout<BN, KPU, US, ACC_BUFS, SFQ, SFR>;
+    using L = Layout<BN, KPU, US, ACC_BUFS, SFQ, SFR, A4>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, derived by pointer arithmetic so the compiler keeps it in the shared window
     uint8_t *smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -206,6 +216,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         tc::tma_prefetch_desc(&tmap_w);
         tc::tma_prefetch_desc(&tmap_x);
         tc::tma_prefetch_desc(&tmap_sf);
+        if (A4) tc::tma_prefetch_desc(&tmap_sfb);
         if (p.tma_out) tc::tma_prefetch_desc(&tmap_out);
     }
     if (warp == 1) {
@@ -216,9 +227,19 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Raw scale tiles of 4-k-tile unit g into raw slot rs: the weight rows' [128 x 16 B] and, for
+    // W4A4, the tokens' [BN x 16 B] (the caller has armed sfr_full[rs] for SFR_BYTES).
+    auto load_raw_scales = [&](int g, int rs) {
+        int kts, ns, mts;
+        sched.fill_at(4 * g, p.m_tiles, kts, ns, mts);
+        tc::tma_load_2d(smem + L::SFR_OFF + rs * L::SFR_BYTES, &tmap_sf, &sfr_full[rs], 4 * kts, ns);
+        if constexpr (A4)
+            tc::tma_load_2d(smem + L::SFR_OFF + rs * L::SFR_BYTES + L::SFR_B_OFF, &tmap_sfb, &sfr_full[rs], 4 * kts,
+                            mts * BN);
+    };
 
     // Unit scale (2^0) for the activation operand: 0x7F in every byte of the B-scale columns.
-    if (warp >= EPI_WARP0) {
+    if (!A4 && warp >= EPI_WARP0) {
         const uint32_t base = tmem + L::T_SFB + ((32u * (warp & 3)) << 16);
         tc::tmem_st4(base, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
         tc::tmem_st4(base + 4, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
@@ -229,12 +250,10 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     // the first US ring fills' weights and the first SFR scale tiles are requested now, while that
     // kernel still runs; the fills' activation halves follow after the wait below.
     int pre = 0;  // ring fills whose weights went out early (producer thread)
-    if (p.w_early && threadIdx.x == 0) {
+    if (!A4 && p.w_early && threadIdx.x == 0) {
         for (int g = 0; g < min(n_k / 4, SFR); ++g) {
-            int kts, ns;
-            sched.fill_at(4 * g, p.m_tiles, kts, ns);
             tc::mbar_arrive_expect_tx(&sfr_full[g], L::SFR_BYTES);
-            tc::tma_load_2d(smem + L::SFR_OFF + g * L::SFR_BYTES, &tmap_sf, &sfr_full[g], 4 * kts, ns);
+            load_raw_scales(g, g);
             atomicMax(sfr_issued, g + 1);
         }
         const uint64_t w_policy = tc::make_policy_evict_first();
@@ -266,10 +285,8 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             if (!p.w_early) {
                 // the first SFR units' raw scale tiles (later ones come from the scale warps)
                 for (int g = 0; g < min(n_units, SFR); ++g) {
-                    int kts, ns;
-                    sched.fill_at(4 * g, p.m_tiles, kts, ns);
                     tc::mbar_arrive_expect_tx(&sfr_full[g], L::SFR_BYTES);
-                    tc::tma_load_2d(smem + L::SFR_OFF + g * L::SFR_BYTES, &tmap_sf, &sfr_full[g], 4 * kts, ns);
+                    load_raw_scales(g, g);
                     atomicMax(sfr_issued, g + 1);
                 }
             }
@@ -348,8 +365,9 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint64_t ad = tc::smem_desc(wa + 32 * kk, 16, 1024, 2);
                             const uint64_t bd = tc::smem_desc(xa + 32 * kk, 16, 1024, 2);
-                            tc::mma_mxf8f6f4(t_acc, ad, bd, tc::idesc_mxf8f6f4(5, 0, BM, BN, kk, 0), sfa,
-                                             tmem + L::T_SFB, (first && j == 0 && kk == 0) ? 0u : 1u);
+                            const uint32_t sfb = A4 ? tmem + L::T_SFB + L::SFBW * (sq * KPU + j) : tmem + L::T_SFB;
+                            tc::mma_mxf8f6f4(t_acc, ad, bd, tc::idesc_mxf8f6f4(5, A4 ? 5 : 0, BM, BN, kk, A4 ? kk : 0),
+                                             sfa, sfb, (first && j == 0 && kk == 0) ? 0u : 1u);
                         }
                     }
                     tc::tc_commit(&empty[sl]);
@@ -392,6 +410,23 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 const uint32_t sw = *reinterpret_cast<const uint32_t *>(raw + 4 * ((i & 3) + j));
                 tc::tmem_st4(tmem + L::T_SFA + 4 * (sq * KPU + j) + ((32u * q) << 16), sw, sw, sw, sw);
             }
+            if constexpr (A4) {
+                // token scales: token t = lane + 32c in column c of the slot, the same in every
+                // lane quarter (each warp writes its own quarter)
+                const uint8_t *rawb = smem + L::SFR_OFF + rs * L::SFR_BYTES + L::SFR_B_OFF;
+#pragma unroll
+                for (int j = 0; j < KPU; ++j) {
+                    uint32_t v[L::SFBW];
+#pragma unroll
+                    for (int c = 0; c < L::SFBW; ++c) {
+                        const int t = lane + 32 * c;
+                        v[c] = t < BN ? *reinterpret_cast<const uint32_t *>(rawb + t * 16 + 4 * ((i & 3) + j)) : 0u;
+                    }
+                    const uint32_t ta = tmem + L::T_SFB + L::SFBW * (sq * KPU + j) + ((32u * q) << 16);
+                    tc::tmem_st4(ta, v[0], v[1], v[2], v[3]);
+                    if constexpr (L::SFBW == 8) tc::tmem_st4(ta + 4, v[4], v[5], v[6], v[7]);
+                }
+            }
             tc::tmem_st_wait();
             tc::tc_fence_before();
             __syncwarp();
@@ -404,10 +439,8 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             // tile into the same slot, so scale loads never hold up the producer's data loads
             if (((i + KPU) & 3) == 0 && warp == SCALE_WARP0 && lane == 0 && g + SFR < n_k / 4) {
                 if ((w = wait_or_fail(&sfr_empty[rs], (g / SFR) & 1, abort_flag, p.status, ST_TIMEOUT_SCALE, g)) == 0) {
-                    int kts, ns;
-                    sched.fill_at(4 * (g + SFR), p.m_tiles, kts, ns);
                     tc::mbar_arrive_expect_tx(&sfr_full[rs], L::SFR_BYTES);
-                    tc::tma_load_2d(smem + L::SFR_OFF + rs * L::SFR_BYTES, &tmap_sf, &sfr_full[rs], 4 * kts, ns);
+                    load_raw_scales(g + SFR, rs);
                     atomicMax(sfr_issued, g + SFR + 1);
                 }
             }
@@ -461,7 +494,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             const int n0 = (t / p.m_tiles) * BM, m0 = (t % p.m_tiles) * BN;
             // the tile's per-token scales, staged once in shared memory (the load overlaps the wait)
             float *xs_s = reinterpret_cast<float *>(smem + L::XS_OFF);
-            for (int i = row; i < BN; i += BM) xs_s[i] = (m0 + i < p.M) ? __ldg(p.xs + m0 + i) : 0.0f;
+            for (int i = row; i < BN; i += BM) xs_s[i] = (m0 + i < p.M) ? (A4 ? 1.0f : __ldg(p.xs + m0 + i)) : 0.0f;
             int w = 0;
             if (lane == 0) w = tc::mbar_wait(&acc_full[b], (seg / ACC_BUFS) & 1, abort_flag, WAIT_BUDGET);
             w = __shfl_sync(0xffffffffu, w, 0);
@@ -660,11 +693,20 @@ size_t workspace_for(const Cfg &c)
     return partial_bytes(c) + (size_t)c.m_tiles * c.n_tiles * 4;
 }
 
-template <int BN, int KPU, int US, int ACC_BUFS, int SFQ, int SFR>
-w4a8_status launch(const uint8_t *wp, const uint8_t *xq, Params prm, cudaStream_t stream)
+template <int BN, int KPU, int US, int ACC_BUFS, int SFQ, int SFR, bool A4 = false>
+w4a8_status launch(const uint8_t *wp, const uint8_t *xq, Params prm, cudaStream_t stream,
+                   const uint8_t *xe = nullptr)
 {
-    using L = Layout<BN, KPU, US, ACC_BUFS, SFQ, SFR>;
-    CUtensorMap tw, tx, tsf, tout;
+    using L = Layout<BN, KPU, US, ACC_BUFS, SFQ, SFR, A4>;
+    CUtensorMap tw, tx, tsf, tout, tsfb;
+    memset(&tsfb, 0, sizeof(tsfb));
+    // W4A4: activations are 4-bit codes [M, K/2] read like the weights, their e8m0 [M, K/32] as
+    // [BN tokens x 16 bytes] tiles
+    if (A4 && (!tch::tmap_3d_ktiles(&tx, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, xq, prm.M, prm.K / 2, 64,
+                                    prm.K / 128, BN, KPU) ||
+               !tch::tmap_2d(&tsfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, xe, prm.M, prm.K / 32, prm.K / 32, BN, 16,
+                             CU_TENSOR_MAP_SWIZZLE_NONE)))
+        return W4A8_ERR_CUDA;
     // output through TMA when its rows are 16-byte strided and the base 16-byte aligned
     memset(&tout, 0, sizeof(tout));
     prm.tma_out = (prm.N % 8 == 0) && w4a8_aligned(prm.out, 16) &&
@@ -674,11 +716,11 @@ w4a8_status launch(const uint8_t *wp, const uint8_t *xq, Params prm, cudaStream_
     // activations (bytes; a row is K bytes, a k-tile 128)
     if (!tch::tmap_3d_ktiles(&tw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wp, prm.N, prm.K / 2, 64, prm.K / 128, BM,
                              KPU) ||
-        !tch::tmap_3d_ktiles(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, prm.M, prm.K, 128, prm.K / 128, BN, KPU) ||
+        (!A4 && !tch::tmap_3d_ktiles(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, prm.M, prm.K, 128, prm.K / 128, BN, KPU)) ||
         !tch::tmap_2d(&tsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, prm.we, prm.N, prm.K / 32, prm.K / 32, BM, 16,
                       CU_TENSOR_MAP_SWIZZLE_NONE))
         return W4A8_ERR_CUDA;
-    auto kern = mxfp4_tc_kernel<BN, KPU, US, ACC_BUFS, SFQ, SFR>;
+    auto kern = mxfp4_tc_kernel<BN, KPU, US, ACC_BUFS, SFQ, SFR, A4>;
     static int attr_done[64] = {0};
     if (!tch::set_smem_once(kern, L::TOTAL, attr_done)) return W4A8_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -691,7 +733,7 @@ w4a8_status launch(const uint8_t *wp, const uint8_t *xq, Params prm, cudaStream_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, tw, tx, tsf, tout, prm) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kern, tw, tx, tsf, tout, tsfb, prm) != cudaSuccess) {
         cudaGetLastError();
         return W4A8_ERR_CUDA;
     }
@@ -726,12 +768,9 @@ size_t w4a8_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int policy)
     return workspace_for(choose(M, N, K));
 }
 
-w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const uint8_t *wp, const uint8_t *we,
-                                 uint16_t *out, int64_t M, int64_t N, int64_t K, void *workspace, int,
-                                 bool w_early, cudaStream_t stream)
+static bool make_params(Params &prm, const Cfg &c, const float *x_scale, const uint8_t *wp, const uint8_t *we,
+                        uint16_t *out, int64_t M, int64_t N, int64_t K, void *workspace, bool w_early)
 {
-    const Cfg c = choose(M, N, K);
-    Params prm;
     prm.wp = wp;
     prm.we = we;
     prm.xs = x_scale;
@@ -739,7 +778,6 @@ w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const 
     prm.partials = static_cast<float *>(workspace);
     prm.counters = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) + partial_bytes(c));
     prm.status = w4a8_device_status_ptr();
-    if (!prm.status) return W4A8_ERR_CUDA;
     prm.M = (int)M;
     prm.N = (int)N;
     prm.K = (int)K;
@@ -755,6 +793,16 @@ w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const 
     // a single token tile reads every weight once: keep it from displacing other lines in L2
     prm.evict_first = c.m_tiles == 1;
     prm.w_early = w_early ? 1 : 0;
+    return prm.status != nullptr;
+}
+
+w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const uint8_t *wp, const uint8_t *we,
+                                 uint16_t *out, int64_t M, int64_t N, int64_t K, void *workspace, int,
+                                 bool w_early, cudaStream_t stream)
+{
+    const Cfg c = choose(M, N, K);
+    Params prm;
+    if (!make_params(prm, c, x_scale, wp, we, out, M, N, K, workspace, w_early)) return W4A8_ERR_CUDA;
     switch (c.BN) {
     case 16: return launch<16, 4, 3, 2, 3, 2>(wp, xq, prm, stream);
     case 32: return launch<32, 4, 2, 2, 2, 4>(wp, xq, prm, stream);
@@ -764,3 +812,25 @@ w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const 
     }
 }
 
+bool w4a8_tc_mxfp4_a4_supported(const void *xa, const void *xe, const void *wp, const void *we, const void *out,
+                                int64_t M, int64_t N, int64_t K)
+{
+    // the activation codes are read like the weights (32-byte aligned), their scales like the weights'
+    return w4a8_tc_mxfp4_supported(xa, wp, we, out, M, N, K) && w4a8_aligned(xa, 32) && w4a8_aligned(xe, 16);
+}
+
+w4a8_status w4a8_launch_mxfp4_a4_tc(const uint8_t *xa, const uint8_t *xe, const uint8_t *wp, const uint8_t *we,
+                                    uint16_t *out, int64_t M, int64_t N, int64_t K, void *workspace, int,
+                                    cudaStream_t stream)
+{
+    const Cfg c = choose(M, N, K);
+    Params prm;
+    if (!make_params(prm, c, nullptr, wp, we, out, M, N, K, workspace, false)) return W4A8_ERR_CUDA;
+    switch (c.BN) {
+    case 16: return launch<16, 4, 3, 2, 3, 2, true>(wp, xa, prm, stream, xe);
+    case 32: return launch<32, 4, 2, 2, 2, 4, true>(wp, xa, prm, stream, xe);
+    case 64: return launch<64, 4, 2, 2, 2, 4, true>(wp, xa, prm, stream, xe);
+    case 128: return launch<128, 2, 3, 2, 6, 4, true>(wp, xa, prm, stream, xe);
+    default: return launch<256, 2, 2, 1, 4, 3, true>(wp, xa, prm, stream, xe);
+    }
+}

@@ -340,3 +340,13 @@ extern "C" w4a8_status bf16_to_mxfp4_requant(const uint16_t *w_bf16, int64_t N, 
     return w4a8::launch_requant(w4a8::SrcBf16{w_bf16}, w4a8::one_partition(N), N, K, mode, out_packed, out_e8m0,
                                 err_ssq, stream);
 }
+
+// W4A4 activation quant ("vllm-radiance (MXFP4)", section "Native MXFP4": MXFP4 activations,
+// group 32, e8m0): each token row of x by the OCP rule ("radiance_nvfp4.py", _block_exponent
+// "ocp", _encode_blocks), i.e. the bf16 source of the requant kernel in ocp mode without the
+// error sums.
+extern "C" w4a8_status w4a4_act_quant(const uint16_t *x_bf16, uint8_t *xa_packed, uint8_t *xa_e8m0, int64_t M,
+                                      int64_t K, cudaStream_t stream)
+{
+    return bf16_to_mxfp4_requant(x_bf16, M, K, 0, xa_packed, xa_e8m0, nullptr, stream);
+}

@@ -88,6 +88,15 @@ struct Sched {
         kt = (int)(u - (long long)t * U) * 4 + (i & 3);
         n0 = (int)((unsigned)t / (unsigned)m_tiles) * BM;
     }
+    // the same, plus the token tile index of k-tile i's tile
+    __device__ void fill_at(int i, int m_tiles, int &kt, int &n0, int &mt) const
+    {
+        const long long u = unit_at(i / 4);
+        const int t = (int)div_nonneg(u, U);
+        kt = (int)(u - (long long)t * U) * 4 + (i & 3);
+        n0 = (int)((unsigned)t / (unsigned)m_tiles) * BM;
+        mt = (int)((unsigned)t % (unsigned)m_tiles);
+    }
     // tile of the k-th segment in processing order, and its unit range [a, b)
     __device__ int seg_tile(int k) const
     {

@@ -530,3 +530,88 @@ def test_int5_rejects(lib):
     st = lib.load().w4a8_int5g128_linear(xq.data_ptr(), xs.data_ptr(), qw.data_ptr(), None, s.data_ptr(), None,
                                          out.data_ptr(), 1, 16, 128, None, 0, None)
     assert st == 1  # W4A8_ERR_INVALID_ARG: no fifth-bit plane
+
+
+# --- W4A4 ("vllm-radiance (MXFP4)", section "Native MXFP4": MXFP4 activations)
+
+def _a4_gemm(lib, orc, x, w, e, pairs=None):
+    xa, xe = lib.act_quant_mxfp4(to_dev_bf16(x))
+    out = lib.mxfp4_a4_linear(xa, xe, to_dev(w), to_dev(e))
+    lib.check_device_status()
+    ha, he = host(xa), host(xe)
+    oa, oe = orc.act_quant_mxfp4(x)
+    assert np.array_equal(ha, oa) and np.array_equal(he, oe), "W4A4 activation codes or scales differ"
+    got = bf16_to_f64(out)
+    if pairs is None:
+        return got, orc.mxfp4_a4_linear(ha, he, w, e)
+    im, inn = pairs
+    return got[im, inn], orc.mxfp4_a4_linear_pairs(ha, he, w, e, im, inn)
+
+
+@pytest.mark.parametrize("M,K", [(1, 32), (3, 96), (9, 5120), (64, 17408), (130, 1024)])
+def test_w4a4_act_quant_bit_exact(lib, orc, M, K):
+    x = synth.activations(M, K, seed=M + K, outliers=True)
+    x[0, :min(K, 64)] = 0  # an all-zero block (and for K <= 64 an all-zero row)
+    xa, xe = lib.act_quant_mxfp4(to_dev_bf16(x))
+    torch.cuda.synchronize()
+    oa, oe = orc.act_quant_mxfp4(x)
+    assert np.array_equal(host(xa), oa) and np.array_equal(host(xe), oe)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (4, 256, 512), (33, 200, 256), (65, 256, 384), (3, 96, 96),
+                                   # K a multiple of 512: the tensor-core path (stream-K splits,
+                                   # ragged token and weight-row tails, every token tile width)
+                                   (1, 128, 512), (5, 384, 1024), (17, 200, 512), (33, 520, 1536),
+                                   (64, 1000, 2048), (65, 256, 512), (130, 520, 1024),
+                                   (257, 384, 512), (300, 640, 1536), (16, 4096, 512)])
+def test_w4a4_linear_small(lib, orc, policy, M, N, K):
+    # prefill recipe: per-token magnitudes spread by a log-normal factor, so every token of a
+    # tile has its own block exponents
+    x, w, e = synth.prefill_case(M, N, K, seed=M * 5 + N)
+    got, ref = _a4_gemm(lib, orc, x, w, e)
+    gemm_check(got, ref, f"w4a4 M={M} N={N} K={K} policy={policy}")
+
+
+@pytest.mark.parametrize("shape", [GATE_UP, DOWN], ids=["gate_up", "down"])
+@pytest.mark.parametrize("M", [1, 8, 32, 64, 4096])
+def test_w4a4_full_sampled(lib, orc, shape, M):
+    N, K = shape
+    x, w, e = synth.prefill_case(M, N, K, seed=1)
+    if M > 64:
+        rows = np.unique(np.concatenate([[0, 127, 128, 255, 256, M - 1], synth.uniform_ints(8, 0, M - 1, 1, 5)]))
+        cols = np.unique(np.concatenate([[0, 127, 128, N - 1], synth.uniform_ints(32, 0, N - 1, 1, 6)]))
+        pairs = (np.repeat(rows, cols.size), np.tile(cols, rows.size))
+    else:
+        pairs = _sample_pairs(M, N, 96)
+    got, ref = _a4_gemm(lib, orc, x, w, e, pairs=pairs)
+    gemm_check(got, ref, f"w4a4 M={M} N={N} K={K}")
+
+
+def test_w4a4_less_accurate_than_w4a8(lib, orc):
+    # the pages' numerics claim: fp8 activations are more accurate than MXFP4 ones.  Both paths
+    # against the exact product of the bf16 activations and the dequantized weights.
+    M, N, K = 16, 512, 2048
+    x = synth.activations(M, K, seed=31)
+    _, w, e = synth.decode_case(1, N, K, seed=31)
+    exact = synth.bf16_bits_to_float(x).astype(np.float64) @ orc.dequant_mxfp4(w, e).T
+    xd = to_dev_bf16(x)
+    xq, xs = lib.act_quant(xd)
+    o8 = bf16_to_f64(lib.mxfp4_linear(xq, xs, to_dev(w), to_dev(e)))
+    xa, xe = lib.act_quant_mxfp4(xd)
+    o4 = bf16_to_f64(lib.mxfp4_a4_linear(xa, xe, to_dev(w), to_dev(e)))
+    rel = lambda o: np.linalg.norm(o - exact) / np.linalg.norm(exact)
+    r8, r4 = rel(o8), rel(o4)
+    assert r8 < 0.05 and r4 < 0.25 and r4 > 2.0 * r8, (r8, r4)
+
+
+def test_w4a4_rejects(lib):
+    xa = torch.zeros((1, 64), dtype=torch.uint8, device="cuda")
+    xe = torch.zeros((1, 4), dtype=torch.uint8, device="cuda")
+    w = torch.zeros((16, 64), dtype=torch.uint8, device="cuda")
+    we = torch.zeros((16, 4), dtype=torch.uint8, device="cuda")
+    with pytest.raises(ValueError):
+        lib.mxfp4_a4_linear(xa, xe[:, :2], w, we)
+    out = torch.empty((1, 16), dtype=torch.bfloat16, device="cuda")
+    st = lib.load().w4a4_mxfp4_linear(xa.data_ptr(), xe.data_ptr(), w.data_ptr(), we.data_ptr(), out.data_ptr(),
+                                      1, 16, 120, None, 0, None)
+    assert st == 2  # W4A8_ERR_UNSUPPORTED_SHAPE: K % 32

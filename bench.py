@@ -641,6 +641,51 @@ def run_extras(lib, dev, peaks):
         tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
         i5[f"{name}_M{M}"] = {"ms": round(ms, 3), "tflops": round(tf, 1), "frac_of_fp8_peak": round(tf / fp8_peak, 4)}
         del qws, qhs, scs, z5
+    # ---- W4A4 (MXFP4 activations by the OCP rule): GEMM decode weight GB/s, prefill TFLOP/s,
+    # activation quant latency, and the relative error of W4A4 and W4A8 against the exact product
+    a4 = {}
+    for name, (N, K) in SHAPES:
+        _, wp, we = synth.decode_case(1, N, K, 0)
+        wb = N * K // 2 + N * K // 32
+        wps = [to_dev(wp) for _ in range(3)]
+        wes = [to_dev(we) for _ in range(3)]
+        for M in (1, 64, 4096):
+            x = torch.randn((M, K), device=dev).to(torch.bfloat16)
+            xa, xe = lib.act_quant_mxfp4(x)
+            o = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ws = lib.make_workspace(lib.workspace_bytes(M, N, K), dev)
+            if M < 4096:
+                fns = [lambda a=a, b=b: lib.mxfp4_a4_linear(xa, xe, a, b, out=o, workspace=ws) for a, b in zip(wps, wes)]
+                ms = timeit_rot(fns)
+                gbs = wb / (ms * 1e-3) / 1e9
+                a4[f"{name}_M{M}"] = {"us": round(ms * 1e3, 2), "weight GB/s": round(gbs, 1),
+                                      "frac_of_hbm": round(gbs / hbm, 4)}
+                ms = timeit(lambda: lib.act_quant_mxfp4(x, xa, xe), reps=20)
+                a4[f"act_quant_{name}_M{M}"] = {"us": round(ms * 1e3, 2)}
+            else:
+                ms = timeit(lambda: lib.mxfp4_a4_linear(xa, xe, wps[0], wes[0], out=o, workspace=ws), reps=2)
+                tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+                a4[f"{name}_M{M}"] = {"ms": round(ms, 3), "tflops": round(tf, 1),
+                                      "frac_of_fp8_peak": round(tf / fp8_peak, 4)}
+        del wps, wes
+    M, N, K = 16, 4096, 5120
+    x = torch.randn((M, K), device=dev).to(torch.bfloat16)
+    _, wp, we = synth.decode_case(1, N, K, 1)
+    wpd, wed = to_dev(wp), to_dev(we)
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    codes = np.stack([wp & 0x0F, wp >> 4], -1).reshape(N, K)
+    wv = grid[codes & 7] * np.where(codes & 8, -1.0, 1.0) * np.repeat(np.exp2(we.astype(np.float64) - 127), 32, 1)
+    wf = torch.from_numpy(wv).to(dev)  # the MXFP4 weights' exact values
+    exact = x.double() @ wf.T
+    xq, xs = lib.act_quant(x)
+    xa, xe = lib.act_quant_mxfp4(x)
+    rel = lambda o: float(torch.linalg.norm(o.double() - exact) / torch.linalg.norm(exact))
+    a4["rel_error_vs_exact"] = {"w4a8": round(rel(lib.mxfp4_linear(xq, xs, wpd, wed)), 5),
+                                "w4a4": round(rel(lib.mxfp4_a4_linear(xa, xe, wpd, wed)), 5),
+                                "case": f"M={M} N={N} K={K}, x ~ N(0,1) bf16, uniform MXFP4 weights"}
+    out["w4a4"] = {"decode_bound": "hbm", "prefill_bound": "tensor (fp8 rate: e2m1 x e2m1 in kind::mxf8f6f4)",
+                   "cases": a4}
+
     out["int5g128"] = {"decode_bound": "hbm", "prefill_bound": "tensor (fp8 peak)",
                        "weight_bytes": "N*K*(1/2 + 1/8 + 2/128) (+ K/128*N zero bytes for asym)", "cases": i5}
     return out

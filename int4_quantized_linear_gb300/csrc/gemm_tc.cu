@@ -665,10 +665,24 @@ struct Cfg {
     int R, D, Gsk;
 };
 
+// Token-tile width for M > 128, from measurements on GB300 (gate_up, down and qkv at M = 512,
+// 2048 and 4096).  A 256-token tile has one accumulator (two do not fit in tensor memory), so its
+// epilogue does not overlap the next tile's MMAs; that pays off only when it is amortized over a
+// long K or over many tiles per CTA.  Otherwise 192-token tiles (two accumulators) are fastest
+// when there are at least three per CTA, and 128-token tiles, which spread better over the SMs,
+// below that.
+static int prefill_bn(int64_t M, int64_t N, int64_t K)
+{
+    if (K >= 16384) return M >= 1024 ? 256 : 128;
+    if (M >= 3072) return 256;
+    const long long n_tiles = (N + BM - 1) / BM;
+    return n_tiles * ((M + 191) / 192) >= 3ll * tch::num_sms() ? 192 : 128;
+}
+
 Cfg choose(int64_t M, int64_t N, int64_t K)
 {
     Cfg c;
-    c.BN = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+    c.BN = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : prefill_bn(M, N, K);
     c.n_tiles = (int)((N + BM - 1) / BM);
     c.m_tiles = (int)((M + c.BN - 1) / c.BN);
     c.U = (int)(K / 512);
@@ -808,6 +822,7 @@ w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const 
     case 32: return launch<32, 4, 2, 2, 2, 4>(wp, xq, prm, stream);
     case 64: return launch<64, 4, 2, 2, 2, 4>(wp, xq, prm, stream);
     case 128: return launch<128, 2, 3, 2, 6, 4>(wp, xq, prm, stream);
+    case 192: return launch<192, 2, 2, 2, 2, 4>(wp, xq, prm, stream);
     default: return launch<256, 2, 2, 1, 4, 4>(wp, xq, prm, stream);
     }
 }
@@ -831,6 +846,7 @@ w4a8_status w4a8_launch_mxfp4_a4_tc(const uint8_t *xa, const uint8_t *xe, const 
     case 32: return launch<32, 4, 2, 2, 2, 4, true>(wp, xa, prm, stream, xe);
     case 64: return launch<64, 4, 2, 2, 2, 4, true>(wp, xa, prm, stream, xe);
     case 128: return launch<128, 2, 3, 2, 6, 4, true>(wp, xa, prm, stream, xe);
+    case 192: return launch<192, 2, 2, 2, 2, 4, true>(wp, xa, prm, stream, xe);
     default: return launch<256, 2, 2, 1, 4, 3, true>(wp, xa, prm, stream, xe);
     }
 }

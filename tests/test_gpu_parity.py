@@ -615,3 +615,16 @@ def test_w4a4_rejects(lib):
     st = lib.load().w4a4_mxfp4_linear(xa.data_ptr(), xe.data_ptr(), w.data_ptr(), we.data_ptr(), out.data_ptr(),
                                       1, 16, 120, None, 0, None)
     assert st == 2  # W4A8_ERR_UNSUPPORTED_SHAPE: K % 32
+
+
+@pytest.mark.parametrize("a4", [False, True], ids=["w4a8", "w4a4"])
+def test_mxfp4_prefill_192_token_tiles(lib, orc, a4):
+    # M = 1000, 76 weight tiles, K = 512: six 192-token tiles per weight tile (the last one 40
+    # tokens) -- the two-accumulator prefill tiling with a ragged token tail
+    M, N, K = 1000, 9728, 512
+    x, w, e = synth.prefill_case(M, N, K, seed=77)
+    rows = np.array([0, 1, 191, 192, 383, 384, 959, 960, 998, 999])
+    cols = np.unique(np.concatenate([[0, 127, 128, N - 1], synth.uniform_ints(40, 0, N - 1, 77, 6)]))
+    pairs = (np.repeat(rows, cols.size), np.tile(cols, rows.size))
+    got, ref = (_a4_gemm if a4 else _mx_gemm)(lib, orc, x, w, e, pairs=pairs)
+    gemm_check(got, ref, f"192-token tiles a4={a4}")

@@ -665,18 +665,17 @@ struct Cfg {
     int R, D, Gsk;
 };
 
-// Token-tile width for M > 128, from measurements on GB300 (gate_up, down and qkv at M = 512,
-// 2048 and 4096).  A 256-token tile has one accumulator (two do not fit in tensor memory), so its
-// epilogue does not overlap the next tile's MMAs; that pays off only when it is amortized over a
-// long K or over many tiles per CTA.  Otherwise 192-token tiles (two accumulators) are fastest
-// when there are at least three per CTA, and 128-token tiles, which spread better over the SMs,
-// below that.
+// Token-tile width for M > 128, from measurements on GB300 (gate_up, down and qkv at M = 512 to
+// 4096).  A 256-token tile has one accumulator (two do not fit in tensor memory), so its epilogue
+// does not overlap the next tile's MMAs; that pays off only when it is amortized over a long K
+// or over many tiles per CTA.  Otherwise 192-token tiles (two accumulators) are fastest when there
+// are at least five per CTA, and 128-token tiles, which spread better over the SMs, below that.
 static int prefill_bn(int64_t M, int64_t N, int64_t K)
 {
-    if (K >= 16384) return M >= 1024 ? 256 : 128;
+    if (K >= 16384) return M > 1024 ? 256 : 128;
     if (M >= 3072) return 256;
     const long long n_tiles = (N + BM - 1) / BM;
-    return n_tiles * ((M + 191) / 192) >= 3ll * tch::num_sms() ? 192 : 128;
+    return n_tiles * ((M + 191) / 192) >= 5ll * tch::num_sms() ? 192 : 128;
 }
 
 Cfg choose(int64_t M, int64_t N, int64_t K)

@@ -619,9 +619,9 @@ def test_w4a4_rejects(lib):
 
 @pytest.mark.parametrize("a4", [False, True], ids=["w4a8", "w4a4"])
 def test_mxfp4_prefill_192_token_tiles(lib, orc, a4):
-    # M = 1000, 76 weight tiles, K = 512: six 192-token tiles per weight tile (the last one 40
-    # tokens) -- the two-accumulator prefill tiling with a ragged token tail
-    M, N, K = 1000, 9728, 512
+    # M = 1000, 127 weight tiles, K = 512: six 192-token tiles per weight tile (the last one 40
+    # tokens), five per CTA -- the two-accumulator prefill tiling with a ragged token tail
+    M, N, K = 1000, 16256, 512
     x, w, e = synth.prefill_case(M, N, K, seed=77)
     rows = np.array([0, 1, 191, 192, 383, 384, 959, 960, 998, 999])
     cols = np.unique(np.concatenate([[0, 127, 128, N - 1], synth.uniform_ints(40, 0, N - 1, 77, 6)]))

@@ -257,11 +257,22 @@ static w4a8_status launch_requant(const Src &src, const Partitions &parts, int64
     if (err_ssq && cudaMemsetAsync(err_ssq, 0, sizeof(double) * 2 * parts.P, stream) != cudaSuccess)
         return W4A8_ERR_CUDA;
     const int64_t blocks = N * (K / 32);
-    int dev = 0, sms = 0, per_sm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_kernel<Src>, RQ_THREADS, 0) != cudaSuccess)
-        return W4A8_ERR_CUDA;
+    // SM count and residency per device, queried once (a per-call query costs microseconds of
+    // host time, as much as the kernel itself for a few activation rows)
+    constexpr int MAX_DEV = 64;
+    static int sms_of[MAX_DEV] = {0}, per_sm_of[MAX_DEV] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return W4A8_ERR_CUDA;
+    int sms = dev < MAX_DEV ? sms_of[dev] : 0, per_sm = dev < MAX_DEV ? per_sm_of[dev] : 0;
+    if (sms == 0) {
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_kernel<Src>, RQ_THREADS, 0) != cudaSuccess)
+            return W4A8_ERR_CUDA;
+        if (dev < MAX_DEV) {
+            per_sm_of[dev] = per_sm;
+            sms_of[dev] = sms;
+        }
+    }
     const int64_t need = (blocks + RQ_THREADS - 1) / RQ_THREADS;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sms * std::max(per_sm, 1)));
     requant_kernel<Src><<<(unsigned)grid, RQ_THREADS, 0, stream>>>(src, parts, N, K, mode, out_packed, out_e8m0,

@@ -5,8 +5,9 @@
 Builds synthetic inputs of the given shape (the same recipe as the benchmark), runs the
 per-token activation quant once and the MXFP4 GEMM ``--calls`` times on ``cuda:0``, then checks
 the library's device status word; exits non-zero if a bounded wait ran out.  Meant as the
-target of ``ncu -k regex:mxfp4_tc -c <calls>`` (``regex:int4_tc`` with ``--int4``): it launches
-nothing else of note.
+target of ``ncu -k regex:mxfp4_tc -c <calls>`` (``regex:int4_tc`` with ``--int4`` or ``--int5``;
+``--w4a4`` runs the MXFP4-activation path, whose GEMM is also ``mxfp4_tc``): it launches nothing
+else of note.
 """
 from __future__ import annotations
 
@@ -26,6 +27,8 @@ def main(argv=None) -> int:
     ap.add_argument("--k", type=int, default=synth.GATE_UP[1])
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--int4", action="store_true", help="the AutoRound int4 g128 GEMM instead of MXFP4")
+    ap.add_argument("--int5", action="store_true", help="the int5 g128 GEMM (zero point 16) instead of MXFP4")
+    ap.add_argument("--w4a4", action="store_true", help="MXFP4 activations (W4A4) instead of fp8 ones")
     args = ap.parse_args(argv)
     M, N, K = args.m, args.n, args.k
     lib.load()
@@ -33,7 +36,21 @@ def main(argv=None) -> int:
     x = torch.from_numpy(np.ascontiguousarray(synth.activations(M, K, seed=M)).view(np.int16)).to(dev)
     xq, xs = lib.act_quant(x.view(torch.bfloat16))
     out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    if args.int4:
+    if args.int5:
+        qw, qh, sc = synth.int5_weights(N, K, 0)
+        qd, hd = torch.from_numpy(qw).to(dev), torch.from_numpy(qh).to(dev)
+        sd = torch.from_numpy(sc).to(dev).view(torch.float16)
+        ws = lib.make_workspace(lib.int5_workspace_bytes(M, N, K), dev)
+        for _ in range(args.calls):
+            lib.int5g128_linear(xq, xs, qd, hd, sd, out=out, workspace=ws)
+    elif args.w4a4:
+        w, e = synth.mxfp4_weights(N, K, 0, 118, 121)
+        wd, ed = torch.from_numpy(w).to(dev), torch.from_numpy(e).to(dev)
+        xa, xe = lib.act_quant_mxfp4(x.view(torch.bfloat16))
+        ws = lib.make_workspace(lib.workspace_bytes(M, N, K), dev)
+        for _ in range(args.calls):
+            lib.mxfp4_a4_linear(xa, xe, wd, ed, out=out, workspace=ws)
+    elif args.int4:
         qw, sc, _ = synth.int4_weights(N, K, 0)
         qd = torch.from_numpy(qw).to(dev)
         sd = torch.from_numpy(sc).to(dev).view(torch.float16)
@@ -49,7 +66,8 @@ def main(argv=None) -> int:
             lib.mxfp4_linear(xq, xs, wd, ed, out=out, workspace=ws)
     torch.cuda.synchronize()
     lib.check_device_status()
-    print(f"ok {'int4' if args.int4 else 'mxfp4'} M={M} N={N} K={K} calls={args.calls}")
+    kind = "int5" if args.int5 else "w4a4" if args.w4a4 else "int4" if args.int4 else "mxfp4"
+    print(f"ok {kind} M={M} N={N} K={K} calls={args.calls}")
     return 0
 
 

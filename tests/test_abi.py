@@ -67,6 +67,23 @@ def test_host_validation_without_gpu(clib):
     assert clib.nvfp4_to_mxfp4_requant(fake, fake, fake, r, 2, 7, 48, 2, fake, fake, NULL, NULL) == 2
     assert clib.nvfp4_to_mxfp4_requant(fake, fake, fake, r, 0, 7, 64, 2, fake, fake, NULL, NULL) == 1
     assert clib.w4a8_workspace_bytes(0, 8, 64) == 0
+    # asymmetric int4, int5, the other requant sources and W4A4: the same host-side checks
+    assert clib.w4a8_int4g128_asym_linear(fake, fake, fake, fake, NULL, fake, 2, 8, 128, NULL, 0, NULL) == 1
+    assert clib.w4a8_int4g128_asym_linear(fake, fake, fake, fake, fake, fake, 2, 8, 64, NULL, 0, NULL) == 2
+    assert clib.w4a8_int5g128_linear(fake, fake, fake, NULL, fake, NULL, fake, 2, 16, 128, NULL, 0, NULL) == 1
+    assert clib.w4a8_int5g128_linear(fake, fake, fake, fake, fake, NULL, fake, 2, 16, 192, NULL, 0, NULL) == 2
+    assert clib.w4a8_int5g128_linear(odd, fake, fake, fake, fake, NULL, fake, 2, 16, 128, NULL, 0, NULL) == 3
+    assert clib.w4a8_int5g128_linear(NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, 16, 128, NULL, 0, NULL) == 0
+    assert clib.fp8_channel_to_mxfp4_requant(fake, fake, 4, 48, 0, fake, fake, NULL, NULL) == 2
+    assert clib.fp8_channel_to_mxfp4_requant(fake, fake, 4, 64, 3, fake, fake, NULL, NULL) == 1
+    assert clib.bf16_to_mxfp4_requant(fake, 4, 48, 0, fake, fake, NULL, NULL) == 2
+    assert clib.bf16_to_mxfp4_requant(odd, 4, 64, 0, fake, fake, NULL, NULL) == 3
+    assert clib.w4a4_act_quant(fake, fake, fake, 2, 48, NULL) == 2
+    assert clib.w4a4_act_quant(fake, fake, fake, 0, 64, NULL) == 0
+    assert clib.w4a4_mxfp4_linear(fake, fake, fake, fake, fake, 2, 8, 48, NULL, 0, NULL) == 2
+    assert clib.w4a4_mxfp4_linear(fake, NULL, fake, fake, fake, 2, 8, 64, NULL, 0, NULL) == 1
+    assert clib.w4a4_mxfp4_linear(odd, fake, fake, fake, fake, 2, 8, 64, NULL, 0, NULL) == 3
+    assert clib.w4a8_int5g128_workspace_bytes(0, 8, 128) == 0
 
 
 def test_symmetric_zero_point_check():

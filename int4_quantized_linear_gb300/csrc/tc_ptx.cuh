@@ -281,13 +281,6 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar)
         : "memory");
 }
 
-// Copy 128 rows x 16 bytes from shared memory (no-swizzle descriptor) to TMEM lanes 0-127,
-// four 32-bit columns starting at taddr.
-__device__ __forceinline__ void tc_cp_128x128b(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 // 32 lanes x 16 consecutive 32-bit columns -> 16 registers per thread.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
 {

@@ -699,7 +699,7 @@ def run_extras(lib, dev, peaks):
                 gbs = wb / (ms * 1e-3) / 1e9
                 a4[f"{name}_M{M}"] = {"us": round(ms * 1e3, 2), "weight GB/s": round(gbs, 1),
                                       "frac_of_hbm": round(gbs / hbm, 4)}
-                ms = timeit(lambda: lib.act_quant_mxfp4(x, xa, xe), reps=20)
+                ms = timeit_rot([lambda: lib.act_quant_mxfp4(x, xa, xe)], reps=24)
                 a4[f"act_quant_{name}_M{M}"] = {"us": round(ms * 1e3, 2)}
             else:
                 ms = timeit(lambda: lib.mxfp4_a4_linear(xa, xe, wps[0], wes[0], out=o, workspace=ws), reps=2)

@@ -224,10 +224,9 @@ W4A8_API w4a8_status w4a8_int4g128_asym_linear(const uint8_t *xq, const float *x
  *   scales_fp16 [K/128, N] fp16 bits
  *   zeros   [K/128, N] uint8 holding z in 0..31, or NULL (symmetric)
  *   workspace: sized by w4a8_int5g128_workspace_bytes; errors as for w4a8_int4g128_linear.
- * K must be a multiple of 128.  The tensor-core kernel converts the fifth bits into a second
- * e4m3 operand (-16 * 2^-9 where the bit is 0) whose MMAs add into the same accumulator as the
- * nibble operand's; with zeros it also keeps the activations' group sums in a second
- * accumulator and applies (z - 16) per column in the fp32 promotion. */
+ * K must be a multiple of 128.  The tensor-core kernel converts each code into the e4m3 byte of
+ * (c - 16) * 2^-9 (exact for every 5-bit code); with zeros it also keeps the activations' group
+ * sums in a second accumulator and applies (z - 16) per column in the fp32 promotion. */
 W4A8_API w4a8_status w4a8_int5g128_linear(const uint8_t *xq, const float *x_scale, const int32_t *qweight,
                                           const uint8_t *qhigh, const uint16_t *scales_fp16,
                                           const uint8_t *zeros, uint16_t *out_bf16, int64_t M, int64_t N,

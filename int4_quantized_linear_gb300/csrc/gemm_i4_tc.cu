@@ -11,19 +11,22 @@
 // and two byte permutes per eight codes), and the zero point rides on four more MMAs per k-tile
 // whose A operand is the constant e4m3 -2^-6 (= -8 * 2^-9) in every element:
 //   sum_k c_k 2^-9 x_k + sum_k (-8 * 2^-9) x_k = 2^-9 * sum_k (c_k - 8) x_k,
-// all inputs exact, accumulated in fp32 tensor memory.  The group scale is not a power of two
-// and cannot ride on the instruction's block scale, so each group's partial is read back and
-// promoted into fp32 registers as acc += (512 * s[g,n]) * partial.
+// all inputs exact, accumulated in fp32 tensor memory.  ((c - 8) * 2^-9 is an exact e4m3 value
+// too, but building those signed bytes costs the converter warps about three times the integer
+// work, and they, not the four extra MMAs, then set the pace: 48 -> 58 us at decode.)  With
+// per-column zero points (asymmetric) the constant-operand MMAs write a second accumulator,
+// which the promotion scales by z / 8.  The group scale is not a power of two and cannot ride on
+// the instruction's block scale, so each group's partial is read back and promoted into fp32
+// registers as acc += (512 * s[g,n]) * partial.
 //
 //   * swap-AB as in the MXFP4 kernel: the weights are the MMA "M" operand (128 output columns n
 //     per tile, one per tensor-memory lane) and the tokens the "N" operand (16, 32 or 64);
 //   * TMA brings the checkpoint words as stored ([K/8, N] int32, 8 consecutive k of one column
 //     per word, 512 contiguous bytes per box row) plus the activation tiles;
 //   * eight converter warps turn each k-tile (128 k x 128 columns) into the e4m3 operand tile the
-//     instruction reads (K-major, 128-byte swizzle), eight codes per five integer instructions;
-//     the constant zero-point operand is one 1 KB swizzle atom that every 8-row group of the
-//     instruction reads (stride between groups 0);
-//   * a k-tile is one group, so every k-tile's eight MMAs go to a fresh accumulator buffer in
+//     instruction reads (K-major, 128-byte swizzle); the constant zero-point operand is one 1 KB
+//     swizzle atom that every 8-row group of the instruction reads (stride 0);
+//   * a k-tile is one group, so every k-tile's MMAs go to a fresh accumulator buffer in
 //     tensor memory (four buffers rotate); four promotion warps read it, scale by s[g,n] (read
 //     from global memory a unit ahead) and add into registers; at the end of a tile the same
 //     warps write bf16 through a shared-memory stage and TMA stores, or the fp32 partial of a
@@ -32,11 +35,12 @@
 //
 // int5 ("vllm-radiance (MXFP4)", section "int5 (W5A8)": 5-bit codes c, value c - 16, the low
 // nibbles in the same word layout and the fifth bit in a plane of one byte per word, bit j of
-// byte (i, n) for k = 8i + j).  Codes 16-31 are not linear in the e4m3 byte, so the fifth bit
-// gets an operand tile of its own: e4m3 -2^-5 (= -16 * 2^-9) where the bit is 0 and 0 where it
-// is 1.  Its four MMAs take the place of the constant zero-point MMAs:
-//   sum_k lo_k 2^-9 x_k + sum_k (-16 * 2^-9)(1 - hi_k) x_k = 2^-9 * sum_k (c_k - 16) x_k.
-// With a zero point z per (group, column) the constant-atom MMAs come back, into the second
+// byte (i, n) for k = 8i + j).  (c - 16) * 2^-9 is exact in e4m3 as well: for c >= 16 it is the
+// nibble's own byte (0x00-0x0F), for c < 16 the sign bit over 16 - nibble, i.e. 0x90 - nibble
+// (0x10 is 2^-5 = 16 * 2^-9).  So the fifth bit only picks between the nibble and 0x90 - nibble,
+// and the symmetric int5 kernel needs no zero-point MMAs at all (here the converter's extra work
+// pays: a separate fifth-bit operand tile would cost its stores and four MMAs).  With a zero
+// point z per (group, column) the constant-atom MMAs write the group sums into the second
 // accumulator as for asymmetric int4, and promotion adds ((z - 16) / 8) times it.
 //
 // Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 5 gate, 2-4, 6-8, 10, 11 converters,
@@ -109,8 +113,8 @@ __device__ __forceinline__ void trace_ev(const Params &p, int ev, int i)
     if (p.trace != nullptr && blockIdx.x == 0 && i < 256) p.trace[ev * 256 + i] = (unsigned long long)clock64();
 }
 
-// Shared memory: the zero-point operand atom (1 KB), NA converted operand tiles (and, for int5,
-// NA fifth-bit operand tiles), then a ring of US fills, each holding KPU k-tiles of activations
+// Shared memory: the zero-point operand atom (1 KB), NA converted operand tiles, then a ring of
+// US fills, each holding KPU k-tiles of activations
 // (BN x 128 bytes, swizzled) and of checkpoint words ([16 word rows][128 columns]), then (int5)
 // KPU k-tiles of the fifth-bit plane ([16 byte rows][128 columns]).
 template <int BN, int US, int NA, int NB, bool ASYM = false, bool I5 = false>
@@ -124,8 +128,7 @@ struct Layout {
     static constexpr int X_SLOT = KPU * X_TILE;
     static constexpr int Z_OFF = 0;                // 8 rows x 128 bytes of e4m3 -2^-6
     static constexpr int A_OFF = Z_OFF + 1024;
-    static constexpr int H_OFF = A_OFF + NA * A_TILE;  // int5: the fifth-bit operand tiles
-    static constexpr int X_OFF = H_OFF + (I5 ? NA * A_TILE : 0);
+    static constexpr int X_OFF = A_OFF + NA * A_TILE;
     static constexpr int RAW_OFF = X_OFF + US * X_SLOT;
     static constexpr int BAR_OFF = RAW_OFF + US * RAW_SLOT;
     static constexpr int XS_OFF = BAR_OFF + 512;
@@ -155,17 +158,25 @@ __device__ __forceinline__ uint2 i4x8_to_bytes(uint32_t w)
 
 constexpr uint32_t E4M3_MINUS_2POW_M6 = 0x88u;  // sign 1, exponent field 1, mantissa 0: -2^-6
 
-// The fifth bits of eight int5 codes (bit j for k = 8i + j) -> one operand byte per code, low
-// byte first, in two words: e4m3 -2^-5 (0x90: sign 1, exponent field 2, mantissa 0) where the
-// bit is 0 and 0x00 where it is 1.  A multiply by 1 + 2^7 + 2^14 + 2^21 moves bit j of a nibble
-// to bit 8j (the four shifted copies do not overlap, so nothing carries); the mask keeps those
-// bits and the multiply by 0x90 turns each 0/1 byte into 0x00/0x90.
-__device__ __forceinline__ uint2 i5_high_to_bytes(uint32_t b)
+// Bits 0, 2, 4 and 6 of b (the others clear) -> 0xFF or 0x00 in bytes 0..3.  The multiply by
+// 1 + 2^6 + 2^12 + 2^18 puts bit 2j at bit 8j; the other copies land on even positions that are
+// not multiples of 8 (where two coincide the carry stops one bit higher, still off 8j), and the
+// mask keeps bits 8j only.
+__device__ __forceinline__ uint32_t spread_even_bits(uint32_t b)
 {
-    const uint32_t nb = ~b;
-    const uint32_t lo = ((nb & 0xFu) * 0x00204081u) & 0x01010101u;
-    const uint32_t hi = (((nb >> 4) & 0xFu) * 0x00204081u) & 0x01010101u;
-    return make_uint2(lo * 0x90u, hi * 0x90u);
+    return ((b * 0x00041041u) & 0x01010101u) * 0xFFu;
+}
+
+// Eight int5 codes: the nibbles of word w and the fifth bits of plane byte hb (bit j for code j)
+// -> the e4m3 bytes of (c - 16) * 2^-9, low byte first: the nibble where the fifth bit is set,
+// 0x90 - nibble where it is clear (no byte borrows: 0x90 > 15).
+__device__ __forceinline__ uint2 i5x8_to_signed_bytes(uint32_t w, uint32_t hb)
+{
+    const uint32_t ev = w & 0x0F0F0F0Fu, od = (w >> 4) & 0x0F0F0F0Fu;
+    const uint32_t he = spread_even_bits(hb & 0x55u), ho = spread_even_bits((hb >> 1) & 0x55u);
+    const uint32_t e = (ev & he) | ((0x90909090u - ev) & ~he);
+    const uint32_t o = (od & ho) | ((0x90909090u - od) & ~ho);
+    return make_uint2(__byte_perm(e, o, 0x5140), __byte_perm(e, o, 0x7362));
 }
 
 template <int BN, int US, int NA, int NB, bool ASYM, bool I5>
@@ -219,8 +230,8 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         tc::tmem_relinquish();
     }
     // the zero-point operand atom (a swizzle only permutes its equal bytes), made visible to the
-    // tensor core before the barrier below
-    if (threadIdx.x < 64) {
+    // tensor core before the barrier below; the symmetric int5 kernel does not read it
+    if ((!I5 || ASYM) && threadIdx.x < 64) {
         const uint32_t z = E4M3_MINUS_2POW_M6 * 0x01010101u;
         reinterpret_cast<uint4 *>(smem + L::Z_OFF)[threadIdx.x] = make_uint4(z, z, z, z);
         tc::fence_proxy_async_smem();
@@ -279,28 +290,24 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             uint32_t wv[8];  // all 8 words first, so the conversions below run side by side
 #pragma unroll
             for (int k = 0; k < 8; ++k) wv[k] = raw[(8 * h + k) * BM];
+            uint32_t hb[8];  // int5: the plane bytes of the same word rows (one per word)
+            if constexpr (I5) {
+                const uint8_t *pl = smem + L::RAW_OFF + sl * L::RAW_SLOT + L::PLANE_OFF + (j * 16 + 8 * h) * BM + r;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) hb[k] = pl[k * BM];
+            }
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {  // 16-byte chunk c = k 16c .. 16c+15 = words 2c, 2c+1
                 const int c = 4 * h + cc;
-                const uint2 lo = i4x8_to_bytes(wv[2 * cc]);
-                const uint2 hi = i4x8_to_bytes(wv[2 * cc + 1]);
-                *reinterpret_cast<uint4 *>(dst + ((c ^ (r & 7)) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
-            }
-            if constexpr (I5) {
-                // the fifth bits of the same 64 codes: plane bytes of the same word rows, to the
-                // same swizzled places of this k-tile's fifth-bit operand tile
-                const uint8_t *pl = smem + L::RAW_OFF + sl * L::RAW_SLOT + L::PLANE_OFF + (j * 16 + 8 * h) * BM + r;
-                uint8_t *hdst = smem + L::H_OFF + a * L::A_TILE + r * 128;
-                uint32_t hb[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) hb[k] = pl[k * BM];
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int c = 4 * h + cc;
-                    const uint2 lo = i5_high_to_bytes(hb[2 * cc]);
-                    const uint2 hi = i5_high_to_bytes(hb[2 * cc + 1]);
-                    *reinterpret_cast<uint4 *>(hdst + ((c ^ (r & 7)) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+                uint2 lo, hi;
+                if constexpr (I5) {
+                    lo = i5x8_to_signed_bytes(wv[2 * cc], hb[2 * cc]);
+                    hi = i5x8_to_signed_bytes(wv[2 * cc + 1], hb[2 * cc + 1]);
+                } else {
+                    lo = i4x8_to_bytes(wv[2 * cc]);
+                    hi = i4x8_to_bytes(wv[2 * cc + 1]);
                 }
+                *reinterpret_cast<uint4 *>(dst + ((c ^ (r & 7)) << 4)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
             }
             tc::fence_proxy_async_smem();  // generic writes -> visible to the tensor core
             __syncwarp();
@@ -334,17 +341,9 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                 for (int kk = 0; kk < 4; ++kk)
                     tc::mma_f8f6f4(tmem + b * BN, tc::smem_desc(aa + 32 * kk, 16, 1024, 2),
                                    tc::smem_desc(xa + 32 * kk, 16, 1024, 2), idesc, kk > 0 ? 1u : 0u);
-                if constexpr (I5) {
-                    // int5: the fifth-bit operand (-16 * 2^-9 where the bit is 0) into the same
-                    // accumulator, which then holds 2^-9 * sum (c - 16) x
-                    const uint32_t ha = tc::smem_u32(smem + L::H_OFF + a * L::A_TILE);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc::mma_f8f6f4(tmem + b * BN, tc::smem_desc(ha + 32 * kk, 16, 1024, 2),
-                                       tc::smem_desc(xa + 32 * kk, 16, 1024, 2), idesc, 1u);
-                }
-                // zero point: the constant atom for every 8-row group (stride 0); with per-column
-                // zero points (asymmetric) into a buffer of its own, scaled per column in promotion
+                // zero point: the constant atom for every 8-row group (stride 0), into the same
+                // accumulator (int4, zero point 8), or with per-column zero points into a buffer of
+                // its own, scaled per column in promotion; the symmetric int5 operand holds c - 16
                 if constexpr (!I5 || ASYM) {
                     const uint32_t zacc = tmem + (ASYM ? NB + b : b) * BN;
 #pragma unroll
@@ -720,17 +719,17 @@ w4a8_status w4a8_launch_int5_tc(const uint8_t *xq, const float *x_scale, const i
     Params prm;
     if (!make_params(prm, c, x_scale, s16, out, M, N, K, workspace)) return W4A8_ERR_CUDA;
     prm.z5 = zeros;
-    // the fifth-bit tiles double the converted operand area: two of each, ring depth 3 / 2 / 2
+    // the plane makes each ring fill 8 KB larger than int4's: ring depth 3 / 2 / 2
     if (zeros != nullptr) {
         switch (c.BN) {
-        case 16: return launch<16, 3, 2, 4, true, true>(qw, xq, prm, stream, qh);
-        case 32: return launch<32, 2, 2, 4, true, true>(qw, xq, prm, stream, qh);
-        default: return launch<64, 2, 2, 4, true, true>(qw, xq, prm, stream, qh);
+        case 16: return launch<16, 3, 3, 4, true, true>(qw, xq, prm, stream, qh);
+        case 32: return launch<32, 2, 3, 4, true, true>(qw, xq, prm, stream, qh);
+        default: return launch<64, 2, 3, 4, true, true>(qw, xq, prm, stream, qh);
         }
     }
     switch (c.BN) {
-    case 16: return launch<16, 3, 2, 4, false, true>(qw, xq, prm, stream, qh);
-    case 32: return launch<32, 2, 2, 4, false, true>(qw, xq, prm, stream, qh);
-    default: return launch<64, 2, 2, 4, false, true>(qw, xq, prm, stream, qh);
+    case 16: return launch<16, 3, 3, 4, false, true>(qw, xq, prm, stream, qh);
+    case 32: return launch<32, 2, 3, 4, false, true>(qw, xq, prm, stream, qh);
+    default: return launch<64, 2, 3, 4, false, true>(qw, xq, prm, stream, qh);
     }
 }

@@ -2,24 +2,27 @@
 
 Workload (one step): for each of the two served shapes -- gate_up N=34816 K=5120 and down
 N=5120 K=17408 -- and each decode batch M in {1, 8, 32, 64}: per-token fp8 activation quant
-of x [M, K] followed by the MXFP4 W4A8 GEMM (one w4a8_mxfp4_linear_bf16 call, two kernels
-chained by programmatic dependent launch), 16 kernel launches in all.  Each (shape, M)
-pair owns its own weight copy, so one step streams 568 MB of weights (more than the 129 MB
-L2): every GEMM reads its weights from HBM.  The step is captured once in a CUDA graph and
-replayed.
+of x [M, K] followed by the MXFP4 W4A8 GEMM (one w4a8_mxfp4_linear_bf16 call).  Each (shape, M)
+pair owns its own weight copy, so one step streams 568 MB of weights (more than the 129 MB L2):
+every GEMM reads its weights from HBM.  The step is captured once in a CUDA graph and replayed.
 
 Metric: decode weight GB/s = weight bytes (N*K*(1/2 + 1/32) per GEMM) per step / step time.
 
 Also reported on the same line:
-  roofline      the decode GEMM kernel's achieved weight GB/s against the measured HBM copy
-                bandwidth, from CUDA events around each GEMM in a graph replay pass;
-  e2e           the same metric through the public Python API with host buffers: pinned host
-                x -> device, act quant + GEMM, bf16 output -> host, every step;
-  cpu_baseline  the CPU oracle on a bounded sample of the same workload;
-  prefill / int4 / requant   the other hot-path kernels on their workloads (--extras).
+  roofline          the decode GEMM kernel against the measured HBM copy bandwidth: the step's
+                    eight GEMMs back to back in one graph (the kernel as it runs inside the step);
+                    the cold, event-bracketed per-GEMM figure is kept as frac_cold;
+  decode_cases      every decode-band GEMM format (W4A8, W4A4, int4, int5) per (shape, M) under
+                    one protocol: a graph of back-to-back calls cycling over weight copies > L2;
+  prefill_roofline  the M=4096 prefill GEMMs against the dense fp8 peak measured in the same run;
+  e2e               the same metric through the public Python API with host buffers: pinned host
+                    x -> device, act quant + GEMM, bf16 output -> host, every step;
+  cpu_baseline      the CPU oracle on a fixed sample of the same workload (the same sample, per
+                    pass, that --impl reference times);
+  extras            the other hot-path kernels (act quant, requant, asymmetric int4, ...).
 
---impl reference times the CPU oracle (the only reference implementation this project has)
-on the same workload, as a bounded sample per step.
+--impl reference times the CPU oracle (the only reference implementation this project has) on
+the same workload: one pass of the fixed sample per step.
 Multi-GPU (torchrun): independent replicas, one per GPU; value = all ranks' bytes / max time.
 """
 from __future__ import annotations
@@ -45,10 +48,26 @@ DECODE_M = [1, 8, 32, 64]
 METRIC = "W4A8 GEMM: decode weight GB/s and prefill TFLOP/s, % of GB300 roofline"
 WORKLOAD = ("decode band MXFP4 W4A8: M in {1,8,32,64} x {gate_up N=34816 K=5120, down N=5120 "
             "K=17408}; act quant + GEMM per (shape, M), one w4a8_mxfp4_linear_bf16 call each")
+# Oracle sample: per (shape, M) case, every token row and SAMPLE_COLS output columns spread
+# over N by stride; one pass = activation quant of the rows + the sampled GEMM outputs.
+SAMPLE_COLS = 64
+# Decode-band per-case protocol shared by every format: a graph of CHAIN_REPS back-to-back calls
+# of one (shape, M) case cycling over weight copies whose total exceeds L2.
+CHAIN_REPS = 24
 
 
 def weight_bytes(N, K):
     return N * K // 2 + N * K // 32
+
+
+STEP_BYTES = sum(weight_bytes(N, K) for _, (N, K) in SHAPES for _ in DECODE_M)
+
+
+def bench_config(world):
+    """The workload description shared by both arms (the driver compares them)."""
+    return {"workload": WORKLOAD, "weight_bytes_per_step": STEP_BYTES,
+            "l2": "inputs larger than L2: 8 distinct weight copies, 568 MB per step",
+            "parallelism": f"replicas x{world}"}
 
 
 def decode_traffic():
@@ -154,72 +173,170 @@ def aggregate(elapsed_ms, step_bytes, steps, world, dist=None, device="cpu"):
     return world * step_bytes * steps / (elapsed_ms * 1e-3) / 1e9, elapsed_ms
 
 
-def oracle_sample(orc, cases, budget_s):
-    """Time the oracle GEMM (act quant of the sample rows + dequantize-and-matmul) over a
-    column sample of every (shape, M) case; returns (weight bytes processed, seconds)."""
-    done_bytes = 0
-    total_t = 0.0
-    per_case = budget_s / len(cases)
-    for (name, (N, K), M, x, w, e) in cases:
-        # calibrate columns so this case costs about per_case seconds
-        cols = 8
-        t_start = time.perf_counter()
-        xq, xs = orc.act_quant(x)
-        while True:
-            n_idx = np.arange(cols) % N
-            im = np.repeat(np.arange(M), cols)
-            inn = np.tile(n_idx, M)
-            t0 = time.perf_counter()
-            orc.mxfp4_linear_pairs(xq, xs, w, e, im, inn)
-            dt = time.perf_counter() - t0
-            if dt >= per_case * 0.5 or cols >= N:
-                break
-            cols = min(N, int(cols * max(2.0, per_case / max(dt, 1e-4))))
-        total_t += time.perf_counter() - t_start
-        done_bytes += cols * (K // 2 + K // 32)
-    return done_bytes, total_t
-
-
-def make_host_cases(seed=0):
-    cases = []
+def make_oracle_sample(seed=0):
+    """The fixed oracle sample: per (shape, M) case of the step, the case's activations (the same
+    seeded x the GPU arm uses), its weights, and SAMPLE_COLS output columns spread over N."""
+    sample = []
     for name, (N, K) in SHAPES:
         w, e = synth.mxfp4_weights(N, K, seed, 118, 121)
+        cols = (np.arange(SAMPLE_COLS, dtype=np.int64) * N) // SAMPLE_COLS
         for M in DECODE_M:
-            cases.append((name, (N, K), M, synth.activations(M, K, seed + M), w, e))
-    return cases
+            x = synth.activations(M, K, seed=seed + M)
+            im = np.repeat(np.arange(M, dtype=np.int64), SAMPLE_COLS)
+            inn = np.tile(cols, M)
+            sample.append((x, w, e, im, inn, SAMPLE_COLS * (K // 2 + K // 32)))
+    return sample
+
+
+SAMPLE_NOTE = (f"one pass = oracle act quant of every token row + {SAMPLE_COLS} output columns (spread over N "
+               f"by stride) of each of the 8 (shape, M) cases; weight GB/s = sampled weight bytes / time")
+
+
+def oracle_pass(orc, sample):
+    """One pass of the oracle over the fixed sample; returns the weight bytes it covered."""
+    done = 0
+    for x, w, e, im, inn, nbytes in sample:
+        xq, xs = orc.act_quant(x)
+        orc.mxfp4_linear_pairs(xq, xs, w, e, im, inn)
+        done += nbytes
+    return done
+
+
+def oracle_timed(orc, sample, budget_s):
+    """Whole passes until budget_s has elapsed (at least one); every timed pass is counted."""
+    oracle_pass(orc, sample)  # warm-up: page in the weights
+    done, t0 = 0, time.perf_counter()
+    while True:
+        done += oracle_pass(orc, sample)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s:
+            return done, dt
+
+
+def oracle_other(orc, budget_s=1.5):
+    """The oracle's other hot-path steps on bounded samples of their workloads: activation quant
+    (M=64, K=17408), NVFP4 -> MXFP4 requant (2048 rows of gate_up, mse), and a prefill GEMM sample
+    (gate_up, M=4096, 16 output columns)."""
+    out = {}
+
+    def rep(fn):
+        fn()
+        n, t0 = 0, time.perf_counter()
+        while True:
+            fn()
+            n += 1
+            dt = time.perf_counter() - t0
+            if dt >= budget_s:
+                return n, dt
+
+    M, K = 64, 17408
+    x = synth.activations(M, K, seed=M)
+    n, dt = rep(lambda: orc.act_quant(x))
+    out["act_quant_M64_K17408"] = {"GB/s": round(n * (3 * M * K + 4 * M) / dt / 1e9, 4),
+                                   "us_per_pass": round(1e6 * dt / n, 1)}
+    R, K = 2048, synth.GATE_UP[1]
+    nv_p, nv_s = synth.nvfp4_tensor_bytes(R, K, 0)
+    div = np.array([2688.0], np.float32)
+    pr = np.array([R], np.int64)
+    n, dt = rep(lambda: orc.requant(nv_p, nv_s, div, pr, "mse"))
+    by = R * K // 2 + R * K // 16 + R * K // 2 + R * K // 32
+    out["requant_mse_2048_rows"] = {"GB/s": round(n * by / dt / 1e9, 4), "ms_per_pass": round(1e3 * dt / n, 1)}
+    (N, K), M, C = synth.GATE_UP, 4096, 16
+    x, wp, we = synth.prefill_case(M, N, K, 0)
+    xq, xs = orc.act_quant(x)
+    cols = (np.arange(C, dtype=np.int64) * N) // C
+    im = np.repeat(np.arange(M, dtype=np.int64), C)
+    inn = np.tile(cols, M)
+    n, dt = rep(lambda: orc.mxfp4_linear_pairs(xq, xs, wp, we, im, inn))
+    out["prefill_gate_up_M4096_16cols"] = {"TFLOP/s": round(n * 2.0 * M * C * K / dt / 1e12, 6),
+                                           "ms_per_pass": round(1e3 * dt / n, 1)}
+    return out
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle, one pass of the fixed sample per step."""
     if rank != 0:
         return
     import oracle as orc
     orc.build()
-    cases = make_host_cases()
-    budget = float(os.environ.get("W4A8_REF_STEP_S", "1.0"))
+    sample = make_oracle_sample()
     for _ in range(args.warmup):
-        oracle_sample(orc, cases, budget * 0.25)
-    tot_b, tot_t = 0, 0.0
+        oracle_pass(orc, sample)
+    done, t0 = 0, time.perf_counter()
     for _ in range(args.steps):
-        b, t = oracle_sample(orc, cases, budget)
-        tot_b += b
-        tot_t += t
-    value = tot_b / tot_t / 1e9
+        done += oracle_pass(orc, sample)
+    dt = time.perf_counter() - t0
+    value = done / dt / 1e9
     cores = orc.num_threads()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64 (oracle: e4m3 x e2m1 dequantized exactly, fp64 accumulate)",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "parallelism": "cpu oracle",
-                                        "sample": "output-column sample per (shape, M)"},
+        "data": "synthetic", "config": bench_config(1),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"~{budget:.1f} s of oracle GEMM per step over column samples of all 8 (shape, M) cases"},
+                         "sample": SAMPLE_NOTE + "; one pass per step"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
 # ---------------------------------------------------------------------------------- GPU side
+
+def chain_time(torch, dev, fns, reps=CHAIN_REPS):
+    """Mean time (ms) of one call when `reps` calls run back to back, cycling over `fns` (calls
+    on different weight copies, so the working set exceeds L2): the calls are captured in one
+    CUDA graph, so consecutive library kernels overlap their set-up through programmatic
+    dependent launch exactly as they do inside a decode step, and host launch cost is excluded."""
+    s = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(s):
+        for f in fns:
+            f()
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(reps):
+            fns[i % len(fns)]()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    with torch.cuda.stream(s):
+        g.replay()
+        g.replay()
+    b.record(s)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / (2 * reps)
+
+
+def measure_fp8_peak(torch, dev):
+    """Dense fp8 (e4m3) GEMM rate of this GPU: torch._scaled_mm (cuBLASLt) on 8192^3, best of 10
+    event-timed calls after warm-up.  Returns TFLOP/s, or None if the call is not available."""
+    try:
+        n = 8192
+        a = torch.randn((n, n), device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn((n, n), device=dev).to(torch.float8_e4m3fn).t()  # column-major operand
+        one = torch.ones((), device=dev, dtype=torch.float32)
+        for _ in range(3):
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(10):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        del a, b
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except (RuntimeError, AttributeError, TypeError):
+        return None
+
 
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -256,6 +373,7 @@ def run_ours(args, rank, world, local_rank):
             calls.append(dict(name=name, N=N, K=K, M=M, w=w, e=e, x=x, x_host=x_host, xq=xq, xs=xs,
                               out=out, ws=ws, lws=lws, bytes=weight_bytes(N, K)))
     step_bytes = sum(c["bytes"] for c in calls)
+    assert step_bytes == STEP_BYTES
     clib = lib.load()
     stream = torch.cuda.Stream(device=dev)
 
@@ -268,10 +386,20 @@ def run_ours(args, rank, world, local_rank):
         if st:
             raise lib.W4A8Error("w4a8_mxfp4_linear_bf16", st)
 
+    def gemm(c, s, w=None, e=None):
+        ws = c["ws"]
+        st = clib.w4a8_mxfp4_linear(c["xq"].data_ptr(), c["xs"].data_ptr(), (c["w"] if w is None else w).data_ptr(),
+                                    (c["e"] if e is None else e).data_ptr(), c["out"].data_ptr(), c["M"], c["N"],
+                                    c["K"], None if ws is None else ws.data_ptr(), 0 if ws is None else ws.numel(), s)
+        if st:
+            raise lib.W4A8Error("w4a8_mxfp4_linear", st)
+
     # eager warm-up (also makes the library's lazy per-device set-up happen outside capture)
     with torch.cuda.stream(stream):
         for c in calls:
             launch(c, stream.cuda_stream)
+            clib.w4a8_act_quant(c["x"].data_ptr(), c["xq"].data_ptr(), c["xs"].data_ptr(), c["M"], c["K"],
+                                stream.cuda_stream)
     stream.synchronize()
     lib.check_device_status(stream)  # a bounded wait that ran out means the kernels are broken
 
@@ -280,25 +408,22 @@ def run_ours(args, rank, world, local_rank):
     with torch.cuda.graph(graph, stream=stream):
         for c in calls:
             launch(c, stream.cuda_stream)
-    ev_graph = None
-    evs = None
-    try:
-        evs = [(torch.cuda.Event(enable_timing=True, external=True),
-                torch.cuda.Event(enable_timing=True, external=True)) for _ in calls]
-        ev_graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(ev_graph, stream=stream):
-            for c, (a, b) in zip(calls, evs):
-                st = clib.w4a8_act_quant(c["x"].data_ptr(), c["xq"].data_ptr(), c["xs"].data_ptr(),
-                                         c["M"], c["K"], stream.cuda_stream)
-                a.record(stream)
-                ws = c["ws"]
-                clib.w4a8_mxfp4_linear(c["xq"].data_ptr(), c["xs"].data_ptr(), c["w"].data_ptr(),
-                                       c["e"].data_ptr(), c["out"].data_ptr(), c["M"], c["N"], c["K"],
-                                       None if ws is None else ws.data_ptr(),
-                                       0 if ws is None else ws.numel(), stream.cuda_stream)
-                b.record(stream)
-    except (TypeError, RuntimeError):
-        ev_graph = None
+    evs = [(torch.cuda.Event(enable_timing=True, external=True),
+            torch.cuda.Event(enable_timing=True, external=True)) for _ in calls]
+    ev_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ev_graph, stream=stream):
+        for c, (a, b) in zip(calls, evs):
+            clib.w4a8_act_quant(c["x"].data_ptr(), c["xq"].data_ptr(), c["xs"].data_ptr(), c["M"], c["K"],
+                                stream.cuda_stream)
+            a.record(stream)
+            gemm(c, stream.cuda_stream)
+            b.record(stream)
+    # the step's eight GEMMs back to back (activations already quantized): the kernel's rate
+    # as it runs inside the step
+    cgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(cgraph, stream=stream):
+        for c in calls:
+            gemm(c, stream.cuda_stream)
 
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -331,62 +456,62 @@ def run_ours(args, rank, world, local_rank):
     value, elapsed_ms = aggregate(e0.elapsed_time(e1), step_bytes, args.steps, world, dist, dev)
     ms_per_step = elapsed_ms / args.steps
 
-    # ---- per-kernel durations of the decode GEMM (same graph, event-bracketed GEMMs)
-    gemm_ms = [0.0] * len(calls)
-    reps = max(3, min(args.steps, 50))
-    if ev_graph is not None:
+    # ---- the GEMM inside the step: the eight GEMMs chained in one graph
+    reps = max(5, min(args.steps, 50))
+    for _ in range(3):
+        cgraph.replay()
+    torch.cuda.synchronize()
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    with torch.cuda.stream(stream):
         for _ in range(reps):
-            ev_graph.replay()
-            torch.cuda.synchronize()
-            for i, (a, b) in enumerate(evs):
-                gemm_ms[i] += a.elapsed_time(b) / reps
-    # ---- the same 8 GEMMs back to back (one graph, chained by programmatic dependent launch,
-    # activations already quantized by the runs above): the kernels' sustained rate in a chain
-    chain_us = None
-    try:
-        cgraph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(cgraph, stream=stream):
-            for c in calls:
-                ws = c["ws"]
-                clib.w4a8_mxfp4_linear(c["xq"].data_ptr(), c["xs"].data_ptr(), c["w"].data_ptr(),
-                                       c["e"].data_ptr(), c["out"].data_ptr(), c["M"], c["N"], c["K"],
-                                       None if ws is None else ws.data_ptr(),
-                                       0 if ws is None else ws.numel(), stream.cuda_stream)
-        for _ in range(3):
             cgraph.replay()
+    c1.record(stream)
+    torch.cuda.synchronize()
+    chain_us = 1e3 * c0.elapsed_time(c1) / reps
+    # ---- each GEMM bracketed by events (starts cold, without overlap with its neighbours)
+    gemm_ms = [0.0] * len(calls)
+    for _ in range(reps):
+        ev_graph.replay()
         torch.cuda.synchronize()
-        c0 = torch.cuda.Event(enable_timing=True)
-        c1 = torch.cuda.Event(enable_timing=True)
-        c0.record(stream)
-        with torch.cuda.stream(stream):
-            for _ in range(reps):
-                cgraph.replay()
-        c1.record(stream)
-        torch.cuda.synchronize()
-        chain_us = 1e3 * c0.elapsed_time(c1) / reps
-    except (TypeError, RuntimeError):
-        chain_us = None
-    t_kern_end = time.time()
+        for i, (a, b) in enumerate(evs):
+            gemm_ms[i] += a.elapsed_time(b) / reps
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
 
     peaks, peak_src = load_peaks()
+    hbm = peaks["hbm_gbs"]
     traffic = decode_traffic()
-    roofline = None
-    if ev_graph is not None:
-        ach = sum(c["bytes"] for c in calls) / (sum(gemm_ms) * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": ach / peaks["hbm_gbs"], "traffic": traffic,
-                    "algorithmic_bytes_per_launch": sum(c["bytes"] for c in calls) / len(calls),
-                    "kernel": "decode-band MXFP4 GEMM (w4a8_mxfp4_linear, M<=64)",
-                    "peak_source": peak_src,
-                    "per_case_us": {f"{c['name']}_M{c['M']}": round(1e3 * g, 2) for c, g in zip(calls, gemm_ms)},
-                    "timing": "each GEMM bracketed by CUDA events in a replica of the step graph (so "
-                              "it starts cold, without programmatic overlap with its neighbours)"}
-        if chain_us:
-            roofline["gemm_chain"] = {"us_per_step": round(chain_us, 2),
-                                      "GB/s": round(step_bytes / (chain_us * 1e-6) / 1e9, 1),
-                                      "note": "the 8 GEMMs back to back in one graph, no activation quant"}
+    step_us = 1e3 * ms_per_step
+    # The GEMMs' time per step cannot exceed the step (which adds the activation quant); if the
+    # separate chain measurement ever did, the whole step is charged to the GEMM instead.
+    consistent = chain_us <= step_us
+    gemm_us = chain_us if consistent else step_us
+    ach = step_bytes / (gemm_us * 1e-6) / 1e9
+    ach_cold = step_bytes / (sum(gemm_ms) * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "traffic": traffic, "algorithmic_bytes_per_launch": step_bytes / len(calls),
+                "kernel": "decode-band MXFP4 GEMM (w4a8_mxfp4_linear, M<=64)", "peak_source": peak_src,
+                "gemm_us_per_step": round(gemm_us, 2), "step_us": round(step_us, 2),
+                "gemm_within_step": consistent,
+                "timing": "the step's 8 GEMMs back to back in one CUDA graph (programmatic dependent launch "
+                          "between them, as inside the step), CUDA events on the launching stream",
+                "frac_cold": ach_cold / hbm,
+                "cold_per_case_us": {f"{c['name']}_M{c['M']}": round(1e3 * g, 2) for c, g in zip(calls, gemm_ms)}}
+
+    # ---- W4A8 decode per case, in the shared per-case protocol (the other formats: extras)
+    decode_cases = {"protocol": f"graph of {CHAIN_REPS} back-to-back calls of one (shape, M) case cycling over "
+                                "weight copies (> L2); per-call mean",
+                    "w4a8": {}}
+    for name, _ in SHAPES:
+        cs = [c for c in calls if c["name"] == name]
+        for c in cs:
+            fns = [lambda c=c, o=o, s=stream: gemm(c, torch.cuda.current_stream().cuda_stream, o["w"], o["e"])
+                   for o in cs]
+            us = 1e3 * chain_time(torch, dev, fns)
+            decode_cases["w4a8"][f"{name}_M{c['M']}"] = {"us": round(us, 2), "frac_of_hbm": round(
+                c["bytes"] / (us * 1e-6) / 1e9 / hbm, 4)}
 
     # ---- e2e through the public API with host buffers
     h2d = sum(c["M"] * c["K"] * 2 for c in calls)
@@ -452,10 +577,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e2m1 (fp32 accumulate)",
-        "data": "synthetic",
-        "config": {"workload": WORKLOAD, "weight_bytes_per_step": step_bytes,
-                   "l2": "inputs larger than L2: 8 distinct weight copies, 568 MB per step",
-                   "graph": "step captured in a CUDA graph", "parallelism": f"replicas x{world}"},
+        "data": "synthetic", "config": bench_config(world),
         "roofline": roofline,
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -464,24 +586,39 @@ def run_ours(args, rank, world, local_rank):
                         "graph and replayed, wall-clock timed",
                 "eager_value": e2e_eager_val},
         "gpu_launches": 2 * len(calls) * args.steps,
+        "decode_cases": decode_cases,
     }
+    del calls, graph, ev_graph, cgraph, g_e2e
+    torch.cuda.empty_cache()
     if not args.no_extras and rank == 0:
-        line["extras"] = run_extras(lib, dev, peaks)
+        extras, prefill_roofline = run_extras(lib, dev, peaks)
+        line["prefill_roofline"] = prefill_roofline
+        for k in ("w4a4", "int4", "int5"):
+            line["decode_cases"][k] = extras.pop("decode_" + k)
+        line["extras"] = extras
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle as orc
         orc.build()
-        b, t = oracle_sample(orc, make_host_cases(), float(os.environ.get("W4A8_CPU_BASELINE_S", "12")))
-        line["cpu_baseline"] = {"value": b / t / 1e9, "unit": "GB/s", "cores": orc.num_threads(),
-                                "kind": "oracle",
-                                "sample": f"oracle act quant + GEMM on output-column samples of all 8 (shape, M) cases, {t:.1f} s"}
+        sample = make_oracle_sample()
+        b, t = oracle_timed(orc, sample, float(os.environ.get("W4A8_CPU_BASELINE_S", "10")))
+        line["cpu_baseline"] = {"value": b / t / 1e9, "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
+                                "sample": SAMPLE_NOTE + f"; whole passes for {t:.1f} s",
+                                "other_steps": oracle_other(orc)}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
 def run_extras(lib, dev, peaks):
-    """Prefill, int4 and requant kernels on their workloads (event-timed, inputs > L2)."""
+    """The other hot-path kernels on their workloads (event-timed, working sets > L2).  Returns
+    (extras, prefill_roofline); extras holds decode_w4a4 / decode_int4 / decode_int5 per-case
+    figures in the shared decode protocol, lifted to the line's decode_cases by the caller."""
     import torch
     out = {}
+    hbm = peaks["hbm_gbs"]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+
+    def copies(nbytes):
+        return max(3, -(-2 * l2 // nbytes))
 
     def timeit(fn, reps=5):
         fn()
@@ -498,35 +635,19 @@ def run_extras(lib, dev, peaks):
     def to_dev(arr):
         return torch.from_numpy(np.ascontiguousarray(arr)).to(dev)
 
-    def timeit_rot(fns, reps=24):
-        """Average time of one call, cycling over calls that touch different buffers (so the
-        working set exceeds L2); the calls are captured in a CUDA graph, so host-side launch
-        cost does not enter the figure."""
-        s = torch.cuda.Stream(device=dev)
-        with torch.cuda.stream(s):
-            for f in fns:
-                f()
-        s.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            for i in range(reps):
-                fns[i % len(fns)]()
-        g.replay()
-        torch.cuda.synchronize()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(s)
-        with torch.cuda.stream(s):
-            g.replay()
-        b.record(s)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / reps
+    def dec_entry(us, nbytes):
+        return {"us": round(us, 2), "frac_of_hbm": round(nbytes / (us * 1e-6) / 1e9 / hbm, 4)}
 
-    fp8_peak = 2.0 * peaks.get("bf16_tflops", 1900.0)
+    # ---- dense fp8 peak, measured now (the prefill roofline's denominator)
+    fp8_meas = measure_fp8_peak(torch, dev)
+    fp8_peak = fp8_meas if fp8_meas else 2.0 * peaks.get("bf16_tflops", 1900.0)
+    fp8_src = ("measured: torch._scaled_mm e4m3 8192^3 (cuBLASLt), best of 10" if fp8_meas else
+               "fallback: 2 x measured bf16 burst")
+
+    # ---- MXFP4 prefill: TFLOP/s against the fp8 peak
     pf = {}
     for name, (N, K) in SHAPES + [("qkv", synth.QKV)]:
         w, e = synth.mxfp4_weights(N, K, 0, 118, 124)
-        # three weight copies in rotation, so weights + activations exceed L2 between calls
         wds = [to_dev(w) for _ in range(3)]
         eds = [to_dev(e) for _ in range(3)]
         for M in (512, 2048, 4096):
@@ -535,16 +656,15 @@ def run_extras(lib, dev, peaks):
             o = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             ws = lib.make_workspace(lib.workspace_bytes(M, N, K), dev)
             fns = [lambda a=a, b=b: lib.mxfp4_linear(xq, xs, a, b, out=o, workspace=ws) for a, b in zip(wds, eds)]
-            ms = timeit_rot(fns, reps=12)
+            ms = chain_time(torch, dev, fns, reps=12)
             tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
-            pf[f"{name}_M{M}"] = {"ms": round(ms, 4), "tflops": round(tf, 1),
-                                  "frac_of_fp8_peak": round(tf / fp8_peak, 4)}
+            pf[f"{name}_M{M}"] = {"ms": round(ms, 4), "tflops": round(tf, 1), "frac": round(tf / fp8_peak, 4)}
         del wds, eds
-    out["prefill"] = {"fp8_peak_tflops": fp8_peak,
-                      "peak_note": "2 x measured bf16 burst (fp8 dense rate is twice bf16)",
-                      "timing": "CUDA graph of 12 calls over 3 weight copies, persistent workspace", "cases": pf}
-    hbm = peaks["hbm_gbs"]
-
+    prefill_roofline = {"bound": "tensor", "unit": "TFLOP/s", "peak": round(fp8_peak, 1), "peak_source": fp8_src,
+                        "kernel": "MXFP4 W4A8 GEMM, kind::mxf8f6f4 (fp8 rate)",
+                        "timing": "graph of 12 calls over 3 weight copies, per-call mean",
+                        "cases": {k: v for k, v in pf.items() if k.endswith("M4096")}}
+    out["prefill"] = {"fp8_peak_tflops": fp8_peak, "peak_source": fp8_src, "cases": pf}
 
     # ---- per-token activation quant: 2MK bytes read, MK + 4M written
     aq = {}
@@ -554,7 +674,7 @@ def run_extras(lib, dev, peaks):
         qs_ = [(torch.empty((M, K), dtype=torch.uint8, device=dev), torch.empty((M,), dtype=torch.float32, device=dev))
                for _ in xs_]
         fns = [lambda x=x, q=q: lib.act_quant(x, q[0], q[1]) for x, q in zip(xs_, qs_)]
-        ms = timeit_rot(fns)
+        ms = chain_time(torch, dev, fns)
         gbs = (3 * M * K + 4 * M) / (ms * 1e-3) / 1e9
         aq[f"M{M}_K{K}"] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4)}
         del xs_, qs_
@@ -592,39 +712,40 @@ def run_extras(lib, dev, peaks):
     by = 2 * N * K + N * K // 2 + N * K // 32
     gbs = by / (ms * 1e-3) / 1e9
     other["bf16_mse"] = {"us": round(ms * 1e3, 1), "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4), "bytes": by}
-    out["requant_other_sources"] = {"bound": "alu (as the NVFP4 requant)", "peak_gbs": hbm,
+    out["requant_other_sources"] = {"bound": "hbm", "peak_gbs": hbm,
                                     "config": "gate_up N=34816 K=5120, one partition, mse rule, with error sums",
                                     "cases": other}
     del wb, o_p, o_e
 
-    # ---- AutoRound int4 g128: decode weight GB/s, prefill TFLOP/s
-    i4 = {}
+    # ---- AutoRound int4 g128: decode (shared protocol), prefill TFLOP/s at M=4096
+    dec_i4, i4 = {}, {}
     for name, (N, K) in SHAPES:
         qw, sc, _ = synth.int4_weights(N, K, 0)
         wb = N * K // 2 + N * K // 64
-        n_copies = 3
-        qws = [to_dev(qw) for _ in range(n_copies)]
-        scs = [to_dev(sc).view(torch.float16) for _ in range(n_copies)]
-        for M in (1, 8, 64):
+        nc = copies(wb)
+        qws = [to_dev(qw) for _ in range(nc)]
+        scs = [to_dev(sc).view(torch.float16) for _ in range(nc)]
+        for M in DECODE_M:
             x = torch.randn((M, K), device=dev).to(torch.bfloat16)
             xq, xs = lib.act_quant(x)
             o = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             ws = lib.make_workspace(lib.int4_workspace_bytes(M, N, K), dev)
             fns = [lambda a=a, b=b: lib.int4g128_linear(xq, xs, a, b, out=o, workspace=ws) for a, b in zip(qws, scs)]
-            ms = timeit_rot(fns)
-            gbs = wb / (ms * 1e-3) / 1e9
-            i4[f"{name}_M{M}"] = {"us": round(ms * 1e3, 2), "weight GB/s": round(gbs, 1),
-                                  "frac_of_hbm": round(gbs / hbm, 4)}
+            dec_i4[f"{name}_M{M}"] = dec_entry(1e3 * chain_time(torch, dev, fns), wb)
         M = 4096
         x = torch.randn((M, K), device=dev).to(torch.bfloat16)
         xq, xs = lib.act_quant(x)
         o = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         ws = lib.make_workspace(lib.int4_workspace_bytes(M, N, K), dev)
-        ms = timeit(lambda: lib.int4g128_linear(xq, xs, qws[0], scs[0], out=o, workspace=ws), reps=2)
+        fns = [lambda a=a, b=b: lib.int4g128_linear(xq, xs, a, b, out=o, workspace=ws) for a, b in zip(qws[:3], scs[:3])]
+        ms = chain_time(torch, dev, fns, reps=6)
         tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
         i4[f"{name}_M{M}"] = {"ms": round(ms, 3), "tflops": round(tf, 1), "frac_of_fp8_peak": round(tf / fp8_peak, 4)}
+        prefill_roofline["cases"][f"int4_{name}_M{M}"] = {"ms": round(ms, 4), "tflops": round(tf, 1),
+                                                          "frac": round(tf / fp8_peak, 4)}
         del qws, scs
-    out["int4g128"] = {"decode_bound": "hbm", "prefill_bound": "tensor (fp8 peak)", "cases": i4}
+    out["decode_int4"] = dec_i4
+    out["int4g128_prefill"] = {"bound": "tensor (fp8 peak)", "cases": i4}
 
     # ---- asymmetric int4 g128 (per-group, per-column zero points): decode GB/s, M = 1 and 64
     i4a = {}
@@ -632,8 +753,9 @@ def run_extras(lib, dev, peaks):
         qw, sc, _ = synth.int4_weights(N, K, 0)
         qz = to_dev(synth.int4_asym_zeros(N, K, 0))
         wb = N * K // 2 + N * K // 64 + (K // 128) * ((N + 7) // 8) * 4
-        qws = [to_dev(qw) for _ in range(3)]
-        scs = [to_dev(sc).view(torch.float16) for _ in range(3)]
+        nc = copies(wb)
+        qws = [to_dev(qw) for _ in range(nc)]
+        scs = [to_dev(sc).view(torch.float16) for _ in range(nc)]
         for M in (1, 64):
             x = torch.randn((M, K), device=dev).to(torch.bfloat16)
             xq, xs = lib.act_quant(x)
@@ -641,68 +763,78 @@ def run_extras(lib, dev, peaks):
             ws = lib.make_workspace(lib.int4_workspace_bytes(M, N, K), dev)
             fns = [lambda a=a, b=b: lib.int4g128_asym_linear(xq, xs, a, b, qz, out=o, workspace=ws)
                    for a, b in zip(qws, scs)]
-            ms = timeit_rot(fns)
-            gbs = wb / (ms * 1e-3) / 1e9
-            i4a[f"{name}_M{M}"] = {"us": round(ms * 1e3, 2), "weight GB/s": round(gbs, 1),
-                                   "frac_of_hbm": round(gbs / hbm, 4)}
+            i4a[f"{name}_M{M}"] = dec_entry(1e3 * chain_time(torch, dev, fns), wb)
         del qws, scs, qz
-    out["int4g128_asym"] = {"decode_bound": "hbm", "cases": i4a}
+    out["int4g128_asym_decode"] = {"bound": "hbm", "cases": i4a}
 
-    # ---- int5 g128 (fifth-bit plane; zero point 16, or a byte per group and column): decode
-    # weight GB/s at M = 1 and 64, prefill TFLOP/s at M = 4096
-    i5 = {}
+    # ---- int5 g128 (fifth-bit plane; zero point 16, or a byte per group and column): decode in
+    # the shared protocol (zero point 16), with zero points at M = 1 and 64, prefill at M = 4096
+    dec_i5, i5 = {}, {}
     for name, (N, K) in SHAPES:
         qw, qh, sc = synth.int5_weights(N, K, 0)
         z5 = to_dev(synth.int5_zeros(N, K, 0))
         wb = N * K // 2 + N * K // 8 + N * K // 64
-        qws = [to_dev(qw) for _ in range(3)]
-        qhs = [to_dev(qh) for _ in range(3)]
-        scs = [to_dev(sc).view(torch.float16) for _ in range(3)]
-        for M in (1, 64):
+        nc = copies(wb)
+        qws = [to_dev(qw) for _ in range(nc)]
+        qhs = [to_dev(qh) for _ in range(nc)]
+        scs = [to_dev(sc).view(torch.float16) for _ in range(nc)]
+        for M in DECODE_M:
             x = torch.randn((M, K), device=dev).to(torch.bfloat16)
             xq, xs = lib.act_quant(x)
             o = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             ws = lib.make_workspace(lib.int5_workspace_bytes(M, N, K), dev)
             for tag, z in (("", None), ("_asym", z5)):
+                if z is not None and M not in (1, 64):
+                    continue
                 fns = [lambda a=a, h=h, b=b, z=z: lib.int5g128_linear(xq, xs, a, h, b, z, out=o, workspace=ws)
                        for a, h, b in zip(qws, qhs, scs)]
-                ms = timeit_rot(fns)
-                by = wb + (0 if z is None else (K // 128) * N)
-                gbs = by / (ms * 1e-3) / 1e9
-                i5[f"{name}_M{M}{tag}"] = {"us": round(ms * 1e3, 2), "weight GB/s": round(gbs, 1),
-                                           "frac_of_hbm": round(gbs / hbm, 4)}
+                e = dec_entry(1e3 * chain_time(torch, dev, fns), wb + (0 if z is None else (K // 128) * N))
+                if z is None:
+                    dec_i5[f"{name}_M{M}"] = e
+                else:
+                    i5[f"{name}_M{M}_asym"] = e
         M = 4096
         x = torch.randn((M, K), device=dev).to(torch.bfloat16)
         xq, xs = lib.act_quant(x)
         o = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         ws = lib.make_workspace(lib.int5_workspace_bytes(M, N, K), dev)
-        ms = timeit(lambda: lib.int5g128_linear(xq, xs, qws[0], qhs[0], scs[0], out=o, workspace=ws), reps=2)
+        fns = [lambda a=a, h=h, b=b: lib.int5g128_linear(xq, xs, a, h, b, out=o, workspace=ws)
+               for a, h, b in zip(qws[:3], qhs[:3], scs[:3])]
+        ms = chain_time(torch, dev, fns, reps=6)
         tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
         i5[f"{name}_M{M}"] = {"ms": round(ms, 3), "tflops": round(tf, 1), "frac_of_fp8_peak": round(tf / fp8_peak, 4)}
+        prefill_roofline["cases"][f"int5_{name}_M{M}"] = {"ms": round(ms, 4), "tflops": round(tf, 1),
+                                                          "frac": round(tf / fp8_peak, 4)}
         del qws, qhs, scs, z5
-    # ---- W4A4 (MXFP4 activations by the OCP rule): GEMM decode weight GB/s, prefill TFLOP/s,
-    # activation quant latency, and the relative error of W4A4 and W4A8 against the exact product
-    a4 = {}
+    out["decode_int5"] = dec_i5
+    out["int5g128"] = {"weight_bytes": "N*K*(1/2 + 1/8 + 2/128) (+ K/128*N zero bytes with zero points)",
+                       "cases": i5}
+
+    # ---- W4A4 (MXFP4 activations by the OCP rule): decode GEMM in the shared protocol, prefill
+    # TFLOP/s, activation quant latency, and the relative error of W4A4 and W4A8 against the exact
+    # product
+    dec_a4, a4 = {}, {}
     for name, (N, K) in SHAPES:
         _, wp, we = synth.decode_case(1, N, K, 0)
         wb = N * K // 2 + N * K // 32
-        wps = [to_dev(wp) for _ in range(3)]
-        wes = [to_dev(we) for _ in range(3)]
-        for M in (1, 64, 4096):
+        nc = copies(wb)
+        wps = [to_dev(wp) for _ in range(nc)]
+        wes = [to_dev(we) for _ in range(nc)]
+        for M in DECODE_M + [4096]:
             x = torch.randn((M, K), device=dev).to(torch.bfloat16)
             xa, xe = lib.act_quant_mxfp4(x)
             o = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             ws = lib.make_workspace(lib.workspace_bytes(M, N, K), dev)
             if M < 4096:
                 fns = [lambda a=a, b=b: lib.mxfp4_a4_linear(xa, xe, a, b, out=o, workspace=ws) for a, b in zip(wps, wes)]
-                ms = timeit_rot(fns)
-                gbs = wb / (ms * 1e-3) / 1e9
-                a4[f"{name}_M{M}"] = {"us": round(ms * 1e3, 2), "weight GB/s": round(gbs, 1),
-                                      "frac_of_hbm": round(gbs / hbm, 4)}
-                ms = timeit_rot([lambda: lib.act_quant_mxfp4(x, xa, xe)], reps=24)
-                a4[f"act_quant_{name}_M{M}"] = {"us": round(ms * 1e3, 2)}
+                dec_a4[f"{name}_M{M}"] = dec_entry(1e3 * chain_time(torch, dev, fns), wb)
+                if M in (1, 64):
+                    ms = chain_time(torch, dev, [lambda: lib.act_quant_mxfp4(x, xa, xe)])
+                    a4[f"act_quant_{name}_M{M}"] = {"us": round(ms * 1e3, 2)}
             else:
-                ms = timeit(lambda: lib.mxfp4_a4_linear(xa, xe, wps[0], wes[0], out=o, workspace=ws), reps=2)
+                fns = [lambda a=a, b=b: lib.mxfp4_a4_linear(xa, xe, a, b, out=o, workspace=ws)
+                       for a, b in zip(wps[:3], wes[:3])]
+                ms = chain_time(torch, dev, fns, reps=6)
                 tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
                 a4[f"{name}_M{M}"] = {"ms": round(ms, 3), "tflops": round(tf, 1),
                                       "frac_of_fp8_peak": round(tf / fp8_peak, 4)}
@@ -722,12 +854,9 @@ def run_extras(lib, dev, peaks):
     a4["rel_error_vs_exact"] = {"w4a8": round(rel(lib.mxfp4_linear(xq, xs, wpd, wed)), 5),
                                 "w4a4": round(rel(lib.mxfp4_a4_linear(xa, xe, wpd, wed)), 5),
                                 "case": f"M={M} N={N} K={K}, x ~ N(0,1) bf16, uniform MXFP4 weights"}
-    out["w4a4"] = {"decode_bound": "hbm", "prefill_bound": "tensor (fp8 rate: e2m1 x e2m1 in kind::mxf8f6f4)",
-                   "cases": a4}
-
-    out["int5g128"] = {"decode_bound": "hbm", "prefill_bound": "tensor (fp8 peak)",
-                       "weight_bytes": "N*K*(1/2 + 1/8 + 2/128) (+ K/128*N zero bytes for asym)", "cases": i5}
-    return out
+    out["decode_w4a4"] = dec_a4
+    out["w4a4"] = {"prefill_bound": "tensor (fp8 rate: e2m1 x e2m1 in kind::mxf8f6f4)", "cases": a4}
+    return out, prefill_roofline
 
 
 def main():
@@ -737,7 +866,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the other hot-path kernels (prefill, act quant, requant, int4)")
+                    help="skip the other hot-path kernels (prefill, act quant, requant, int4, int5, W4A4)")
     ap.add_argument("--extras", action="store_true", help="(default) kept for compatibility")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

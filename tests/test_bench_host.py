@@ -49,10 +49,24 @@ def test_aggregate_single_rank():
 
 
 def test_reference_arm_line():
-    env = dict(os.environ, W4A8_REF_STEP_S="0.2")
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
-                        "--warmup", "3"], capture_output=True, text=True, env=env, timeout=600, cwd=ROOT)
+                        "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["unit"] == "GB/s"
+    import bench
+    # the same workload description as the GPU arm's line, so the two lines compare
+    assert line["config"] == bench.bench_config(1)
+
+
+def test_oracle_sample_is_fixed():
+    """Both arms time the same fixed sample: its bytes per pass do not depend on timing."""
+    import bench
+    import oracle as orc
+    orc.build()
+    sample = bench.make_oracle_sample()
+    assert len(sample) == 8
+    per_pass = sum(s[-1] for s in sample)
+    assert per_pass == bench.SAMPLE_COLS * sum(K // 2 + K // 32 for _, (N, K) in bench.SHAPES for _ in bench.DECODE_M)
+    assert bench.oracle_pass(orc, sample) == per_pass

@@ -109,20 +109,27 @@ W4A8_API w4a8_status w4a8_mxfp4_linear_bf16(const uint16_t *x_bf16, const uint8_
 /* Bytes of workspace w4a8_mxfp4_linear_bf16 needs for this shape. */
 W4A8_API size_t w4a8_mxfp4_linear_bf16_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
-/* w4a8_mxfp4_linear for callers that cannot allocate device memory (no counterpart in the
- * pages; an addition of this library).  Code being captured into a CUDA graph, serving engines
- * that keep all device memory in their own pool, and plugin interfaces that pass only inputs and
- * outputs have no way to supply a workspace.  This call keeps the GEMM's scratch (fp32 partial
- * tiles and arrival counters) in a fixed array of w4a8_noalloc_scratch_bytes() bytes (12 MiB)
- * inside the library's device image, which every GPU that loads the library holds until the
- * process exits.  It calls no cudaMalloc or cudaFree.
+/* w4a8_mxfp4_linear for callers that cannot allocate device memory.  The pages have no
+ * counterpart; this is an addition of this library.  The regular entry point needs a
+ * caller-provided workspace.  Some callers cannot provide one: serving engines that reserve all
+ * device memory for their own pool up front and treat an allocation outside it as an error, and
+ * plugin or custom-operator interfaces that pass a kernel only its inputs and outputs.  This call
+ * keeps the GEMM's scratch (fp32 partial tiles and arrival counters) in a fixed array of
+ * w4a8_noalloc_scratch_bytes() bytes (12 MiB) in the library's device image, which every GPU that
+ * loads the library holds until the process exits.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
  *   Arguments, layouts and the result are those of w4a8_mxfp4_linear, minus the workspace.
- *   Sizes whose scratch would exceed the array (larger token counts, very wide outputs) are
- *   rejected with W4A8_ERR_WORKSPACE; w4a8_workspace_bytes(M, N, K) gives the need.
- *   The first call on a device looks up the array's device address (cudaGetSymbolAddress); make
- *   that first call before any stream capture.  The arrival counters are cleared on the stream
- *   at every call.  All calls share the one array: calls that can run at the same time on the
- *   GPU (other streams, other threads) race on it and must be serialized by the caller. */
+ *   Sizes whose scratch would exceed the array (prefill-sized token counts, very wide outputs)
+ *   are rejected with W4A8_ERR_WORKSPACE before anything is launched; w4a8_workspace_bytes(M, N,
+ *   K) gives the need.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it per device and context, so a
+ *   call after a device reset looks it up again.  Make that first call on a device before any
+ *   stream capture.
+ *   The arrival counters, which must start at zero, are cleared on the stream at every call (the
+ *   partial tiles need no clearing).  All calls share the one array, which keeps the last call's
+ *   contents: calls that overlap on the GPU (other streams, other threads) race on it and must
+ *   be serialized by the caller. */
 W4A8_API w4a8_status w4a8_mxfp4_linear_noalloc(const uint8_t *xq, const float *x_scale,
                                                const uint8_t *w_packed, const uint8_t *w_e8m0,
                                                uint16_t *out_bf16, int64_t M, int64_t N, int64_t K,
@@ -278,14 +285,24 @@ W4A8_API w4a8_status w4a8_check_device_status(cudaStream_t stream);
  * event) and clears it.  Returns a w4a8_status value. */
 W4A8_API int w4a8_debug_status_words(unsigned int *out4);
 
-/* Diagnostic: while device_buffer (device, 6 x 256 + 16 x 512 uint64, zero-filled, or NULL to
- * stop) is set, the tensor-core MXFP4 GEMM records, for its first CTA, clock64() stamps of
- * pipeline events (6 rows of 256: k-tile issued, scale slot free, scales written, fill released
- * to the MMA warp, fill issued, fill's scales seen), and for every CTA (up to 512) 16 global-timer
- * stamps (entry, set-up done, epilogue done, exit, last-tile epilogue steps, first and last fill
- * released, MMA issue done, first accumulator ready, last-tile partials staged and summed).
- * Process-wide; for performance investigation only. */
-W4A8_API void w4a8_debug_set_trace(void *device_buffer);
+/* Which kernel a GEMM call with these arguments would run.  The entry points choose inside the
+ * call (the tensor-core kernels need, among other things, K a multiple of 512 and the alignments
+ * stated above); these queries report that choice without launching anything, so a caller can
+ * tell when a shape falls back to the CUDA-core kernels, which are 10-100x slower and meant only
+ * for shapes the tensor-core kernels do not take.  The arguments are the ones the entry point
+ * would get (device pointers, only their values are inspected).  Returns W4A8_PATH_TENSOR_CORE,
+ * W4A8_PATH_CUDA_CORE, or 0 when the entry point would reject the arguments.  The answer follows
+ * the current w4a8_set_gemm_policy setting. */
+#define W4A8_PATH_TENSOR_CORE 1
+#define W4A8_PATH_CUDA_CORE 2
+W4A8_API int w4a8_mxfp4_path(const void *xq, const void *w_packed, const void *w_e8m0, const void *out_bf16,
+                             int64_t M, int64_t N, int64_t K);
+W4A8_API int w4a8_int4g128_path(const void *xq, const void *qweight, const void *scales_fp16,
+                                const void *out_bf16, int64_t M, int64_t N, int64_t K);
+W4A8_API int w4a8_int5g128_path(const void *xq, const void *qweight, const void *qhigh, const void *scales_fp16,
+                                const void *out_bf16, int64_t M, int64_t N, int64_t K);
+W4A8_API int w4a4_mxfp4_path(const void *xa_packed, const void *xa_e8m0, const void *w_packed,
+                             const void *w_e8m0, const void *out_bf16, int64_t M, int64_t N, int64_t K);
 
 /* Decode-band threshold: M <= this takes the decode tiling (64). */
 W4A8_API int w4a8_decode_max_m(void);

@@ -25,9 +25,10 @@ EXPORTS = ("w4a8_act_quant", "w4a8_mxfp4_linear", "w4a8_workspace_bytes",
            "w4a8_int4g128_linear", "w4a8_int4g128_asym_linear", "w4a8_int4g128_workspace_bytes",
            "w4a8_int5g128_linear", "w4a8_int5g128_workspace_bytes", "w4a4_act_quant", "w4a4_mxfp4_linear",
            "w4a8_status_string", "w4a8_set_gemm_policy", "w4a8_check_device_status",
-           "w4a8_decode_max_m", "w4a8_debug_status_words", "w4a8_debug_set_trace",
+           "w4a8_decode_max_m", "w4a8_debug_status_words",
            "w4a8_mxfp4_linear_noalloc", "w4a8_noalloc_scratch_bytes",
-           "w4a8_mxfp4_linear_bf16", "w4a8_mxfp4_linear_bf16_workspace_bytes")
+           "w4a8_mxfp4_linear_bf16", "w4a8_mxfp4_linear_bf16_workspace_bytes",
+           "w4a8_mxfp4_path", "w4a8_int4g128_path", "w4a8_int5g128_path", "w4a4_mxfp4_path")
 
 
 class W4A8Error(RuntimeError):
@@ -71,11 +72,14 @@ def load(build_if_missing: bool = True):
         "w4a8_check_device_status": (I, [P]),
         "w4a8_decode_max_m": (I, []),
         "w4a8_debug_status_words": (I, [P]),
-        "w4a8_debug_set_trace": (None, [P]),
         "w4a8_mxfp4_linear_noalloc": (I, [P, P, P, P, P, I64, I64, I64, P]),
         "w4a8_noalloc_scratch_bytes": (SZ, []),
         "w4a8_mxfp4_linear_bf16": (I, [P, P, P, P, I64, I64, I64, P, SZ, P]),
         "w4a8_mxfp4_linear_bf16_workspace_bytes": (SZ, [I64, I64, I64]),
+        "w4a8_mxfp4_path": (I, [P, P, P, P, I64, I64, I64]),
+        "w4a8_int4g128_path": (I, [P, P, P, P, I64, I64, I64]),
+        "w4a8_int5g128_path": (I, [P, P, P, P, P, I64, I64, I64]),
+        "w4a4_mxfp4_path": (I, [P, P, P, P, P, I64, I64, I64]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -117,6 +121,29 @@ def set_gemm_policy(policy: int) -> None:
 
 def decode_max_m() -> int:
     return load().w4a8_decode_max_m()
+
+
+PATHS = {0: "invalid", 1: "tensor-core", 2: "cuda-core"}
+
+
+def mxfp4_path(xq, w_packed, w_e8m0, out) -> str:
+    """Which kernel w4a8_mxfp4_linear would run for these tensors ("tensor-core" or "cuda-core")."""
+    M, K = xq.shape
+    N = w_packed.shape[0]
+    return PATHS[load().w4a8_mxfp4_path(_ptr(xq), _ptr(w_packed), _ptr(w_e8m0), _ptr(out), M, N, K)]
+
+
+def int4g128_path(xq, qweight, scales_fp16, out) -> str:
+    M, K = xq.shape
+    N = qweight.shape[1]
+    return PATHS[load().w4a8_int4g128_path(_ptr(xq), _ptr(qweight), _ptr(scales_fp16), _ptr(out), M, N, K)]
+
+
+def int5g128_path(xq, qweight, qhigh, scales_fp16, out) -> str:
+    M, K = xq.shape
+    N = qweight.shape[1]
+    return PATHS[load().w4a8_int5g128_path(_ptr(xq), _ptr(qweight), _ptr(qhigh), _ptr(scales_fp16), _ptr(out),
+                                           M, N, K)]
 
 
 def check_device_status(stream=None) -> None:

@@ -5,6 +5,9 @@
 // tiling, chosen inside the native call so no shape branch is visible to the caller;
 // "radiance_autoround.py", autoround_linear: the prefill/decode choice is made natively).
 #include <atomic>
+#include <mutex>
+
+#include <cuda.h>
 
 #include "common.cuh"
 #include "dispatch.h"
@@ -14,24 +17,72 @@ static std::atomic<int> g_policy{0};
 // Device status word written by bounded waits that give up (0 = clean).
 __device__ unsigned int g_w4a8_device_status[4] = {0, 0, 0, 0};
 
+struct W4a8SymbolCache {
+    std::mutex mu;
+    void *ctx[64] = {nullptr};
+    void *addr[64] = {nullptr};
+};
+
+W4a8SymbolCache *w4a8_symbol_cache_new() { return new W4a8SymbolCache(); }
+
+// cuCtxGetCurrent through the runtime's driver entry point (the library links no libcuda).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+static CtxGetCurrentFn ctx_get_current()
+{
+    static std::atomic<CtxGetCurrentFn> fn{nullptr};
+    CtxGetCurrentFn f = fn.load(std::memory_order_acquire);
+    if (!f) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess) {
+            f = reinterpret_cast<CtxGetCurrentFn>(p);
+            fn.store(f, std::memory_order_release);
+        }
+    }
+    return f;
+}
+
+void *w4a8_symbol_address(const void *symbol, W4a8SymbolCache *cache)
+{
+    int dev = 0;
+    if (!cache || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    CtxGetCurrentFn get = ctx_get_current();
+    CUcontext ctx = nullptr;
+    if (!get || get(&ctx) != CUDA_SUCCESS) return nullptr;
+    if (!ctx) {
+        // no context on this thread yet: the runtime call makes the device's primary context
+        // current (the address it returns is then the one launches from this thread use)
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess || get(&ctx) != CUDA_SUCCESS || !ctx) return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(cache->mu);
+    if (cache->ctx[dev] != (void *)ctx || !cache->addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess) return nullptr;
+        cache->addr[dev] = p;
+        cache->ctx[dev] = (void *)ctx;
+    }
+    return cache->addr[dev];
+}
+
 unsigned int *w4a8_device_status_ptr()
 {
-    static unsigned int *ptr[64] = {nullptr};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_w4a8_device_status) != cudaSuccess) return nullptr;
-        ptr[dev] = static_cast<unsigned int *>(p);
-    }
-    return ptr[dev];
+    static W4a8SymbolCache *cache = w4a8_symbol_cache_new();
+    return static_cast<unsigned int *>(w4a8_symbol_address((const void *)&g_w4a8_device_status, cache));
 }
 
 int w4a8_gemm_policy() { return g_policy.load(std::memory_order_relaxed); }
 
+#ifdef W4A8_TRACE
+// Development aid: a device buffer for the tensor-core kernels' pipeline timestamps (see the
+// trace helpers in gemm_tc.cu); only builds with W4A8_TRACE defined have the setter.
 static std::atomic<void *> g_trace{nullptr};
 void *w4a8_debug_trace_ptr() { return g_trace.load(std::memory_order_relaxed); }
-extern "C" void w4a8_debug_set_trace(void *device_buffer) { g_trace.store(device_buffer, std::memory_order_relaxed); }
+extern "C" W4A8_API void w4a8_debug_set_trace(void *device_buffer) { g_trace.store(device_buffer, std::memory_order_relaxed); }
+#else
+void *w4a8_debug_trace_ptr() { return nullptr; }
+#endif
 
 extern "C" void w4a8_set_gemm_policy(int policy) { g_policy.store(policy, std::memory_order_relaxed); }
 
@@ -74,16 +125,18 @@ extern "C" int w4a8_debug_status_words(unsigned int *out4)
     return W4A8_OK;
 }
 
+// Workspace sizes are the largest any kernel choice needs for the shape (the CUDA-core kernels
+// need none), so a size queried under one kernel-selection policy stays valid under another.
 extern "C" size_t w4a8_workspace_bytes(int64_t M, int64_t N, int64_t K)
 {
     if (M <= 0 || N <= 0 || K <= 0) return 0;
-    return w4a8_tc_workspace_bytes(M, N, K, w4a8_gemm_policy());
+    return w4a8_tc_workspace_bytes(M, N, K);
 }
 
 extern "C" size_t w4a8_int4g128_workspace_bytes(int64_t M, int64_t N, int64_t K)
 {
     if (M <= 0 || N <= 0 || K <= 0) return 0;
-    return w4a8_tc_int4_workspace_bytes(M, N, K, w4a8_gemm_policy());
+    return w4a8_tc_int4_workspace_bytes(M, N, K);
 }
 
 extern "C" w4a8_status w4a8_mxfp4_linear(const uint8_t *xq, const float *x_scale,
@@ -101,7 +154,7 @@ extern "C" w4a8_status w4a8_mxfp4_linear(const uint8_t *xq, const float *x_scale
         return W4A8_ERR_MISALIGNED;
     const int policy = w4a8_gemm_policy();
     if (policy != 1 && w4a8_tc_mxfp4_supported(xq, w_packed, w_e8m0, out_bf16, M, N, K)) {
-        const size_t need = w4a8_tc_workspace_bytes(M, N, K, policy);
+        const size_t need = w4a8_tc_workspace_bytes(M, N, K);
         if (need && (!workspace || workspace_bytes < need)) return W4A8_ERR_WORKSPACE;
         if (need && !w4a8_aligned(workspace, 16)) return W4A8_ERR_MISALIGNED;
         return w4a8_launch_mxfp4_tc(xq, x_scale, w_packed, w_e8m0, out_bf16, M, N, K, workspace,
@@ -143,7 +196,7 @@ extern "C" w4a8_status w4a8_mxfp4_linear_bf16(const uint16_t *x_bf16, const uint
     if (st != W4A8_OK) return st;
     const int policy = w4a8_gemm_policy();
     if (policy != 1 && w4a8_tc_mxfp4_supported(xq, w_packed, w_e8m0, out_bf16, M, N, K)) {
-        const size_t g_need = w4a8_tc_workspace_bytes(M, N, K, policy);
+        const size_t g_need = w4a8_tc_workspace_bytes(M, N, K);
         if (g_need > gws_bytes) return W4A8_ERR_WORKSPACE;
         // the GEMM directly follows the activation quant: it may fetch weights before waiting
         return w4a8_launch_mxfp4_tc(xq, xs, w_packed, w_e8m0, out_bf16, M, N, K, gws, policy, true, stream);
@@ -165,7 +218,7 @@ static w4a8_status int4g128_linear_impl(const uint8_t *xq, const float *x_scale,
         return W4A8_ERR_MISALIGNED;
     const int policy = w4a8_gemm_policy();
     if (policy != 1 && w4a8_tc_int4_supported(xq, qweight, scales_fp16, out_bf16, M, N, K)) {
-        const size_t need = w4a8_tc_int4_workspace_bytes(M, N, K, policy);
+        const size_t need = w4a8_tc_int4_workspace_bytes(M, N, K);
         if (need && (!workspace || workspace_bytes < need)) return W4A8_ERR_WORKSPACE;
         if (need && !w4a8_aligned(workspace, 16)) return W4A8_ERR_MISALIGNED;
         return w4a8_launch_int4_tc(xq, x_scale, qweight, scales_fp16, out_bf16, M, N, K, workspace, policy,
@@ -216,7 +269,7 @@ extern "C" w4a8_status w4a8_int5g128_linear(const uint8_t *xq, const float *x_sc
         return W4A8_ERR_MISALIGNED;
     const int policy = w4a8_gemm_policy();
     if (policy != 1 && w4a8_tc_int5_supported(xq, qweight, qhigh, scales_fp16, out_bf16, M, N, K)) {
-        const size_t need = w4a8_tc_int4_workspace_bytes(M, N, K, policy);
+        const size_t need = w4a8_tc_int4_workspace_bytes(M, N, K);
         if (need && (!workspace || workspace_bytes < need)) return W4A8_ERR_WORKSPACE;
         if (need && !w4a8_aligned(workspace, 16)) return W4A8_ERR_MISALIGNED;
         return w4a8_launch_int5_tc(xq, x_scale, qweight, qhigh, scales_fp16, zeros, out_bf16, M, N, K, workspace,
@@ -238,11 +291,56 @@ extern "C" w4a8_status w4a4_mxfp4_linear(const uint8_t *xa_packed, const uint8_t
         return W4A8_ERR_MISALIGNED;
     const int policy = w4a8_gemm_policy();
     if (policy != 1 && w4a8_tc_mxfp4_a4_supported(xa_packed, xa_e8m0, w_packed, w_e8m0, out_bf16, M, N, K)) {
-        const size_t need = w4a8_tc_workspace_bytes(M, N, K, policy);
+        const size_t need = w4a8_tc_workspace_bytes(M, N, K);
         if (need && (!workspace || workspace_bytes < need)) return W4A8_ERR_WORKSPACE;
         if (need && !w4a8_aligned(workspace, 16)) return W4A8_ERR_MISALIGNED;
         return w4a8_launch_mxfp4_a4_tc(xa_packed, xa_e8m0, w_packed, w_e8m0, out_bf16, M, N, K, workspace, policy,
                                        stream);
     }
     return w4a8_launch_mxfp4_a4_simt(xa_packed, xa_e8m0, w_packed, w_e8m0, out_bf16, M, N, K, stream);
+}
+
+// ------------------------------------------------------------------ kernel-path queries
+// Each mirrors its entry point's validation and dispatch without launching anything.
+
+static int path_of(bool valid, bool tensor_core)
+{
+    if (!valid) return 0;
+    return (w4a8_gemm_policy() != 1 && tensor_core) ? W4A8_PATH_TENSOR_CORE : W4A8_PATH_CUDA_CORE;
+}
+
+extern "C" int w4a8_mxfp4_path(const void *xq, const void *w_packed, const void *w_e8m0, const void *out_bf16,
+                               int64_t M, int64_t N, int64_t K)
+{
+    const bool valid = M > 0 && N > 0 && K > 0 && K % 32 == 0 && xq && w_packed && w_e8m0 && out_bf16 &&
+                       w4a8_aligned(xq, 16) && w4a8_aligned(w_packed, 16) && w4a8_aligned(out_bf16, 2);
+    return path_of(valid, valid && w4a8_tc_mxfp4_supported(xq, w_packed, w_e8m0, out_bf16, M, N, K));
+}
+
+extern "C" int w4a8_int4g128_path(const void *xq, const void *qweight, const void *scales_fp16,
+                                  const void *out_bf16, int64_t M, int64_t N, int64_t K)
+{
+    const bool valid = M > 0 && N > 0 && K > 0 && K % 128 == 0 && xq && qweight && scales_fp16 && out_bf16 &&
+                       w4a8_aligned(xq, 16) && w4a8_aligned(qweight, 4) && w4a8_aligned(scales_fp16, 2) &&
+                       w4a8_aligned(out_bf16, 2);
+    return path_of(valid, valid && w4a8_tc_int4_supported(xq, qweight, scales_fp16, out_bf16, M, N, K));
+}
+
+extern "C" int w4a8_int5g128_path(const void *xq, const void *qweight, const void *qhigh, const void *scales_fp16,
+                                  const void *out_bf16, int64_t M, int64_t N, int64_t K)
+{
+    const bool valid = M > 0 && N > 0 && K > 0 && K % 128 == 0 && xq && qweight && qhigh && scales_fp16 &&
+                       out_bf16 && w4a8_aligned(xq, 16) && w4a8_aligned(qweight, 4) &&
+                       w4a8_aligned(scales_fp16, 2) && w4a8_aligned(out_bf16, 2);
+    return path_of(valid, valid && w4a8_tc_int5_supported(xq, qweight, qhigh, scales_fp16, out_bf16, M, N, K));
+}
+
+extern "C" int w4a4_mxfp4_path(const void *xa_packed, const void *xa_e8m0, const void *w_packed,
+                               const void *w_e8m0, const void *out_bf16, int64_t M, int64_t N, int64_t K)
+{
+    const bool valid = M > 0 && N > 0 && K > 0 && K % 32 == 0 && xa_packed && xa_e8m0 && w_packed && w_e8m0 &&
+                       out_bf16 && w4a8_aligned(xa_packed, 16) && w4a8_aligned(w_packed, 16) &&
+                       w4a8_aligned(out_bf16, 2);
+    return path_of(valid,
+                   valid && w4a8_tc_mxfp4_a4_supported(xa_packed, xa_e8m0, w_packed, w_e8m0, out_bf16, M, N, K));
 }

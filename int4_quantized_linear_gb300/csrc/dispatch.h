@@ -13,6 +13,15 @@ int w4a8_gemm_policy();
 void *w4a8_debug_trace_ptr();
 unsigned int *w4a8_device_status_ptr();
 
+// Device address of one of the library's __device__ variables on the current device.  The
+// address is looked up with cudaGetSymbolAddress (with the device current) and cached per
+// device together with the context it came from; a call from another context (after a device
+// reset or a primary-context teardown, which load the module again, possibly elsewhere) looks
+// it up again.  Thread-safe.  Returns null if the lookup fails.
+struct W4a8SymbolCache;
+W4a8SymbolCache *w4a8_symbol_cache_new();
+void *w4a8_symbol_address(const void *symbol, W4a8SymbolCache *cache);
+
 w4a8_status w4a8_launch_mxfp4_simt(const uint8_t *xq, const float *x_scale, const uint8_t *wp,
                                    const uint8_t *we, uint16_t *out, int64_t M, int64_t N,
                                    int64_t K, cudaStream_t stream);
@@ -25,7 +34,7 @@ w4a8_status w4a8_launch_int4_simt(const uint8_t *xq, const float *x_scale, const
 // Tensor-core (tcgen05) paths.
 bool w4a8_tc_mxfp4_supported(const void *xq, const void *wp, const void *we, const void *out,
                              int64_t M, int64_t N, int64_t K);
-size_t w4a8_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int policy);
+size_t w4a8_tc_workspace_bytes(int64_t M, int64_t N, int64_t K);
 size_t w4a8_tc_workspace_counters_offset(int64_t M, int64_t N, int64_t K);
 // w_early: the kernel just before this one on the stream is the library's activation quant
 // (chained by programmatic dependent launch), so weights may be read before waiting on it.
@@ -40,7 +49,7 @@ w4a8_status w4a8_launch_act_quant(const uint16_t *x_bf16, uint8_t *xq, float *x_
 
 bool w4a8_tc_int4_supported(const void *xq, const void *qw, const void *s16, const void *out,
                             int64_t M, int64_t N, int64_t K);
-size_t w4a8_tc_int4_workspace_bytes(int64_t M, int64_t N, int64_t K, int policy);
+size_t w4a8_tc_int4_workspace_bytes(int64_t M, int64_t N, int64_t K);
 w4a8_status w4a8_launch_int4_tc(const uint8_t *xq, const float *x_scale, const int32_t *qw,
                                 const uint16_t *s16, uint16_t *out, int64_t M, int64_t N,
                                 int64_t K, void *workspace, int policy, cudaStream_t stream,

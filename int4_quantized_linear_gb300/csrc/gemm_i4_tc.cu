@@ -45,6 +45,7 @@
 //
 // Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 5 gate, 2-4, 6-8, 10, 11 converters,
 // 12-15 promotion and epilogue (9 idle).
+#include <atomic>
 #include <cstring>
 
 #include "common.cuh"
@@ -105,12 +106,15 @@ struct Params {
     unsigned long long *trace;  // optional pipeline timeline of CTA 0 (diagnostics), or null
 };
 
-// Pipeline timeline (diagnostics): CTA 0 records clock64() per k-tile i < 256 for each event:
+// Pipeline timeline (a development aid, compiled in only when W4A8_TRACE is defined): CTA 0
+// records clock64() per k-tile i < 256 for each event:
 // 0 fill issued (index = fill), 1 converter start, 2 converter done, 3 MMA released,
 // 4 promotion start, 5 promotion done, 6 MMA warp met the gate, 7-14 each converter warp done.
 __device__ __forceinline__ void trace_ev(const Params &p, int ev, int i)
 {
+#ifdef W4A8_TRACE
     if (p.trace != nullptr && blockIdx.x == 0 && i < 256) p.trace[ev * 256 + i] = (unsigned long long)clock64();
+#endif
 }
 
 // Shared memory: the zero-point operand atom (1 KB), NA converted operand tiles, then a ring of
@@ -613,7 +617,7 @@ static w4a8_status launch(const int32_t *qw, const uint8_t *xq, Params prm, cuda
         !tch::tmap_3d_ktiles(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, prm.M, prm.K, 128, prm.K / 128, BN, KPU))
         return W4A8_ERR_CUDA;
     auto kern = int4_tc_kernel<BN, US, NA, NB, ASYM, I5>;
-    static int attr_done[64] = {0};
+    static std::atomic<int> attr_done[64];
     if (!tch::set_smem_once(kern, L::TOTAL, attr_done)) return W4A8_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(prm.G);
@@ -648,9 +652,9 @@ bool w4a8_tc_int4_supported(const void *xq, const void *qw, const void *s16, con
     return w4a8::tch::encode_fn() != nullptr;
 }
 
-size_t w4a8_tc_int4_workspace_bytes(int64_t M, int64_t N, int64_t K, int policy)
+size_t w4a8_tc_int4_workspace_bytes(int64_t M, int64_t N, int64_t K)
 {
-    if (policy == 1 || K % 512 != 0 || K <= 0 || M <= 0 || N <= 0) return 0;
+    if (K % 512 != 0 || K <= 0 || M <= 0 || N <= 0) return 0;
     const Cfg c = w4a8::tci::choose(M, N, K);
     return partial_bytes(c) + (size_t)c.m_tiles * c.n_tiles * 4;
 }

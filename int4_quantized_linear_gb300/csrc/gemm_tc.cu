@@ -52,6 +52,7 @@
 //
 // Every mbarrier wait is bounded; a wait that runs out sets a bit in the library's device status
 // word and the CTA winds down (draining what it started) instead of hanging.
+#include <atomic>
 #include <cstring>
 
 #include "common.cuh"
@@ -94,12 +95,15 @@ struct Params {
     unsigned long long *trace;  // optional pipeline timeline of CTA 0 (diagnostics), or null
 };
 
-// Pipeline timeline (diagnostics): CTA 0 records clock64() per k-tile i < TRACE_N for each event.
+// Pipeline timeline (a development aid, compiled in only when W4A8_TRACE is defined): CTA 0
+// records clock64() per k-tile i < TRACE_N for each event.
 constexpr int TRACE_N = 256;
 enum { TR_TMA_ISSUED = 0, TR_SCALE_DATA, TR_SCALE_DONE, TR_MMA_READY, TR_TMA_FILL, TR_GATE_SFF, TR_EVENTS };
 __device__ __forceinline__ void trace_ev(const Params &p, int ev, int i)
 {
+#ifdef W4A8_TRACE
     if (p.trace != nullptr && blockIdx.x == 0 && i < TRACE_N) p.trace[ev * TRACE_N + i] = (unsigned long long)clock64();
+#endif
 }
 // Phase stamps (global timer, ns) of every CTA (up to 512), at [TR_EVENTS * TRACE_N + 16 * cta + k]:
 // k = 0 entry, 1 set-up done, 2 epilogue done, 3 exit; for the CTA's last tile the epilogue's
@@ -109,11 +113,13 @@ __device__ __forceinline__ void trace_ev(const Params &p, int ev, int i)
 constexpr int TRACE_PHASES = 16;
 __device__ __forceinline__ void trace_phase(const Params &p, int k)
 {
+#ifdef W4A8_TRACE
     if (p.trace != nullptr && blockIdx.x < 512) {
         unsigned long long ns;
         asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(ns));
         p.trace[TR_EVENTS * TRACE_N + TRACE_PHASES * blockIdx.x + k] = ns;
     }
+#endif
 }
 
 // Shared memory: a ring of US slots, each holding KPU k-tiles of padded weights (16 KB each)
@@ -734,7 +740,7 @@ w4a8_status launch(const uint8_t *wp, const uint8_t *xq, Params prm, cudaStream_
                       CU_TENSOR_MAP_SWIZZLE_NONE))
         return W4A8_ERR_CUDA;
     auto kern = mxfp4_tc_kernel<BN, KPU, US, ACC_BUFS, SFQ, SFR, A4>;
-    static int attr_done[64] = {0};
+    static std::atomic<int> attr_done[64];
     if (!tch::set_smem_once(kern, L::TOTAL, attr_done)) return W4A8_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(prm.G);
@@ -775,9 +781,9 @@ size_t w4a8_tc_workspace_counters_offset(int64_t M, int64_t N, int64_t K)
     return partial_bytes(choose(M, N, K));
 }
 
-size_t w4a8_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, int policy)
+size_t w4a8_tc_workspace_bytes(int64_t M, int64_t N, int64_t K)
 {
-    if (policy == 1 || K % 512 != 0 || K <= 0 || M <= 0 || N <= 0) return 0;
+    if (K % 512 != 0 || K <= 0 || M <= 0 || N <= 0) return 0;
     return workspace_for(choose(M, N, K));
 }
 

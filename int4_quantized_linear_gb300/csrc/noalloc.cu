@@ -1,12 +1,13 @@
 // noalloc.cu -- an MXFP4 linear entry point for callers that cannot allocate device memory.
 //
-// Some callers have no way to hand this library a workspace: code that is being captured into
-// a CUDA graph (cudaMalloc is not a stream operation and must not run during capture), serving
-// engines that reserve all device memory in their own pool up front and forbid allocations
-// outside it, and plugin interfaces that pass only input and output pointers.  This entry point
-// runs the tensor-core MXFP4 GEMM with its stream-K scratch (fp32 partial tiles and arrival
-// counters) in a fixed-size array that lives in the library's device image instead of a
-// caller-provided workspace.  Every GPU that loads the library holds the array until exit.
+// The regular entry point takes a caller-provided workspace for its split-K scratch.  Some
+// callers have no way to provide one: serving engines that reserve all device memory for their
+// own pool up front and treat any allocation outside it as an error (it could fail, or push the
+// process past its memory budget), and plugin or custom-operator interfaces that hand a kernel
+// only its input and output pointers.  This entry point runs the same tensor-core MXFP4 GEMM
+// with its stream-K scratch (fp32 partial tiles and arrival counters) in a fixed-size array in
+// the library's device image.  Every GPU that loads the library holds that array until the
+// process exits.
 #include "common.cuh"
 #include "dispatch.h"
 
@@ -16,20 +17,15 @@
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[W4A8_NOALLOC_SCRATCH_BYTES];
 
-// Device address of the scratch array for the current device.  The array's name is only a
-// host-side handle; the address must come from cudaGetSymbolAddress, once per device, with that
-// device current.
+// Device address of the scratch array on the current device.  In host code the array's name is
+// only a host-side stand-in, never a device address: a kernel given it would fault or, where the
+// GPU can reach host memory, silently use the wrong memory.  The address comes from
+// cudaGetSymbolAddress with the device current, looked up on the first call on each device
+// (and again if the device's context changed since, e.g. after a device reset).
 static void *noalloc_scratch_ptr()
 {
-    static void *ptr[64] = {nullptr};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-        ptr[dev] = p;
-    }
-    return ptr[dev];
+    static W4a8SymbolCache *cache = w4a8_symbol_cache_new();
+    return w4a8_symbol_address((const void *)&g_noalloc_scratch, cache);
 }
 
 extern "C" size_t w4a8_noalloc_scratch_bytes(void) { return W4A8_NOALLOC_SCRATCH_BYTES; }
@@ -49,7 +45,7 @@ extern "C" w4a8_status w4a8_mxfp4_linear_noalloc(const uint8_t *xq, const float 
     const int policy = w4a8_gemm_policy();
     if (policy == 1 || !w4a8_tc_mxfp4_supported(xq, w_packed, w_e8m0, out_bf16, M, N, K))
         return w4a8_launch_mxfp4_simt(xq, x_scale, w_packed, w_e8m0, out_bf16, M, N, K, stream);
-    const size_t need = w4a8_tc_workspace_bytes(M, N, K, policy);
+    const size_t need = w4a8_tc_workspace_bytes(M, N, K);
     if (need > W4A8_NOALLOC_SCRATCH_BYTES) return W4A8_ERR_WORKSPACE;
     void *scratch = noalloc_scratch_ptr();
     if (!scratch) return W4A8_ERR_CUDA;

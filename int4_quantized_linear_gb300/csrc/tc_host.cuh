@@ -6,21 +6,28 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace w4a8 {
 namespace tch {
 
+// The per-process and per-device caches below are filled on first use; threads that race on a
+// first use compute and store the same value, and the atomics make that race well defined.
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};
+    PFN_cuTensorMapEncodeTiled_v12000 f = fn.load(std::memory_order_acquire);
+    if (!f) {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+            q == cudaDriverEntryPointSuccess) {
+            f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+            fn.store(f, std::memory_order_release);
+        }
     }
-    return fn;
+    return f;
 }
 
 // 2-D tensor map over a row-major [rows, cols] array of 1-byte (or 4-bit) elements.
@@ -58,27 +65,28 @@ inline bool tmap_3d_ktiles(CUtensorMap *m, CUtensorMapDataType type, const void 
 
 inline int num_sms()
 {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (!cache[dev]) {
-        int v = 0;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (!v) {
         cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        cache[dev] = v > 0 ? v : 148;
+        v = v > 0 ? v : 148;
+        cache[dev].store(v, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return v;
 }
 
-// Set the dynamic shared-memory limit of a kernel once per device.
+// Set the dynamic shared-memory limit of a kernel once per device (setting it twice is harmless).
 template <typename K>
-inline bool set_smem_once(K kern, int bytes, int (&done)[64])
+inline bool set_smem_once(K kern, int bytes, std::atomic<int> (&done)[64])
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-    if (!done[dev]) {
+    if (!done[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
             return false;
-        done[dev] = 1;
+        done[dev].store(1, std::memory_order_release);
     }
     return true;
 }

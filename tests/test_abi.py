@@ -95,3 +95,31 @@ def test_symmetric_zero_point_check():
     for bad in ((8, 128, True), (4, 64, True), (4, 128, False)):
         with pytest.raises(ValueError):
             binding.check_autoround_config(*bad)
+
+
+def test_path_queries_without_gpu(clib):
+    fake = ctypes.c_void_p(0x1000)
+    odd = ctypes.c_void_p(0x1001)
+    # invalid arguments: the entry point would reject them
+    assert clib.w4a8_mxfp4_path(fake, fake, fake, fake, 2, 8, 48) == 0     # K % 32
+    assert clib.w4a8_mxfp4_path(odd, fake, fake, fake, 2, 8, 64) == 0      # misaligned xq
+    assert clib.w4a8_mxfp4_path(NULL, fake, fake, fake, 2, 8, 64) == 0
+    assert clib.w4a8_int4g128_path(fake, fake, fake, fake, 2, 8, 64) == 0  # K % 128
+    assert clib.w4a8_int5g128_path(fake, fake, NULL, fake, fake, 2, 8, 128) == 0
+    assert clib.w4a4_mxfp4_path(fake, fake, fake, fake, fake, 0, 8, 512) == 0
+    # valid, but K % 512 != 0: only the CUDA-core kernels take it
+    assert clib.w4a8_mxfp4_path(fake, fake, fake, fake, 2, 8, 96) == 2
+    assert clib.w4a8_int4g128_path(fake, fake, fake, fake, 2, 8, 384) == 2
+    assert clib.w4a8_int5g128_path(fake, fake, fake, fake, fake, 2, 16, 384) == 2
+    assert clib.w4a4_mxfp4_path(fake, fake, fake, fake, fake, 2, 8, 96) == 2
+
+
+def test_workspace_sizes_do_not_depend_on_policy(clib):
+    shapes = [(1, 34816, 5120), (64, 5120, 17408), (4096, 10240, 5120)]
+    sizes = {}
+    for policy in (0, 1, 2):
+        clib.w4a8_set_gemm_policy(policy)
+        sizes[policy] = [(clib.w4a8_workspace_bytes(*s), clib.w4a8_int4g128_workspace_bytes(*s)) for s in shapes]
+    clib.w4a8_set_gemm_policy(0)
+    assert sizes[0] == sizes[1] == sizes[2]
+    assert all(a > 0 and b > 0 for a, b in sizes[0])

@@ -1,10 +1,12 @@
 """The allocation-free MXFP4 entry point (w4a8_mxfp4_linear_noalloc), called through the C ABI.
 
-It exists for callers that cannot allocate device memory -- code captured into a CUDA graph,
-engines that own all device memory in their own pool, plugin interfaces that pass only inputs
-and outputs -- and keeps its scratch in a fixed array inside the library.  This file is named to
-be collected last, so a run that stops at the first failure has already run every other test;
-it also passes on its own in a fresh process.
+Some callers of this library cannot hand it a workspace: serving engines that reserve all device
+memory for their own pool and treat any other allocation as an error, and plugin interfaces that
+pass a kernel only its inputs and outputs.  For them the no-alloc entry point keeps the split-K
+scratch in a fixed array inside the library.  These tests check that two calls in a row through it
+give the regular entry point's result and the oracle's (on sampled outputs), and that sizes beyond
+the array are refused.  The file is named so pytest collects it last: a run that stops at the first
+failure has then run every other test.  It also passes on its own in a fresh process.
 """
 import ctypes
 
@@ -19,7 +21,7 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("M,N,K", [(8, 5120, 17408), (64, 4096, 5120), (1, 34816, 5120)])
-def test_noalloc_matches_workspace_entry_point(lib, M, N, K):
+def test_noalloc_matches_workspace_entry_point(lib, orc, M, N, K):
     clib = lib.load()
     assert clib.w4a8_noalloc_scratch_bytes() == 12 << 20
     # these shapes use the tensor-core path with stream-K scratch
@@ -37,6 +39,12 @@ def test_noalloc_matches_workspace_entry_point(lib, M, N, K):
         assert st == 0, lib.STATUS.get(st, st)
         lib.check_device_status()
         gemm_check(bf16_to_f64(out), bf16_to_f64(ref), f"noalloc M={M} N={N} K={K}")
+        # and against the oracle, fed the same fp8 codes, on outputs sampled across every tile
+        rng = np.random.default_rng(M)
+        im = rng.integers(0, M, 512)
+        inn = rng.integers(0, N, 512)
+        o_ref = orc.mxfp4_linear_pairs(xq.cpu().numpy(), xs.cpu().numpy(), w, e, im, inn)
+        gemm_check(bf16_to_f64(out)[im, inn], o_ref, f"noalloc vs oracle M={M} N={N} K={K}")
 
 
 def test_noalloc_rejects_oversized(lib):

@@ -51,9 +51,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
     nvcc = _nvcc()
 
+    # W4A8_EXTRA_NVCC_FLAGS: extra compiler options for this build (e.g. -DW4A8_TRACE to compile in
+    # the pipeline timestamps, or a tuning constant such as -DW4A8_L2_PREFETCH_FILLS=4)
+    extra = os.environ.get("W4A8_EXTRA_NVCC_FLAGS", "").split()
+
     def compile_one(src):
         obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc] + ARCH + NVCC_FLAGS + ["-c", src, "-o", obj]
+        cmd = [nvcc] + ARCH + NVCC_FLAGS + extra + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, obj, r
 

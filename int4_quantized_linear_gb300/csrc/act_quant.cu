@@ -80,17 +80,7 @@ act_quant_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ xq,
     if (threadIdx.x == 0 && blockIdx.y == 0) x_scale[m] = s;
 
     uint2 *out = reinterpret_cast<uint2 *>(xq + m * K);
-    auto quant8 = [&](const uint4 &w) {
-        const uint32_t h[4] = {w.x, w.y, w.z, w.w};
-        uint32_t q[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float lo = __fdiv_rn(bf16_bits_to_float(h[j] & 0xffffu), s);
-            const float hi = __fdiv_rn(bf16_bits_to_float(h[j] >> 16), s);
-            q[j] = float2_to_e4m3x2(lo, hi);
-        }
-        return make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
-    };
+    auto quant8 = [&](const uint4 &w) { return quant8_e4m3(w, s); };
     if (cached) {
 #pragma unroll
         for (int i = 0; i < AQ_CACHE; ++i) {

@@ -192,9 +192,15 @@ extern "C" w4a8_status w4a8_mxfp4_linear_bf16(const uint16_t *x_bf16, const uint
     uint8_t *gws = reinterpret_cast<uint8_t *>(xs) + round256((size_t)M * 4);
     const size_t gws_bytes = workspace_bytes - (size_t)(gws - xq);
 
+    const int policy = w4a8_gemm_policy();
+    // a few tokens: one kernel, the activation quant fused into the GEMM's prologue
+    if (policy != 1 && w4a8_tc_mxfp4_aq_takes(M, K) &&
+        w4a8_tc_mxfp4_supported(x_bf16, w_packed, w_e8m0, out_bf16, M, N, K)) {
+        if (w4a8_tc_workspace_bytes(M, N, K) > gws_bytes) return W4A8_ERR_WORKSPACE;
+        return w4a8_launch_mxfp4_tc_aq(x_bf16, w_packed, w_e8m0, out_bf16, M, N, K, gws, stream);
+    }
     w4a8_status st = w4a8_launch_act_quant(x_bf16, xq, xs, M, K, stream);
     if (st != W4A8_OK) return st;
-    const int policy = w4a8_gemm_policy();
     if (policy != 1 && w4a8_tc_mxfp4_supported(xq, w_packed, w_e8m0, out_bf16, M, N, K)) {
         const size_t g_need = w4a8_tc_workspace_bytes(M, N, K);
         if (g_need > gws_bytes) return W4A8_ERR_WORKSPACE;

@@ -30,6 +30,24 @@ W4A8_DEVICE uint16_t float2_to_e4m3x2(float lo, float hi)
     return r;
 }
 
+// Eight bf16 activations (a 16-byte chunk, low element first) -> their eight e4m3 codes for the
+// per-token scale s: each x / s with a correctly rounded fp32 division, then round to nearest
+// even with saturation at 448 ("radiance_autoround.py", autoround_linear: the dynamic per-token
+// fp8 cast).  Shared by the activation-quant kernel and the GEMM's fused quant, so both produce
+// the same bytes.
+W4A8_DEVICE uint2 quant8_e4m3(const uint4 &w, float s)
+{
+    const uint32_t h[4] = {w.x, w.y, w.z, w.w};
+    uint32_t q[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float lo = __fdiv_rn(__uint_as_float(h[j] << 16), s);
+        const float hi = __fdiv_rn(__uint_as_float(h[j] & 0xffff0000u), s);
+        q[j] = float2_to_e4m3x2(lo, hi);
+    }
+    return make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+}
+
 // Two e2m1 codes in one byte (low nibble = first element) -> two fp32 values, exact.
 W4A8_DEVICE float2 e2m1x2_to_float2(uint32_t byte)
 {

@@ -42,6 +42,16 @@ w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const 
                                  const uint8_t *we, uint16_t *out, int64_t M, int64_t N,
                                  int64_t K, void *workspace, int policy, bool w_early,
                                  cudaStream_t stream);
+// The MXFP4 GEMM with the per-token activation quant fused in (the 16-token decode tiling, M up
+// to 8, rows of at most W4A8_FUSED_AQ_MAX_X_BYTES of bf16 in all): every CTA takes the row amax
+// from L2 and quantizes its own fills' activations into shared memory; bit-identical to the
+// activation-quant kernel followed by the GEMM.
+#ifndef W4A8_FUSED_AQ_MAX_X_BYTES
+#define W4A8_FUSED_AQ_MAX_X_BYTES (96u << 10)
+#endif
+bool w4a8_tc_mxfp4_aq_takes(int64_t M, int64_t K);
+w4a8_status w4a8_launch_mxfp4_tc_aq(const uint16_t *x_bf16, const uint8_t *wp, const uint8_t *we, uint16_t *out,
+                                    int64_t M, int64_t N, int64_t K, void *workspace, cudaStream_t stream);
 // Per-token activation quant launched with programmatic dependent launch (waits for the
 // previous kernel before reading x, then lets the next kernel start).
 w4a8_status w4a8_launch_act_quant(const uint16_t *x_bf16, uint8_t *xq, float *x_scale, int64_t M,
@@ -54,6 +64,16 @@ w4a8_status w4a8_launch_int4_tc(const uint8_t *xq, const float *x_scale, const i
                                 const uint16_t *s16, uint16_t *out, int64_t M, int64_t N,
                                 int64_t K, void *workspace, int policy, cudaStream_t stream,
                                 const int32_t *qzeros = nullptr);
+
+// Prefill tiling of the symmetric int4 / int5 GEMM (gemm_i4_pf.cu): 256-token tiles, signed
+// operand codes, no zero-point MMAs.  Taken for M > W4A8_INT4_PF_MIN_M without per-group zero
+// points; w4a8_int4_pf_takes also says no when the build cannot run it.
+#define W4A8_INT4_PF_MIN_M 128
+bool w4a8_int4_pf_takes(int64_t M, bool int5);
+size_t w4a8_int4_pf_workspace_bytes(int64_t M, int64_t N, int64_t K);
+w4a8_status w4a8_launch_int4_pf(const uint8_t *xq, const float *x_scale, const int32_t *qw, const uint8_t *qh,
+                                const uint16_t *s16, uint16_t *out, int64_t M, int64_t N, int64_t K, void *workspace,
+                                cudaStream_t stream);
 
 // int5 g128: qh is the fifth-bit plane [K/8, N], zeros the per-(group, column) zero points
 // [K/128, N] or null (zero point 16).

@@ -12,8 +12,9 @@
 // whose A operand is the constant e4m3 -2^-6 (= -8 * 2^-9) in every element:
 //   sum_k c_k 2^-9 x_k + sum_k (-8 * 2^-9) x_k = 2^-9 * sum_k (c_k - 8) x_k,
 // all inputs exact, accumulated in fp32 tensor memory.  ((c - 8) * 2^-9 is an exact e4m3 value
-// too, but building those signed bytes costs the converter warps about three times the integer
-// work, and they, not the four extra MMAs, then set the pace: 48 -> 58 us at decode.)  With
+// too, and the prefill kernel (gemm_i4_pf.cu) builds it with three byte permutes per four codes;
+// at decode even that makes the converter warps the busiest unit, 48 -> 52 us for gate_up at M=1,
+// so this kernel keeps the nibble bytes and the four extra MMAs.)  With
 // per-column zero points (asymmetric) the constant-operand MMAs write a second accumulator,
 // which the promotion scales by z / 8.  The group scale is not a power of two and cannot ride on
 // the instruction's block scale, so each group's partial is read back and promoted into fp32
@@ -45,6 +46,7 @@
 //
 // Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 5 gate, 2-4, 6-8, 10, 11 converters,
 // 12-15 promotion and epilogue (9 idle).
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 
@@ -53,6 +55,7 @@
 #include "tc_host.cuh"
 #include "tc_ptx.cuh"
 #include "tc_sched.cuh"
+#include "wcodes.cuh"
 
 namespace w4a8 {
 namespace tci {
@@ -150,38 +153,6 @@ struct Layout {
     static_assert(8 * (2 * US + NA + 2 * NB + 1) + 32 <= 512, "barrier area");
     static_assert(NA <= NB, "a converted tile's release rides on the group-accumulator barrier");
 };
-
-// Eight int4 codes of one word (k = 8i..8i+7, low nibble first) -> the eight codes as bytes,
-// low byte first, in two words: each byte read as e4m3 is c * 2^-9.
-__device__ __forceinline__ uint2 i4x8_to_bytes(uint32_t w)
-{
-    const uint32_t ev = w & 0x0F0F0F0Fu;          // codes 0, 2, 4, 6
-    const uint32_t od = (w >> 4) & 0x0F0F0F0Fu;   // codes 1, 3, 5, 7
-    return make_uint2(__byte_perm(ev, od, 0x5140), __byte_perm(ev, od, 0x7362));
-}
-
-constexpr uint32_t E4M3_MINUS_2POW_M6 = 0x88u;  // sign 1, exponent field 1, mantissa 0: -2^-6
-
-// Bits 0, 2, 4 and 6 of b (the others clear) -> 0xFF or 0x00 in bytes 0..3.  The multiply by
-// 1 + 2^6 + 2^12 + 2^18 puts bit 2j at bit 8j; the other copies land on even positions that are
-// not multiples of 8 (where two coincide the carry stops one bit higher, still off 8j), and the
-// mask keeps bits 8j only.
-__device__ __forceinline__ uint32_t spread_even_bits(uint32_t b)
-{
-    return ((b * 0x00041041u) & 0x01010101u) * 0xFFu;
-}
-
-// Eight int5 codes: the nibbles of word w and the fifth bits of plane byte hb (bit j for code j)
-// -> the e4m3 bytes of (c - 16) * 2^-9, low byte first: the nibble where the fifth bit is set,
-// 0x90 - nibble where it is clear (no byte borrows: 0x90 > 15).
-__device__ __forceinline__ uint2 i5x8_to_signed_bytes(uint32_t w, uint32_t hb)
-{
-    const uint32_t ev = w & 0x0F0F0F0Fu, od = (w >> 4) & 0x0F0F0F0Fu;
-    const uint32_t he = spread_even_bits(hb & 0x55u), ho = spread_even_bits((hb >> 1) & 0x55u);
-    const uint32_t e = (ev & he) | ((0x90909090u - ev) & ~he);
-    const uint32_t o = (od & ho) | ((0x90909090u - od) & ~ho);
-    return make_uint2(__byte_perm(e, o, 0x5140), __byte_perm(e, o, 0x7362));
-}
 
 template <int BN, int US, int NA, int NB, bool ASYM, bool I5>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -656,7 +627,9 @@ size_t w4a8_tc_int4_workspace_bytes(int64_t M, int64_t N, int64_t K)
 {
     if (K % 512 != 0 || K <= 0 || M <= 0 || N <= 0) return 0;
     const Cfg c = w4a8::tci::choose(M, N, K);
-    return partial_bytes(c) + (size_t)c.m_tiles * c.n_tiles * 4;
+    const size_t own = partial_bytes(c) + (size_t)c.m_tiles * c.n_tiles * 4;
+    // prefill sizes may take the 256-token kernel instead: enough for either
+    return M > W4A8_INT4_PF_MIN_M ? std::max(own, w4a8_int4_pf_workspace_bytes(M, N, K)) : own;
 }
 
 static bool make_params(Params &prm, const Cfg &c, const float *x_scale, const uint16_t *s16, uint16_t *out,
@@ -690,6 +663,8 @@ w4a8_status w4a8_launch_int4_tc(const uint8_t *xq, const float *x_scale, const i
                                 uint16_t *out, int64_t M, int64_t N, int64_t K, void *workspace, int,
                                 cudaStream_t stream, const int32_t *qzeros)
 {
+    if (qzeros == nullptr && w4a8_int4_pf_takes(M, false))
+        return w4a8_launch_int4_pf(xq, x_scale, qw, nullptr, s16, out, M, N, K, workspace, stream);
     const Cfg c = w4a8::tci::choose(M, N, K);
     Params prm;
     if (!make_params(prm, c, x_scale, s16, out, M, N, K, workspace)) return W4A8_ERR_CUDA;
@@ -719,6 +694,8 @@ w4a8_status w4a8_launch_int5_tc(const uint8_t *xq, const float *x_scale, const i
                                 const uint16_t *s16, const uint8_t *zeros, uint16_t *out, int64_t M, int64_t N,
                                 int64_t K, void *workspace, int, cudaStream_t stream)
 {
+    if (zeros == nullptr && w4a8_int4_pf_takes(M, true))
+        return w4a8_launch_int4_pf(xq, x_scale, qw, qh, s16, out, M, N, K, workspace, stream);
     const Cfg c = w4a8::tci::choose(M, N, K);
     Params prm;
     if (!make_params(prm, c, x_scale, s16, out, M, N, K, workspace)) return W4A8_ERR_CUDA;

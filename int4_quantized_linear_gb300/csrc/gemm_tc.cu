@@ -67,17 +67,29 @@ namespace tcg {
 using namespace tcs;
 
 constexpr int NUM_THREADS = 352;   // 11 warps
+// With the activation quant fused in (AQ): four more warps (11-14) quantize each ring fill's
+// activation tile into shared memory, so the kernel has 15.
+constexpr int AQ_WARP0 = 11;
+constexpr int AQ_WARPS = 4;
+constexpr int AQ_THREADS = 32 * AQ_WARPS;
+constexpr int AQ_BARRIER = 3;      // named barrier of the row-amax step (quantizer + epilogue warps)
+constexpr int AQ_STEP_THREADS = AQ_THREADS + 128;
+template <bool AQ>
+constexpr int num_threads() { return AQ ? NUM_THREADS + AQ_THREADS : NUM_THREADS; }
 constexpr int SCALE_WARP0 = 2;     // warps 2-5
 constexpr int EPI_WARP0 = 6;       // warps 6-9
 constexpr int GATE_WARP = 10;
 constexpr int GATE_BARRIER = 2;    // named barrier shared by the gate warp and the MMA warp
 
-enum : unsigned { ST_TIMEOUT_PRODUCER = 1, ST_TIMEOUT_GATE = 2, ST_TIMEOUT_SCALE = 4, ST_TIMEOUT_EPI = 8 };
+enum : unsigned { ST_TIMEOUT_PRODUCER = 1, ST_TIMEOUT_GATE = 2, ST_TIMEOUT_SCALE = 4, ST_TIMEOUT_EPI = 8,
+                  ST_TIMEOUT_AQ = 16 };
+constexpr int AQ_MAX_M = 8;        // tokens the fused activation quant takes (one 8-item batch per fill)
 
 struct Params {
     const uint8_t *wp;     // [N, K/2] packed e2m1 codes
     const uint8_t *we;     // [N, K/32] e8m0
     const float *xs;       // [M] per-token scale
+    const uint16_t *x;     // AQ: [M, K] bf16 activations, quantized inside the kernel
     uint16_t *out;         // [M, N] bf16
     float *partials;       // [G][2][BN][128] fp32 stream-K partial tiles
     int *counters;         // [tiles] arrival counters, zero between calls
@@ -122,13 +134,65 @@ __device__ __forceinline__ void trace_phase(const Params &p, int k)
 #endif
 }
 
+// Fused activation quant, first step, run by the quantizer and epilogue warps together (256
+// threads, pidx 0..255): each token row's amax over all K, taken on the bf16 bit patterns (for
+// finite values |x| orders like the 15 low bits) as w4a8_act_quant takes it, then the per-token
+// scale amax / 448 (correctly rounded; 1.0 for an all-zero row) into s_out[m].  The rows are read
+// from L2 in batches of sixteen 16-byte chunks per thread, so each thread keeps sixteen loads in
+// flight (a 5120-wide row of up to 8 tokens takes two round trips).
+__device__ __forceinline__ void aq_row_scales(const uint16_t *x, int M, int K, int pidx, float *s_out, unsigned *rmax)
+{
+    if (pidx < M) rmax[pidx] = 0u;
+    tc::named_bar_sync(AQ_BARRIER, AQ_STEP_THREADS);
+    const int nchunk = K / 8;
+    const int total = M * nchunk;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x);
+    int m_cur = pidx / nchunk;
+    uint32_t a2 = 0;  // two 15-bit magnitudes packed, per-halfword max
+    auto flush = [&]() {
+        const uint32_t hb = max(a2 & 0xffffu, a2 >> 16);
+        if (hb) atomicMax(&rmax[m_cur], hb);
+    };
+    for (int base = pidx; base < total; base += 16 * AQ_STEP_THREADS) {
+        uint4 v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int idx = base + j * AQ_STEP_THREADS;
+            v[j] = idx < total ? __ldg(src + idx) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int idx = base + j * AQ_STEP_THREADS;
+            if (idx < total) {
+                const int m = idx / nchunk;
+                if (m != m_cur) {
+                    flush();
+                    m_cur = m;
+                    a2 = 0;
+                }
+                a2 = __vmaxu2(a2, v[j].x & 0x7fff7fffu);
+                a2 = __vmaxu2(a2, v[j].y & 0x7fff7fffu);
+                a2 = __vmaxu2(a2, v[j].z & 0x7fff7fffu);
+                a2 = __vmaxu2(a2, v[j].w & 0x7fff7fffu);
+            }
+        }
+    }
+    if (pidx < total) flush();
+    tc::named_bar_sync(AQ_BARRIER, AQ_STEP_THREADS);
+    if (pidx < M) {
+        const float amax = bf16_bits_to_float(rmax[pidx]);
+        s_out[pidx] = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    }
+    tc::named_bar_sync(AQ_BARRIER, AQ_STEP_THREADS);
+}
+
 // Shared memory: a ring of US slots, each holding KPU k-tiles of padded weights (16 KB each)
 // and activations (BN x 128 bytes each), plus a ring of SFR raw scale tiles (4 k-tiles each).
 // Tensor memory: ACC_BUFS accumulators of BN columns, the unit B scales, and a ring of SFQ
 // scale slots (KPU k-tiles of A scales each) that the scale warps fill ahead of the data.  With
 // SFQ == US (the decode tilings) a scale slot is tied to its ring slot and freed by the same
 // commit, one commit per fill fewer.
-template <int BN, int KPU, int US, int ACC_BUFS, int SFQ, int SFR, bool A4 = false>
+template <int BN, int KPU, int US, int ACC_BUFS, int SFQ, int SFR, bool A4 = false, bool AQ = false>
 struct Layout {
     static constexpr int W_TILE = BM * 128;             // one padded weight k-tile
     static constexpr int X_TILE = BN * 128;             // one activation k-tile (swizzled)
@@ -144,9 +208,11 @@ struct Layout {
     static constexpr int XS_OFF = BAR_OFF + 512;        // barriers and flags below, then the tile's token scales
     static constexpr int NSTAGE = BN == 16 ? 1 : 2;     // output staging: [16 tokens][128 rows] bf16 buffers
     static constexpr int STAGE_BYTES = 16 * BM * 2;
-    static constexpr int STAGE_OFF = (XS_OFF + BN * 4 + 1023) / 1024 * 1024;
+    static constexpr int AQ_OFF = XS_OFF + BN * 4;      // AQ: per-token scales [BN], row maxima [BN]
+    static constexpr int AQ_BYTES = AQ ? 2 * BN * 4 : 0;
+    static constexpr int STAGE_OFF = (AQ_OFF + AQ_BYTES + 1023) / 1024 * 1024;
     static constexpr int TOTAL = STAGE_OFF + NSTAGE * STAGE_BYTES + 1024;  // + alignment slack
-    static constexpr int TX_BYTES = KPU * (BM * 64 + (A4 ? BN * 64 : X_TILE));  // 4-bit boxes count packed bytes
+    static constexpr int TX_BYTES = KPU * (BM * 64 + (A4 ? BN * 64 : AQ ? 0 : X_TILE));  // 4-bit boxes count packed bytes
     static constexpr int SF_SLOTS = KPU * SFQ;          // TMEM scale k-tile slots, 4 columns each
     static constexpr int SFBW = BN <= 128 ? 4 : 8;      // W4A4: TMEM columns per B-scale k-tile slot
     static constexpr int T_SFB = ACC_BUFS * BN;         // TMEM column of the B scales (unit, or W4A4's ring)
@@ -161,13 +227,14 @@ struct Layout {
     static_assert((X_TILE % 1024) == 0 && (X_OFF % 1024) == 0, "swizzled tiles are 1024-aligned");
 };
 
-template <int BN, int KPU, int US, int ACC_BUFS, int SFQ, int SFR, bool A4>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <int BN, int KPU, int US, int ACC_BUFS, int SFQ, int SFR, bool A4, bool AQ>
+__global__ void __launch_bounds__(num_threads<AQ>(), 1)
 mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_sf, const __grid_constant__ CUtensorMap tmap_out,
                 const __grid_constant__ CUtensorMap tmap_sfb, const Params p)
 {
-    using L = Layout<BN, KPU, US, ACC_BUFS, SFQ, SFR, A4>;
+    using L = Layout<BN, KPU, US, ACC_BUFS, SFQ, SFR, A4, AQ>;
+    static_assert(!(AQ && (A4 || BN != 16)), "the fused activation quant serves the 16-token decode tiling");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, derived by pointer arithmetic so the compiler keeps it in the shared window
     uint8_t *smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -196,7 +263,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < US; ++s) {
-            tc::mbar_init(&full[s], 1);   // producer expect_tx
+            tc::mbar_init(&full[s], AQ ? 1 + AQ_WARPS : 1);  // producer expect_tx (+ the quantizer warps)
             tc::mbar_init(&empty[s], 1);  // tcgen05.commit after the slot's last MMAs
         }
         for (int s = 0; s < SFQ; ++s) {
@@ -220,7 +287,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         *sfr_issued = 0;
         tc::fence_mbar_init();
         tc::tma_prefetch_desc(&tmap_w);
-        tc::tma_prefetch_desc(&tmap_x);
+        if (!AQ) tc::tma_prefetch_desc(&tmap_x);
         tc::tma_prefetch_desc(&tmap_sf);
         if (A4) tc::tma_prefetch_desc(&tmap_sfb);
         if (p.tma_out) tc::tma_prefetch_desc(&tmap_out);
@@ -314,7 +381,10 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 
                 // prefill tilings: every activation tile is read again by the CTAs working on
                 // other weight tiles, so it is kept in L2 over the streaming weights and outputs
-                if constexpr (BN >= 128)
+                // (with the fused activation quant the quantizer warps write the tiles instead)
+                if constexpr (AQ)
+                    ;
+                else if constexpr (BN >= 128)
                     tc::tma_load_3d_hint(smem + L::X_OFF + sl * L::X_SLOT, &tmap_x, &full[sl], 0, m0, kt,
                                          tc::make_policy_evict_last());
                 else
@@ -453,6 +523,71 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             w = __shfl_sync(0xffffffffu, w, 0);
 
         }
+    } else if (AQ && warp >= AQ_WARP0) {
+        // ------------------------------------------------------------ activation quantizers (11-14)
+        // With the activation quant fused in, these four warps write each ring fill's activation
+        // tile themselves: the fill's 512 values of each token row are read from L2 two fills
+        // ahead (so no fill waits on an L2 round trip), divided by the token's scale and rounded to
+        // e4m3 (the code of w4a8_act_quant), and stored at the places the 128-byte-swizzled TMA
+        // box would use.
+        float *aq_s = reinterpret_cast<float *>(smem + L::AQ_OFF);
+        const int qt = threadIdx.x - AQ_WARP0 * 32;  // 0 .. AQ_THREADS - 1
+        // every slot's activation tile starts as zeros; rows >= M are never written again
+        for (int o = qt; o < US * L::X_SLOT / 16; o += AQ_THREADS)
+            reinterpret_cast<uint4 *>(smem + L::X_OFF)[o] = make_uint4(0u, 0u, 0u, 0u);
+        aq_row_scales(p.x, p.M, p.K, 128 + qt, aq_s, reinterpret_cast<unsigned *>(aq_s + BN));
+        constexpr int PER_ROW = KPU * 16;                       // 8-value chunks of a row in one fill
+        constexpr int MAX_IT = (AQ_MAX_M * PER_ROW + AQ_THREADS - 1) / AQ_THREADS;  // chunks per thread and fill
+        constexpr int DEPTH = 3;                                // fills whose values are in flight
+        const int items = p.M * PER_ROW;
+        const int n_f = n_k / KPU;
+        uint4 v[DEPTH][MAX_IT];
+        auto load_fill = [&](int f, uint4 (&dst)[MAX_IT]) {
+            int kt, n0;
+            sched.fill_at(f * KPU, p.m_tiles, kt, n0);
+            const int k0 = kt * 128;  // the fill covers k0 .. k0 + 128 * KPU - 1
+#pragma unroll
+            for (int j = 0; j < MAX_IT; ++j) {
+                const int it = qt + AQ_THREADS * j;
+                if (it < items) {
+                    const int m = it / PER_ROW, c8 = it - m * PER_ROW;
+                    dst[j] = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)m * p.K + k0 + c8 * 8));
+                }
+            }
+        };
+#pragma unroll
+        for (int st = 0; st < DEPTH - 1; ++st)
+            if (st < n_f) load_fill(st, v[st]);
+        bool gave_up = false;
+        for (int f0 = 0; f0 < n_f && !gave_up; f0 += DEPTH) {
+            // unrolled over the stages so every register index is a constant
+#pragma unroll
+            for (int st = 0; st < DEPTH; ++st) {
+                const int f = f0 + st;
+                if (f >= n_f || gave_up) break;
+                if (f + DEPTH - 1 < n_f) load_fill(f + DEPTH - 1, v[(st + DEPTH - 1) % DEPTH]);
+                const int sl = f % US;
+                if (warp_wait(&empty[sl], ((f / US) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_AQ, f, lane)) {
+                    gave_up = true;
+                    break;
+                }
+                uint8_t *slot = smem + L::X_OFF + sl * L::X_SLOT;
+#pragma unroll
+                for (int j = 0; j < MAX_IT; ++j) {
+                    const int it = qt + AQ_THREADS * j;
+                    if (it < items) {
+                        const int m = it / PER_ROW, c8 = it - m * PER_ROW;
+                        const int kb = (c8 & 15) * 8;  // byte of the k-tile row: chunk kb / 16, half kb & 8
+                        *reinterpret_cast<uint2 *>(slot + (c8 >> 4) * L::X_TILE + m * 128 +
+                                                   ((((kb >> 4) ^ (m & 7)) << 4) | (kb & 8))) =
+                            quant8_e4m3(v[st][j], aq_s[m]);
+                    }
+                }
+                tc::fence_proxy_async_smem();  // generic writes -> visible to the tensor core
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&full[sl]);
+            }
+        }
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
@@ -460,6 +595,9 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         const int row = 32 * q + lane;
         const bool issuer = (threadIdx.x == EPI_WARP0 * 32);
         int ck = 0;  // output chunks emitted (staging buffer rotation)
+        if constexpr (AQ)  // the token scales, with the quantizer warps (before any tile is done)
+            aq_row_scales(p.x, p.M, p.K, threadIdx.x - EPI_WARP0 * 32, reinterpret_cast<float *>(smem + L::AQ_OFF),
+                          reinterpret_cast<unsigned *>(smem + L::AQ_OFF) + BN);
         // Write 16 token columns (c0..c0+15 of the tile at m0, n0) of this thread's weight row.
         // With TMA stores the 128 threads stage a [16 tokens][128 rows] bf16 block in shared memory
         // and one thread stores it (out-of-range rows and tokens are clipped by the tensor map);
@@ -500,7 +638,9 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             const int n0 = (t / p.m_tiles) * BM, m0 = (t % p.m_tiles) * BN;
             // the tile's per-token scales, staged once in shared memory (the load overlaps the wait)
             float *xs_s = reinterpret_cast<float *>(smem + L::XS_OFF);
-            for (int i = row; i < BN; i += BM) xs_s[i] = (m0 + i < p.M) ? (A4 ? 1.0f : __ldg(p.xs + m0 + i)) : 0.0f;
+            const float *aq_s = reinterpret_cast<const float *>(smem + L::AQ_OFF);
+            for (int i = row; i < BN; i += BM)
+                xs_s[i] = (m0 + i < p.M) ? (A4 ? 1.0f : AQ ? aq_s[m0 + i] : __ldg(p.xs + m0 + i)) : 0.0f;
             int w = 0;
             if (lane == 0) w = tc::mbar_wait(&acc_full[b], (seg / ACC_BUFS) & 1, abort_flag, WAIT_BUDGET);
             w = __shfl_sync(0xffffffffu, w, 0);
@@ -712,13 +852,14 @@ size_t workspace_for(const Cfg &c)
     return partial_bytes(c) + (size_t)c.m_tiles * c.n_tiles * 4;
 }
 
-template <int BN, int KPU, int US, int ACC_BUFS, int SFQ, int SFR, bool A4 = false>
+template <int BN, int KPU, int US, int ACC_BUFS, int SFQ, int SFR, bool A4 = false, bool AQ = false>
 w4a8_status launch(const uint8_t *wp, const uint8_t *xq, Params prm, cudaStream_t stream,
                    const uint8_t *xe = nullptr)
 {
-    using L = Layout<BN, KPU, US, ACC_BUFS, SFQ, SFR, A4>;
+    using L = Layout<BN, KPU, US, ACC_BUFS, SFQ, SFR, A4, AQ>;
     CUtensorMap tw, tx, tsf, tout, tsfb;
     memset(&tsfb, 0, sizeof(tsfb));
+    memset(&tx, 0, sizeof(tx));
     // W4A4: activations are 4-bit codes [M, K/2] read like the weights, their e8m0 [M, K/32] as
     // [BN tokens x 16 bytes] tiles
     if (A4 && (!tch::tmap_3d_ktiles(&tx, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, xq, prm.M, prm.K / 2, 64,
@@ -735,16 +876,16 @@ w4a8_status launch(const uint8_t *wp, const uint8_t *xq, Params prm, cudaStream_
     // activations (bytes; a row is K bytes, a k-tile 128)
     if (!tch::tmap_3d_ktiles(&tw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, wp, prm.N, prm.K / 2, 64, prm.K / 128, BM,
                              KPU) ||
-        (!A4 && !tch::tmap_3d_ktiles(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, prm.M, prm.K, 128, prm.K / 128, BN, KPU)) ||
+        (!A4 && !AQ && !tch::tmap_3d_ktiles(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, prm.M, prm.K, 128, prm.K / 128, BN, KPU)) ||
         !tch::tmap_2d(&tsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, prm.we, prm.N, prm.K / 32, prm.K / 32, BM, 16,
                       CU_TENSOR_MAP_SWIZZLE_NONE))
         return W4A8_ERR_CUDA;
-    auto kern = mxfp4_tc_kernel<BN, KPU, US, ACC_BUFS, SFQ, SFR, A4>;
+    auto kern = mxfp4_tc_kernel<BN, KPU, US, ACC_BUFS, SFQ, SFR, A4, AQ>;
     static std::atomic<int> attr_done[64];
     if (!tch::set_smem_once(kern, L::TOTAL, attr_done)) return W4A8_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(prm.G);
-    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.blockDim = dim3(num_threads<AQ>());
     cfg.dynamicSmemBytes = L::TOTAL;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -793,6 +934,7 @@ static bool make_params(Params &prm, const Cfg &c, const float *x_scale, const u
     prm.wp = wp;
     prm.we = we;
     prm.xs = x_scale;
+    prm.x = nullptr;
     prm.out = out;
     prm.partials = static_cast<float *>(workspace);
     prm.counters = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) + partial_bytes(c));
@@ -830,6 +972,21 @@ w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const 
     case 192: return launch<192, 2, 2, 2, 2, 4>(wp, xq, prm, stream);
     default: return launch<256, 2, 2, 1, 4, 4>(wp, xq, prm, stream);
     }
+}
+
+bool w4a8_tc_mxfp4_aq_takes(int64_t M, int64_t K)
+{
+    return M >= 1 && M <= AQ_MAX_M && (size_t)M * (size_t)K * 2 <= W4A8_FUSED_AQ_MAX_X_BYTES;
+}
+
+w4a8_status w4a8_launch_mxfp4_tc_aq(const uint16_t *x_bf16, const uint8_t *wp, const uint8_t *we, uint16_t *out,
+                                    int64_t M, int64_t N, int64_t K, void *workspace, cudaStream_t stream)
+{
+    const Cfg c = choose(M, N, K);  // M <= AQ_MAX_M: the 16-token tiling
+    Params prm;
+    if (!make_params(prm, c, nullptr, wp, we, out, M, N, K, workspace, false)) return W4A8_ERR_CUDA;
+    prm.x = x_bf16;
+    return launch<16, 4, 3, 2, 3, 2, false, true>(wp, nullptr, prm, stream);
 }
 
 bool w4a8_tc_mxfp4_a4_supported(const void *xa, const void *xe, const void *wp, const void *we, const void *out,

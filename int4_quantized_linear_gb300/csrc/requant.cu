@@ -58,6 +58,16 @@ W4A8_DEVICE int block_exponent(float amax, int mode)
     return min(127, max(-127, e));
 }
 
+// Two non-negative fp32 values -> their e2m1 codes in one byte (low nibble = a0): the hardware
+// conversion rounds to the nearest grid point {0, .5, 1, 1.5, 2, 3, 4, 6} with ties to the even
+// code and saturates at 6 -- e2m1_index of min(a, 6), whose ties go to the even index.
+W4A8_DEVICE uint32_t e2m1x2_from_nonneg(float a0, float a1)
+{
+    uint32_t r;
+    asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }" : "=r"(r) : "f"(a1), "f"(a0));
+    return r;
+}
+
 // Encode 32 values at exponent e.  Returns the squared error in scale units (fp32, squares
 // rounded and added in ascending k) and the 32 codes as four words of eight nibbles.
 W4A8_DEVICE float encode_block(const float (&w)[32], int e, uint32_t (&codes)[4])
@@ -67,20 +77,20 @@ W4A8_DEVICE float encode_block(const float (&w)[32], int e, uint32_t (&codes)[4]
 #pragma unroll
     for (int j = 0; j < 4; ++j) codes[j] = 0;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-        float av = fabsf(__fmul_rn(w[k], inv));
-        float a = fminf(av, 6.0f);
-        // e2m1_index: step 0.5 below 2, step 1 below 4, step 2 above; round half to even
-        float f = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
-        float finv = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
-        float off = a < 2.0f ? 0.0f : (a < 4.0f ? 2.0f : 4.0f);
-        float q = rintf(__fmul_rn(a, f));
-        float g = __fmul_rn(q, finv);  // the grid value; exact (powers of two)
-        uint32_t idx = (uint32_t)(q + off);
-        float d = __fsub_rn(av, g);
-        S = __fadd_rn(S, __fmul_rn(d, d));
-        uint32_t c = idx | ((idx != 0u && signbit(w[k])) ? 8u : 0u);
-        codes[k >> 3] |= c << (4 * (k & 7));
+    for (int k = 0; k < 32; k += 2) {
+        // |v| = |w| 2^-e is exact (a power-of-two product); it may exceed 6 (up to 12 one binade
+        // finer), and the error is taken against the unclamped value
+        const float a0 = fabsf(__fmul_rn(w[k], inv)), a1 = fabsf(__fmul_rn(w[k + 1], inv));
+        const uint32_t b = e2m1x2_from_nonneg(a0, a1);
+        const float2 g = e2m1x2_to_float2(b);  // the chosen grid values (exact)
+        const float d0 = __fsub_rn(a0, g.x), d1 = __fsub_rn(a1, g.y);
+        S = __fadd_rn(S, __fmul_rn(d0, d0));
+        S = __fadd_rn(S, __fmul_rn(d1, d1));
+        // the sign bit only on a nonzero index, so -0 and small negatives give code 0, never 8
+        const uint32_t i0 = b & 7u, i1 = (b >> 4) & 7u;
+        const uint32_t c0 = i0 | ((i0 != 0u && signbit(w[k])) ? 8u : 0u);
+        const uint32_t c1 = i1 | ((i1 != 0u && signbit(w[k + 1])) ? 8u : 0u);
+        codes[k >> 3] |= (c0 | (c1 << 4)) << (4 * (k & 7));
     }
     return S;
 }

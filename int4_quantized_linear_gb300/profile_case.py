@@ -1,4 +1,4 @@
-"""One small, self-checking invocation of the decode/prefill MXFP4 path, for profilers.
+"""One small, self-checking invocation of one hot-path kernel, for profilers.
 
     python -m int4_quantized_linear_gb300.profile_case --m 1 --n 34816 --k 5120 --calls 3
 
@@ -7,7 +7,9 @@ per-token activation quant once and the MXFP4 GEMM ``--calls`` times on ``cuda:0
 the library's device status word; exits non-zero if a bounded wait ran out.  Meant as the
 target of ``ncu -k regex:mxfp4_tc -c <calls>`` (``regex:int4_tc`` with ``--int4`` or ``--int5``;
 ``--w4a4`` runs the MXFP4-activation path, whose GEMM is also ``mxfp4_tc``): it launches nothing
-else of note.
+else of note.  ``--act-quant`` runs only the per-token activation quant of x [M, K]
+(``regex:act_quant``) and ``--requant MODE`` the NVFP4 -> MXFP4 requant of an [N, K] merged
+weight of two equal partitions (``regex:requant``), each ``--calls`` times.
 """
 from __future__ import annotations
 
@@ -29,12 +31,30 @@ def main(argv=None) -> int:
     ap.add_argument("--int4", action="store_true", help="the AutoRound int4 g128 GEMM instead of MXFP4")
     ap.add_argument("--int5", action="store_true", help="the int5 g128 GEMM (zero point 16) instead of MXFP4")
     ap.add_argument("--w4a4", action="store_true", help="MXFP4 activations (W4A4) instead of fp8 ones")
+    ap.add_argument("--act-quant", action="store_true", help="only the per-token activation quant")
+    ap.add_argument("--requant", choices=["ocp", "noclip", "mse"], help="only the NVFP4 -> MXFP4 requant")
     args = ap.parse_args(argv)
     M, N, K = args.m, args.n, args.k
     lib.load()
     dev = torch.device("cuda", 0)
+    if args.requant:
+        nv_p, nv_s = synth.nvfp4_tensor_bytes(N, K, 0)
+        nvp, nvs = torch.from_numpy(nv_p).to(dev), torch.from_numpy(nv_s).to(dev)
+        div = torch.tensor([2688.0, 10752.0], dtype=torch.float32, device=dev)
+        parts = [N // 2, N - N // 2]
+        for _ in range(args.calls):
+            lib.requant(nvp, nvs, div, parts, args.requant, err_ssq=True)
+        torch.cuda.synchronize()
+        print(f"ok requant {args.requant} N={N} K={K} calls={args.calls}")
+        return 0
     x = torch.from_numpy(np.ascontiguousarray(synth.activations(M, K, seed=M)).view(np.int16)).to(dev)
     xq, xs = lib.act_quant(x.view(torch.bfloat16))
+    if args.act_quant:
+        for _ in range(args.calls - 1):
+            lib.act_quant(x.view(torch.bfloat16), xq, xs)
+        torch.cuda.synchronize()
+        print(f"ok act_quant M={M} K={K} calls={args.calls}")
+        return 0
     out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     if args.int5:
         qw, qh, sc = synth.int5_weights(N, K, 0)

@@ -121,6 +121,64 @@ def test_requant_full_gate_up(lib, orc):
         assert abs(rel_g - orc.rel_rms(rs)) <= 1e-5 * orc.rel_rms(rs)
 
 
+def _page_exponent_disagreements(packed, scale, div, parts, e_exact, mode):
+    """How often the page's fp32 exponent formulas ("radiance_nvfp4.py", _block_exponent:
+    floor(log2(amax)) - 2 for ocp, ceil(log2(amax / 6)) for noclip, torch.log2 in fp32) differ from
+    the exact rule the library and the oracle implement, on the blocks with amax > 0.  The
+    dequantized weights follow dequant_nvfp4 in fp32 on the GPU."""
+    grid = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], device="cuda")
+    N = packed.shape[0]
+    pk = to_dev(packed)
+    codes = torch.stack([pk & 0x0F, pk >> 4], -1).reshape(N, -1).long()
+    val = grid[codes & 7] * torch.where((codes & 8) != 0, -1.0, 1.0)
+    sc = to_dev(scale).view(torch.float8_e4m3fn).float()
+    rows = torch.repeat_interleave(torch.arange(len(parts), device="cuda"), torch.tensor(parts, device="cuda"))
+    t = sc / to_dev(div)[rows][:, None]                       # fl(s / divisor)
+    w = val * torch.repeat_interleave(t, 16, dim=1)           # fl(G * t)
+    amax = w.abs().reshape(N, -1, 32).amax(-1)
+    pos = amax > 0
+    if mode == "ocp":
+        page = torch.floor(torch.log2(amax)) - 2
+    else:
+        page = torch.ceil(torch.log2(amax / 6.0))
+    exact = (to_dev(e_exact).float() - 127.0)
+    return int(((page != exact) & pos).sum()), int(pos.sum())
+
+
+@pytest.mark.slow
+def test_requant_gate_up_relrms_report(lib, orc):
+    """Config: the merged gate_up [34816, 5120], W ~ N(0, 0.02), two 17408-row partitions each
+    NVFP4-quantized with its own divisor 6*448/amax, requantized by every rule: bit-exact codes and
+    e8m0, and the per-layer relRMS from the GPU's error sums ("radiance_nvfp4.py",
+    process_weights_after_loading) equal to the oracle's.  Prints the figures and the direct
+    bf16 -> MXFP4 relRMS of the same weights (the pages' context: 0.158 requantized, 0.112 direct,
+    on real checkpoint tensors) and the page-formula exponent diagnostic."""
+    import json
+    N, K = GATE_UP
+    parts = list(synth.GATE_UP_PARTITIONS)
+    w = synth.gaussian_weights(N, K, 0.02, 0)
+    packed, scale, div = orc.nvfp4_quantize(w, parts)
+    report = {"divisors": [float(d) for d in div]}
+    for mode in ("ocp", "noclip", "mse"):
+        gp, ge, gs = lib.requant(to_dev(packed), to_dev(scale), to_dev(div), parts, mode)
+        rp, re_, rs = orc.requant(packed, scale, div, parts, mode)
+        assert np.array_equal(host(ge), re_), mode
+        assert np.array_equal(host(gp), rp), mode
+        g = host(gs)
+        rel = orc.rel_rms(g)
+        assert abs(rel - orc.rel_rms(rs)) <= 1e-5 * orc.rel_rms(rs)
+        report[mode] = {"relrms": rel, "per_partition": [float(np.sqrt(e / s)) for e, s in g]}
+        if mode != "mse":
+            bad, total = _page_exponent_disagreements(packed, scale, div, parts, re_, mode)
+            report[mode]["page_formula_disagreements"] = [bad, total]
+    # mse picks the lower-error exponent per block, so it can only help
+    assert report["mse"]["relrms"] <= report["noclip"]["relrms"]
+    wb = synth.to_bf16_bits(w)
+    _, _, gs = lib.requant_bf16(to_dev_bf16(wb), "mse")
+    report["direct_bf16_mse_relrms"] = orc.rel_rms(host(gs))
+    print("REQUANT_REPORT " + json.dumps(report))
+
+
 @pytest.mark.parametrize("mode", ["ocp", "noclip", "mse"])
 @pytest.mark.parametrize("N,K", [(1, 32), (70, 384), (257, 1024)])
 def test_requant_fp8_channel_bit_exact(lib, orc, mode, N, K):
@@ -309,6 +367,32 @@ def test_linear_fused_matches_two_calls(lib, orc, policy, M, N, K):
     gemm_check(bf16_to_f64(fused), orc.mxfp4_linear(host(xq), host(xs), w, e), f"fused M={M} N={N} K={K}")
 
 
+# Up to 8 tokens (and at most 96 KB of bf16 activations) the quant runs inside the GEMM: every
+# CTA takes the rows' amax from L2 and writes its fills' e4m3 tiles into shared memory itself.
+@pytest.mark.parametrize("M,N,K", [(1, 520, 512), (2, 256, 1024), (3, 1000, 2048), (5, 4096, 5120),
+                                   (8, 384, 5120), (4, 256, 10240), (1, 5120, 17408),
+                                   # past the activation-size limit: the two-kernel chain again
+                                   (8, 512, 17408)])
+def test_linear_fused_quant_in_gemm(lib, orc, M, N, K):
+    x, w, e = synth.decode_case(M, N, K, seed=M * 5 + N)
+    x = x.copy()
+    x[0, :7] = 0x8000                      # -0 values
+    if M > 2:
+        x[2, :] = 0                        # an all-zero row: scale 1, codes 0
+    xd, wd, ed = to_dev_bf16(x), to_dev(w), to_dev(e)
+    fused = lib.linear(xd, wd, ed)
+    xq, xs = lib.act_quant(xd)
+    two = lib.mxfp4_linear(xq, xs, wd, ed)
+    lib.check_device_status()
+    assert torch.equal(fused.view(torch.int16), two.view(torch.int16))
+    hq, hs = orc.act_quant(x)
+    im, inn = _sample_pairs(M, N, seed=M)
+    gemm_check(bf16_to_f64(fused)[im, inn], orc.mxfp4_linear_pairs(hq, hs, w, e, im, inn),
+               f"fused quant M={M} N={N} K={K}")
+    if M > 2:
+        assert np.all(bf16_to_f64(fused)[2] == 0.0)
+
+
 @pytest.mark.parametrize("shape", [GATE_UP, DOWN], ids=["gate_up", "down"])
 @pytest.mark.parametrize("M", [1, 64])
 def test_linear_fused_decode_full_sampled(lib, orc, shape, M):
@@ -399,6 +483,51 @@ def test_int4_full_sampled(lib, orc, shape, M):
         pairs = _sample_pairs(M, N, 96)
     got, ref = _i4_gemm(lib, orc, x, qw, s16, qz, pairs=pairs)
     gemm_check(got, ref, f"int4 M={M} N={N} K={K}")
+
+
+# M > 128 without zero points takes the 256-token prefill tiling (signed operand codes, no
+# zero-point MMAs): several token tiles with a ragged last one, ragged column tiles, N % 8 != 0
+# (plain output stores), split tiles only (small shapes) and whole tiles beside stream-K splits
+# (192 tiles on the GPU's SMs).
+PREFILL_I4 = [(129, 132, 512), (256, 256, 512), (300, 1004, 1024), (513, 392, 2048), (600, 640, 1536),
+              (512, 12288, 512)]
+
+
+def _prefill_pairs(M, N, seed):
+    rows = np.unique(np.concatenate([[0, 127, 128, 255, 256, M - 1], synth.uniform_ints(24, 0, M - 1, seed, 5)]))
+    cols = np.unique(np.concatenate([[0, 127, 128, N - 1], synth.uniform_ints(48, 0, N - 1, seed, 6)]))
+    return np.repeat(rows, cols.size), np.tile(cols, rows.size)
+
+
+@pytest.mark.parametrize("M,N,K", PREFILL_I4)
+def test_int4_prefill_tiling(lib, orc, M, N, K):
+    x, qw, s16, qz = synth.int4_case(M, N, K, seed=M + 7)
+    pairs = _prefill_pairs(M, N, 7) if M * N > 1 << 20 else None
+    got, ref = _i4_gemm(lib, orc, x, qw, s16, qz, pairs=pairs)
+    gemm_check(got, ref, f"int4 prefill M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(129, 144, 512), (256, 256, 512), (300, 1008, 1024), (513, 400, 2048),
+                                   (512, 12288, 512)])
+def test_int5_prefill_tiling(lib, orc, M, N, K):
+    x = synth.activations(M, K, seed=M + 8)
+    qw, qh, s16 = synth.int5_weights(N, K, seed=M + 8)
+    pairs = _prefill_pairs(M, N, 8) if M * N > 1 << 20 else None
+    got, ref = _i5_gemm(lib, orc, x, qw, qh, s16, pairs=pairs)
+    gemm_check(got, ref, f"int5 prefill M={M} N={N} K={K}")
+
+
+def test_int4_prefill_extreme_codes(lib, orc):
+    # every code 0 (value -8) and every code 15 (value 7), and an all-zero activation row: the
+    # signed operand bytes at both ends and a row whose output must be exactly zero
+    M, N, K = 260, 256, 1024
+    x, _, s16, qz = synth.int4_case(M, N, K, seed=21)
+    x[3, :] = 0
+    for word in (0x00000000, 0xFFFFFFFF, 0x0F0F0F0F):
+        qw = np.full((K // 8, N), word, np.uint32).view(np.int32)
+        got, ref = _i4_gemm(lib, orc, x, qw, s16, qz)
+        gemm_check(got, ref, f"int4 prefill codes {word:#x}")
+        assert np.all(got[3] == 0.0)
 
 
 def _i4_asym_gemm(lib, orc, x, qw, s16, qz, pairs=None):

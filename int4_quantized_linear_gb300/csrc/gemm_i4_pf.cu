@@ -56,12 +56,21 @@ constexpr int GATE_WARP = 2;
 constexpr int WORD_WARP = 3;      // producer of the checkpoint-word ring
 constexpr int CONV_WARP0 = 4;     // warps 4-7
 constexpr int EPI_WARP0 = 8;      // warps 8-15: lane quarter warp & 3, token half (warp >> 2) & 1
-constexpr int US = 4;             // activation ring slots, one k-tile (BN x 128 bytes) each
-constexpr int RS = 4;             // checkpoint-word ring slots, one k-tile each
-constexpr int NA = 2;             // converted operand tiles
+constexpr int XK = 2;             // k-tiles per activation fill (256 contiguous bytes per token row)
+constexpr int US = 2;             // activation ring fills
 constexpr int NB = 2;             // group accumulators of BN columns in tensor memory
-constexpr int ND = 4;             // k-tile completion barriers (at least US, NA and NB)
-static_assert(ND >= US && ND >= NA && ND >= NB, "completion barriers");
+constexpr int ND = 4;             // k-tile completion barriers
+// checkpoint-word ring slots (one k-tile each) and converted operand tiles: int5's slots carry
+// the fifth-bit plane too, so it keeps one operand tile fewer
+template <bool I5>
+struct Depth {
+    static constexpr int RS = I5 ? 4 : 3;
+    static constexpr int NA = I5 ? 2 : 3;
+};
+static_assert(ND >= US * XK && ND >= 3 && ND >= NB, "completion barriers");
+#ifndef W4A8_PF_TMA_STORE
+#define W4A8_PF_TMA_STORE 1
+#endif
 constexpr int GATE_BARRIER = 2;   // gate warp + MMA warp
 constexpr int EPI_BARRIER = 3;    // the eight promotion warps
 constexpr int HALF_BARRIER0 = 4;  // 4 and 5: the four warps of one token half
@@ -93,20 +102,35 @@ struct Params {
     long long RU;          // stream-K units
     int R, D, G, Gsk;      // work split (see Sched)
     int tma_out;           // output through TMA stores (else plain stores)
+    unsigned long long *trace;  // optional pipeline timeline of CTA 0 (diagnostics), or null
 };
+
+// Pipeline timeline (a development aid, compiled in only when W4A8_TRACE is defined): CTA 0
+// records clock64() per k-tile i < TRACE_N: 0 activations issued, 1 words issued, 2 words seen
+// by the converters, 3 operand tile written, 4 MMAs released by the gate, 5 group accumulator
+// seen by the promotion (warp 8), 6 released by warp 8, 7 released by warp 12.
+constexpr int TRACE_N = 512;
+__device__ __forceinline__ void trace_ev(const Params &p, int ev, int i)
+{
+#ifdef W4A8_TRACE
+    if (p.trace != nullptr && blockIdx.x == 0 && i < TRACE_N) p.trace[ev * TRACE_N + i] = (unsigned long long)clock64();
+#endif
+}
 
 // Shared memory: the activation ring, the checkpoint-word ring, the converted operand tiles, two
 // output staging buffers per token half, the tile's token scales, then barriers and flags.
 template <bool I5>
 struct Layout {
+    static constexpr int RS = Depth<I5>::RS, NA = Depth<I5>::NA;
     static constexpr int X_TILE = BN * 128;      // [256 tokens][128 k] e4m3, 128-byte swizzle
+    static constexpr int X_FILL = XK * X_TILE;
     static constexpr int A_TILE = BM * 128;      // [128 columns][128 k] e4m3, 128-byte swizzle
     static constexpr int STAGE_BYTES = 16 * BM * 2;  // [16 tokens][128 columns] bf16
     static constexpr int W_TILE = 16 * BM * 4;     // [16 word rows][128 columns] int32
     static constexpr int H_TILE = I5 ? 16 * BM : 0;  // [16 rows][128 columns] fifth-bit bytes
     static constexpr int R_SLOT = W_TILE + H_TILE;
     static constexpr int X_OFF = 0;
-    static constexpr int R_OFF = X_OFF + US * X_TILE;
+    static constexpr int R_OFF = X_OFF + US * X_FILL;
     static constexpr int A_OFF = R_OFF + RS * R_SLOT;
     static constexpr int STAGE_OFF = A_OFF + NA * A_TILE;
     static constexpr int XS_OFF = STAGE_OFF + 4 * STAGE_BYTES;
@@ -149,6 +173,7 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
                const Params p)
 {
     using L = Layout<I5>;
+    constexpr int RS = L::RS, NA = L::NA;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *x_full = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);  // activation slot landed
@@ -216,16 +241,19 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             // -------------------------------------------------------- TMA producer: activations
             if (lane == 0) {
                 const uint64_t keep = tc::make_policy_evict_last();  // re-read by the other column tiles
-                for (int i = 0; i < n_k && !*abort_flag; ++i) {
-                    const int s = i % US;
-                    if (i >= US && wait_or_fail(&done[(i - US) % ND], ((i - US) / ND) & 1, abort_flag, p.status,
-                                                ST_TIMEOUT_PRODUCER, i))
+                // fill f holds k-tiles XK f .. XK f + XK - 1 (a unit holds a whole number of fills);
+                // its slot is free once the last k-tile of fill f - US is done
+                for (int f = 0; f < n_k / XK && !*abort_flag; ++f) {
+                    const int s = f % US, last = XK * (f - US) + XK - 1;
+                    if (f >= US && wait_or_fail(&done[last % ND], (last / ND) & 1, abort_flag, p.status,
+                                                ST_TIMEOUT_PRODUCER, f))
                         break;
                     int n0, m0, kt;
-                    coords(i, n0, m0, kt);
-                    tc::mbar_arrive_expect_tx(&x_full[s], L::X_TILE);
-                    tc::tma_load_3d_hint(smem + L::X_OFF + s * L::X_TILE, &tmap_x, &x_full[s], 0, m0, kt, keep);
-                    *issued = i + 1;
+                    coords(XK * f, n0, m0, kt);
+                    tc::mbar_arrive_expect_tx(&x_full[s], L::X_FILL);
+                    tc::tma_load_3d_hint(smem + L::X_OFF + s * L::X_FILL, &tmap_x, &x_full[s], 0, m0, kt, keep);
+                    *issued = f + 1;
+                    trace_ev(p, 0, XK * f);
                 }
             }
             __syncwarp();
@@ -243,6 +271,7 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
                     tc::tma_load_2d(dst, &tmap_q, &r_full[s], n0, 16 * kt);
                     if constexpr (I5) tc::tma_load_2d(dst + L::W_TILE, &tmap_h, &r_full[s], n0, 16 * kt);
                     *r_issued = i + 1;
+                    trace_ev(p, 1, i);
                 }
             }
             __syncwarp();
@@ -255,19 +284,20 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             if (!gate) tc::tc_fence_after();
             const uint32_t idesc = tc::idesc_f8f6f4(0, 0, BM, BN);
             for (int i = 0; i < n_k; ++i) {
-                const int s = i % US, a = i % NA, b = i % NB;
+                const int xf = i / XK, s = xf % US, a = i % NA, b = i % NB;
                 if (gate) {
                     if (!*abort_flag)
                         warp_wait(&g_empty[b], ((i / NB) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_GATE, i, lane);
                     if (!*abort_flag) warp_wait(&a_full[a], (i / NA) & 1, abort_flag, p.status, ST_TIMEOUT_GATE, i, lane);
-                    if (!*abort_flag) warp_wait(&x_full[s], (i / US) & 1, abort_flag, p.status, ST_TIMEOUT_GATE, i, lane);
+                    if (!*abort_flag) warp_wait(&x_full[s], (xf / US) & 1, abort_flag, p.status, ST_TIMEOUT_GATE, i, lane);
                 }
                 const bool aborted = tc::named_bar_or(GATE_BARRIER, 64, gate && *abort_flag);
                 if (aborted) break;
                 if (!gate && lane == 0) {
+                    trace_ev(p, 4, i);
                     tc::tc_fence_after();
                     const uint32_t aa = tc::smem_u32(smem + L::A_OFF + a * L::A_TILE);
-                    const uint32_t xa = tc::smem_u32(smem + L::X_OFF + s * L::X_TILE);
+                    const uint32_t xa = tc::smem_u32(smem + L::X_OFF + s * L::X_FILL + (i % XK) * L::X_TILE);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         tc::mma_f8f6f4(tmem + b * BN, tc::smem_desc(aa + 32 * kk, 16, 1024, 2),
@@ -291,6 +321,7 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
         for (int i = 0; i < n_k; ++i) {
             const int s = i % RS, a = i % NA;
             if (warp_wait(&r_full[s], (i / RS) & 1, abort_flag, p.status, ST_TIMEOUT_CONV, i, lane)) break;
+            if (r == 0) trace_ev(p, 2, i);
             // the operand tile is free once k-tile i - NA's MMAs are done
             if (i >= NA && warp_wait(&done[(i - NA) % ND], ((i - NA) / ND) & 1, abort_flag, p.status,
                                      ST_TIMEOUT_CONV, i, lane))
@@ -321,6 +352,7 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             tc::fence_proxy_async_smem();  // generic writes -> visible to the tensor core
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&a_full[a]);
+            if (r == 0) trace_ev(p, 3, i);
         }
     } else {
         regs_inc<Regs<I5>::EPI>();
@@ -381,12 +413,9 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             const long long t_lo = (long long)t * p.U, t_hi = t_lo + p.U;
             const bool whole = (u == t_lo) && (ue == t_hi);
             const int n0 = (t / p.m_tiles) * BM, m0 = (t % p.m_tiles) * BN;
-            // this half's token scales (the previous tile's readers are past the barrier)
-            tc::named_bar_sync(half_bar, 128);
-            {
-                const int m = m0 + 128 * h + r;
-                xs_s[r] = m < p.M ? __ldg(p.xs + m) : 0.0f;
-            }
+            // this half's token scales: loaded now, stored to shared memory after the tile's k-tiles
+            // (no wait on the load at the start of the tile; the previous tile's readers are done)
+            const float xs_r = (m0 + 128 * h + r < p.M) ? __ldg(p.xs + m0 + 128 * h + r) : 0.0f;
             float acc[128];
 #pragma unroll
             for (int c = 0; c < 128; ++c) acc[c] = 0.0f;
@@ -410,6 +439,7 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
                     break;
                 }
                 tc::tc_fence_after();
+                if (threadIdx.x == EPI_WARP0 * 32) trace_ev(p, 5, i);
                 const float s = jj == 0 ? sc_cur[0] : jj == 1 ? sc_cur[1] : jj == 2 ? sc_cur[2] : sc_cur[3];
                 const uint32_t tb = tmem + b * BN + 128 * h + ((32u * q) << 16);
                 // two 32-column buffers: the next load is in flight while the last one is added
@@ -433,7 +463,10 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
                 tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&g_empty[b]);
+                if (threadIdx.x == EPI_WARP0 * 32) trace_ev(p, 6, i);
+                if (threadIdx.x == (EPI_WARP0 + 4) * 32) trace_ev(p, 7, i);
             }
+            xs_s[r] = xs_r;
             // all eight warps leave together if any gave up (this also publishes xs_s)
             if (tc::named_bar_or(EPI_BARRIER, 256, gave_up)) break;
             if (whole) {
@@ -572,11 +605,11 @@ static w4a8_status launch(const uint8_t *xq, Params prm, cudaStream_t stream)
         (I5 && !tch::tmap_2d(&th, CU_TENSOR_MAP_DATA_TYPE_UINT8, prm.qh, prm.K / 8, prm.N, (uint64_t)prm.N, 16, BM,
                              CU_TENSOR_MAP_SWIZZLE_NONE)))
         return W4A8_ERR_CUDA;
-    prm.tma_out = (prm.N % 8 == 0) && w4a8_aligned(prm.out, 16) &&
+    prm.tma_out = W4A8_PF_TMA_STORE && (prm.N % 8 == 0) && w4a8_aligned(prm.out, 16) &&
                   tch::tmap_2d(&tout, CU_TENSOR_MAP_DATA_TYPE_UINT16, prm.out, prm.M, prm.N, (uint64_t)prm.N * 2, 16,
                                BM, CU_TENSOR_MAP_SWIZZLE_NONE);
-    // activations as [k-tile][token][128 bytes], one k-tile of 256 tokens per box
-    if (!tch::tmap_3d_ktiles(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, prm.M, prm.K, 128, prm.K / 128, BN, 1))
+    // activations as [k-tile][token][128 bytes], XK k-tiles of 256 tokens per box
+    if (!tch::tmap_3d_ktiles(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, prm.M, prm.K, 128, prm.K / 128, BN, XK))
         return W4A8_ERR_CUDA;
     auto kern = int4_pf_kernel<I5>;
     static std::atomic<int> attr_done[64];
@@ -643,5 +676,6 @@ w4a8_status w4a8_launch_int4_pf(const uint8_t *xq, const float *x_scale, const i
     prm.G = c.k.G;
     prm.Gsk = c.k.Gsk;
     prm.tma_out = 0;
+    prm.trace = static_cast<unsigned long long *>(w4a8_debug_trace_ptr());
     return qh ? launch<true>(xq, prm, stream) : launch<false>(xq, prm, stream);
 }

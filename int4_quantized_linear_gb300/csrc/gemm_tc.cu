@@ -67,10 +67,10 @@ namespace tcg {
 using namespace tcs;
 
 constexpr int NUM_THREADS = 352;   // 11 warps
-// With the activation quant fused in (AQ): four more warps (11-14) quantize each ring fill's
-// activation tile into shared memory, so the kernel has 15.
+// With the activation quant fused in (AQ): one more warp per ring slot (11-13) writes each ring
+// fill's activation tile into shared memory, so the kernel has 14.
 constexpr int AQ_WARP0 = 11;
-constexpr int AQ_WARPS = 4;
+constexpr int AQ_WARPS = 3;        // = the ring slots of the 16-token tiling
 constexpr int AQ_THREADS = 32 * AQ_WARPS;
 constexpr int AQ_BARRIER = 3;      // named barrier of the row-amax step (quantizer + epilogue warps)
 constexpr int AQ_STEP_THREADS = AQ_THREADS + 128;
@@ -110,7 +110,8 @@ struct Params {
 // Pipeline timeline (a development aid, compiled in only when W4A8_TRACE is defined): CTA 0
 // records clock64() per k-tile i < TRACE_N for each event.
 constexpr int TRACE_N = 256;
-enum { TR_TMA_ISSUED = 0, TR_SCALE_DATA, TR_SCALE_DONE, TR_MMA_READY, TR_TMA_FILL, TR_GATE_SFF, TR_EVENTS };
+enum { TR_TMA_ISSUED = 0, TR_SCALE_DATA, TR_SCALE_DONE, TR_MMA_READY, TR_TMA_FILL, TR_GATE_SFF, TR_AQ_SLOT, TR_AQ_DONE,
+       TR_EVENTS };
 __device__ __forceinline__ void trace_ev(const Params &p, int ev, int i)
 {
 #ifdef W4A8_TRACE
@@ -134,12 +135,13 @@ __device__ __forceinline__ void trace_phase(const Params &p, int k)
 #endif
 }
 
-// Fused activation quant, first step, run by the quantizer and epilogue warps together (256
-// threads, pidx 0..255): each token row's amax over all K, taken on the bf16 bit patterns (for
+// Fused activation quant, first step, run by the quantizer and epilogue warps together
+// (AQ_STEP_THREADS threads, pidx 0 .. AQ_STEP_THREADS - 1): each token row's amax over all K, taken on the bf16 bit patterns (for
 // finite values |x| orders like the 15 low bits) as w4a8_act_quant takes it, then the per-token
 // scale amax / 448 (correctly rounded; 1.0 for an all-zero row) into s_out[m].  The rows are read
-// from L2 in batches of sixteen 16-byte chunks per thread, so each thread keeps sixteen loads in
-// flight (a 5120-wide row of up to 8 tokens takes two round trips).
+// from L2 in batches of BATCH 16-byte chunks per thread, so each thread keeps that many loads in
+// flight (every thread walks the same chunks whatever its batch size).
+template <int BATCH>
 __device__ __forceinline__ void aq_row_scales(const uint16_t *x, int M, int K, int pidx, float *s_out, unsigned *rmax)
 {
     if (pidx < M) rmax[pidx] = 0u;
@@ -153,15 +155,15 @@ __device__ __forceinline__ void aq_row_scales(const uint16_t *x, int M, int K, i
         const uint32_t hb = max(a2 & 0xffffu, a2 >> 16);
         if (hb) atomicMax(&rmax[m_cur], hb);
     };
-    for (int base = pidx; base < total; base += 16 * AQ_STEP_THREADS) {
-        uint4 v[16];
+    for (int base = pidx; base < total; base += BATCH * AQ_STEP_THREADS) {
+        uint4 v[BATCH];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < BATCH; ++j) {
             const int idx = base + j * AQ_STEP_THREADS;
             v[j] = idx < total ? __ldg(src + idx) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < BATCH; ++j) {
             const int idx = base + j * AQ_STEP_THREADS;
             if (idx < total) {
                 const int m = idx / nchunk;
@@ -235,6 +237,8 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 {
     using L = Layout<BN, KPU, US, ACC_BUFS, SFQ, SFR, A4, AQ>;
     static_assert(!(AQ && (A4 || BN != 16)), "the fused activation quant serves the 16-token decode tiling");
+    // each quantizer warp owns one ring slot, so it waits on that slot's barriers in phase order
+    static_assert(!AQ || US == AQ_WARPS, "one quantizer warp per ring slot");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, derived by pointer arithmetic so the compiler keeps it in the shared window
     uint8_t *smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -263,7 +267,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < US; ++s) {
-            tc::mbar_init(&full[s], AQ ? 1 + AQ_WARPS : 1);  // producer expect_tx (+ the quantizer warps)
+            tc::mbar_init(&full[s], AQ ? 2 : 1);  // producer expect_tx (+ the fill's quantizer warp)
             tc::mbar_init(&empty[s], 1);  // tcgen05.commit after the slot's last MMAs
         }
         for (int s = 0; s < SFQ; ++s) {
@@ -524,69 +528,61 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 
         }
     } else if (AQ && warp >= AQ_WARP0) {
-        // ------------------------------------------------------------ activation quantizers (11-14)
-        // With the activation quant fused in, these four warps write each ring fill's activation
-        // tile themselves: the fill's 512 values of each token row are read from L2 two fills
-        // ahead (so no fill waits on an L2 round trip), divided by the token's scale and rounded to
-        // e4m3 (the code of w4a8_act_quant), and stored at the places the 128-byte-swizzled TMA
-        // box would use.
+        // ------------------------------------------------------------ activation quantizers (11-13)
+        // With the activation quant fused in, these warps write each ring fill's activation tile
+        // themselves.  Warp q owns ring slot q and so takes fills q, q + US, ...: it waits on that
+        // slot's barriers in phase order (a parity wait is only exact one phase ahead), reads its
+        // next fill's values from L2 as soon as it has written one, US fills ahead, and when the
+        // slot frees it divides them by the token's scale, rounds to e4m3 (the code of
+        // w4a8_act_quant) and stores them where the 128-byte-swizzled TMA box would put them.
         float *aq_s = reinterpret_cast<float *>(smem + L::AQ_OFF);
+        const int qw = warp - AQ_WARP0;
         const int qt = threadIdx.x - AQ_WARP0 * 32;  // 0 .. AQ_THREADS - 1
-        // every slot's activation tile starts as zeros; rows >= M are never written again
-        for (int o = qt; o < US * L::X_SLOT / 16; o += AQ_THREADS)
-            reinterpret_cast<uint4 *>(smem + L::X_OFF)[o] = make_uint4(0u, 0u, 0u, 0u);
-        aq_row_scales(p.x, p.M, p.K, 128 + qt, aq_s, reinterpret_cast<unsigned *>(aq_s + BN));
-        constexpr int PER_ROW = KPU * 16;                       // 8-value chunks of a row in one fill
-        constexpr int MAX_IT = (AQ_MAX_M * PER_ROW + AQ_THREADS - 1) / AQ_THREADS;  // chunks per thread and fill
-        constexpr int DEPTH = 3;                                // fills whose values are in flight
+        constexpr int PER_ROW = KPU * 16;                // 8-value chunks of a row in one fill
+        constexpr int MAX_IT = AQ_MAX_M * PER_ROW / 32;  // chunks per lane and fill
         const int items = p.M * PER_ROW;
         const int n_f = n_k / KPU;
-        uint4 v[DEPTH][MAX_IT];
-        auto load_fill = [&](int f, uint4 (&dst)[MAX_IT]) {
+        uint4 v[MAX_IT];
+        auto load_fill = [&](int f) {
             int kt, n0;
             sched.fill_at(f * KPU, p.m_tiles, kt, n0);
             const int k0 = kt * 128;  // the fill covers k0 .. k0 + 128 * KPU - 1
 #pragma unroll
             for (int j = 0; j < MAX_IT; ++j) {
-                const int it = qt + AQ_THREADS * j;
+                const int it = lane + 32 * j;
                 if (it < items) {
                     const int m = it / PER_ROW, c8 = it - m * PER_ROW;
-                    dst[j] = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)m * p.K + k0 + c8 * 8));
+                    v[j] = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)m * p.K + k0 + c8 * 8));
                 }
             }
         };
+        if (qw < n_f) load_fill(qw);  // in flight during the amax step
+        // every slot's activation tile starts as zeros; rows >= M are never written again
+        for (int o = qt; o < US * L::X_SLOT / 16; o += AQ_THREADS)
+            reinterpret_cast<uint4 *>(smem + L::X_OFF)[o] = make_uint4(0u, 0u, 0u, 0u);
+        aq_row_scales<8>(p.x, p.M, p.K, 128 + qt, aq_s, reinterpret_cast<unsigned *>(aq_s + BN));
+        for (int f = qw; f < n_f; f += AQ_WARPS) {
+            const int sl = f % US;
+            if (warp_wait(&empty[sl], ((f / US) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_AQ, f, lane)) break;
+            if (lane == 0) trace_ev(p, TR_AQ_SLOT, f);
+            uint8_t *slot = smem + L::X_OFF + sl * L::X_SLOT;
 #pragma unroll
-        for (int st = 0; st < DEPTH - 1; ++st)
-            if (st < n_f) load_fill(st, v[st]);
-        bool gave_up = false;
-        for (int f0 = 0; f0 < n_f && !gave_up; f0 += DEPTH) {
-            // unrolled over the stages so every register index is a constant
-#pragma unroll
-            for (int st = 0; st < DEPTH; ++st) {
-                const int f = f0 + st;
-                if (f >= n_f || gave_up) break;
-                if (f + DEPTH - 1 < n_f) load_fill(f + DEPTH - 1, v[(st + DEPTH - 1) % DEPTH]);
-                const int sl = f % US;
-                if (warp_wait(&empty[sl], ((f / US) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_AQ, f, lane)) {
-                    gave_up = true;
-                    break;
+            for (int j = 0; j < MAX_IT; ++j) {
+                const int it = lane + 32 * j;
+                if (it < items) {
+                    const int m = it / PER_ROW, c8 = it - m * PER_ROW;
+                    const int kb = (c8 & 15) * 8;  // byte of the k-tile row: chunk kb / 16, half kb & 8
+                    *reinterpret_cast<uint2 *>(slot + (c8 >> 4) * L::X_TILE + m * 128 +
+                                               ((((kb >> 4) ^ (m & 7)) << 4) | (kb & 8))) = quant8_e4m3(v[j], aq_s[m]);
                 }
-                uint8_t *slot = smem + L::X_OFF + sl * L::X_SLOT;
-#pragma unroll
-                for (int j = 0; j < MAX_IT; ++j) {
-                    const int it = qt + AQ_THREADS * j;
-                    if (it < items) {
-                        const int m = it / PER_ROW, c8 = it - m * PER_ROW;
-                        const int kb = (c8 & 15) * 8;  // byte of the k-tile row: chunk kb / 16, half kb & 8
-                        *reinterpret_cast<uint2 *>(slot + (c8 >> 4) * L::X_TILE + m * 128 +
-                                                   ((((kb >> 4) ^ (m & 7)) << 4) | (kb & 8))) =
-                            quant8_e4m3(v[st][j], aq_s[m]);
-                    }
-                }
-                tc::fence_proxy_async_smem();  // generic writes -> visible to the tensor core
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&full[sl]);
             }
+            tc::fence_proxy_async_smem();  // generic writes -> visible to the tensor core
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(&full[sl]);
+                trace_ev(p, TR_AQ_DONE, f);
+            }
+            if (f + AQ_WARPS < n_f) load_fill(f + AQ_WARPS);
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -596,7 +592,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         const bool issuer = (threadIdx.x == EPI_WARP0 * 32);
         int ck = 0;  // output chunks emitted (staging buffer rotation)
         if constexpr (AQ)  // the token scales, with the quantizer warps (before any tile is done)
-            aq_row_scales(p.x, p.M, p.K, threadIdx.x - EPI_WARP0 * 32, reinterpret_cast<float *>(smem + L::AQ_OFF),
+            aq_row_scales<16>(p.x, p.M, p.K, threadIdx.x - EPI_WARP0 * 32, reinterpret_cast<float *>(smem + L::AQ_OFF),
                           reinterpret_cast<unsigned *>(smem + L::AQ_OFF) + BN);
         // Write 16 token columns (c0..c0+15 of the tile at m0, n0) of this thread's weight row.
         // With TMA stores the 128 threads stage a [16 tokens][128 rows] bf16 block in shared memory

@@ -32,6 +32,9 @@ def main(argv=None) -> int:
     ap.add_argument("--int5", action="store_true", help="the int5 g128 GEMM (zero point 16) instead of MXFP4")
     ap.add_argument("--w4a4", action="store_true", help="MXFP4 activations (W4A4) instead of fp8 ones")
     ap.add_argument("--act-quant", action="store_true", help="only the per-token activation quant")
+    ap.add_argument("--fused", action="store_true",
+                    help="the whole linear from bf16 x (w4a8_mxfp4_linear_bf16; up to 8 tokens the quant runs "
+                         "inside the GEMM)")
     ap.add_argument("--requant", choices=["ocp", "noclip", "mse"], help="only the NVFP4 -> MXFP4 requant")
     args = ap.parse_args(argv)
     M, N, K = args.m, args.n, args.k
@@ -70,6 +73,12 @@ def main(argv=None) -> int:
         ws = lib.make_workspace(lib.workspace_bytes(M, N, K), dev)
         for _ in range(args.calls):
             lib.mxfp4_a4_linear(xa, xe, wd, ed, out=out, workspace=ws)
+    elif args.fused:
+        w, e = synth.mxfp4_weights(N, K, 0, 118, 121)
+        wd, ed = torch.from_numpy(w).to(dev), torch.from_numpy(e).to(dev)
+        lws = lib.make_linear_workspace(M, N, K, dev)
+        for _ in range(args.calls):
+            lib.linear(x.view(torch.bfloat16), wd, ed, out=out, workspace=lws)
     elif args.int4:
         qw, sc, _ = synth.int4_weights(N, K, 0)
         qd = torch.from_numpy(qw).to(dev)
@@ -86,7 +95,7 @@ def main(argv=None) -> int:
             lib.mxfp4_linear(xq, xs, wd, ed, out=out, workspace=ws)
     torch.cuda.synchronize()
     lib.check_device_status()
-    kind = "int5" if args.int5 else "w4a4" if args.w4a4 else "int4" if args.int4 else "mxfp4"
+    kind = "int5" if args.int5 else "w4a4" if args.w4a4 else "int4" if args.int4 else "fused" if args.fused else "mxfp4"
     print(f"ok {kind} M={M} N={N} K={K} calls={args.calls}")
     return 0
 

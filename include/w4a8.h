@@ -109,6 +109,25 @@ W4A8_API w4a8_status w4a8_mxfp4_linear_bf16(const uint16_t *x_bf16, const uint8_
 /* Bytes of workspace w4a8_mxfp4_linear_bf16 needs for this shape. */
 W4A8_API size_t w4a8_mxfp4_linear_bf16_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
+/* The same linear as w4a8_mxfp4_linear_bf16 in ONE kernel launch, for one or two tokens: every
+ * CTA of the GEMM reads the rows' bf16 activations, takes their per-token amax and writes the e4m3
+ * tiles of its own K range straight into shared memory, so no quantized copy of x goes through
+ * HBM.  The result is bit-identical to w4a8_mxfp4_linear_bf16.  Arguments, alignment and
+ * workspace (size, layout and zero-counter contract) are those of w4a8_mxfp4_linear_bf16; the
+ * activation part of the workspace is left untouched.
+ * Takes 1 <= M <= 2, M*K*2 bytes of activations at most 96 KiB, and the shapes the tensor-core
+ * MXFP4 kernel takes (K % 512 == 0, the alignments of w4a8_mxfp4_linear); anything else returns
+ * W4A8_ERR_UNSUPPORTED_SHAPE (M == 0 or N == 0 returns W4A8_OK).  It ignores
+ * w4a8_set_gemm_policy.
+ * On the measured GB300 this form is SLOWER than the two-kernel chain behind
+ * w4a8_mxfp4_linear_bf16 (about 30 us against 25 us for one token through a 34816 x 5120 weight), because
+ * each CTA repeats the amax pass over x and quantizes on its scale-staging warps; it is offered
+ * for callers that count launches (e.g. a launch-limited graph), not as the fast path. */
+W4A8_API w4a8_status w4a8_mxfp4_linear_bf16_single(const uint16_t *x_bf16, const uint8_t *w_packed,
+                                                   const uint8_t *w_e8m0, uint16_t *out_bf16, int64_t M,
+                                                   int64_t N, int64_t K, void *workspace,
+                                                   size_t workspace_bytes, cudaStream_t stream);
+
 /* w4a8_mxfp4_linear for callers that cannot allocate device memory.  The pages have no
  * counterpart; this is an addition of this library.  The regular entry point needs a
  * caller-provided workspace.  Some callers cannot provide one: serving engines that reserve all

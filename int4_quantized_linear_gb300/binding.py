@@ -28,6 +28,7 @@ EXPORTS = ("w4a8_act_quant", "w4a8_mxfp4_linear", "w4a8_workspace_bytes",
            "w4a8_decode_max_m", "w4a8_debug_status_words",
            "w4a8_mxfp4_linear_noalloc", "w4a8_noalloc_scratch_bytes",
            "w4a8_mxfp4_linear_bf16", "w4a8_mxfp4_linear_bf16_workspace_bytes",
+           "w4a8_mxfp4_linear_bf16_single",
            "w4a8_mxfp4_path", "w4a8_int4g128_path", "w4a8_int5g128_path", "w4a4_mxfp4_path")
 
 
@@ -76,6 +77,7 @@ def load(build_if_missing: bool = True):
         "w4a8_noalloc_scratch_bytes": (SZ, []),
         "w4a8_mxfp4_linear_bf16": (I, [P, P, P, P, I64, I64, I64, P, SZ, P]),
         "w4a8_mxfp4_linear_bf16_workspace_bytes": (SZ, [I64, I64, I64]),
+        "w4a8_mxfp4_linear_bf16_single": (I, [P, P, P, P, I64, I64, I64, P, SZ, P]),
         "w4a8_mxfp4_path": (I, [P, P, P, P, I64, I64, I64]),
         "w4a8_int4g128_path": (I, [P, P, P, P, I64, I64, I64]),
         "w4a8_int5g128_path": (I, [P, P, P, P, P, I64, I64, I64]),
@@ -434,9 +436,11 @@ def make_linear_workspace(M: int, N: int, K: int, device) -> torch.Tensor:
 
 
 def linear(x: torch.Tensor, w_packed: torch.Tensor, w_e8m0: torch.Tensor, out=None,
-           workspace=None, stream=None) -> torch.Tensor:
+           workspace=None, stream=None, single_kernel: bool = False) -> torch.Tensor:
     """The whole W4A8 MXFP4 linear from bf16 activations in one native call: per-token fp8
-    activation quant, then the GEMM (w4a8_mxfp4_linear_bf16)."""
+    activation quant, then the GEMM (w4a8_mxfp4_linear_bf16).  single_kernel=True runs it as one
+    launch with the quant inside the GEMM (w4a8_mxfp4_linear_bf16_single: 1 or 2 tokens, same
+    bytes, slower than the default two-kernel chain on GB300)."""
     _dev(x, "x", torch.bfloat16)
     _dev(w_packed, "w_packed", torch.uint8)
     _dev(w_e8m0, "w_e8m0", torch.uint8)
@@ -449,7 +453,8 @@ def linear(x: torch.Tensor, w_packed: torch.Tensor, w_e8m0: torch.Tensor, out=No
     if workspace is None:
         workspace = make_linear_workspace(M, N, K, x.device)
     wsb = workspace.numel() * workspace.element_size()
-    _check("w4a8_mxfp4_linear_bf16", load().w4a8_mxfp4_linear_bf16(
+    fn = "w4a8_mxfp4_linear_bf16_single" if single_kernel else "w4a8_mxfp4_linear_bf16"
+    _check(fn, getattr(load(), fn)(
         _ptr(x), _ptr(w_packed), _ptr(w_e8m0), _ptr(out), M, N, K, _ptr(workspace), wsb,
         _stream(stream)))
     return out

@@ -193,12 +193,6 @@ extern "C" w4a8_status w4a8_mxfp4_linear_bf16(const uint16_t *x_bf16, const uint
     const size_t gws_bytes = workspace_bytes - (size_t)(gws - xq);
 
     const int policy = w4a8_gemm_policy();
-    // a few tokens: one kernel, the activation quant fused into the GEMM's prologue
-    if (policy != 1 && w4a8_tc_mxfp4_aq_takes(M, K) &&
-        w4a8_tc_mxfp4_supported(x_bf16, w_packed, w_e8m0, out_bf16, M, N, K)) {
-        if (w4a8_tc_workspace_bytes(M, N, K) > gws_bytes) return W4A8_ERR_WORKSPACE;
-        return w4a8_launch_mxfp4_tc_aq(x_bf16, w_packed, w_e8m0, out_bf16, M, N, K, gws, stream);
-    }
     w4a8_status st = w4a8_launch_act_quant(x_bf16, xq, xs, M, K, stream);
     if (st != W4A8_OK) return st;
     if (policy != 1 && w4a8_tc_mxfp4_supported(xq, w_packed, w_e8m0, out_bf16, M, N, K)) {
@@ -208,6 +202,27 @@ extern "C" w4a8_status w4a8_mxfp4_linear_bf16(const uint16_t *x_bf16, const uint
         return w4a8_launch_mxfp4_tc(xq, xs, w_packed, w_e8m0, out_bf16, M, N, K, gws, policy, true, stream);
     }
     return w4a8_launch_mxfp4_simt(xq, xs, w_packed, w_e8m0, out_bf16, M, N, K, stream);
+}
+
+// The same linear as one kernel: the GEMM quantizes the activations itself.  Same arguments and
+// workspace layout as w4a8_mxfp4_linear_bf16; only the GEMM-scratch part of the workspace is used.
+extern "C" w4a8_status w4a8_mxfp4_linear_bf16_single(const uint16_t *x_bf16, const uint8_t *w_packed,
+                                                     const uint8_t *w_e8m0, uint16_t *out_bf16, int64_t M,
+                                                     int64_t N, int64_t K, void *workspace,
+                                                     size_t workspace_bytes, cudaStream_t stream)
+{
+    if (M < 0 || N < 0 || K < 0) return W4A8_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return W4A8_OK;
+    if (K == 0 || !x_bf16 || !w_packed || !w_e8m0 || !out_bf16) return W4A8_ERR_INVALID_ARG;
+    if (K % 32 != 0 || !w4a8_tc_mxfp4_aq_takes(M, K)) return W4A8_ERR_UNSUPPORTED_SHAPE;
+    if (!w4a8_aligned(x_bf16, 16) || !w4a8_aligned(w_packed, 16) || !w4a8_aligned(out_bf16, 2))
+        return W4A8_ERR_MISALIGNED;
+    if (!w4a8_tc_mxfp4_supported(x_bf16, w_packed, w_e8m0, out_bf16, M, N, K)) return W4A8_ERR_UNSUPPORTED_SHAPE;
+    const size_t need = w4a8_mxfp4_linear_bf16_workspace_bytes(M, N, K);
+    if (!workspace || workspace_bytes < need) return W4A8_ERR_WORKSPACE;
+    if (!w4a8_aligned(workspace, 256)) return W4A8_ERR_MISALIGNED;
+    uint8_t *gws = static_cast<uint8_t *>(workspace) + round256((size_t)M * (size_t)K) + round256((size_t)M * 4);
+    return w4a8_launch_mxfp4_tc_aq(x_bf16, w_packed, w_e8m0, out_bf16, M, N, K, gws, stream);
 }
 
 static w4a8_status int4g128_linear_impl(const uint8_t *xq, const float *x_scale, const int32_t *qweight,

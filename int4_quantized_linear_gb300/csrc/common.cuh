@@ -40,12 +40,20 @@ W4A8_DEVICE uint2 quant8_e4m3(const uint4 &w, float s)
     const uint32_t h[4] = {w.x, w.y, w.z, w.w};
     uint32_t q[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float lo = __fdiv_rn(__uint_as_float(h[j] << 16), s);
-        const float hi = __fdiv_rn(__uint_as_float(h[j] & 0xffff0000u), s);
-        q[j] = float2_to_e4m3x2(lo, hi);
-    }
+    for (int j = 0; j < 4; ++j)
+        q[j] = float2_to_e4m3x2(__fdiv_rn(__uint_as_float(h[j] << 16), s),
+                                __fdiv_rn(__uint_as_float(h[j] & 0xffff0000u), s));
     return make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+}
+
+// The same for four bf16 activations (8 bytes) -> four e4m3 codes, low byte first.
+W4A8_DEVICE uint32_t quant4_e4m3(const uint2 &w, float s)
+{
+    const uint32_t lo = float2_to_e4m3x2(__fdiv_rn(__uint_as_float(w.x << 16), s),
+                                         __fdiv_rn(__uint_as_float(w.x & 0xffff0000u), s));
+    const uint32_t hi = float2_to_e4m3x2(__fdiv_rn(__uint_as_float(w.y << 16), s),
+                                         __fdiv_rn(__uint_as_float(w.y & 0xffff0000u), s));
+    return lo | (hi << 16);
 }
 
 // Two e2m1 codes in one byte (low nibble = first element) -> two fp32 values, exact.

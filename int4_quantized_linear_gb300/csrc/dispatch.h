@@ -43,9 +43,9 @@ w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const 
                                  int64_t K, void *workspace, int policy, bool w_early,
                                  cudaStream_t stream);
 // The MXFP4 GEMM with the per-token activation quant fused in (the 16-token decode tiling, M up
-// to 8, rows of at most W4A8_FUSED_AQ_MAX_X_BYTES of bf16 in all): every CTA takes the row amax
+// to 2, rows of at most W4A8_FUSED_AQ_MAX_X_BYTES of bf16 in all): every CTA takes the row amax
 // from L2 and quantizes its own fills' activations into shared memory; bit-identical to the
-// activation-quant kernel followed by the GEMM.
+// activation-quant kernel followed by the GEMM.  Only w4a8_mxfp4_linear_bf16_single runs it.
 #ifndef W4A8_FUSED_AQ_MAX_X_BYTES
 #define W4A8_FUSED_AQ_MAX_X_BYTES (96u << 10)
 #endif

@@ -68,9 +68,6 @@ struct Depth {
     static constexpr int NA = I5 ? 2 : 3;
 };
 static_assert(ND >= US * XK && ND >= 3 && ND >= NB, "completion barriers");
-#ifndef W4A8_PF_TMA_STORE
-#define W4A8_PF_TMA_STORE 1
-#endif
 constexpr int GATE_BARRIER = 2;   // gate warp + MMA warp
 constexpr int EPI_BARRIER = 3;    // the eight promotion warps
 constexpr int HALF_BARRIER0 = 4;  // 4 and 5: the four warps of one token half
@@ -605,7 +602,7 @@ static w4a8_status launch(const uint8_t *xq, Params prm, cudaStream_t stream)
         (I5 && !tch::tmap_2d(&th, CU_TENSOR_MAP_DATA_TYPE_UINT8, prm.qh, prm.K / 8, prm.N, (uint64_t)prm.N, 16, BM,
                              CU_TENSOR_MAP_SWIZZLE_NONE)))
         return W4A8_ERR_CUDA;
-    prm.tma_out = W4A8_PF_TMA_STORE && (prm.N % 8 == 0) && w4a8_aligned(prm.out, 16) &&
+    prm.tma_out = (prm.N % 8 == 0) && w4a8_aligned(prm.out, 16) &&
                   tch::tmap_2d(&tout, CU_TENSOR_MAP_DATA_TYPE_UINT16, prm.out, prm.M, prm.N, (uint64_t)prm.N * 2, 16,
                                BM, CU_TENSOR_MAP_SWIZZLE_NONE);
     // activations as [k-tile][token][128 bytes], XK k-tiles of 256 tokens per box

@@ -67,15 +67,12 @@ namespace tcg {
 using namespace tcs;
 
 constexpr int NUM_THREADS = 352;   // 11 warps
-// With the activation quant fused in (AQ): one more warp per ring slot (11-13) writes each ring
-// fill's activation tile into shared memory, so the kernel has 14.
-constexpr int AQ_WARP0 = 11;
-constexpr int AQ_WARPS = 3;        // = the ring slots of the 16-token tiling
-constexpr int AQ_THREADS = 32 * AQ_WARPS;
-constexpr int AQ_BARRIER = 3;      // named barrier of the row-amax step (quantizer + epilogue warps)
-constexpr int AQ_STEP_THREADS = AQ_THREADS + 128;
-template <bool AQ>
-constexpr int num_threads() { return AQ ? NUM_THREADS + AQ_THREADS : NUM_THREADS; }
+// With the activation quant fused in (AQ) the four scale warps also write each ring fill's
+// activation codes: no extra warps, so the kernel keeps 168 registers per thread (more warps would
+// cut that to 128 and spill; with shared memory taking nearly all of the L1 array, every spill
+// reload is an L2 round trip).
+constexpr int AQ_BARRIER = 3;         // named barrier of the row-amax step (scale + epilogue warps)
+constexpr int AQ_STEP_THREADS = 256;
 constexpr int SCALE_WARP0 = 2;     // warps 2-5
 constexpr int EPI_WARP0 = 6;       // warps 6-9
 constexpr int GATE_WARP = 10;
@@ -83,7 +80,7 @@ constexpr int GATE_BARRIER = 2;    // named barrier shared by the gate warp and 
 
 enum : unsigned { ST_TIMEOUT_PRODUCER = 1, ST_TIMEOUT_GATE = 2, ST_TIMEOUT_SCALE = 4, ST_TIMEOUT_EPI = 8,
                   ST_TIMEOUT_AQ = 16 };
-constexpr int AQ_MAX_M = 8;        // tokens the fused activation quant takes (one 8-item batch per fill)
+constexpr int AQ_MAX_M = 2;        // tokens the fused activation quant takes (4 values per token and scale-warp thread)
 
 struct Params {
     const uint8_t *wp;     // [N, K/2] packed e2m1 codes
@@ -230,15 +227,14 @@ struct Layout {
 };
 
 template <int BN, int KPU, int US, int ACC_BUFS, int SFQ, int SFR, bool A4, bool AQ>
-__global__ void __launch_bounds__(num_threads<AQ>(), 1)
+__global__ void __launch_bounds__(NUM_THREADS, 1)
 mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_sf, const __grid_constant__ CUtensorMap tmap_out,
                 const __grid_constant__ CUtensorMap tmap_sfb, const Params p)
 {
     using L = Layout<BN, KPU, US, ACC_BUFS, SFQ, SFR, A4, AQ>;
     static_assert(!(AQ && (A4 || BN != 16)), "the fused activation quant serves the 16-token decode tiling");
-    // each quantizer warp owns one ring slot, so it waits on that slot's barriers in phase order
-    static_assert(!AQ || US == AQ_WARPS, "one quantizer warp per ring slot");
+    static_assert(!AQ || KPU * 128 / 4 == 128, "one 4-value chunk per token, scale-warp thread and fill");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, derived by pointer arithmetic so the compiler keeps it in the shared window
     uint8_t *smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -267,7 +263,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < US; ++s) {
-            tc::mbar_init(&full[s], AQ ? 2 : 1);  // producer expect_tx (+ the fill's quantizer warp)
+            tc::mbar_init(&full[s], AQ ? 5 : 1);  // producer expect_tx (+ the four scale warps)
             tc::mbar_init(&empty[s], 1);  // tcgen05.commit after the slot's last MMAs
         }
         for (int s = 0; s < SFQ; ++s) {
@@ -471,6 +467,43 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
         // need not have arrived, so this work stays off the path from TMA to MMA.
         const int q = warp & 3;
         const int row = 32 * q + lane;
+        // Fused activation quant: thread st_t owns 4-value chunk st_t of every fill (the fill's k
+        // offsets 4 st_t .. 4 st_t + 3) for each token.  It loads fill f + 2's values and rounds
+        // fill f + 1's to e4m3 (the code of w4a8_act_quant) right after finishing fill f, so when
+        // fill f + 1's slot frees only the stores are left; the codes go where the
+        // 128-byte-swizzled TMA box would put them.
+        const int st_t = threadIdx.x - SCALE_WARP0 * 32;  // 0..127
+        const int aq_kb = (st_t & 31) * 4;                // byte of the k-tile row
+        float *aq_s = reinterpret_cast<float *>(smem + L::AQ_OFF);
+        uint2 v_next[AQ_MAX_M];
+        uint32_t qc[AQ_MAX_M];
+#pragma unroll
+        for (int m = 0; m < AQ_MAX_M; ++m) {
+            v_next[m] = make_uint2(0u, 0u);
+            qc[m] = 0u;
+        }
+        auto load_fill = [&](int f, uint2 (&dst)[AQ_MAX_M]) {
+            if (f < n_k / KPU) {
+                int kt, n0;
+                sched.fill_at(f * KPU, p.m_tiles, kt, n0);
+#pragma unroll
+                for (int m = 0; m < AQ_MAX_M; ++m)
+                    if (m < p.M)
+                        dst[m] = __ldg(reinterpret_cast<const uint2 *>(p.x + (size_t)m * p.K + kt * 128 + st_t * 4));
+            }
+        };
+        if constexpr (AQ) {
+            uint2 v0[AQ_MAX_M];
+            load_fill(0, v0);  // in flight during the amax step
+            load_fill(1, v_next);
+            // every slot's activation tile starts as zeros; rows >= M are never written again
+            for (int o = st_t; o < US * L::X_SLOT / 16; o += 128)
+                reinterpret_cast<uint4 *>(smem + L::X_OFF)[o] = make_uint4(0u, 0u, 0u, 0u);
+            aq_row_scales<8>(p.x, p.M, p.K, 128 + st_t, aq_s, reinterpret_cast<unsigned *>(aq_s + BN));
+#pragma unroll
+            for (int m = 0; m < AQ_MAX_M; ++m)
+                if (m < p.M) qc[m] = quant4_e4m3(v0[m], aq_s[m]);
+        }
         int w = 0;
         for (int i = 0; i < n_k && !w; i += KPU) {
             const int g = i >> 2, rs = g % SFR;
@@ -507,13 +540,24 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                     if constexpr (L::SFBW == 8) tc::tmem_st4(ta + 4, v[4], v[5], v[6], v[7]);
                 }
             }
+            if constexpr (AQ) {
+                uint8_t *xt = smem + L::X_OFF + (f % US) * L::X_SLOT + (st_t >> 5) * L::X_TILE;  // k-tile st_t / 32
+#pragma unroll
+                for (int m = 0; m < AQ_MAX_M; ++m)
+                    if (m < p.M)
+                        *reinterpret_cast<uint32_t *>(xt + m * 128 + ((((aq_kb >> 4) ^ (m & 7)) << 4) | (aq_kb & 15))) =
+                            qc[m];
+                tc::fence_proxy_async_smem();  // generic writes -> visible to the tensor core
+            }
             tc::tmem_st_wait();
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 tc::mbar_arrive(&sff[sq]);
+                if (AQ) tc::mbar_arrive(&full[f % US]);
                 if (((i + KPU) & 3) == 0) tc::mbar_arrive(&sfr_empty[rs]);
                 if (warp == SCALE_WARP0) trace_ev(p, TR_SCALE_DONE, f);
+                if (AQ && warp == SCALE_WARP0) trace_ev(p, TR_AQ_DONE, f);
             }
             // the unit's raw tile is consumed by all four warps: one thread loads unit g + SFR's
             // tile into the same slot, so scale loads never hold up the producer's data loads
@@ -525,64 +569,14 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 }
             }
             w = __shfl_sync(0xffffffffu, w, 0);
-
-        }
-    } else if (AQ && warp >= AQ_WARP0) {
-        // ------------------------------------------------------------ activation quantizers (11-13)
-        // With the activation quant fused in, these warps write each ring fill's activation tile
-        // themselves.  Warp q owns ring slot q and so takes fills q, q + US, ...: it waits on that
-        // slot's barriers in phase order (a parity wait is only exact one phase ahead), reads its
-        // next fill's values from L2 as soon as it has written one, US fills ahead, and when the
-        // slot frees it divides them by the token's scale, rounds to e4m3 (the code of
-        // w4a8_act_quant) and stores them where the 128-byte-swizzled TMA box would put them.
-        float *aq_s = reinterpret_cast<float *>(smem + L::AQ_OFF);
-        const int qw = warp - AQ_WARP0;
-        const int qt = threadIdx.x - AQ_WARP0 * 32;  // 0 .. AQ_THREADS - 1
-        constexpr int PER_ROW = KPU * 16;                // 8-value chunks of a row in one fill
-        constexpr int MAX_IT = AQ_MAX_M * PER_ROW / 32;  // chunks per lane and fill
-        const int items = p.M * PER_ROW;
-        const int n_f = n_k / KPU;
-        uint4 v[MAX_IT];
-        auto load_fill = [&](int f) {
-            int kt, n0;
-            sched.fill_at(f * KPU, p.m_tiles, kt, n0);
-            const int k0 = kt * 128;  // the fill covers k0 .. k0 + 128 * KPU - 1
+            if constexpr (AQ) {  // the next fill's codes, and the values of the one after
+                if (f + 1 < n_k / KPU) {
 #pragma unroll
-            for (int j = 0; j < MAX_IT; ++j) {
-                const int it = lane + 32 * j;
-                if (it < items) {
-                    const int m = it / PER_ROW, c8 = it - m * PER_ROW;
-                    v[j] = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)m * p.K + k0 + c8 * 8));
+                    for (int m = 0; m < AQ_MAX_M; ++m)
+                        if (m < p.M) qc[m] = quant4_e4m3(v_next[m], aq_s[m]);
                 }
+                load_fill(f + 2, v_next);
             }
-        };
-        if (qw < n_f) load_fill(qw);  // in flight during the amax step
-        // every slot's activation tile starts as zeros; rows >= M are never written again
-        for (int o = qt; o < US * L::X_SLOT / 16; o += AQ_THREADS)
-            reinterpret_cast<uint4 *>(smem + L::X_OFF)[o] = make_uint4(0u, 0u, 0u, 0u);
-        aq_row_scales<8>(p.x, p.M, p.K, 128 + qt, aq_s, reinterpret_cast<unsigned *>(aq_s + BN));
-        for (int f = qw; f < n_f; f += AQ_WARPS) {
-            const int sl = f % US;
-            if (warp_wait(&empty[sl], ((f / US) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_AQ, f, lane)) break;
-            if (lane == 0) trace_ev(p, TR_AQ_SLOT, f);
-            uint8_t *slot = smem + L::X_OFF + sl * L::X_SLOT;
-#pragma unroll
-            for (int j = 0; j < MAX_IT; ++j) {
-                const int it = lane + 32 * j;
-                if (it < items) {
-                    const int m = it / PER_ROW, c8 = it - m * PER_ROW;
-                    const int kb = (c8 & 15) * 8;  // byte of the k-tile row: chunk kb / 16, half kb & 8
-                    *reinterpret_cast<uint2 *>(slot + (c8 >> 4) * L::X_TILE + m * 128 +
-                                               ((((kb >> 4) ^ (m & 7)) << 4) | (kb & 8))) = quant8_e4m3(v[j], aq_s[m]);
-                }
-            }
-            tc::fence_proxy_async_smem();  // generic writes -> visible to the tensor core
-            __syncwarp();
-            if (lane == 0) {
-                tc::mbar_arrive(&full[sl]);
-                trace_ev(p, TR_AQ_DONE, f);
-            }
-            if (f + AQ_WARPS < n_f) load_fill(f + AQ_WARPS);
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -881,7 +875,7 @@ w4a8_status launch(const uint8_t *wp, const uint8_t *xq, Params prm, cudaStream_
     if (!tch::set_smem_once(kern, L::TOTAL, attr_done)) return W4A8_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(prm.G);
-    cfg.blockDim = dim3(num_threads<AQ>());
+    cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = L::TOTAL;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -84,6 +84,13 @@ def test_host_validation_without_gpu(clib):
     assert clib.w4a4_mxfp4_linear(fake, NULL, fake, fake, fake, 2, 8, 64, NULL, 0, NULL) == 1
     assert clib.w4a4_mxfp4_linear(odd, fake, fake, fake, fake, 2, 8, 64, NULL, 0, NULL) == 3
     assert clib.w4a8_int5g128_workspace_bytes(0, 8, 128) == 0
+    # the one-launch bf16 linear: 1 or 2 tokens only, same pointer and alignment checks
+    single = clib.w4a8_mxfp4_linear_bf16_single
+    assert single(fake, fake, fake, fake, 3, 8, 512, fake, 1 << 20, NULL) == 2
+    assert single(fake, fake, fake, fake, 1, 8, 49152 + 512, fake, 1 << 20, NULL) == 2
+    assert single(odd, fake, fake, fake, 1, 8, 512, fake, 1 << 20, NULL) == 3
+    assert single(NULL, fake, fake, fake, 1, 8, 512, fake, 1 << 20, NULL) == 1
+    assert single(NULL, NULL, NULL, NULL, 0, 8, 512, NULL, 0, NULL) == 0
 
 
 def test_symmetric_zero_point_check():

@@ -367,30 +367,48 @@ def test_linear_fused_matches_two_calls(lib, orc, policy, M, N, K):
     gemm_check(bf16_to_f64(fused), orc.mxfp4_linear(host(xq), host(xs), w, e), f"fused M={M} N={N} K={K}")
 
 
-# Up to 8 tokens (and at most 96 KB of bf16 activations) the quant runs inside the GEMM: every
-# CTA takes the rows' amax from L2 and writes its fills' e4m3 tiles into shared memory itself.
-@pytest.mark.parametrize("M,N,K", [(1, 520, 512), (2, 256, 1024), (3, 1000, 2048), (5, 4096, 5120),
-                                   (8, 384, 5120), (4, 256, 10240), (1, 5120, 17408),
-                                   # past the activation-size limit: the two-kernel chain again
-                                   (8, 512, 17408)])
+# The one-launch form (w4a8_mxfp4_linear_bf16_single): every CTA takes the rows' amax from L2 and
+# writes its fills' e4m3 tiles into shared memory itself.  It must give the bytes of the two-kernel
+# chain, for 1 or 2 tokens and up to 96 KB of bf16 activations; past that it refuses the shape.
+@pytest.mark.parametrize("M,N,K", [(1, 520, 512), (2, 256, 1024), (1, 1000, 2048), (2, 4096, 5120),
+                                   (1, 384, 5120), (2, 256, 10240), (1, 5120, 17408),
+                                   (2, 34816, 5120), (1, 160, 49152)])
 def test_linear_fused_quant_in_gemm(lib, orc, M, N, K):
     x, w, e = synth.decode_case(M, N, K, seed=M * 5 + N)
     x = x.copy()
     x[0, :7] = 0x8000                      # -0 values
-    if M > 2:
-        x[2, :] = 0                        # an all-zero row: scale 1, codes 0
+    if M > 1:
+        x[1, 3::5] = 0                     # zeros inside a row
     xd, wd, ed = to_dev_bf16(x), to_dev(w), to_dev(e)
-    fused = lib.linear(xd, wd, ed)
-    xq, xs = lib.act_quant(xd)
-    two = lib.mxfp4_linear(xq, xs, wd, ed)
+    one = lib.linear(xd, wd, ed, single_kernel=True)
+    two = lib.linear(xd, wd, ed)
     lib.check_device_status()
-    assert torch.equal(fused.view(torch.int16), two.view(torch.int16))
+    assert torch.equal(one.view(torch.int16), two.view(torch.int16))
     hq, hs = orc.act_quant(x)
     im, inn = _sample_pairs(M, N, seed=M)
-    gemm_check(bf16_to_f64(fused)[im, inn], orc.mxfp4_linear_pairs(hq, hs, w, e, im, inn),
-               f"fused quant M={M} N={N} K={K}")
-    if M > 2:
-        assert np.all(bf16_to_f64(fused)[2] == 0.0)
+    gemm_check(bf16_to_f64(one)[im, inn], orc.mxfp4_linear_pairs(hq, hs, w, e, im, inn),
+               f"one-launch linear M={M} N={N} K={K}")
+
+
+def test_linear_single_all_zero_row(lib):
+    """An all-zero token gets scale 1 and zero codes, so its output row is exactly zero."""
+    x, w, e = synth.decode_case(2, 512, 2048, seed=3)
+    x = x.copy()
+    x[1, :] = 0
+    one = lib.linear(to_dev_bf16(x), to_dev(w), to_dev(e), single_kernel=True)
+    lib.check_device_status()
+    assert np.all(bf16_to_f64(one)[1] == 0.0)
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 256, 1024), (1, 256, 1000 * 32), (1, 256, 49152 + 512), (1, 256, 992)])
+def test_linear_single_rejects_shapes(lib, M, N, K):
+    """More than 2 tokens, more than 96 KB of activations, or K not a multiple of 512: refused."""
+    xd = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+    wd = torch.zeros((N, K // 2), dtype=torch.uint8, device="cuda")
+    ed = torch.full((N, K // 32), 127, dtype=torch.uint8, device="cuda")
+    with pytest.raises(lib.W4A8Error) as ei:
+        lib.linear(xd, wd, ed, single_kernel=True)
+    assert ei.value.status == 2
 
 
 @pytest.mark.parametrize("shape", [GATE_UP, DOWN], ids=["gate_up", "down"])

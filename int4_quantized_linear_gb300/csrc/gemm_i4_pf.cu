@@ -105,7 +105,10 @@ struct Params {
 // Pipeline timeline (a development aid, compiled in only when W4A8_TRACE is defined): CTA 0
 // records clock64() per k-tile i < TRACE_N: 0 activations issued, 1 words issued, 2 words seen
 // by the converters, 3 operand tile written, 4 MMAs released by the gate, 5 group accumulator
-// seen by the promotion (warp 8), 6 released by warp 8, 7 released by warp 12.
+// seen by the promotion (warp 8), 6 released by warp 8, 7 released by warp 12, 8-10 the gate past
+// its waits for the group accumulator, the operand tile and the activations (in the order 10, 9, 8),
+// 11 the tile's output issued, 12 the promotion warps done with the tile (warp 8, indexed by the
+// k-tile that ended the tile), 13 warp 8 starting a tile (indexed by its first k-tile).
 constexpr int TRACE_N = 512;
 __device__ __forceinline__ void trace_ev(const Params &p, int ev, int i)
 {
@@ -282,11 +285,17 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             const uint32_t idesc = tc::idesc_f8f6f4(0, 0, BM, BN);
             for (int i = 0; i < n_k; ++i) {
                 const int xf = i / XK, s = xf % US, a = i % NA, b = i % NB;
-                if (gate) {
+                if (gate && lane == 0) {
+                    // the activations and the operand tile are usually ready long before the group
+                    // accumulator comes free, so that wait goes last: once it passes, the MMAs are
+                    // released at once
+                    if (!*abort_flag) wait_or_fail(&x_full[s], (xf / US) & 1, abort_flag, p.status, ST_TIMEOUT_GATE, i);
+                    trace_ev(p, 10, i);
+                    if (!*abort_flag) wait_or_fail(&a_full[a], (i / NA) & 1, abort_flag, p.status, ST_TIMEOUT_GATE, i);
+                    trace_ev(p, 9, i);
                     if (!*abort_flag)
-                        warp_wait(&g_empty[b], ((i / NB) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_GATE, i, lane);
-                    if (!*abort_flag) warp_wait(&a_full[a], (i / NA) & 1, abort_flag, p.status, ST_TIMEOUT_GATE, i, lane);
-                    if (!*abort_flag) warp_wait(&x_full[s], (xf / US) & 1, abort_flag, p.status, ST_TIMEOUT_GATE, i, lane);
+                        wait_or_fail(&g_empty[b], ((i / NB) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_GATE, i);
+                    trace_ev(p, 8, i);
                 }
                 const bool aborted = tc::named_bar_or(GATE_BARRIER, 64, gate && *abort_flag);
                 if (aborted) break;
@@ -416,6 +425,7 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             float acc[128];
 #pragma unroll
             for (int c = 0; c < 128; ++c) acc[c] = 0.0f;
+            if (threadIdx.x == EPI_WARP0 * 32) trace_ev(p, 13, i);
             bool gave_up = false;
             for (const int i_end = i + 4 * (int)(ue - u); i < i_end; ++i) {
                 const int b = i % NB, jj = i & 3;
@@ -455,17 +465,18 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
 #pragma unroll
                 for (int j = 0; j < 32; ++j) acc[64 + j] = fmaf(s, __uint_as_float(va[j]), acc[64 + j]);
                 tc::tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) acc[96 + j] = fmaf(s, __uint_as_float(vb[j]), acc[96 + j]);
                 tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&g_empty[b]);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc[96 + j] = fmaf(s, __uint_as_float(vb[j]), acc[96 + j]);
                 if (threadIdx.x == EPI_WARP0 * 32) trace_ev(p, 6, i);
                 if (threadIdx.x == (EPI_WARP0 + 4) * 32) trace_ev(p, 7, i);
             }
             xs_s[r] = xs_r;
             // all eight warps leave together if any gave up (this also publishes xs_s)
             if (tc::named_bar_or(EPI_BARRIER, 256, gave_up)) break;
+            if (threadIdx.x == EPI_WARP0 * 32) trace_ev(p, 12, i - 1);
             if (whole) {
 #pragma unroll
                 for (int c0 = 0; c0 < 128; c0 += 16) {
@@ -523,6 +534,7 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
                 }
                 tc::named_bar_sync(EPI_BARRIER, 256);  // last_flag is reused by the next tile
             }
+            if (threadIdx.x == EPI_WARP0 * 32) trace_ev(p, 11, i - 1);
         }
         if (issuer) tc::bulk_wait_group_all();  // output stores done before shared memory goes away
     }

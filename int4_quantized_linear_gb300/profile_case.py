@@ -5,7 +5,8 @@
 Builds synthetic inputs of the given shape (the same recipe as the benchmark), runs the
 per-token activation quant once and the MXFP4 GEMM ``--calls`` times on ``cuda:0``, then checks
 the library's device status word; exits non-zero if a bounded wait ran out.  Meant as the
-target of ``ncu -k regex:mxfp4_tc -c <calls>`` (``regex:int4_tc`` with ``--int4`` or ``--int5``;
+target of ``ncu -k regex:mxfp4_tc -c <calls>`` (``regex:int4_tc`` with ``--int4`` or ``--int5`` up to
+128 tokens, ``regex:int4_pf`` above;
 ``--w4a4`` runs the MXFP4-activation path, whose GEMM is also ``mxfp4_tc``): it launches nothing
 else of note.  ``--act-quant`` runs only the per-token activation quant of x [M, K]
 (``regex:act_quant``) and ``--requant MODE`` the NVFP4 -> MXFP4 requant of an [N, K] merged
@@ -33,8 +34,9 @@ def main(argv=None) -> int:
     ap.add_argument("--w4a4", action="store_true", help="MXFP4 activations (W4A4) instead of fp8 ones")
     ap.add_argument("--act-quant", action="store_true", help="only the per-token activation quant")
     ap.add_argument("--fused", action="store_true",
-                    help="the whole linear from bf16 x (w4a8_mxfp4_linear_bf16; up to 8 tokens the quant runs "
-                         "inside the GEMM)")
+                    help="the whole linear from bf16 x (w4a8_mxfp4_linear_bf16: activation quant, then the GEMM)")
+    ap.add_argument("--single", action="store_true",
+                    help="the whole linear from bf16 x as one kernel (w4a8_mxfp4_linear_bf16_single, 1-2 tokens)")
     ap.add_argument("--requant", choices=["ocp", "noclip", "mse"], help="only the NVFP4 -> MXFP4 requant")
     args = ap.parse_args(argv)
     M, N, K = args.m, args.n, args.k
@@ -73,12 +75,12 @@ def main(argv=None) -> int:
         ws = lib.make_workspace(lib.workspace_bytes(M, N, K), dev)
         for _ in range(args.calls):
             lib.mxfp4_a4_linear(xa, xe, wd, ed, out=out, workspace=ws)
-    elif args.fused:
+    elif args.fused or args.single:
         w, e = synth.mxfp4_weights(N, K, 0, 118, 121)
         wd, ed = torch.from_numpy(w).to(dev), torch.from_numpy(e).to(dev)
         lws = lib.make_linear_workspace(M, N, K, dev)
         for _ in range(args.calls):
-            lib.linear(x.view(torch.bfloat16), wd, ed, out=out, workspace=lws)
+            lib.linear(x.view(torch.bfloat16), wd, ed, out=out, workspace=lws, single_kernel=args.single)
     elif args.int4:
         qw, sc, _ = synth.int4_weights(N, K, 0)
         qd = torch.from_numpy(qw).to(dev)
@@ -95,7 +97,7 @@ def main(argv=None) -> int:
             lib.mxfp4_linear(xq, xs, wd, ed, out=out, workspace=ws)
     torch.cuda.synchronize()
     lib.check_device_status()
-    kind = "int5" if args.int5 else "w4a4" if args.w4a4 else "int4" if args.int4 else "fused" if args.fused else "mxfp4"
+    kind = "int5" if args.int5 else "w4a4" if args.w4a4 else "int4" if args.int4 else "single" if args.single else "fused" if args.fused else "mxfp4"
     print(f"ok {kind} M={M} N={N} K={K} calls={args.calls}")
     return 0
 

@@ -512,7 +512,8 @@ PREFILL_I4 = [(129, 132, 512), (256, 256, 512), (300, 1004, 1024), (513, 392, 20
 
 
 def _prefill_pairs(M, N, seed):
-    rows = np.unique(np.concatenate([[0, 127, 128, 255, 256, M - 1], synth.uniform_ints(24, 0, M - 1, seed, 5)]))
+    edges = [r for r in (0, 95, 96, 127, 128, 191, 192, 255, 256, 383, 384) if r < M] + [M - 1]
+    rows = np.unique(np.concatenate([edges, synth.uniform_ints(24, 0, M - 1, seed, 5)]))
     cols = np.unique(np.concatenate([[0, 127, 128, N - 1], synth.uniform_ints(48, 0, N - 1, seed, 6)]))
     return np.repeat(rows, cols.size), np.tile(cols, rows.size)
 

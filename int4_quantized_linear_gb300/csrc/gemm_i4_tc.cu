@@ -299,11 +299,11 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         const uint32_t idesc = tc::idesc_f8f6f4(0, 0, BM, BN);
         for (int i = 0; i < n_k; ++i) {
             const int f = i / KPU, sl = f % US, j = i % KPU, a = i % NA, b = i % NB;
-            if (gate) {
+            if (gate && lane == 0) {  // lane 0 waits, the converted tile first; the barrier releases the rest
+                if (!*abort_flag) wait_or_fail(&a_full[a], (i / NA) & 1, abort_flag, p.status, ST_TIMEOUT_GATE, i);
                 if (!*abort_flag)
-                    warp_wait(&g_empty[b], ((i / NB) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_GATE, i, lane);
-                if (!*abort_flag) warp_wait(&a_full[a], (i / NA) & 1, abort_flag, p.status, ST_TIMEOUT_GATE, i, lane);
-                if (lane == 0) trace_ev(p, 3, i);
+                    wait_or_fail(&g_empty[b], ((i / NB) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_GATE, i);
+                trace_ev(p, 3, i);
             }
             const bool aborted = tc::named_bar_or(GATE_BARRIER, 64, gate && *abort_flag);
             if (gate && lane == 0) trace_ev(p, 6, i);

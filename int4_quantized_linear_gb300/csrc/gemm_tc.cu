@@ -414,19 +414,15 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             for (bool first = true; f < f_end; ++f, first = false) {
                 const int sl = f % US;
                 const int sq = f % SFQ;
-                if (gate) {
+                if (gate && lane == 0) {  // lane 0 waits; the named barrier releases the rest
                     if (!*abort_flag && first)
-                        warp_wait(&acc_empty[b], ((seg / ACC_BUFS) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_GATE, seg, lane);
-                    if (!*abort_flag)
-                        warp_wait(&sff[sq], (f / SFQ) & 1, abort_flag, p.status, ST_TIMEOUT_GATE, f, lane);
-                    if (lane == 0) trace_ev(p, TR_GATE_SFF, f);
-                    if (!*abort_flag)
-                        warp_wait(&full[sl], (f / US) & 1, abort_flag, p.status, ST_TIMEOUT_GATE, f, lane);
-                    if (lane == 0) {
-                        trace_ev(p, TR_MMA_READY, f);
-                        if (f == 0) trace_phase(p, 8);
-                        if (f == n_k / KPU - 1) trace_phase(p, 9);
-                    }
+                        wait_or_fail(&acc_empty[b], ((seg / ACC_BUFS) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_GATE, seg);
+                    if (!*abort_flag) wait_or_fail(&sff[sq], (f / SFQ) & 1, abort_flag, p.status, ST_TIMEOUT_GATE, f);
+                    trace_ev(p, TR_GATE_SFF, f);
+                    if (!*abort_flag) wait_or_fail(&full[sl], (f / US) & 1, abort_flag, p.status, ST_TIMEOUT_GATE, f);
+                    trace_ev(p, TR_MMA_READY, f);
+                    if (f == 0) trace_phase(p, 8);
+                    if (f == n_k / KPU - 1) trace_phase(p, 9);
                 }
                 // the gate's abort state rides on the barrier: the MMA thread reads no memory here
                 const bool aborted = tc::named_bar_or(GATE_BARRIER, 64, gate && *abort_flag);

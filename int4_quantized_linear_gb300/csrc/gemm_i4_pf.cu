@@ -70,15 +70,16 @@ struct Depth {
 static_assert(ND >= US * XK && ND >= 3 && ND >= NB, "completion barriers");
 constexpr int GATE_BARRIER = 2;   // gate warp + MMA warp
 constexpr int EPI_BARRIER = 3;    // the eight promotion warps
-constexpr int HALF_BARRIER0 = 4;  // 4 and 5: the four warps of one token half
 // Registers per thread after the split (warpgroups 0, 1, then 2 and 3); the kernel is launched
 // with 128 per thread (the host checks), and the split never asks for more than that in all.
-// int5's converters keep the fifth-bit bytes of two k-tiles as well.
+// 56 / 80 / 184 is the split at which neither the int4 nor the int5 build spills (40 / 64 / 200
+// spilled ~48 bytes per thread, and with shared memory filling the L1 array a spill reload is
+// an L2 round trip).
 template <bool I5>
 struct Regs {
-    static constexpr int CTRL = 40;
-    static constexpr int CONV = I5 ? 72 : 64;
-    static constexpr int EPI = 200;
+    static constexpr int CTRL = 56;
+    static constexpr int CONV = 80;
+    static constexpr int EPI = 184;
     static_assert(128 * (CTRL + CONV + 2 * EPI) <= NUM_THREADS * 128, "register split");
 };
 
@@ -125,7 +126,7 @@ struct Layout {
     static constexpr int X_TILE = BN * 128;      // [256 tokens][128 k] e4m3, 128-byte swizzle
     static constexpr int X_FILL = XK * X_TILE;
     static constexpr int A_TILE = BM * 128;      // [128 columns][128 k] e4m3, 128-byte swizzle
-    static constexpr int STAGE_BYTES = 16 * BM * 2;  // [16 tokens][128 columns] bf16
+    static constexpr int STAGE_BYTES = 16 * 32 * 2;  // [16 tokens][32 columns] bf16, one per warp and buffer
     static constexpr int W_TILE = 16 * BM * 4;     // [16 word rows][128 columns] int32
     static constexpr int H_TILE = I5 ? 16 * BM : 0;  // [16 rows][128 columns] fifth-bit bytes
     static constexpr int R_SLOT = W_TILE + H_TILE;
@@ -133,7 +134,7 @@ struct Layout {
     static constexpr int R_OFF = X_OFF + US * X_FILL;
     static constexpr int A_OFF = R_OFF + RS * R_SLOT;
     static constexpr int STAGE_OFF = A_OFF + NA * A_TILE;
-    static constexpr int XS_OFF = STAGE_OFF + 4 * STAGE_BYTES;
+    static constexpr int XS_OFF = STAGE_OFF + 16 * STAGE_BYTES;  // 8 promotion warps x 2 buffers
     static constexpr int BAR_OFF = XS_OFF + BN * 4;
     static constexpr int TOTAL = BAR_OFF + 256 + 1024;  // + alignment slack
     static constexpr int TMEM_COLS = NB * BN;    // 512
@@ -367,27 +368,27 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
         // and token columns 128h..128h+127 of the tile (h = (w >> 2) & 1).
         const int q = warp & 3, h = (warp >> 2) & 1;
         const int r = 32 * q + lane;
-        const int half_bar = HALF_BARRIER0 + h;
-        const bool issuer = (threadIdx.x == (EPI_WARP0 + 4 * h) * 32);  // one per half
         float *xs_s = reinterpret_cast<float *>(smem + L::XS_OFF) + 128 * h;
         int ck = 0;  // output chunks emitted by this half (staging buffer rotation)
         // Write 16 token columns (tile columns c0..c0+15 of this half) of this thread's weight
-        // column: through a [16 tokens][128 columns] bf16 stage and one TMA store (the half's 128
-        // threads call together), or plain stores.
+        // column: each warp through a [16 tokens][32 columns] bf16 stage of its own (two of them,
+        // alternating) and one TMA store issued by its lane 0 -- no barrier across warps -- or
+        // plain stores.
         auto emit = [&](const float (&o)[16], int c0, int m0, int n0) {
             const int n = n0 + r;
             if (p.tma_out) {
-                uint16_t *stg = reinterpret_cast<uint16_t *>(smem + L::STAGE_OFF + (2 * h + (ck & 1)) * L::STAGE_BYTES);
+                uint16_t *stg = reinterpret_cast<uint16_t *>(smem + L::STAGE_OFF +
+                                                             (2 * (warp - EPI_WARP0) + (ck & 1)) * L::STAGE_BYTES);
                 if (ck >= 2) {  // the store that last used this buffer has read it
-                    if (issuer) tc::bulk_wait_group_read<1>();
-                    tc::named_bar_sync(half_bar, 128);
+                    if (lane == 0) tc::bulk_wait_group_read<1>();
+                    __syncwarp();
                 }
 #pragma unroll
-                for (int j = 0; j < 16; ++j) stg[j * BM + r] = float_to_bf16_bits(o[j]);
+                for (int j = 0; j < 16; ++j) stg[j * 32 + lane] = float_to_bf16_bits(o[j]);
                 tc::fence_proxy_async_smem();
-                tc::named_bar_sync(half_bar, 128);
-                if (issuer) {
-                    tc::tma_store_2d_hint(&tmap_out, stg, n0, m0 + c0, tc::make_policy_evict_first());
+                __syncwarp();
+                if (lane == 0 && n0 + 32 * q < p.N) {  // (a warp wholly past the last column stores nothing)
+                    tc::tma_store_2d_hint(&tmap_out, stg, n0 + 32 * q, m0 + c0, tc::make_policy_evict_first());
                     tc::bulk_commit_group();
                 }
                 ++ck;
@@ -536,7 +537,7 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             }
             if (threadIdx.x == EPI_WARP0 * 32) trace_ev(p, 11, i - 1);
         }
-        if (issuer) tc::bulk_wait_group_all();  // output stores done before shared memory goes away
+        if (lane == 0) tc::bulk_wait_group_all();  // output stores done before shared memory goes away
     }
 
     tc::tc_fence_before();
@@ -616,7 +617,7 @@ static w4a8_status launch(const uint8_t *xq, Params prm, cudaStream_t stream)
         return W4A8_ERR_CUDA;
     prm.tma_out = (prm.N % 8 == 0) && w4a8_aligned(prm.out, 16) &&
                   tch::tmap_2d(&tout, CU_TENSOR_MAP_DATA_TYPE_UINT16, prm.out, prm.M, prm.N, (uint64_t)prm.N * 2, 16,
-                               BM, CU_TENSOR_MAP_SWIZZLE_NONE);
+                               32, CU_TENSOR_MAP_SWIZZLE_NONE);
     // activations as [k-tile][token][128 bytes], XK k-tiles of 256 tokens per box
     if (!tch::tmap_3d_ktiles(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, prm.M, prm.K, 128, prm.K / 128, BN, XK))
         return W4A8_ERR_CUDA;

@@ -143,16 +143,6 @@ struct Layout {
     static_assert(X_TILE % 1024 == 0 && A_TILE % 1024 == 0 && A_OFF % 1024 == 0, "swizzled tiles");
 };
 
-template <int N>
-__device__ __forceinline__ void regs_dec()
-{
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void regs_inc()
-{
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
 
 // 32 lanes x 32 consecutive 32-bit columns -> 32 registers per thread.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
@@ -237,7 +227,7 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
     };
 
     if (warp < CONV_WARP0) {
-        regs_dec<Regs<I5>::CTRL>();
+        tc::regs_dec<Regs<I5>::CTRL>();
         if (warp == 0) {
             // -------------------------------------------------------- TMA producer: activations
             if (lane == 0) {
@@ -317,7 +307,7 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             __syncwarp();
         }
     } else if (warp < EPI_WARP0) {
-        regs_dec<Regs<I5>::CONV>();
+        tc::regs_dec<Regs<I5>::CONV>();
         // ------------------------------------------------------------ converters (4-7)
         // Thread = one weight column r of the tile: it reads the column's 16 words of a k-tile (int5:
         // and their 16 fifth-bit bytes) from the word ring (consecutive columns are consecutive
@@ -362,7 +352,7 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             if (r == 0) trace_ev(p, 3, i);
         }
     } else {
-        regs_inc<Regs<I5>::EPI>();
+        tc::regs_inc<Regs<I5>::EPI>();
         // ------------------------------------------------------------ promotion and epilogue (8-15)
         // Warp w reads tensor-memory lanes 32q..32q+31 (q = w & 3: weight columns n0 + 32q + lane)
         // and token columns 128h..128h+127 of the tile (h = (w >> 2) & 1).

@@ -70,6 +70,14 @@ constexpr int MMA_WARP = 1;
 constexpr int GATE_WARP = 5;      // warp 9 has no role
 constexpr int EPI_WARP0 = 12;     // warps 12-15: promotion + epilogue, lane quarter = warp & 3
 constexpr int N_CONV_WARPS = 8;   // warps 2, 3, 4, 6, 7, 8, 10, 11
+// 64-token tiles without zero points: the promotion warps (warpgroup 3) hold 64 accumulators
+// plus a 16-column load; at the launch's 128 registers per thread that spilled, and with shared
+// memory filling the L1 array every reload is an L2 round trip.  So those builds move registers
+// from warpgroups 0-2 to warpgroup 3 with setmaxnreg (the asymmetric builds spill more under
+// any split, so they keep 128 everywhere).
+constexpr int REGS_REST_BN64 = 112;
+constexpr int REGS_EPI_BN64 = 136;
+static_assert(3 * 128 * REGS_REST_BN64 + 128 * REGS_EPI_BN64 <= NUM_THREADS * 118, "register split");
 
 // Converter index 0..7 of a warp, or -1.
 __device__ __forceinline__ int conv_index(int warp)
@@ -218,6 +226,12 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     // programmatic dependent launch: global memory only after the previous kernel completed
     tc::grid_dependency_wait();
     tc::grid_dependents_launch();
+    if constexpr (BN >= 64 && !ASYM) {
+        if (warp >= EPI_WARP0)
+            tc::regs_inc<REGS_EPI_BN64>();
+        else
+            tc::regs_dec<REGS_REST_BN64>();
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -588,6 +602,18 @@ static w4a8_status launch(const int32_t *qw, const uint8_t *xq, Params prm, cuda
         !tch::tmap_3d_ktiles(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, prm.M, prm.K, 128, prm.K / 128, BN, KPU))
         return W4A8_ERR_CUDA;
     auto kern = int4_tc_kernel<BN, US, NA, NB, ASYM, I5>;
+    if constexpr (BN >= 64 && !ASYM) {
+        // the register split assumes at least 118 registers per thread at launch; a build with
+        // fewer would leave setmaxnreg.inc waiting, so it is refused
+        static std::atomic<int> regs_state{0};  // 0 unknown, 1 enough, 2 too few
+        int rs = regs_state.load(std::memory_order_acquire);
+        if (rs == 0) {
+            cudaFuncAttributes fa;
+            rs = (cudaFuncGetAttributes(&fa, kern) == cudaSuccess && fa.numRegs >= 118) ? 1 : 2;
+            regs_state.store(rs, std::memory_order_release);
+        }
+        if (rs != 1) return W4A8_ERR_CUDA;
+    }
     static std::atomic<int> attr_done[64];
     if (!tch::set_smem_once(kern, L::TOTAL, attr_done)) return W4A8_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};

@@ -301,6 +301,20 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v
                  : "memory");
 }
 
+// Per-warpgroup register budget (every warp of a warpgroup executes the same one).  An increase
+// draws on the registers the CTA was launched with, so the budgets of all warpgroups must add up
+// to no more than that (the host checks the built kernel's count before it launches).
+template <int N>
+__device__ __forceinline__ void regs_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Programmatic dependent launch controls (no-ops when the kernel was not launched with it).

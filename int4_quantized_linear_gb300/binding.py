@@ -87,6 +87,11 @@ def load(build_if_missing: bool = True):
         f = getattr(lib, name)
         f.restype = res
         f.argtypes = args
+    # builds with the pipeline timestamps compiled in export a setter for their device buffer; its
+    # argument is a 64-bit pointer, which ctypes would otherwise pass as a truncated C int
+    if hasattr(lib, "w4a8_debug_set_trace"):
+        lib.w4a8_debug_set_trace.restype = None
+        lib.w4a8_debug_set_trace.argtypes = [P]
     _lib = lib
     return lib
 

@@ -65,7 +65,8 @@ constexpr int ND = 4;             // k-tile completion barriers
 template <bool I5>
 struct Depth {
     static constexpr int RS = I5 ? 4 : 3;
-    static constexpr int NA = I5 ? 2 : 3;
+    static constexpr int NA = 2;
+    static constexpr int CHUNK = I5 ? 16 : 32;  // tokens per output store (int4 has the room for 32)
 };
 static_assert(ND >= US * XK && ND >= 3 && ND >= NB, "completion barriers");
 constexpr int GATE_BARRIER = 2;   // gate warp + MMA warp
@@ -126,7 +127,7 @@ struct Layout {
     static constexpr int X_TILE = BN * 128;      // [256 tokens][128 k] e4m3, 128-byte swizzle
     static constexpr int X_FILL = XK * X_TILE;
     static constexpr int A_TILE = BM * 128;      // [128 columns][128 k] e4m3, 128-byte swizzle
-    static constexpr int STAGE_BYTES = 16 * 32 * 2;  // [16 tokens][32 columns] bf16, one per warp and buffer
+    static constexpr int STAGE_BYTES = Depth<I5>::CHUNK * 32 * 2;  // [CHUNK tokens][32 columns] bf16, per warp and buffer
     static constexpr int W_TILE = 16 * BM * 4;     // [16 word rows][128 columns] int32
     static constexpr int H_TILE = I5 ? 16 * BM : 0;  // [16 rows][128 columns] fifth-bit bytes
     static constexpr int R_SLOT = W_TILE + H_TILE;
@@ -361,27 +362,34 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
         float *xs_s = reinterpret_cast<float *>(smem + L::XS_OFF) + 128 * h;
         int ck = 0;  // output chunks emitted by this half (staging buffer rotation)
         // Write 16 token columns (tile columns c0..c0+15 of this half) of this thread's weight
-        // column: each warp through a [16 tokens][32 columns] bf16 stage of its own (two of them,
-        // alternating) and one TMA store issued by its lane 0 -- no barrier across warps -- or
-        // plain stores.
-        auto emit = [&](const float (&o)[16], int c0, int m0, int n0) {
+        // column: each warp through a [CHUNK tokens][32 columns] bf16 stage of its own (two of
+        // them, alternating), filled 16 tokens at a time, and one TMA store per CHUNK tokens issued
+        // by its lane 0 -- no barrier across warps -- or plain stores.  `last`: no more tokens
+        // follow in this half, so a partly filled stage goes out (its unwritten rows are tokens at
+        // or past M, which the store clips).
+        constexpr int CHUNK = Depth<I5>::CHUNK;
+        auto emit = [&](const float (&o)[16], int c0, int m0, int n0, bool last) {
             const int n = n0 + r;
             if (p.tma_out) {
+                const int sub = (c0 / 16) % (CHUNK / 16);  // which 16 tokens of the stage
                 uint16_t *stg = reinterpret_cast<uint16_t *>(smem + L::STAGE_OFF +
                                                              (2 * (warp - EPI_WARP0) + (ck & 1)) * L::STAGE_BYTES);
-                if (ck >= 2) {  // the store that last used this buffer has read it
+                if (sub == 0 && ck >= 2) {  // the store that last used this buffer has read it
                     if (lane == 0) tc::bulk_wait_group_read<1>();
                     __syncwarp();
                 }
 #pragma unroll
-                for (int j = 0; j < 16; ++j) stg[j * 32 + lane] = float_to_bf16_bits(o[j]);
-                tc::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0 && n0 + 32 * q < p.N) {  // (a warp wholly past the last column stores nothing)
-                    tc::tma_store_2d_hint(&tmap_out, stg, n0 + 32 * q, m0 + c0, tc::make_policy_evict_first());
-                    tc::bulk_commit_group();
+                for (int j = 0; j < 16; ++j) stg[(16 * sub + j) * 32 + lane] = float_to_bf16_bits(o[j]);
+                if (sub == CHUNK / 16 - 1 || last) {
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && n0 + 32 * q < p.N) {  // (a warp wholly past the last column stores nothing)
+                        tc::tma_store_2d_hint(&tmap_out, stg, n0 + 32 * q, m0 + c0 - 16 * sub,
+                                              tc::make_policy_evict_first());
+                        tc::bulk_commit_group();
+                    }
+                    ++ck;
                 }
-                ++ck;
             } else if (n < p.N) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
@@ -475,7 +483,7 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
                         float o[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) o[j] = acc[c0 + j] * xs_s[c0 + j];
-                        emit(o, 128 * h + c0, m0, n0);
+                        emit(o, 128 * h + c0, m0, n0, c0 + 16 >= 128 || m0 + 128 * h + c0 + 16 >= p.M);
                     }
                 }
             } else {
@@ -519,7 +527,7 @@ int4_pf_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
                         }
 #pragma unroll
                         for (int j = 0; j < 16; ++j) sum[j] *= xs_s[c0 + j];
-                        emit(sum, 128 * h + c0, m0, n0);
+                        emit(sum, 128 * h + c0, m0, n0, c0 + 16 >= m_cnt);
                     }
                     if (threadIdx.x == EPI_WARP0 * 32) p.counters[t] = 0;
                 }
@@ -606,8 +614,8 @@ static w4a8_status launch(const uint8_t *xq, Params prm, cudaStream_t stream)
                              CU_TENSOR_MAP_SWIZZLE_NONE)))
         return W4A8_ERR_CUDA;
     prm.tma_out = (prm.N % 8 == 0) && w4a8_aligned(prm.out, 16) &&
-                  tch::tmap_2d(&tout, CU_TENSOR_MAP_DATA_TYPE_UINT16, prm.out, prm.M, prm.N, (uint64_t)prm.N * 2, 16,
-                               32, CU_TENSOR_MAP_SWIZZLE_NONE);
+                  tch::tmap_2d(&tout, CU_TENSOR_MAP_DATA_TYPE_UINT16, prm.out, prm.M, prm.N, (uint64_t)prm.N * 2,
+                               Depth<I5>::CHUNK, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
     // activations as [k-tile][token][128 bytes], XK k-tiles of 256 tokens per box
     if (!tch::tmap_3d_ktiles(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, prm.M, prm.K, 128, prm.K / 128, BN, XK))
         return W4A8_ERR_CUDA;

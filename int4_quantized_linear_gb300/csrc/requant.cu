@@ -58,10 +58,11 @@ W4A8_DEVICE int block_exponent(float amax, int mode)
     return min(127, max(-127, e));
 }
 
-// Two non-negative fp32 values -> their e2m1 codes in one byte (low nibble = a0): the hardware
-// conversion rounds to the nearest grid point {0, .5, 1, 1.5, 2, 3, 4, 6} with ties to the even
-// code and saturates at 6 -- e2m1_index of min(a, 6), whose ties go to the even index.
-W4A8_DEVICE uint32_t e2m1x2_from_nonneg(float a0, float a1)
+// Two fp32 values -> their signed e2m1 codes in one byte (low nibble = a0): the hardware
+// conversion rounds |a| to the nearest grid point {0, .5, 1, 1.5, 2, 3, 4, 6} with ties to the
+// even code and saturates at 6 -- e2m1_index of min(|a|, 6), whose ties go to the even index --
+// and keeps the sign, also on a zero magnitude (-0 and small negatives give code 8).
+W4A8_DEVICE uint32_t e2m1x2_from_float(float a0, float a1)
 {
     uint32_t r;
     asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }" : "=r"(r) : "f"(a1), "f"(a0));
@@ -69,7 +70,9 @@ W4A8_DEVICE uint32_t e2m1x2_from_nonneg(float a0, float a1)
 }
 
 // Encode 32 values at exponent e.  Returns the squared error in scale units (fp32, squares
-// rounded and added in ascending k) and the 32 codes as four words of eight nibbles.
+// rounded and added in ascending k; only when ERR, else 0) and the 32 codes as four words of
+// eight nibbles.
+template <bool ERR>
 W4A8_DEVICE float encode_block(const float (&w)[32], int e, uint32_t (&codes)[4])
 {
     const float inv = exp2i(-e);
@@ -78,26 +81,33 @@ W4A8_DEVICE float encode_block(const float (&w)[32], int e, uint32_t (&codes)[4]
     for (int j = 0; j < 4; ++j) codes[j] = 0;
 #pragma unroll
     for (int k = 0; k < 32; k += 2) {
-        // |v| = |w| 2^-e is exact (a power-of-two product); it may exceed 6 (up to 12 one binade
-        // finer), and the error is taken against the unclamped value
-        const float a0 = fabsf(__fmul_rn(w[k], inv)), a1 = fabsf(__fmul_rn(w[k + 1], inv));
-        const uint32_t b = e2m1x2_from_nonneg(a0, a1);
-        const float2 g = e2m1x2_to_float2(b);  // the chosen grid values (exact)
-        const float d0 = __fsub_rn(a0, g.x), d1 = __fsub_rn(a1, g.y);
-        S = __fadd_rn(S, __fmul_rn(d0, d0));
-        S = __fadd_rn(S, __fmul_rn(d1, d1));
-        // the sign bit only on a nonzero index, so -0 and small negatives give code 0, never 8
-        const uint32_t i0 = b & 7u, i1 = (b >> 4) & 7u;
-        const uint32_t c0 = i0 | ((i0 != 0u && signbit(w[k])) ? 8u : 0u);
-        const uint32_t c1 = i1 | ((i1 != 0u && signbit(w[k + 1])) ? 8u : 0u);
-        codes[k >> 3] |= (c0 | (c1 << 4)) << (4 * (k & 7));
+        // v = w 2^-e is exact (a power-of-two product); |v| may exceed 6 (up to 12 one binade
+        // finer), and the error is taken against the unclamped value.  The signed value and its
+        // signed grid point differ by exactly -(|v| - grid) when v < 0, so the square is the same.
+        const float a0 = __fmul_rn(w[k], inv), a1 = __fmul_rn(w[k + 1], inv);
+        const uint32_t b = e2m1x2_from_float(a0, a1);
+        if constexpr (ERR) {
+            const float2 g = e2m1x2_to_float2(b);  // the chosen grid values, signed (exact)
+            const float d0 = __fsub_rn(a0, g.x), d1 = __fsub_rn(a1, g.y);
+            S = __fadd_rn(S, __fmul_rn(d0, d0));
+            S = __fadd_rn(S, __fmul_rn(d1, d1));
+        }
+        codes[k >> 3] |= b << (4 * (k & 7));
+    }
+    // the sign bit only on a nonzero index, so -0 and small negatives give code 0, never 8: per
+    // nibble, (index + 7) carries into bit 3 exactly when the index is nonzero
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t keep = ((codes[j] & 0x77777777u) + 0x77777777u) & 0x88888888u;
+        codes[j] &= 0x77777777u | keep;
     }
     return S;
 }
 
 // R2-R4 on one 32-block of fp32 weights: choose the exponent (R2), encode (R3) and pack (R4).
-// Returns the block exponent e; S receives the squared error in scale units and ssq the
-// block's sum of squared weights.
+// Returns the block exponent e; with ERR, S receives the squared error in scale units and ssq
+// the block's sum of squared weights (the mse rule computes the errors either way).
+template <bool ERR>
 W4A8_DEVICE int quantize_block(const float (&w)[32], int mode, uint4 &out, float &S, float &ssq)
 {
     float amax = 0.0f;
@@ -108,12 +118,12 @@ W4A8_DEVICE int quantize_block(const float (&w)[32], int mode, uint4 &out, float
     if (mode == 2) {
         const int e0 = block_exponent(amax, 1);
         uint32_t c0[4];
-        const float S0 = encode_block(w, e0, c0);
+        const float S0 = encode_block<true>(w, e0, c0);
         bool take1 = false;
         uint32_t c1[4] = {0, 0, 0, 0};
         float S1 = 0.0f;
         if (e0 > -127) {
-            S1 = encode_block(w, e0 - 1, c1);
+            S1 = encode_block<true>(w, e0 - 1, c1);
             take1 = S1 < __fmul_rn(4.0f, S0);
         }
         e = take1 ? e0 - 1 : e0;
@@ -122,7 +132,7 @@ W4A8_DEVICE int quantize_block(const float (&w)[32], int mode, uint4 &out, float
         for (int j = 0; j < 4; ++j) codes[j] = take1 ? c1[j] : c0[j];
     } else {
         e = block_exponent(amax, mode);
-        S = encode_block(w, e, codes);
+        S = encode_block<ERR>(w, e, codes);
     }
     // R4: nibble k of word j is element 8j + k (the even k lands in the low nibble)
     out = make_uint4(codes[0], codes[1], codes[2], codes[3]);
@@ -130,8 +140,10 @@ W4A8_DEVICE int quantize_block(const float (&w)[32], int mode, uint4 &out, float
     // squares rounded and added in fp32, ascending k; blocks are then summed in fp64.  fp64
     // arithmetic per element would cost more than the rest of the kernel on GB300.
     float q = 0.0f;
+    if constexpr (ERR) {
 #pragma unroll
-    for (int k = 0; k < 32; ++k) q = __fadd_rn(q, __fmul_rn(w[k], w[k]));
+        for (int k = 0; k < 32; ++k) q = __fadd_rn(q, __fmul_rn(w[k], w[k]));
+    }
     ssq = q;
     return e;
 }
@@ -139,16 +151,22 @@ W4A8_DEVICE int quantize_block(const float (&w)[32], int mode, uint4 &out, float
 // R1 sources.  Each yields block g's 32 fp32 weights (row n = g / (K / 32)).
 // NVFP4 ("radiance_nvfp4.py", dequant_nvfp4): w = fl(e2m1 * fl(fp32(e4m3 scale per 16) / divisor))
 // for partition p's divisor: 16 packed bytes and two scale bytes per block.
+// The scale byte has 256 values, so the CTA divides each by the partition's divisor once, into a
+// shared table, before the partition's blocks.
 struct SrcNvfp4 {
     const uint8_t *packed, *scale;
     const float *divisor;
-    W4A8_DEVICE void load(int64_t g, int64_t, int p, float (&w)[32]) const
+    W4A8_DEVICE void prepare(int p, float *tab) const
+    {
+        const float dv = divisor[p];
+        for (int c = threadIdx.x; c < 256; c += blockDim.x)
+            tab[c] = __fdiv_rn(e4m3x2_to_float2((uint16_t)c).x, dv);
+    }
+    W4A8_DEVICE void load(int64_t g, int64_t, int, const float *tab, float (&w)[32]) const
     {
         const uint4 pk = *reinterpret_cast<const uint4 *>(packed + g * 16);
         const uint16_t sc = *reinterpret_cast<const uint16_t *>(scale + g * 2);
-        const float dv = divisor[p];
-        const float2 s2 = e4m3x2_to_float2(sc);
-        const float sd0 = __fdiv_rn(s2.x, dv), sd1 = __fdiv_rn(s2.y, dv);
+        const float sd0 = tab[sc & 0xffu], sd1 = tab[sc >> 8];
         const uint32_t words[4] = {pk.x, pk.y, pk.z, pk.w};
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -164,7 +182,8 @@ struct SrcNvfp4 {
 struct SrcFp8Channel {
     const uint8_t *w8;
     const float *scale;
-    W4A8_DEVICE void load(int64_t g, int64_t n, int, float (&w)[32]) const
+    W4A8_DEVICE void prepare(int, float *) const {}
+    W4A8_DEVICE void load(int64_t g, int64_t n, int, const float *, float (&w)[32]) const
     {
         const uint4 a = *reinterpret_cast<const uint4 *>(w8 + g * 32);
         const uint4 b = *reinterpret_cast<const uint4 *>(w8 + g * 32 + 16);
@@ -182,7 +201,8 @@ struct SrcFp8Channel {
 // 64 bytes per block.
 struct SrcBf16 {
     const uint16_t *wb;
-    W4A8_DEVICE void load(int64_t g, int64_t, int, float (&w)[32]) const
+    W4A8_DEVICE void prepare(int, float *) const {}
+    W4A8_DEVICE void load(int64_t g, int64_t, int, const float *, float (&w)[32]) const
     {
         const uint4 *src = reinterpret_cast<const uint4 *>(wb + g * 32);
 #pragma unroll
@@ -202,33 +222,37 @@ struct SrcBf16 {
 // 32-blocks with a grid stride, so a warp handles 32 consecutive blocks of a row (512 bytes of
 // codes each way).  The error sums are kept per thread, reduced per CTA and added to the output
 // with one atomic per CTA and partition.
-template <class Src>
+template <class Src, bool ERR>
 __global__ void __launch_bounds__(RQ_THREADS)
 requant_kernel(const Src src, Partitions parts, int64_t N, int64_t K, int mode,
                uint8_t *__restrict__ out_packed, uint8_t *__restrict__ out_e8m0,
                double *__restrict__ err_ssq)
 {
     __shared__ double red[2][RQ_THREADS / 32];
+    __shared__ float tab[256];
     const int64_t KB = K / 32;
     const int64_t stride = (int64_t)gridDim.x * RQ_THREADS;
     int64_t row_beg = 0;
     for (int p = 0; p < parts.P; ++p) {
         const int64_t row_end = parts.row_end[p];
+        __syncthreads();  // the previous partition's table is no longer read
+        src.prepare(p, tab);
+        __syncthreads();
         double err = 0.0, ssq = 0.0;
         for (int64_t g = row_beg * KB + (int64_t)blockIdx.x * RQ_THREADS + threadIdx.x; g < row_end * KB; g += stride) {
             float w[32];
-            src.load(g, g / KB, p, w);
+            src.load(g, g / KB, p, tab, w);
             uint4 codes;
             float S, q;
-            const int e = quantize_block(w, mode, codes, S, q);
+            const int e = quantize_block<ERR>(w, mode, codes, S, q);
             *reinterpret_cast<uint4 *>(out_packed + g * 16) = codes;
             out_e8m0[g] = (uint8_t)(e + 127);
-            if (err_ssq) {
+            if (ERR) {
                 err += ldexp((double)S, 2 * e);
                 ssq += (double)q;
             }
         }
-        if (err_ssq) {
+        if (ERR) {
             err = warp_sum_d(err);
             ssq = warp_sum_d(ssq);
             if ((threadIdx.x & 31) == 0) {
@@ -270,13 +294,13 @@ static w4a8_status launch_requant(const Src &src, const Partitions &parts, int64
     // SM count and residency per device, queried once (a per-call query costs microseconds of
     // host time, as much as the kernel itself for a few activation rows)
     constexpr int MAX_DEV = 64;
-    static int sms_of[MAX_DEV] = {0}, per_sm_of[MAX_DEV] = {0};
+    static int sms_of[MAX_DEV] = {0}, per_sm_of[MAX_DEV] = {0};  // (both instantiations: same residency)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return W4A8_ERR_CUDA;
     int sms = dev < MAX_DEV ? sms_of[dev] : 0, per_sm = dev < MAX_DEV ? per_sm_of[dev] : 0;
     if (sms == 0) {
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_kernel<Src>, RQ_THREADS, 0) != cudaSuccess)
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_kernel<Src, true>, RQ_THREADS, 0) != cudaSuccess)
             return W4A8_ERR_CUDA;
         if (dev < MAX_DEV) {
             per_sm_of[dev] = per_sm;
@@ -285,8 +309,12 @@ static w4a8_status launch_requant(const Src &src, const Partitions &parts, int64
     }
     const int64_t need = (blocks + RQ_THREADS - 1) / RQ_THREADS;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sms * std::max(per_sm, 1)));
-    requant_kernel<Src><<<(unsigned)grid, RQ_THREADS, 0, stream>>>(src, parts, N, K, mode, out_packed, out_e8m0,
-                                                                    err_ssq);
+    if (err_ssq)
+        requant_kernel<Src, true><<<(unsigned)grid, RQ_THREADS, 0, stream>>>(src, parts, N, K, mode, out_packed,
+                                                                            out_e8m0, err_ssq);
+    else
+        requant_kernel<Src, false><<<(unsigned)grid, RQ_THREADS, 0, stream>>>(src, parts, N, K, mode, out_packed,
+                                                                             out_e8m0, nullptr);
     return w4a8_launch_status();
 }
 

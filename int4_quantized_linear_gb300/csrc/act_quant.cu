@@ -5,8 +5,9 @@
 // the largest e4m3 magnitude, and codes are rounded to nearest even.
 //
 // Grid (M, S): S CTAs per row.  Every CTA of a row reads the whole row once (each thread keeps
-// its 16-byte chunks in registers for rows up to AQ_THREADS * AQ_CACHE * 8 elements; longer rows
-// are re-read from L1/L2 for the second pass) and takes the amax on the bf16 bit patterns (|x|
+// its 16-byte chunks in registers for rows up to AQ_THREADS * CACHE * 8 elements, CACHE 4 for rows
+// of up to 8192 elements and 16 above -- the smaller cache keeps the registers, and so the CTAs an
+// SM can hold, up for short rows; longer rows are re-read from L1/L2 for the second pass) and takes the amax on the bf16 bit patterns (|x|
 // ordering equals the ordering of the 15 low bits for finite values), reduced by warp shuffles
 // and shared memory; it then quantizes only its 1/S slice of the row: each element divided by the
 // scale with a correctly rounded fp32 division, eight e4m3 codes per 8-byte store.  Splitting a
@@ -26,8 +27,9 @@
 namespace w4a8 {
 
 constexpr int AQ_THREADS = 256;
-constexpr int AQ_CACHE = 16;  // chunks of 8 elements kept per thread: rows up to 32768 read once
 
+// CACHE: chunks of 8 elements kept per thread (rows up to AQ_THREADS * CACHE * 8 read once)
+template <int CACHE>
 __global__ void __launch_bounds__(AQ_THREADS)
 act_quant_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ xq,
                  float *__restrict__ x_scale, int64_t K)
@@ -37,16 +39,16 @@ act_quant_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ xq,
     const int64_t m = blockIdx.x;
     const uint4 *row = reinterpret_cast<const uint4 *>(x + m * K);
     const int nchunk = (int)(K / 8);
-    const bool cached = nchunk <= AQ_THREADS * AQ_CACHE;
+    const bool cached = nchunk <= AQ_THREADS * CACHE;
     // this CTA's slice of the row's chunks
     const int c_lo = (int)((long long)nchunk * blockIdx.y / gridDim.y);
     const int c_hi = (int)((long long)nchunk * (blockIdx.y + 1) / gridDim.y);
 
-    uint4 v[AQ_CACHE];
+    uint4 v[CACHE];
     uint32_t amax2 = 0;  // two 15-bit magnitudes packed, per-halfword max
     if (cached) {
 #pragma unroll
-        for (int i = 0; i < AQ_CACHE; ++i) {
+        for (int i = 0; i < CACHE; ++i) {
             const int c = threadIdx.x + i * AQ_THREADS;
             v[i] = c < nchunk ? __ldg(row + c) : make_uint4(0u, 0u, 0u, 0u);
             amax2 = __vmaxu2(amax2, v[i].x & 0x7fff7fffu);
@@ -83,7 +85,7 @@ act_quant_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ xq,
     auto quant8 = [&](const uint4 &w) { return quant8_e4m3(w, s); };
     if (cached) {
 #pragma unroll
-        for (int i = 0; i < AQ_CACHE; ++i) {
+        for (int i = 0; i < CACHE; ++i) {
             const int c = threadIdx.x + i * AQ_THREADS;
             if (c >= c_lo && c < c_hi) out[c] = quant8(v[i]);
         }
@@ -109,7 +111,9 @@ w4a8_status w4a8_launch_act_quant(const uint16_t *x_bf16, uint8_t *xq, float *x_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, w4a8::act_quant_kernel, x_bf16, xq, x_scale, K) != cudaSuccess) {
+    const bool short_rows = K <= 8192;
+    if ((short_rows ? cudaLaunchKernelEx(&cfg, w4a8::act_quant_kernel<4>, x_bf16, xq, x_scale, K)
+                    : cudaLaunchKernelEx(&cfg, w4a8::act_quant_kernel<16>, x_bf16, xq, x_scale, K)) != cudaSuccess) {
         cudaGetLastError();
         return W4A8_ERR_CUDA;
     }

@@ -5,9 +5,9 @@
 // the largest e4m3 magnitude, and codes are rounded to nearest even.
 //
 // Grid (M, S): S CTAs per row.  Every CTA of a row reads the whole row once (each thread keeps
-// its 16-byte chunks in registers for rows up to AQ_THREADS * CACHE * 8 elements, CACHE 4 for rows
-// of up to 8192 elements and 16 above -- the smaller cache keeps the registers, and so the CTAs an
-// SM can hold, up for short rows; longer rows are re-read from L1/L2 for the second pass) and takes the amax on the bf16 bit patterns (|x|
+// its 16-byte chunks in registers for rows up to AQ_THREADS * CACHE * 8 elements, CACHE 4, 12 or
+// 16 by row length -- the smallest that holds the row keeps the registers down and the CTAs an SM
+// can hold up; longer rows are re-read from L1/L2 for the second pass) and takes the amax on the bf16 bit patterns (|x|
 // ordering equals the ordering of the 15 low bits for finite values), reduced by warp shuffles
 // and shared memory; it then quantizes only its 1/S slice of the row: each element divided by the
 // scale with a correctly rounded fp32 division, eight e4m3 codes per 8-byte store.  Splitting a
@@ -111,9 +111,12 @@ w4a8_status w4a8_launch_act_quant(const uint16_t *x_bf16, uint8_t *xq, float *x_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const bool short_rows = K <= 8192;
-    if ((short_rows ? cudaLaunchKernelEx(&cfg, w4a8::act_quant_kernel<4>, x_bf16, xq, x_scale, K)
-                    : cudaLaunchKernelEx(&cfg, w4a8::act_quant_kernel<16>, x_bf16, xq, x_scale, K)) != cudaSuccess) {
+    // the smallest register cache that holds the row (fewer registers, more CTAs per SM)
+    const cudaError_t e =
+        K <= 8192 ? cudaLaunchKernelEx(&cfg, w4a8::act_quant_kernel<4>, x_bf16, xq, x_scale, K)
+        : K <= 24576 ? cudaLaunchKernelEx(&cfg, w4a8::act_quant_kernel<12>, x_bf16, xq, x_scale, K)
+                     : cudaLaunchKernelEx(&cfg, w4a8::act_quant_kernel<16>, x_bf16, xq, x_scale, K);
+    if (e != cudaSuccess) {
         cudaGetLastError();
         return W4A8_ERR_CUDA;
     }

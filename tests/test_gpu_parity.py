@@ -106,6 +106,35 @@ def test_requant_degenerate_blocks(lib, orc):
         assert np.array_equal(host(gp), rp)
 
 
+@pytest.mark.parametrize("mode", ["ocp", "noclip", "mse"])
+def test_requant_without_error_sums(lib, orc, mode):
+    """Without the error report the kernel is built without the error arithmetic (outside the mse
+    rule): codes and e8m0 must still match the oracle bit for bit, for every source.  The blocks
+    mix large values with tiny negatives that round to a zero index (code 0, never 8)."""
+    N, K = 70, 384
+    packed = synth.uniform_bytes(N, K // 2, 11, 1)
+    packed[3, :8] = 0x99                 # -0.5 in both nibbles next to large values
+    packed[3, 8:16] = 0x77               # 6.0
+    scale = synth.uniform_ints(N * K // 16, 0x30, 0x50, 11, 2).astype(np.uint8).reshape(N, K // 16)
+    div = np.array([37.0, 1000.0], np.float32)
+    parts = [30, 40]
+    gp, ge, gs = lib.requant(to_dev(packed), to_dev(scale), to_dev(div), parts, mode, err_ssq=False)
+    assert gs is None
+    rp, re_, _ = orc.requant(packed, scale, div, parts, mode)
+    assert np.array_equal(host(ge), re_) and np.array_equal(host(gp), rp)
+    wb = synth.bf16_weights(N, K, seed=12).copy()
+    wb[5, 0] = 0x4480                    # 1024
+    wb[5, 1:32] = 0xB400                 # -2^-23, far below the block's smallest grid step
+    gp, ge, _ = lib.requant_bf16(to_dev_bf16(wb), mode, err_ssq=False)
+    rp, re_, _ = orc.requant_bf16(wb, mode)
+    assert np.array_equal(host(ge), re_) and np.array_equal(host(gp), rp)
+    assert np.all(host(gp)[5, :16] & 0x88 == 0)  # no sign on the zero indices
+    w8, sc8 = synth.fp8_channel_weights(N, K, seed=13)
+    gp, ge, _ = lib.requant_fp8_channel(to_dev(w8), to_dev(sc8), mode, err_ssq=False)
+    rp, re_, _ = orc.requant_fp8_channel(w8, sc8, mode)
+    assert np.array_equal(host(ge), re_) and np.array_equal(host(gp), rp)
+
+
 @pytest.mark.slow
 def test_requant_full_gate_up(lib, orc):
     N, K = GATE_UP

@@ -795,6 +795,19 @@ def test_w4a4_rejects(lib):
 
 
 @pytest.mark.parametrize("a4", [False, True], ids=["w4a8", "w4a4"])
+def test_mxfp4_prefill_224_token_tiles(lib, orc, a4):
+    # M = 3100, K = 1024: fourteen 224-token tiles per weight tile (the last one 188 tokens) --
+    # the two-accumulator tiling for large M and shorter K, with a ragged token tail
+    M, N, K = 3100, 1152, 1024
+    x, w, e = synth.prefill_case(M, N, K, seed=78)
+    rows = np.array([0, 1, 223, 224, 447, 448, 2911, 2912, 3098, 3099])
+    cols = np.unique(np.concatenate([[0, 127, 128, N - 1], synth.uniform_ints(40, 0, N - 1, 78, 6)]))
+    pairs = (np.repeat(rows, cols.size), np.tile(cols, rows.size))
+    got, ref = (_a4_gemm if a4 else _mx_gemm)(lib, orc, x, w, e, pairs=pairs)
+    gemm_check(got, ref, f"224-token tiles a4={a4}")
+
+
+@pytest.mark.parametrize("a4", [False, True], ids=["w4a8", "w4a4"])
 def test_mxfp4_prefill_192_token_tiles(lib, orc, a4):
     # M = 1000, 127 weight tiles, K = 512: six 192-token tiles per weight tile (the last one 40
     # tokens), five per CTA -- the two-accumulator prefill tiling with a ragged token tail

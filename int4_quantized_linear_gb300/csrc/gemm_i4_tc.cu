@@ -496,7 +496,8 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                 // stream-K: store this CTA's fp32 partial; the last contributor adds all in CTA order
                 float *slot = p.partials + ((size_t)cta * 2 + (t == sched.t_first ? 0 : 1)) * (size_t)(BM * BN);
 #pragma unroll
-                for (int c = 0; c < BN; ++c) tc::st_cg_f32(slot + c * BM + r, acc[c]);
+                for (int c = 0; c < BN; ++c)
+                    if (m0 + c < p.M) tc::st_cg_f32(slot + c * BM + r, acc[c]);  // tokens that exist
                 const int c_first = unit_owner(t_lo, p.RU, p.Gsk);
                 const int c_last = unit_owner(t_hi - 1, p.RU, p.Gsk);
                 tc::named_bar_sync(1, 128);
@@ -519,7 +520,7 @@ int4_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                                 const int sl = (t == (int)(unit_start(c, p.RU, p.Gsk) / p.U)) ? 0 : 1;
                                 const float *src = p.partials + ((size_t)c * 2 + sl) * (size_t)(BM * BN) + c0 * BM + r;
 #pragma unroll
-                                for (int j = 0; j < 16; ++j) v[cc][j] = __ldcg(src + j * BM);
+                                for (int j = 0; j < 16; ++j) v[cc][j] = c0 + j < m_cnt ? __ldcg(src + j * BM) : 0.0f;
                             }
 #pragma unroll
                             for (int cc = 0; cc < 4; ++cc)

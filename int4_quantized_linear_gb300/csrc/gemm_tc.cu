@@ -655,8 +655,10 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                         emit(o, c0, m0, n0);
                     }
                 } else {
+                    // only the tokens that exist: the fix-up reads no column at or past M
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) tc::st_cg_f32(slot + (c0 + j) * BM + row, __uint_as_float(r[j]));
+                    for (int j = 0; j < 16; ++j)
+                        if (m0 + c0 + j < p.M) tc::st_cg_f32(slot + (c0 + j) * BM + row, __uint_as_float(r[j]));
                 }
             }
             // release the accumulator buffer to the MMA issuer
@@ -680,8 +682,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                 if (*last_flag) {
                     const int n_contrib = c_last - c_first + 1;
                     const int m_cnt = min(BN, p.M - m0);
-                    const int m16 = (m_cnt + 15) & ~15;  // columns staged: whole 16-column groups
-                    const uint32_t part_bytes = (uint32_t)m16 * BM * 4;  // first m16 columns of a slot
+                    const uint32_t part_bytes = (uint32_t)m_cnt * BM * 4;  // first m_cnt columns of a slot
                     // The CTA's last tile: every ring fill has been consumed (its accumulator is
                     // complete), so the ring's shared memory is idle.  Bulk copies bring all the
                     // contributors' partials in one round trip instead of one per 16 columns.
@@ -709,7 +710,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                             // same order of additions as below: zero, then the contributors in CTA
                             // order; 16 independent columns per step keep the loads pipelined
                             const float *st = reinterpret_cast<const float *>(smem) + row;
-                            const int stride = m16 * BM;
+                            const int stride = m_cnt * BM;
                             for (int c0 = 0; c0 < m_cnt; c0 += 16) {
                                 float a[16];
 #pragma unroll
@@ -717,7 +718,8 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                                 for (int c = 0; c < n_contrib; ++c) {
                                     const float *sc = st + c * stride + c0 * BM;
 #pragma unroll
-                                    for (int j = 0; j < 16; ++j) a[j] += sc[j * BM];
+                                    for (int j = 0; j < 16; ++j)
+                                        if (c0 + j < m_cnt) a[j] += sc[j * BM];
                                 }
 #pragma unroll
                                 for (int j = 0; j < 16; ++j) a[j] *= xs_s[c0 + j];
@@ -740,7 +742,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                                     const int sl = (t == (int)(unit_start(c, p.RU, p.Gsk) / p.U)) ? 0 : 1;
                                     const float *src = p.partials + ((size_t)c * 2 + sl) * (size_t)(BM * BN) + c0 * BM + row;
 #pragma unroll
-                                    for (int j = 0; j < 16; ++j) v[cc][j] = __ldcg(src + j * BM);
+                                    for (int j = 0; j < 16; ++j) v[cc][j] = c0 + j < m_cnt ? __ldcg(src + j * BM) : 0.0f;
                                 }
 #pragma unroll
                                 for (int cc = 0; cc < 6; ++cc)

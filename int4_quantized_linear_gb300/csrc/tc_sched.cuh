@@ -37,10 +37,14 @@ __device__ __forceinline__ int unit_owner(long long u, long long RU, int G) { re
 // stream-K units [c*RU/Gsk, (c+1)*RU/Gsk) (at least one, so a split tile's contributors are
 // consecutive CTAs), which touch tiles t_first..t_last; the first and last of those may be
 // shared with neighbouring CTAs.
-// Processing order: the split first stream-K tile (if split), then the split last one, then the
-// remaining stream-K tiles, then the whole data-parallel tiles.  The split tiles' fix-up
-// (partial store, arrival count, last-arrival reduction) then runs in the epilogue while the
-// MMAs of whole tiles proceed, and a CTA that owns whole tiles ends on a direct store.
+// Processing order: the two split stream-K tiles (the first and the last, where split) -- the one
+// with fewer of this CTA's units first -- then the remaining stream-K tiles, then the whole
+// data-parallel tiles.  The split tiles' fix-up (partial store, arrival count, last-arrival
+// reduction) then runs in the epilogue while the MMAs of whole tiles proceed, and a CTA that owns
+// whole tiles ends on a direct store.  Short split segment first: its partial is in long before the
+// tile's other contributors finish, so the CTA is not that tile's last arrival; a long first
+// segment ends with its neighbours' and often makes the CTA reduce that tile mid-way and then
+// reduce its last tile too, two fix-ups in a row at the end of the kernel.
 // a / b for a >= 0, b > 0: a 32-bit division when a fits (the common case), else 64-bit.
 __device__ __forceinline__ long long div_nonneg(long long a, int b)
 {
@@ -48,9 +52,10 @@ __device__ __forceinline__ long long div_nonneg(long long a, int b)
 }
 
 struct Sched {
-    long long u_begin, u_end, A, L;  // stream-K unit range, units kept in place / moved up front
+    long long u_begin, u_end, A, L;  // stream-K unit range, units of the split first / last tile
+    long long A0;                    // units processed before the split last tile's (A or 0)
     int U, t_first, t_last, S_sk, S, dp_t0, D, n_sk, n_units;
-    bool pf, pl;
+    bool pf, pl, lf;                 // first / last stream-K tile split; lf: the last one goes first
     __device__ Sched(int cta, int Gsk, long long RU, int D_, int R, int U_) : U(U_), D(D_)
     {
         u_begin = cta < Gsk ? (long long)cta * RU / Gsk : RU;
@@ -63,6 +68,8 @@ struct Sched {
         pl = S_sk >= 2 && (ue % U_) != 0;
         A = pf ? min(ue, (long long)(t_first + 1) * U_) - ub : 0;
         L = pl ? ue - (long long)t_last * U_ : 0;
+        lf = pf && pl && L < A;
+        A0 = lf ? 0 : A;
         dp_t0 = R + cta * D_;
         S = S_sk + D_;
         n_sk = (int)(ue - ub);
@@ -72,8 +79,8 @@ struct Sched {
     __device__ long long unit_at(long long p) const
     {
         if (p < n_sk) {
-            if (p < A) return u_begin + p;
-            if (p < A + L) return (long long)t_last * U + (p - A);
+            if (p < A0) return u_begin + p;
+            if (p < A0 + L) return (long long)t_last * U + (p - A0);
             return u_begin + (p - L);
         }
         const unsigned q = (unsigned)(p - n_sk);  // < D * U: fits in 32 bits
@@ -102,7 +109,7 @@ struct Sched {
     {
         if (k >= S_sk) return dp_t0 + (k - S_sk);
         int s = k;
-        if (pl) s = pf ? (k == 0 ? 0 : (k == 1 ? S_sk - 1 : k - 1)) : (k == 0 ? S_sk - 1 : k - 1);
+        if (pl) s = (pf && !lf) ? (k == 0 ? 0 : (k == 1 ? S_sk - 1 : k - 1)) : (k == 0 ? S_sk - 1 : k - 1);
         return t_first + s;
     }
     __device__ void seg_units(int k, long long &a, long long &b) const

@@ -38,11 +38,28 @@ def _deps():
             + [os.path.join(ROOT, "include", "w4a8.h"), os.path.abspath(__file__)])
 
 
+def _extra_flags():
+    # W4A8_EXTRA_NVCC_FLAGS: extra compiler options for this build (e.g. -DW4A8_TRACE to compile in
+    # the pipeline timestamps, or a tuning constant such as -DW4A8_L2_PREFETCH_FILLS=4)
+    return os.environ.get("W4A8_EXTRA_NVCC_FLAGS", "").split()
+
+
+def _flags_path():
+    return LIB_PATH + ".flags"
+
+
 def up_to_date() -> bool:
     if not os.path.exists(LIB_PATH):
         return False
     t = os.path.getmtime(LIB_PATH)
-    return all(os.path.getmtime(d) <= t for d in _deps())
+    if not all(os.path.getmtime(d) <= t for d in _deps()):
+        return False
+    # a library built with other extra options (a diagnostic build, say) is rebuilt
+    try:
+        with open(_flags_path()) as f:
+            return f.read() == " ".join(_extra_flags())
+    except OSError:
+        return not _extra_flags()
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -51,9 +68,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
     nvcc = _nvcc()
 
-    # W4A8_EXTRA_NVCC_FLAGS: extra compiler options for this build (e.g. -DW4A8_TRACE to compile in
-    # the pipeline timestamps, or a tuning constant such as -DW4A8_L2_PREFETCH_FILLS=4)
-    extra = os.environ.get("W4A8_EXTRA_NVCC_FLAGS", "").split()
+    extra = _extra_flags()
 
     def compile_one(src):
         obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
@@ -75,6 +90,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout + r.stderr)
     os.replace(tmp, LIB_PATH)
+    with open(_flags_path(), "w") as f:
+        f.write(" ".join(extra))
     return LIB_PATH
 
 

@@ -28,18 +28,42 @@ namespace w4a8 {
 
 constexpr int AQ_THREADS = 256;
 
+// Optional timeline (a development aid, compiled in only when W4A8_TRACE is defined): global timer
+// stamps (ns) of every CTA c < 256 at trace[AQ_TRACE_OFF + 4 c + k], k = 0 entry, 1 past the wait
+// on the previous kernel, 3 thread 0's share of the row loaded, 2 done.
+constexpr int AQ_TRACE_OFF = 16384;
+__device__ __forceinline__ void aq_stamp(unsigned long long *trace, int k)
+{
+#ifdef W4A8_TRACE
+    const unsigned c = blockIdx.x * gridDim.y + blockIdx.y;
+    if (trace != nullptr && c < 256 && threadIdx.x == 0) {
+        unsigned long long ns;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(ns));
+        trace[AQ_TRACE_OFF + 4 * c + k] = ns;
+    }
+#endif
+}
+
 // CACHE: chunks of 8 elements kept per thread (rows up to AQ_THREADS * CACHE * 8 read once)
 template <int CACHE>
 __global__ void __launch_bounds__(AQ_THREADS)
 act_quant_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ xq,
-                 float *__restrict__ x_scale, int64_t K)
+                 float *__restrict__ x_scale, int64_t K, unsigned long long *trace)
 {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    aq_stamp(trace, 0);
     const int64_t m = blockIdx.x;
     const uint4 *row = reinterpret_cast<const uint4 *>(x + m * K);
     const int nchunk = (int)(K / 8);
     const bool cached = nchunk <= AQ_THREADS * CACHE;
+    // While the previous kernel finishes, pull the row into L2: one prefetch per 128-byte line
+    // (every 8th chunk, and the last chunk for a row that ends inside a line).  A prefetch returns
+    // nothing to the kernel, so it is harmless even if that kernel is still writing x: every load
+    // below comes after the wait and reads L2, where the final values land.
+    for (int c = 8 * (int)threadIdx.x; c < nchunk + 7; c += 8 * AQ_THREADS)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(row + min(c, nchunk - 1)));
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    aq_stamp(trace, 1);
     // this CTA's slice of the row's chunks
     const int c_lo = (int)((long long)nchunk * blockIdx.y / gridDim.y);
     const int c_hi = (int)((long long)nchunk * (blockIdx.y + 1) / gridDim.y);
@@ -47,10 +71,14 @@ act_quant_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ xq,
     uint4 v[CACHE];
     uint32_t amax2 = 0;  // two 15-bit magnitudes packed, per-halfword max
     if (cached) {
+        // every load of the row goes out before the first use: one round trip, not CACHE
 #pragma unroll
         for (int i = 0; i < CACHE; ++i) {
             const int c = threadIdx.x + i * AQ_THREADS;
             v[i] = c < nchunk ? __ldg(row + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < CACHE; ++i) {
             amax2 = __vmaxu2(amax2, v[i].x & 0x7fff7fffu);
             amax2 = __vmaxu2(amax2, v[i].y & 0x7fff7fffu);
             amax2 = __vmaxu2(amax2, v[i].z & 0x7fff7fffu);
@@ -65,6 +93,7 @@ act_quant_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ xq,
             amax2 = __vmaxu2(amax2, w.w & 0x7fff7fffu);
         }
     }
+    aq_stamp(trace, 3);
     uint32_t hb = max(amax2 & 0xffffu, amax2 >> 16);
     float amax = bf16_bits_to_float(hb);
     amax = warp_max(amax);
@@ -92,6 +121,7 @@ act_quant_kernel(const uint16_t *__restrict__ x, uint8_t *__restrict__ xq,
     } else {
         for (int c = c_lo + (int)threadIdx.x; c < c_hi; c += AQ_THREADS) out[c] = quant8(row[c]);
     }
+    aq_stamp(trace, 2);
 }
 
 }  // namespace w4a8
@@ -112,10 +142,11 @@ w4a8_status w4a8_launch_act_quant(const uint16_t *x_bf16, uint8_t *xq, float *x_
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // the smallest register cache that holds the row (fewer registers, more CTAs per SM)
+    unsigned long long *trace = static_cast<unsigned long long *>(w4a8_debug_trace_ptr());
     const cudaError_t e =
-        K <= 8192 ? cudaLaunchKernelEx(&cfg, w4a8::act_quant_kernel<4>, x_bf16, xq, x_scale, K)
-        : K <= 24576 ? cudaLaunchKernelEx(&cfg, w4a8::act_quant_kernel<12>, x_bf16, xq, x_scale, K)
-                     : cudaLaunchKernelEx(&cfg, w4a8::act_quant_kernel<16>, x_bf16, xq, x_scale, K);
+        K <= 8192 ? cudaLaunchKernelEx(&cfg, w4a8::act_quant_kernel<4>, x_bf16, xq, x_scale, K, trace)
+        : K <= 24576 ? cudaLaunchKernelEx(&cfg, w4a8::act_quant_kernel<12>, x_bf16, xq, x_scale, K, trace)
+                     : cudaLaunchKernelEx(&cfg, w4a8::act_quant_kernel<16>, x_bf16, xq, x_scale, K, trace);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return W4A8_ERR_CUDA;

@@ -119,7 +119,8 @@ __device__ __forceinline__ void trace_ev(const Params &p, int ev, int i)
 // k = 0 entry, 1 set-up done, 2 epilogue done, 3 exit; for the CTA's last tile the epilogue's
 // 4 accumulator ready, 5 partial stored, 6 arrival counted, 7 fix-up done; 8 first fill released
 // to the MMA warp, 9 last fill released, 10 MMA warp done issuing, 11 first accumulator ready,
-// 12 last tile's partials staged in shared memory, 13 summed and stored.
+// 12 last tile's partials staged in shared memory, 13 summed and stored, 14 / 15 its first 16
+// columns summed / stored.
 constexpr int TRACE_PHASES = 16;
 __device__ __forceinline__ void trace_phase(const Params &p, int k)
 {
@@ -320,8 +321,12 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
     }
     // Early weights: when the kernel before this one in the stream is known to leave the weights
     // alone (the library's own activation quant, which itself waited for everything before it),
-    // the first US ring fills' weights and the first SFR scale tiles are requested now, while that
-    // kernel still runs; the fills' activation halves follow after the wait below.
+    // the first ring fill's weights and the first SFR scale tiles are requested now, while that
+    // kernel still runs; the fill's activation half follows after the wait below.  One fill, not
+    // the whole ring: every SM's early loads land on HBM just as the quant kernel reads its rows,
+    // and a ring's worth from 150 SMs (10-20 MB) slows that kernel, which this one then waits for
+    // (decode step of 8 linears on GB300: 204.4 us with every fill early, 201.6 with one, 204.5
+    // with none).
     int pre = 0;  // ring fills whose weights went out early (producer thread)
     if (!A4 && p.w_early && threadIdx.x == 0) {
         for (int g = 0; g < min(n_k / 4, SFR); ++g) {
@@ -330,7 +335,7 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
             atomicMax(sfr_issued, g + 1);
         }
         const uint64_t w_policy = tc::make_policy_evict_first();
-        for (; pre < min(n_k / KPU, US); ++pre) {
+        for (; pre < min(n_k / KPU, 1); ++pre) {
             int kt, n0;
             sched.fill_at(pre * KPU, p.m_tiles, kt, n0);
             tc::mbar_arrive_expect_tx(&full[pre], L::TX_BYTES);  // weights now, activations later
@@ -686,7 +691,9 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                     // The CTA's last tile: every ring fill has been consumed (its accumulator is
                     // complete), so the ring's shared memory is idle.  Bulk copies bring all the
                     // contributors' partials in one round trip instead of one per 16 columns.
-                    if (last_seg && (size_t)n_contrib * part_bytes <= (size_t)L::SFR_OFF) {
+                    // Up to 16 tokens the plain loads below take one round trip too, without the
+                    // proxy fence and the bulk copy's longer latency.
+                    if (last_seg && m_cnt > 16 && (size_t)n_contrib * part_bytes <= (size_t)L::SFR_OFF) {
                         if (threadIdx.x == EPI_WARP0 * 32) {
                             tc::fence_proxy_async_global();  // partials were written by generic stores
                             tc::mbar_arrive_expect_tx(fix_bar, (uint32_t)n_contrib * part_bytes);
@@ -723,7 +730,9 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                                 }
 #pragma unroll
                                 for (int j = 0; j < 16; ++j) a[j] *= xs_s[c0 + j];
+                                if (c0 == 0 && threadIdx.x == EPI_WARP0 * 32) trace_phase(p, 14);
                                 emit(a, c0, m0, n0);
+                                if (c0 == 0 && threadIdx.x == EPI_WARP0 * 32) trace_phase(p, 15);
                             }
                         }
                         if (threadIdx.x == EPI_WARP0 * 32) trace_phase(p, 13);

@@ -43,11 +43,12 @@ def lib_path() -> str:
 
 
 def load(build_if_missing: bool = True):
-    """Load libw4a8.so (building it in-tree first if it is missing or stale)."""
+    """Load libw4a8.so (building it in-tree first if it is missing or older than its sources; a
+    library built with extra compiler options is loaded as it is)."""
     global _lib
     if _lib is not None:
         return _lib
-    if build_if_missing and not _build.up_to_date():
+    if build_if_missing and not _build.up_to_date(check_flags=False):
         _build.build()
     if not os.path.exists(_build.LIB_PATH):
         raise RuntimeError(f"libw4a8.so not found at {_build.LIB_PATH}; run build()")

@@ -48,12 +48,14 @@ def _flags_path():
     return LIB_PATH + ".flags"
 
 
-def up_to_date() -> bool:
+def up_to_date(check_flags: bool = True) -> bool:
     if not os.path.exists(LIB_PATH):
         return False
     t = os.path.getmtime(LIB_PATH)
     if not all(os.path.getmtime(d) <= t for d in _deps()):
         return False
+    if not check_flags:
+        return True
     # a library built with other extra options (a diagnostic build, say) is rebuilt
     try:
         with open(_flags_path()) as f:

@@ -578,6 +578,24 @@ def test_int4_prefill_extreme_codes(lib, orc):
         assert np.all(got[3] == 0.0)
 
 
+@pytest.mark.parametrize("M", [1, 16])
+def test_int4_decode_extreme_codes(lib, orc, M):
+    # decode tiles (1 and 16 tokens): every code 0 (value -8, the output is the zero point's
+    # term alone), every code 15 (value 7), alternating 15 / 0, and an all-zero activation row
+    # whose output must be exactly zero
+    N, K = 384, 1536
+    x, _, s16, qz = synth.int4_case(M, N, K, seed=22 + M)
+    live = M - 1 if M > 1 else M  # rows checked against the oracle; the last one is zero if M > 1
+    if M > 1:
+        x[M - 1, :] = 0
+    for word in (0x00000000, 0xFFFFFFFF, 0x0F0F0F0F):
+        qw = np.full((K // 8, N), word, np.uint32).view(np.int32)
+        got, ref = _i4_gemm(lib, orc, x, qw, s16, qz)
+        gemm_check(got[:live], ref[:live], f"int4 decode M={M} codes {word:#x}")
+        if M > 1:
+            assert np.all(got[M - 1] == 0.0)
+
+
 def _i4_asym_gemm(lib, orc, x, qw, s16, qz, pairs=None):
     xq, xs = lib.act_quant(to_dev_bf16(x))
     out = lib.int4g128_asym_linear(xq, xs, to_dev(qw), to_dev_fp16(s16), to_dev(qz))

@@ -73,10 +73,13 @@ W4A8_API w4a8_status w4a8_act_quant(const uint16_t *x_bf16, uint8_t *xq, float *
  *   w_e8m0   [N, K/32] block scales (4-byte aligned)
  *   out_bf16 [M, N]   written (4-byte aligned)
  *   workspace: device scratch of at least w4a8_workspace_bytes(M, N, K) bytes (may be NULL
- *   when that is 0).  It holds fp32 split-K partials and per-tile arrival counters; the
- *   counters must be zero before the first call that uses the buffer and are left at zero by
- *   every call, so one buffer can be reused call after call on one stream.  Two calls that
- *   run at the same time must not share a workspace.
+ *   when that is 0).  Its first 16 KiB hold the split tiles' arrival counters and the fp32
+ *   split-K partials follow; the counters must be zero before the first call that uses the
+ *   buffer and are left at zero by every call that completes.  The counters sit at the same
+ *   place for every shape and no partial is ever written there, so one buffer sized for the
+ *   largest need can be reused call after call on one stream, for any sequence of shapes and
+ *   of the entry points that take a workspace.  Two calls that run at the same time must not
+ *   share a workspace.  After a call that reported a device error, zero the buffer again.
  * K must be a multiple of 32.  M <= 64 takes the decode tiling (split-K over K), larger M the
  * prefill tiling; both are chosen inside this call. */
 W4A8_API w4a8_status w4a8_mxfp4_linear(const uint8_t *xq, const float *x_scale, const uint8_t *w_packed,
@@ -95,9 +98,10 @@ W4A8_API size_t w4a8_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *   x_bf16    [M, K] bf16 (16-byte aligned)
  *   w_packed, w_e8m0, out_bf16: as for w4a8_mxfp4_linear
  *   workspace: device scratch of at least w4a8_mxfp4_linear_bf16_workspace_bytes(M, N, K)
- *              bytes, 256-byte aligned.  It receives the quantized activations [M, K] and their
- *              scales [M], then holds the GEMM's scratch, with the zero-counter contract of
- *              w4a8_mxfp4_linear (zero before first use, left at zero by every call).
+ *              bytes, 256-byte aligned.  It holds the GEMM's scratch first (counters at offset 0,
+ *              kept even where the GEMM needs no scratch), then receives the quantized
+ *              activations [M, K] and their scales [M]; the zero-counter contract and the reuse
+ *              across shapes are those of w4a8_mxfp4_linear.
  * The two kernels are chained with programmatic dependent launch: the activation quant waits
  * for the work before it on the stream before touching memory, and the GEMM begins fetching
  * its weights while the quant runs.  K must be a multiple of 32. */

@@ -4,6 +4,7 @@
 // Dispatch ("vllm-radiance (MXFP4)", "The W4A8 fp8-WMMA kernel": a prefill tiling and a decode
 // tiling, chosen inside the native call so no shape branch is visible to the caller;
 // "radiance_autoround.py", autoround_linear: the prefill/decode choice is made natively).
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -163,14 +164,20 @@ extern "C" w4a8_status w4a8_mxfp4_linear(const uint8_t *xq, const float *x_scale
     return w4a8_launch_mxfp4_simt(xq, x_scale, w_packed, w_e8m0, out_bf16, M, N, K, stream);
 }
 
-// Workspace of the fused entry: quantized activations, their scales, then the GEMM's scratch
-// (each part starting on a 256-byte boundary).
+// Workspace of the fused entry: the GEMM's scratch first (its arrival counters at offset 0 for
+// every shape; the counter region is kept even when the GEMM needs no scratch, so the
+// activations never land on it), then the quantized activations and their scales, each part
+// starting on a 256-byte boundary.
 static size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
+static size_t gemm_part(int64_t M, int64_t N, int64_t K)
+{
+    return round256(std::max(w4a8_workspace_bytes(M, N, K), W4A8_COUNTER_BYTES));
+}
 
 extern "C" size_t w4a8_mxfp4_linear_bf16_workspace_bytes(int64_t M, int64_t N, int64_t K)
 {
     if (M <= 0 || N <= 0 || K <= 0) return 0;
-    return round256((size_t)M * (size_t)K) + round256((size_t)M * 4) + w4a8_workspace_bytes(M, N, K);
+    return gemm_part(M, N, K) + round256((size_t)M * (size_t)K) + round256((size_t)M * 4);
 }
 
 extern "C" w4a8_status w4a8_mxfp4_linear_bf16(const uint16_t *x_bf16, const uint8_t *w_packed,
@@ -187,10 +194,10 @@ extern "C" w4a8_status w4a8_mxfp4_linear_bf16(const uint16_t *x_bf16, const uint
     const size_t need = w4a8_mxfp4_linear_bf16_workspace_bytes(M, N, K);
     if (!workspace || workspace_bytes < need) return W4A8_ERR_WORKSPACE;
     if (!w4a8_aligned(workspace, 256)) return W4A8_ERR_MISALIGNED;
-    uint8_t *xq = static_cast<uint8_t *>(workspace);
+    uint8_t *gws = static_cast<uint8_t *>(workspace);
+    const size_t gws_bytes = gemm_part(M, N, K);
+    uint8_t *xq = gws + gws_bytes;
     float *xs = reinterpret_cast<float *>(xq + round256((size_t)M * (size_t)K));
-    uint8_t *gws = reinterpret_cast<uint8_t *>(xs) + round256((size_t)M * 4);
-    const size_t gws_bytes = workspace_bytes - (size_t)(gws - xq);
 
     const int policy = w4a8_gemm_policy();
     w4a8_status st = w4a8_launch_act_quant(x_bf16, xq, xs, M, K, stream);
@@ -221,8 +228,7 @@ extern "C" w4a8_status w4a8_mxfp4_linear_bf16_single(const uint16_t *x_bf16, con
     const size_t need = w4a8_mxfp4_linear_bf16_workspace_bytes(M, N, K);
     if (!workspace || workspace_bytes < need) return W4A8_ERR_WORKSPACE;
     if (!w4a8_aligned(workspace, 256)) return W4A8_ERR_MISALIGNED;
-    uint8_t *gws = static_cast<uint8_t *>(workspace) + round256((size_t)M * (size_t)K) + round256((size_t)M * 4);
-    return w4a8_launch_mxfp4_tc_aq(x_bf16, w_packed, w_e8m0, out_bf16, M, N, K, gws, stream);
+    return w4a8_launch_mxfp4_tc_aq(x_bf16, w_packed, w_e8m0, out_bf16, M, N, K, workspace, stream);
 }
 
 static w4a8_status int4g128_linear_impl(const uint8_t *xq, const float *x_scale, const int32_t *qweight,

@@ -9,6 +9,13 @@
 
 #define W4A8_DECODE_MAX_M 64
 
+// Every GEMM workspace starts with this many bytes of stream-K arrival counters; the fp32 partial
+// tiles follow.  A kernel counts only on its split tiles, whose indices are below its grid size
+// (at most the SM count), and leaves every counter it touched at zero, and no partial tile ever
+// lands in this region -- so one buffer serves any sequence of shapes and entry points.
+#define W4A8_COUNTER_BYTES ((size_t)16384)
+#define W4A8_MAX_COUNTERS ((int)(W4A8_COUNTER_BYTES / 4))
+
 int w4a8_gemm_policy();
 void *w4a8_debug_trace_ptr();
 unsigned int *w4a8_device_status_ptr();
@@ -35,7 +42,6 @@ w4a8_status w4a8_launch_int4_simt(const uint8_t *xq, const float *x_scale, const
 bool w4a8_tc_mxfp4_supported(const void *xq, const void *wp, const void *we, const void *out,
                              int64_t M, int64_t N, int64_t K);
 size_t w4a8_tc_workspace_bytes(int64_t M, int64_t N, int64_t K);
-size_t w4a8_tc_workspace_counters_offset(int64_t M, int64_t N, int64_t K);
 // w_early: the kernel just before this one on the stream is the library's activation quant
 // (chained by programmatic dependent launch), so weights may be read before waiting on it.
 w4a8_status w4a8_launch_mxfp4_tc(const uint8_t *xq, const float *x_scale, const uint8_t *wp,

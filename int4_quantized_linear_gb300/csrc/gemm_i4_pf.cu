@@ -93,7 +93,7 @@ struct Params {
     const float *xs;       // [M] per-token scale
     uint16_t *out;         // [M, N] bf16
     float *partials;       // [G][2][BN][128] fp32 stream-K partial tiles
-    int *counters;         // [tiles] arrival counters, zero between calls
+    int *counters;         // arrival counters of the split tiles (index < G), zero between calls
     unsigned int *status;  // device status block
     int M, N, K;
     int m_tiles, n_tiles;
@@ -654,7 +654,7 @@ size_t w4a8_int4_pf_workspace_bytes(int64_t M, int64_t N, int64_t K)
 {
     if (K % 512 != 0 || K <= 0 || M <= 0 || N <= 0) return 0;
     const Cfg c = choose(M, N, K);
-    return partial_bytes(c) + (size_t)c.m_tiles * c.n_tiles * 4;
+    return W4A8_COUNTER_BYTES + partial_bytes(c);
 }
 
 w4a8_status w4a8_launch_int4_pf(const uint8_t *xq, const float *x_scale, const int32_t *qw, const uint8_t *qh,
@@ -668,10 +668,10 @@ w4a8_status w4a8_launch_int4_pf(const uint8_t *xq, const float *x_scale, const i
     prm.s16 = s16;
     prm.xs = x_scale;
     prm.out = out;
-    prm.partials = static_cast<float *>(workspace);
-    prm.counters = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) + partial_bytes(c));
+    prm.counters = static_cast<int *>(workspace);
+    prm.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + W4A8_COUNTER_BYTES);
     prm.status = w4a8_device_status_ptr();
-    if (!prm.status) return W4A8_ERR_CUDA;
+    if (!prm.status || c.k.G > W4A8_MAX_COUNTERS) return W4A8_ERR_CUDA;
     prm.M = (int)M;
     prm.N = (int)N;
     prm.K = (int)K;

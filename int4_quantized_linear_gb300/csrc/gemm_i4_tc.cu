@@ -106,7 +106,7 @@ struct Params {
     const uint8_t *z5;     // asymmetric int5 only: [K/128, N] zero points
     uint16_t *out;         // [M, N] bf16
     float *partials;       // [G][2][BN][128] fp32 stream-K partial tiles
-    int *counters;         // [tiles] arrival counters, zero between calls
+    int *counters;         // arrival counters of the split tiles (index < G), zero between calls
     unsigned int *status;  // device status block
     int M, N, K;
     int m_tiles, n_tiles;
@@ -654,7 +654,7 @@ size_t w4a8_tc_int4_workspace_bytes(int64_t M, int64_t N, int64_t K)
 {
     if (K % 512 != 0 || K <= 0 || M <= 0 || N <= 0) return 0;
     const Cfg c = w4a8::tci::choose(M, N, K);
-    const size_t own = partial_bytes(c) + (size_t)c.m_tiles * c.n_tiles * 4;
+    const size_t own = W4A8_COUNTER_BYTES + partial_bytes(c);
     // prefill sizes may take the 256-token kernel instead: enough for either
     return M > W4A8_INT4_PF_MIN_M ? std::max(own, w4a8_int4_pf_workspace_bytes(M, N, K)) : own;
 }
@@ -667,8 +667,9 @@ static bool make_params(Params &prm, const Cfg &c, const float *x_scale, const u
     prm.qz = nullptr;
     prm.z5 = nullptr;
     prm.out = out;
-    prm.partials = static_cast<float *>(workspace);
-    prm.counters = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) + partial_bytes(c));
+    if (c.k.G > W4A8_MAX_COUNTERS) return false;  // split tiles are indexed below the grid size
+    prm.counters = static_cast<int *>(workspace);
+    prm.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + W4A8_COUNTER_BYTES);
     prm.status = w4a8_device_status_ptr();
     prm.M = (int)M;
     prm.N = (int)N;

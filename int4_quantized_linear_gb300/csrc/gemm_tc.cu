@@ -89,7 +89,7 @@ struct Params {
     const uint16_t *x;     // AQ: [M, K] bf16 activations, quantized inside the kernel
     uint16_t *out;         // [M, N] bf16
     float *partials;       // [G][2][BN][128] fp32 stream-K partial tiles
-    int *counters;         // [tiles] arrival counters, zero between calls
+    int *counters;         // arrival counters of the split tiles (index < G), zero between calls
     unsigned int *status;  // device status block
     int M, N, K;
     int m_tiles, n_tiles;
@@ -848,7 +848,7 @@ size_t partial_bytes(const Cfg &c)
 
 size_t workspace_for(const Cfg &c)
 {
-    return partial_bytes(c) + (size_t)c.m_tiles * c.n_tiles * 4;
+    return W4A8_COUNTER_BYTES + partial_bytes(c);
 }
 
 template <int BN, int KPU, int US, int ACC_BUFS, int SFQ, int SFR, bool A4 = false, bool AQ = false>
@@ -916,11 +916,6 @@ bool w4a8_tc_mxfp4_supported(const void *xq, const void *wp, const void *we, con
     return w4a8::tch::encode_fn() != nullptr;
 }
 
-size_t w4a8_tc_workspace_counters_offset(int64_t M, int64_t N, int64_t K)
-{
-    return partial_bytes(choose(M, N, K));
-}
-
 size_t w4a8_tc_workspace_bytes(int64_t M, int64_t N, int64_t K)
 {
     if (K % 512 != 0 || K <= 0 || M <= 0 || N <= 0) return 0;
@@ -935,8 +930,9 @@ static bool make_params(Params &prm, const Cfg &c, const float *x_scale, const u
     prm.xs = x_scale;
     prm.x = nullptr;
     prm.out = out;
-    prm.partials = static_cast<float *>(workspace);
-    prm.counters = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) + partial_bytes(c));
+    if (c.G > W4A8_MAX_COUNTERS) return false;  // split tiles are indexed below the grid size
+    prm.counters = static_cast<int *>(workspace);
+    prm.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + W4A8_COUNTER_BYTES);
     prm.status = w4a8_device_status_ptr();
     prm.M = (int)M;
     prm.N = (int)N;

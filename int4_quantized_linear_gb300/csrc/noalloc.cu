@@ -8,6 +8,7 @@
 // with its stream-K scratch (fp32 partial tiles and arrival counters) in a fixed-size array in
 // the library's device image.  Every GPU that loads the library holds that array until the
 // process exits.
+#include <algorithm>
 #include "common.cuh"
 #include "dispatch.h"
 
@@ -49,12 +50,9 @@ extern "C" w4a8_status w4a8_mxfp4_linear_noalloc(const uint8_t *xq, const float 
     if (need > W4A8_NOALLOC_SCRATCH_BYTES) return W4A8_ERR_WORKSPACE;
     void *scratch = noalloc_scratch_ptr();
     if (!scratch) return W4A8_ERR_CUDA;
-    // The arrival counters sit after the partial tiles and must start at zero; a call that gave
-    // up part-way could have left some set, so clear them (a small memset, not an allocation).
-    const size_t counters_off = w4a8_tc_workspace_counters_offset(M, N, K);
-    if (need > counters_off &&
-        cudaMemsetAsync(static_cast<unsigned char *>(scratch) + counters_off, 0, need - counters_off, stream) !=
-            cudaSuccess)
+    // The arrival counters open the scratch and must start at zero; a call that gave up part-way
+    // could have left some set, so clear them (a small memset, not an allocation).
+    if (cudaMemsetAsync(scratch, 0, std::min(need, W4A8_COUNTER_BYTES), stream) != cudaSuccess)
         return W4A8_ERR_CUDA;
     return w4a8_launch_mxfp4_tc(xq, x_scale, w_packed, w_e8m0, out_bf16, M, N, K, scratch, policy, false,
                                 stream);

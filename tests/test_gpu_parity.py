@@ -478,6 +478,32 @@ def test_linear_fused_chained_layers(lib, orc):
     gemm_check(bf16_to_f64(ref2), orc.mxfp4_linear(host(hq), host(hs), w2, e2), "layer 2")
 
 
+def test_workspace_shared_across_shapes(lib):
+    """One workspace buffer, sized for the largest need, serves a sequence of shapes and entry
+    points: the arrival counters sit at a fixed offset that no partial tile ever reaches, so a
+    wide decode tile's partials cannot leave garbage where a narrower one counts.  Every output
+    must equal the same call with a fresh workspace, bit for bit."""
+    N, K = 1024, 2048  # 8 weight tiles of 4 units: every tile split over 4 CTAs
+    cases = [64, 1, 300, 8, 1, 32, 1]
+    need = max(max(lib.workspace_bytes(M, N, K), lib.int4_workspace_bytes(M, N, K),
+                   lib.linear_workspace_bytes(M, N, K)) for M in cases)
+    ws = lib.make_workspace(need + 256, "cuda")
+    ws = ws[(-ws.data_ptr()) % 256:][:need]
+    _, w, e = synth.prefill_case(1, N, K, seed=31)
+    wd, ed = to_dev(w), to_dev(e)
+    _, qw, s16, _ = synth.int4_case(1, N, K, seed=32)
+    qwd, s16d = to_dev(qw), to_dev_fp16(s16)
+    for M in cases:
+        xd = to_dev_bf16(synth.activations(M, K, seed=M))
+        xq, xs = lib.act_quant(xd)
+        got = [lib.mxfp4_linear(xq, xs, wd, ed, workspace=ws), lib.int4g128_linear(xq, xs, qwd, s16d, workspace=ws),
+               lib.linear(xd, wd, ed, workspace=ws)]
+        ref = [lib.mxfp4_linear(xq, xs, wd, ed), lib.int4g128_linear(xq, xs, qwd, s16d), lib.linear(xd, wd, ed)]
+        lib.check_device_status()
+        for g, r, what in zip(got, ref, ("mxfp4", "int4", "bf16 linear")):
+            assert torch.equal(g.view(torch.int16), r.view(torch.int16)), f"{what} M={M}"
+
+
 def test_linear_fused_rejects(lib):
     M, N, K = 2, 128, 512
     x = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")

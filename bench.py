@@ -525,11 +525,19 @@ def run_ours(args, rank, world, local_rank):
     h2d_stream = torch.cuda.Stream(device=dev)
     d2h_stream = torch.cuda.Stream(device=dev)
 
+    # Before call i the compute stream waits for the input copies up to call E2E_WAITS[i]: the first
+    # two calls' inputs, then (before the third call, long after they landed) all the others.  Every
+    # wait on another stream breaks the programmatic-dependent-launch overlap between the two
+    # kernels around it (~4 us), and every copy costs ~5 us of latency, so one wait per call
+    # (241.6 us per step) and one wait for all inputs up front (261 us) both lose to this
+    # (221-227 us; 200 us without any copies).
+    E2E_WAITS = {0: 1, 2: len(calls) - 1}
+
     def e2e_step():
         # per call: pinned host x -> device, the public linear(), device out -> pinned host.  The
-        # copies run on two more streams, one per direction (inputs first, each output as soon as
-        # its GEMM is done), so they overlap the other calls' kernels and each other, as a serving
-        # loop would pipeline them.
+        # copies run on two more streams, one per direction (inputs first, in call order; each
+        # output as soon as its GEMM is done), so they overlap the other calls' kernels and each
+        # other, as a serving loop would pipeline them.
         h2d_stream.wait_stream(stream)
         d2h_stream.wait_stream(stream)
         x_ready, o_ready = [], []
@@ -540,8 +548,9 @@ def run_ours(args, rank, world, local_rank):
                 ev.record(h2d_stream)
                 x_ready.append(ev)
         with torch.cuda.stream(stream):
-            for c, xd, od, ev in zip(calls, dev_x, dev_o, x_ready):
-                stream.wait_event(ev)
+            for i, (c, xd, od) in enumerate(zip(calls, dev_x, dev_o)):
+                if i in E2E_WAITS:
+                    stream.wait_event(x_ready[E2E_WAITS[i]])
                 lib.linear(xd, c["w"], c["e"], out=od, workspace=c["lws"], stream=stream)
                 done = torch.cuda.Event()
                 done.record(stream)
@@ -586,8 +595,9 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "per (shape, M): pinned host x -> device, binding.linear, device out -> pinned host, "
-                        "copies on one stream per direction overlapping the kernels; the step captured in "
-                        "a CUDA graph and replayed, wall-clock timed",
+                        "copies on one stream per direction overlapping the kernels (the compute stream "
+                        "waits for the first two inputs before the first call and for the rest before the "
+                        "third); the step captured in a CUDA graph and replayed, wall-clock timed",
                 "eager_value": e2e_eager_val},
         "gpu_launches": 2 * len(calls) * args.steps,
         "decode_cases": decode_cases,

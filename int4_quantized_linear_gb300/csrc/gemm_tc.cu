@@ -227,6 +227,17 @@ struct Layout {
     static_assert((X_TILE % 1024) == 0 && (X_OFF % 1024) == 0, "swizzled tiles are 1024-aligned");
 };
 
+// Stream-K fix-up of a decode tile (up to 64 tokens): whole partials of a group of contributors
+// per round trip to L2 pays when that takes fewer trips than one per 16-column chunk (64-token
+// tiles with at most three contributors; 32-token tiles always, three contributors a trip).
+template <int BN>
+__device__ __forceinline__ bool narrow_fixup(int n_contrib)
+{
+    if constexpr (BN > 64) return false;
+    else if constexpr (BN == 64) return n_contrib < 4;
+    else return BN == 32;  // 16-token tiles: the chunked path below is the same thing
+}
+
 template <int BN, int KPU, int US, int ACC_BUFS, int SFQ, int SFR, bool A4, bool AQ>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
@@ -736,6 +747,41 @@ mxfp4_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constan
                             }
                         }
                         if (threadIdx.x == EPI_WARP0 * 32) trace_phase(p, 13);
+                    } else if (narrow_fixup<BN>(n_contrib)) {
+                        // decode tiles: a group of contributors' whole partials per round trip (one
+                        // 64-column partial, three of 32 columns, six of 16) instead of one round
+                        // trip per 16-column chunk; the additions run in CTA order as below
+                        constexpr int NT = BN <= 64 ? BN : 16;                     // columns held
+                        constexpr int GC = BN >= 64 ? 1 : (BN <= 64 ? 96 / NT : 1);  // contributors per trip
+                        float acc[NT];
+#pragma unroll
+                        for (int j = 0; j < NT; ++j) acc[j] = 0.0f;
+                        for (int cb = c_first; cb <= c_last; cb += GC) {
+                            float v[GC][NT];
+#pragma unroll
+                            for (int cc = 0; cc < GC; ++cc) {
+                                const int c = min(cb + cc, c_last);  // past the end: reload the last, unused
+                                const int sl = (t == (int)(unit_start(c, p.RU, p.Gsk) / p.U)) ? 0 : 1;
+                                const float *src = p.partials + ((size_t)c * 2 + sl) * (size_t)(BM * BN) + row;
+#pragma unroll
+                                for (int j = 0; j < NT; ++j) v[cc][j] = j < m_cnt ? __ldcg(src + j * BM) : 0.0f;
+                            }
+#pragma unroll
+                            for (int cc = 0; cc < GC; ++cc)
+                                if (cb + cc <= c_last) {
+#pragma unroll
+                                    for (int j = 0; j < NT; ++j) acc[j] += v[cc][j];
+                                }
+                        }
+#pragma unroll
+                        for (int c0 = 0; c0 < NT; c0 += 16) {
+                            if (c0 < m_cnt) {
+                                float o[16];
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) o[j] = acc[c0 + j] * xs_s[c0 + j];
+                                emit(o, c0, m0, n0);
+                            }
+                        }
                     } else {
                         // 16 columns at a time, up to 6 contributors' loads in flight together; the
                         // additions still run in CTA order, so the result does not depend on timing

@@ -130,3 +130,20 @@ def test_workspace_sizes_do_not_depend_on_policy(clib):
     clib.w4a8_set_gemm_policy(0)
     assert sizes[0] == sizes[1] == sizes[2]
     assert all(a > 0 and b > 0 for a, b in sizes[0])
+
+
+def test_workspace_sizes_hold_the_counter_region(clib):
+    # Every GEMM workspace opens with 16 KiB of arrival counters (the same place for every shape,
+    # so one buffer serves any sequence of shapes), and the bf16 linear's workspace keeps that
+    # region in front of the quantized activations even where the GEMM itself needs no scratch.
+    counters = 16384
+    for M, N, K in [(1, 34816, 5120), (8, 5120, 17408), (64, 5120, 17408), (300, 1024, 2048),
+                    (4096, 10240, 5120), (1, 128, 512)]:
+        g = clib.w4a8_workspace_bytes(M, N, K)
+        assert g >= counters
+        assert clib.w4a8_int4g128_workspace_bytes(M, N, K) >= counters
+        lin = clib.w4a8_mxfp4_linear_bf16_workspace_bytes(M, N, K)
+        assert lin >= g + M * K + 4 * M
+    # K not a multiple of 512: no tensor-core scratch, but the linear keeps the counter region
+    assert clib.w4a8_workspace_bytes(2, 96, 96) == 0
+    assert clib.w4a8_mxfp4_linear_bf16_workspace_bytes(2, 96, 96) >= counters + 2 * 96 + 8
